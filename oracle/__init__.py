@@ -1,0 +1,285 @@
+"""Python access to the oracle (oracle.c): plain double-precision CPU code.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+CPU-baseline leg of bench.py may import this package.  Nothing here imports
+the CUDA path, and the CUDA path never imports this.
+
+Besides thin ctypes wrappers this module holds the oracle's own conversion of
+float32 values to bfloat16 values (round to nearest, ties to even), used to
+give the oracle exactly the bf16 weights a bf16-mode step computes with.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        dp = C.POINTER(C.c_double)
+        ip = C.POINTER(C.c_int)
+        sz = C.c_size_t
+        i = C.c_int
+        d = C.c_double
+        sig = {
+            "or_num_params": (sz, [i, i, i, i, i]),
+            "or_param_offset": (i, [i, i, i, i, i, i, i, C.POINTER(sz), C.POINTER(sz)]),
+            "or_set_threads": (None, [i]),
+            "or_get_threads": (i, []),
+            "or_linear_fwd": (None, [dp, dp, dp, i, i, i, dp]),
+            "or_linear_bwd": (None, [dp, dp, dp, i, i, i, dp, dp, dp]),
+            "or_layernorm_fwd": (None, [dp, dp, dp, i, i, d, dp, dp, dp]),
+            "or_layernorm_bwd": (None, [dp, dp, dp, dp, dp, i, i, dp, dp, dp]),
+            "or_gelu_fwd": (None, [dp, sz, dp]),
+            "or_gelu_bwd": (None, [dp, dp, sz, dp]),
+            "or_attention_fwd": (None, [dp, i, i, i, i, dp, dp]),
+            "or_attention_bwd": (None, [dp, dp, dp, i, i, i, i, dp]),
+            "or_xent": (d, [dp, ip, i, i, dp, dp, d]),
+            "or_embed_fwd": (None, [dp, dp, ip, i, i, i, dp]),
+            "or_embed_bwd": (None, [dp, ip, i, i, i, dp, dp]),
+            "or_adamw": (None, [dp, dp, dp, dp, sz, d, d, d, d, d, i]),
+            "or_gpt2_step": (d, [i, i, i, i, i, dp, ip, ip, i, i, dp, dp]),
+            "or_val_reset": (None, []),
+            "or_val_leaf": (i, [d]),
+            "or_val_add": (i, [i, i]),
+            "or_val_mul": (i, [i, i]),
+            "or_val_pow": (i, [i, d]),
+            "or_val_exp": (i, [i]),
+            "or_val_log": (i, [i]),
+            "or_val_data": (d, [i]),
+            "or_val_grad": (d, [i]),
+            "or_val_backward": (i, [i]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _d(a):
+    """float64 C-contiguous pointer (None passes NULL)."""
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags.c_contiguous
+    return a.ctypes.data_as(C.POINTER(C.c_double))
+
+
+def _i(a):
+    assert a.dtype == np.int32 and a.flags.c_contiguous
+    return a.ctypes.data_as(C.POINTER(C.c_int))
+
+
+def f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def set_threads(n: int) -> None:
+    lib().or_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().or_get_threads())
+
+
+# ---------------------------------------------------------------- layout
+def num_params(L, C_, H, V, maxT) -> int:
+    return int(lib().or_num_params(L, C_, H, V, maxT))
+
+
+def param_offset(L, C_, H, V, maxT, layer, which):
+    off = C.c_size_t()
+    n = C.c_size_t()
+    rc = lib().or_param_offset(L, C_, H, V, maxT, layer, which, C.byref(off), C.byref(n))
+    if rc != 0:
+        raise ValueError("bad tensor index")
+    return int(off.value), int(n.value)
+
+
+# ---------------------------------------------------------------- bf16 values
+def bf16_values(x) -> np.ndarray:
+    """Nearest bfloat16 value of each float32 (ties to even), as float64."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (b >> np.uint64(16)) & np.uint64(1)
+    r = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- ops
+def linear_fwd(x, W, b=None):
+    x, W = f64(x), f64(W)
+    M, K = x.shape
+    N = W.shape[0]
+    y = np.zeros((M, N))
+    lib().or_linear_fwd(_d(x), _d(W), _d(None if b is None else f64(b)), M, K, N, _d(y))
+    return y
+
+
+def linear_bwd(x, W, dy, with_bias=True):
+    x, W, dy = f64(x), f64(W), f64(dy)
+    M, K = x.shape
+    N = W.shape[0]
+    dx, dW = np.zeros_like(x), np.zeros_like(W)
+    db = np.zeros(N) if with_bias else None
+    lib().or_linear_bwd(_d(x), _d(W), _d(dy), M, K, N, _d(dx), _d(dW), _d(db))
+    return dx, dW, db
+
+
+def layernorm_fwd(x, w, b, eps=1e-5):
+    x, w, b = f64(x), f64(w), f64(b)
+    M, Cc = x.shape
+    y = np.zeros_like(x)
+    mean, rstd = np.zeros(M), np.zeros(M)
+    lib().or_layernorm_fwd(_d(x), _d(w), _d(b), M, Cc, eps, _d(y), _d(mean), _d(rstd))
+    return y, mean, rstd
+
+
+def layernorm_bwd(x, w, mean, rstd, dy):
+    x, w, mean, rstd, dy = map(f64, (x, w, mean, rstd, dy))
+    M, Cc = x.shape
+    dx, dw, db = np.zeros_like(x), np.zeros(Cc), np.zeros(Cc)
+    lib().or_layernorm_bwd(_d(x), _d(w), _d(mean), _d(rstd), _d(dy), M, Cc, _d(dx), _d(dw), _d(db))
+    return dx, dw, db
+
+
+def gelu_fwd(u):
+    u = f64(u)
+    g = np.zeros_like(u)
+    lib().or_gelu_fwd(_d(u), u.size, _d(g))
+    return g
+
+
+def gelu_bwd(u, dg):
+    u, dg = f64(u), f64(dg)
+    du = np.zeros_like(u)
+    lib().or_gelu_bwd(_d(u), _d(dg), u.size, _d(du))
+    return du
+
+
+def attention_fwd(qkv, B, T, C_, H):
+    qkv = f64(qkv)
+    y = np.zeros((B * T, C_))
+    P = np.zeros((B, H, T, T))
+    lib().or_attention_fwd(_d(qkv), B, T, C_, H, _d(y), _d(P))
+    return y, P
+
+
+def attention_bwd(qkv, P, dy, B, T, C_, H):
+    qkv, P, dy = f64(qkv), f64(P), f64(dy)
+    dqkv = np.zeros_like(qkv)
+    lib().or_attention_bwd(_d(qkv), _d(P), _d(dy), B, T, C_, H, _d(dqkv))
+    return dqkv
+
+
+def xent(z, targets, want_grad=False):
+    z = f64(z)
+    t = np.ascontiguousarray(targets, dtype=np.int32)
+    M, V = z.shape
+    rl = np.zeros(M)
+    dz = np.zeros_like(z) if want_grad else None
+    loss = lib().or_xent(_d(z), _i(t), M, V, _d(rl), _d(dz), 1.0)
+    return loss, rl, dz
+
+
+def embed_fwd(wte, wpe, tok, B, T):
+    wte, wpe = f64(wte), f64(wpe)
+    tok = np.ascontiguousarray(tok, dtype=np.int32)
+    Cc = wte.shape[1]
+    x = np.zeros((B * T, Cc))
+    lib().or_embed_fwd(_d(wte), _d(wpe), _i(tok), B, T, Cc, _d(x))
+    return x
+
+
+def embed_bwd(dx, tok, B, T, V, maxT):
+    dx = f64(dx)
+    tok = np.ascontiguousarray(tok, dtype=np.int32)
+    Cc = dx.shape[1]
+    dwte, dwpe = np.zeros((V, Cc)), np.zeros((maxT, Cc))
+    lib().or_embed_bwd(_d(dx), _i(tok), B, T, Cc, _d(dwte), _d(dwpe))
+    return dwte, dwpe
+
+
+def adamw(p, g, m, v, lr, beta1, beta2, eps, weight_decay, t):
+    """Updates copies of p, m, v and returns them."""
+    p, g, m, v = (f64(a).copy() for a in (p, g, m, v))
+    lib().or_adamw(_d(p), _d(g), _d(m), _d(v), p.size, lr, beta1, beta2, eps, weight_decay, int(t))
+    return p, m, v
+
+
+# ---------------------------------------------------------------- model
+def gpt2_step(shape, params, tokens, targets, want_grads=True, want_row_loss=False):
+    """One forward+backward of the GPT-2 step.
+
+    shape: object with L, C, H, V, maxT.  params: flat (any float dtype; the
+    values are taken exactly as float64).  tokens/targets: int [B, T].
+    Returns (loss, grads or None, row_loss or None)."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    targets = np.ascontiguousarray(targets, dtype=np.int32)
+    B, T = tokens.shape
+    P = f64(params)
+    n = num_params(shape.L, shape.C, shape.H, shape.V, shape.maxT)
+    if P.size != n:
+        raise ValueError(f"expected {n} parameters, got {P.size}")
+    G = np.zeros(n) if want_grads else None
+    rl = np.zeros(B * T) if want_row_loss else None
+    loss = lib().or_gpt2_step(shape.L, shape.C, shape.H, shape.V, shape.maxT, _d(P),
+                              _i(tokens), _i(targets), B, T, _d(G), _d(rl))
+    return float(loss), G, rl
+
+
+# ---------------------------------------------------------------- scalar tape
+class Value:
+    """A scalar node of the oracle's scalar tape (handle into its pool)."""
+
+    def __init__(self, h: int):
+        if h < 0:
+            raise ValueError("invalid operand")
+        self.h = h
+
+    @staticmethod
+    def leaf(x: float) -> "Value":
+        return Value(lib().or_val_leaf(float(x)))
+
+    def __add__(self, o):
+        return Value(lib().or_val_add(self.h, o.h))
+
+    def __mul__(self, o):
+        return Value(lib().or_val_mul(self.h, o.h))
+
+    def pow(self, e: float):
+        return Value(lib().or_val_pow(self.h, float(e)))
+
+    def exp(self):
+        return Value(lib().or_val_exp(self.h))
+
+    def log(self):
+        return Value(lib().or_val_log(self.h))
+
+    @property
+    def data(self) -> float:
+        return float(lib().or_val_data(self.h))
+
+    @property
+    def grad(self) -> float:
+        return float(lib().or_val_grad(self.h))
+
+    def backward(self) -> int:
+        return int(lib().or_val_backward(self.h))
+
+
+def value_reset() -> None:
+    lib().or_val_reset()
+
+
+def value_backward_raw(handle: int) -> int:
+    return int(lib().or_val_backward(handle))
