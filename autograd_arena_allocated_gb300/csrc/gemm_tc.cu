@@ -1,0 +1,637 @@
+// gemm_tc.cu -- the dense contractions of the step on the 5th-generation
+// tensor cores: tcgen05.mma (bf16 in, fp32 accumulate in tensor memory),
+// operands staged by TMA (cp.async.bulk.tensor, 128-byte swizzle) through an
+// mbarrier ring, accumulators read back with tcgen05.ld for a fused epilogue.
+//
+// Persistent, warp-specialised CTA (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one elected lane)
+//   warp 1      TMEM allocator + MMA issuer (one elected lane)
+//   warps 2..5  epilogue: TMEM -> registers -> bias / GELU / GELU' /
+//               residual -> global (warp w reads TMEM lanes 32*(w%4)..+31)
+// The accumulator is double-buffered in TMEM (2 x BN fp32 columns), so the
+// epilogue of tile i overlaps the main loop of tile i+1.
+//
+// Operand forms (the three GEMMs of a linear layer):
+//   FWD y = x W^T   : A K-major, B K-major
+//   DX  dx = dy W   : A K-major, B MN-major
+//   DW  dW = dy^T x : A MN-major, B MN-major, split over tokens (K) with a
+//                     fixed-order reduction when the output has few tiles.
+//
+// Every mbarrier wait is bounded (about two seconds of clock cycles); on
+// expiry the kernel raises FLAG_TIMEOUT, stops all roles, lets in-flight TMA
+// copies land, frees its tensor memory and returns.
+#include "tt_internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace tt {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one 128B-swizzle row
+constexpr int UMMA_K = 16;
+constexpr int THREADS = 192;
+constexpr int MN_BOX = 64;                  // MN extent of one MN-major TMA box
+constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB: 64 k-rows x 128 bytes
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+struct Params {
+    int M, N, K;
+    int m_tiles, n_tiles, tiles;
+    int kb_total, kb_per_split, splits, units;
+    void* D;
+    long long ldd;
+    int d_f32, n_store, epi, accumulate;
+    const __nv_bfloat16* bias;
+    const __nv_bfloat16* residual;
+    __nv_bfloat16* aux;
+    float* ws;  // split-K partials [splits][M][N]
+    int* flags;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase with the given parity has completed;
+// false if another role aborted or the deadline passed (then FLAG_TIMEOUT).
+constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* flags) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > WAIT_CYCLES) {
+                atomicOr(&flags[FLAG_TIMEOUT], 1);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (all >> 4), version 1, 128-byte swizzle.
+//   K-major tile  (rows of 128 B, 8-row atoms): LBO unused (16), SBO = 1024
+//   MN-major tile (k-rows of 64 MN elements):   LBO = distance between 64-wide
+//                                               MN blocks, SBO = 1024 (8 k-rows)
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
+// operand majors, N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float gelu_tanh(float u) {
+    const float k = 0.7978845608028654f, a = 0.044715f;
+    return 0.5f * u * (1.0f + tanhf(k * (u + a * u * u * u)));
+}
+__device__ __forceinline__ float dgelu_tanh(float u) {
+    const float k = 0.7978845608028654f, a = 0.044715f;
+    float tau = tanhf(k * (u + a * u * u * u));
+    return 0.5f * (1.0f + tau) + 0.5f * u * (1.0f - tau * tau) * k * (1.0f + 3.0f * a * u * u);
+}
+
+// Load 32 consecutive bf16 (64 bytes) as floats; vector path when aligned.
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, int valid, bool vec, float* v) {
+    if (vec && valid >= 32) {
+        const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            uint4 w = q[i];
+            v[8 * i + 0] = bf_lo(w.x); v[8 * i + 1] = bf_hi(w.x);
+            v[8 * i + 2] = bf_lo(w.y); v[8 * i + 3] = bf_hi(w.y);
+            v[8 * i + 4] = bf_lo(w.z); v[8 * i + 5] = bf_hi(w.z);
+            v[8 * i + 6] = bf_lo(w.w); v[8 * i + 7] = bf_hi(w.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++) v[j] = (j < valid) ? __bfloat162float(p[j]) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, int valid, bool vec, const float* v) {
+    if (vec && valid >= 32) {
+        uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            uint4 w;
+            w.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+            w.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+            w.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+            w.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+            q[i] = w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+            if (j < valid) p[j] = __float2bfloat16_rn(v[j]);
+    }
+}
+
+__device__ __forceinline__ void store32_f32(float* p, int valid, bool vec, const float* v) {
+    if (vec && valid >= 32) {
+        float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+        for (int i = 0; i < 8; i++) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+            if (j < valid) p[j] = v[j];
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(THREADS, 1)
+k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          const Params p) {
+    using CF = Cfg<BN>;
+    constexpr int S = CF::STAGES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzle atoms
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* tiles = smem;
+    uint64_t* full = (uint64_t*)(smem + S * CF::STAGE_BYTES);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;   // [2]
+    uint64_t* tempty = tfull + 2;  // [2]
+    uint32_t* tmem_base_holder = (uint32_t*)(tempty + 2);
+    volatile int* abort_flag = (volatile int*)(tmem_base_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4 * 32);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_base_holder)),
+                     "r"((uint32_t)CF::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                const int tile = u / p.splits, split = u - tile * p.splits;
+                const int m0 = (tile % p.m_tiles) * BM;
+                const int n0 = (tile / p.m_tiles) * BN;
+                const int kb0 = split * p.kb_per_split;
+                const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags)) { ok = false; break; }
+                    mbar_expect_tx(&full[stage], CF::STAGE_BYTES);
+                    const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
+                    const uint32_t sb = sa + CF::A_BYTES;
+                    const int k0 = kb * BK;
+                    if (!A_MN) {
+                        tma_load_2d(sa, &tmA, &full[stage], k0, m0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / MN_BOX; j++)
+                            tma_load_2d(sa + j * MN_BOX_BYTES, &tmA, &full[stage], m0 + j * MN_BOX, k0);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(sb, &tmB, &full[stage], k0, n0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / MN_BOX; j++)
+                            tma_load_2d(sb + j * MN_BOX_BYTES, &tmB, &full[stage], n0 + j * MN_BOX, k0);
+                    }
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                long long back = issued < S ? issued : S;
+                int st = stage;
+                uint32_t ph = phase;
+                for (long long i = 0; i < back; i++) {
+                    if (st == 0) { st = S - 1; ph ^= 1; } else { --st; }
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&full[st], ph) && clock64() - t0 < WAIT_CYCLES) {}
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                const int tile = u / p.splits, split = u - tile * p.splits;
+                (void)tile;
+                const int kb0 = split * p.kb_per_split;
+                const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.flags)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
+                    const uint32_t sb = sa + CF::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; k++) {
+                        uint64_t ad, bd;
+                        if (!A_MN) ad = sdesc(sa + k * (UMMA_K * 2), 16, 1024);
+                        else ad = sdesc(sa + k * (UMMA_K / 8) * 1024, MN_BOX_BYTES, 1024);
+                        if (!B_MN) bd = sdesc(sb + k * (UMMA_K * 2), 16, 1024);
+                        else bd = sdesc(sb + k * (UMMA_K / 8) * 1024, MN_BOX_BYTES, 1024);
+                        umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[stage]);  // slot free once these MMAs finish
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);  // accumulator complete
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const bool d_vec = p.d_f32 ? ((p.ldd & 3) == 0) : ((p.ldd & 7) == 0);
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const int tile = u / p.splits, split = u - tile * p.splits;
+            const int m0 = (tile % p.m_tiles) * BM;
+            const int n0 = (tile / p.m_tiles) * BN;
+            if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.flags)) break;
+            tc_fence_after();
+            const int m = m0 + row;
+            const bool row_ok = m < p.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c++) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                const int n = n0 + c * 32;
+                const int valid = min(32, p.n_store - n);
+                if (!row_ok || valid <= 0) continue;
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+                if (p.splits > 1) {
+                    float* w = p.ws + ((long long)split * p.M + m) * p.N + n;
+                    store32_f32(w, valid, (p.N & 3) == 0, v);
+                    continue;
+                }
+                const long long o = (long long)m * p.ldd + n;
+                if (p.d_f32) {
+                    float* d = (float*)p.D + o;
+                    if (p.accumulate) {
+#pragma unroll
+                        for (int j = 0; j < 32; j++)
+                            if (j < valid) v[j] += d[j];
+                    }
+                    store32_f32(d, valid, d_vec, v);
+                    continue;
+                }
+                if (p.bias) {
+                    float b[32];
+                    load32_bf16(p.bias + n, valid, true, b);
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] += b[j];
+                }
+                if (p.epi == EPI_GELU) {
+                    store32_bf16(p.aux + o, valid, d_vec, v);
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = gelu_tanh(v[j]);
+                } else if (p.epi == EPI_DGELU) {
+                    float u_[32];
+                    load32_bf16(p.aux + o, valid, d_vec, u_);
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(u_[j]);
+                }
+                if (p.residual) {
+                    float rr[32];
+                    load32_bf16(p.residual + o, valid, d_vec, rr);
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] += rr[j];
+                }
+                __nv_bfloat16* d = (__nv_bfloat16*)p.D + o;
+                if (p.accumulate) {
+                    float old[32];
+                    load32_bf16(d, valid, d_vec, old);
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] += old[j];
+                }
+                store32_bf16(d, valid, d_vec, v);
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"((uint32_t)CF::TMEM_COLS));
+    }
+}
+
+// D[m, n] (+)= sum_s ws[s][m][n] in split order (fp32 output, n < n_store)
+__global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M, int N, int n_store,
+                                float* __restrict__ D, long long ldd, int accumulate) {
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    long long total = (long long)M * n_store;
+    if (i >= total) return;
+    int m = (int)(i / n_store), n = (int)(i % n_store);
+    float s = 0.0f;
+    for (int k = 0; k < splits; k++) s += ws[((long long)k * M + m) * N + n];
+    float* d = D + (long long)m * ldd + n;
+    *d = accumulate ? *d + s : s;
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+// 2-D bf16 map: inner extent, outer extent, row pitch in elements, box.
+static bool make_map(CUtensorMap* map, const void* base, long long inner, long long outer,
+                     long long pitch, int box_inner, int box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)(pitch * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int BN;
+    Params p;
+    int grid;
+};
+
+static Plan make_plan(const Launch& L, const GemmArgs& g) {
+    Plan pl{};
+    pl.BN = (g.N <= 128) ? 128 : 256;
+    Params& p = pl.p;
+    p.M = g.M;
+    p.N = g.N;
+    p.K = g.K;
+    p.m_tiles = (g.M + BM - 1) / BM;
+    p.n_tiles = (g.N + pl.BN - 1) / pl.BN;
+    p.tiles = p.m_tiles * p.n_tiles;
+    p.kb_total = (g.K + BK - 1) / BK;
+    p.splits = 1;
+    const int sms = L.num_sms > 0 ? L.num_sms : 148;
+    if (!g.a_kmajor && !g.b_kmajor && p.tiles < sms) {
+        // DW form: few output tiles, long contraction over tokens
+        int s = sms / p.tiles;
+        int max_s = p.kb_total / 4;  // at least 4 k-blocks per split
+        if (s > max_s) s = max_s;
+        if (s < 1) s = 1;
+        p.splits = s;
+    }
+    p.kb_per_split = (p.kb_total + p.splits - 1) / p.splits;
+    p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+    p.units = p.tiles * p.splits;
+    pl.grid = p.units < sms ? p.units : sms;
+    p.D = g.D;
+    p.ldd = g.ldd;
+    p.d_f32 = g.d_f32 ? 1 : 0;
+    p.n_store = g.n_store ? g.n_store : g.N;
+    p.epi = g.epi;
+    p.accumulate = g.accumulate ? 1 : 0;
+    p.bias = (const __nv_bfloat16*)g.bias;
+    p.residual = (const __nv_bfloat16*)g.residual;
+    p.aux = (__nv_bfloat16*)g.aux;
+    p.ws = nullptr;
+    p.flags = L.flags;
+    return pl;
+}
+
+}  // namespace tc
+
+bool gemm_tc_eligible(const GemmArgs& g) {
+    if (!g.in_bf16 || g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+    if (g.a_kmajor && g.b_kmajor && g.d_f32) return false;     // forward form writes bf16
+    if (!g.a_kmajor && g.b_kmajor) return false;               // form not used by the step
+    if (!g.a_kmajor && !(g.d_f32 && g.epi == EPI_STORE && !g.bias && !g.residual)) return false;
+    if ((g.lda % 8) || (g.ldb % 8)) return false;              // 16-byte TMA pitches
+    if (((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15)) return false;
+    if (g.bias && ((uintptr_t)g.bias & 15)) return false;
+    if (!tc::encode_fn()) return false;
+    return true;
+}
+
+size_t gemm_tc_workspace_floats(const Launch& L, const GemmArgs& g) {
+    tc::Plan pl = tc::make_plan(L, g);
+    return pl.p.splits > 1 ? (size_t)pl.p.splits * g.M * g.N : 0;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma,
+                      const CUtensorMap& mb) {
+    auto kern = tc::k_gemm_tc<BN, A_MN, B_MN>;
+    static bool attr_done = false;  // one flag per instantiation
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc::Cfg<BN>::SMEM_BYTES) != cudaSuccess)
+            return false;
+        attr_done = true;
+    }
+    L.count();
+    kern<<<pl.grid, tc::THREADS, tc::Cfg<BN>::SMEM_BYTES, L.stream>>>(ma, mb, pl.p);
+    return true;
+}
+
+bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t workspace_floats) {
+    if (!gemm_tc_eligible(g)) return false;
+    tc::Plan pl = tc::make_plan(L, g);
+    if (pl.p.splits > 1) {
+        if (!workspace || workspace_floats < (size_t)pl.p.splits * g.M * g.N) return false;
+        pl.p.ws = workspace;
+    }
+    if (L.dry) return true;
+    const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
+    const int a_rows = g.a_rows ? g.a_rows : g.M;
+    const int b_rows = g.b_rows ? g.b_rows : g.N;
+    const int kval = g.k_valid ? g.k_valid : g.K;
+    CUtensorMap ma, mb;
+    bool ok;
+    if (!a_mn) ok = tc::make_map(&ma, g.A, kval, a_rows, g.lda, tc::BK, tc::BM);
+    else ok = tc::make_map(&ma, g.A, a_rows, kval, g.lda, tc::MN_BOX, tc::BK);
+    if (!ok) return false;
+    if (!b_mn) ok = tc::make_map(&mb, g.B, kval, b_rows, g.ldb, tc::BK, pl.BN);
+    else ok = tc::make_map(&mb, g.B, b_rows, kval, g.ldb, tc::MN_BOX, tc::BK);
+    if (!ok) return false;
+    bool launched;
+    if (pl.BN == 256) {
+        if (!a_mn && !b_mn) launched = launch_tc<256, false, false>(L, pl, ma, mb);
+        else if (!a_mn) launched = launch_tc<256, false, true>(L, pl, ma, mb);
+        else launched = launch_tc<256, true, true>(L, pl, ma, mb);
+    } else {
+        if (!a_mn && !b_mn) launched = launch_tc<128, false, false>(L, pl, ma, mb);
+        else if (!a_mn) launched = launch_tc<128, false, true>(L, pl, ma, mb);
+        else launched = launch_tc<128, true, true>(L, pl, ma, mb);
+    }
+    if (!launched) return false;
+    if (pl.p.splits > 1) {
+        long long total = (long long)g.M * pl.p.n_store;
+        L.count();
+        tc::k_splitk_reduce<<<(unsigned)((total + 255) / 256), 256, 0, L.stream>>>(
+            workspace, pl.p.splits, g.M, g.N, pl.p.n_store, (float*)g.D, g.ldd,
+            g.accumulate ? 1 : 0);
+    }
+    return true;
+}
+
+}  // namespace tt

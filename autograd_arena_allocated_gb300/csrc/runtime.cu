@@ -1,0 +1,1002 @@
+// runtime.cu -- the native runtime behind include/tt.h and include/tt_ops.h:
+// the context, its device arena, the host-side tape, the GPT-2 step built on
+// that tape, AdamW, and the op-level entry points.
+//
+// Arena (tinytorch page, 三.1): one cudaMalloc per context; tensors are cut by
+// bumping an offset (256-byte aligned); tt_ctx_reset rewinds the offset.  A
+// 256-byte header at the start holds the device error flags and is never
+// rewound.  Scratch needed by one kernel is bumped and released right after
+// the launch (stream order guarantees the next user of that memory runs later).
+//
+// Tape (tinytorch 三.2-三.3, microcrad 反向传播): every forward op records its
+// kind, input and output tensors, the parameters it read and what it saved.
+// Backward walks the records in reverse record order -- a reverse topological
+// order, so a tensor has received every contribution to its gradient before
+// its producer's record runs.  Gradients of activations live in the arena:
+// the first contribution allocates and overwrites, later ones accumulate
+// (a residual branch reuses the buffer of the gradient flowing through it).
+//
+// The whole step can be run "dry": the same allocation sequence with no
+// launches, which gives the exact arena requirement before anything runs.
+#include "tt_internal.h"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <unordered_set>
+
+using namespace tt;
+
+static constexpr uint64_t TT_MAGIC = 0x7474617265676e61ULL;  // live context
+static constexpr uint64_t TT_DEAD = 0xdeaddeaddeaddeadULL;    // destroyed
+static constexpr size_t ARENA_ALIGN = 256;
+static constexpr size_t ARENA_HEADER = 256;  // flags live here
+
+struct TapeTensor {
+    void* data = nullptr;
+    void* grad = nullptr;
+    long long rows = 0, cols = 0;
+    int producer = -1;       // record index
+    int consumers = 0;
+    bool grad_is_pre = false;  // grad holds d/d(pre-activation) of a GELU producer
+};
+
+enum RecKind { R_EMBED, R_LN, R_LINEAR, R_ATTN, R_XENT };
+
+struct Record {
+    RecKind kind;
+    int in = -1, out = -1, res = -1;
+    void* pre = nullptr;  // GELU pre-activation (LINEAR with gelu)
+    const void* W = nullptr;
+    const void* b = nullptr;
+    float* dW = nullptr;
+    float* db = nullptr;
+    const void* wpe = nullptr;
+    float* dwpe = nullptr;
+    float* mean = nullptr;
+    float* rstd = nullptr;
+    float* lse = nullptr;
+    const int32_t* idx = nullptr;
+    int M = 0, K = 0, N = 0;
+    int B = 0, T = 0, H = 0, V = 0, maxT = 0;
+    // LINEAR extras (tied LM head)
+    int b_rows = 0, n_store = 0;
+    long long ldy = 0;
+    bool gelu = false;
+};
+
+// ------------------------------------------------------------------ profiling
+enum ProfKind : int {
+    PK_GEMM_FWD, PK_GEMM_DX, PK_GEMM_DW, PK_COLSUM, PK_ATTN_FWD, PK_ATTN_BWD, PK_LN_FWD,
+    PK_LN_BWD, PK_XENT, PK_EMBED_FWD, PK_EMBED_BWD, PK_ADAMW, PK_CAST, PK_COUNT
+};
+static const char* const PROF_NAMES[PK_COUNT] = {
+    "gemm_fwd", "gemm_dx", "gemm_dw", "colsum", "attn_fwd", "attn_bwd", "ln_fwd",
+    "ln_bwd", "xent", "embed_fwd", "embed_bwd", "adamw", "cast"};
+
+struct ProfEntry {
+    int kind;
+    double flops, bytes;
+    cudaEvent_t e0, e1;
+};
+
+struct tt_ctx {
+    uint64_t magic = TT_MAGIC;
+    int device = 0;
+    char* arena = nullptr;
+    size_t cap = 0, off = ARENA_HEADER, high = ARENA_HEADER;
+    cudaStream_t stream = nullptr;
+    uint64_t launches = 0;
+    int num_sms = 148;
+    int gemm_backend = 0;
+    bool has_model = false;
+    tt_gpt2_config cfg{};
+    bool dry = false;
+    bool oom = false;
+    std::vector<TapeTensor> tensors;
+    std::vector<Record> tape;
+    std::unordered_set<const float*> grad_written;
+    float* loss_dev = nullptr;
+    float* row_loss_dev = nullptr;
+    std::string err;
+    bool profiling = false;
+    std::vector<ProfEntry> prof;
+    std::vector<cudaEvent_t> event_pool;
+};
+
+// Brackets the launches of one op with events when profiling is on.
+struct ProfScope {
+    tt_ctx* c;
+    int idx = -1;
+    static cudaEvent_t take(tt_ctx* c) {
+        if (!c->event_pool.empty()) {
+            cudaEvent_t e = c->event_pool.back();
+            c->event_pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+    ProfScope(tt_ctx* c_, int kind, double flops, double bytes) : c(c_) {
+        if (!c->profiling || c->dry || c->oom) return;
+        ProfEntry e{kind, flops, bytes, take(c), take(c)};
+        cudaEventRecord(e.e0, c->stream);
+        c->prof.push_back(e);
+        idx = (int)c->prof.size() - 1;
+    }
+    ~ProfScope() {
+        if (idx >= 0) cudaEventRecord(c->prof[idx].e1, c->stream);
+    }
+};
+
+// ------------------------------------------------------------------ helpers
+static bool live(const tt_ctx* c) { return c && c->magic == TT_MAGIC; }
+
+static tt_status fail(tt_ctx* c, tt_status s, const char* fmt, ...) {
+    if (c) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        c->err = buf;
+    }
+    return s;
+}
+
+static Launch launch_of(tt_ctx* c) {
+    Launch L;
+    L.stream = c->stream;
+    L.flags = (int*)c->arena;
+    L.launches = &c->launches;
+    L.dry = c->dry;
+    L.gemm_backend = c->gemm_backend;
+    L.num_sms = c->num_sms;
+    return L;
+}
+
+// Bump allocation; in dry mode only the offsets move.
+static void* arena_alloc(tt_ctx* c, size_t bytes) {
+    size_t at = (c->off + ARENA_ALIGN - 1) & ~(ARENA_ALIGN - 1);
+    size_t end = at + ((bytes + ARENA_ALIGN - 1) & ~(ARENA_ALIGN - 1));
+    if (end > c->cap) {
+        c->oom = true;
+        c->off = end;  // keep counting so that a dry run reports the full need
+        c->high = std::max(c->high, end);
+        return nullptr;
+    }
+    c->off = end;
+    c->high = std::max(c->high, end);
+    return c->dry ? (void*)(uintptr_t)(0x100000ull + at) : (void*)(c->arena + at);
+}
+
+static size_t esize(tt_dtype d) { return d == TT_BF16 ? 2 : 4; }
+
+static int new_tensor(tt_ctx* c, long long rows, long long cols, size_t elem) {
+    TapeTensor t;
+    t.rows = rows;
+    t.cols = cols;
+    t.data = arena_alloc(c, (size_t)(rows * cols) * elem);
+    c->tensors.push_back(t);
+    return (int)c->tensors.size() - 1;
+}
+
+// ------------------------------------------------------------------ GEMM dispatch
+namespace tt {
+size_t gemm_workspace_floats(const Launch& L, const GemmArgs& g) {
+    if (L.gemm_backend == 0 && gemm_tc_eligible(g)) return gemm_tc_workspace_floats(L, g);
+    return 0;
+}
+
+bool gemm(const Launch& L, const GemmArgs& g, float* ws, size_t ws_floats) {
+    if (L.gemm_backend == 0 && gemm_tc_eligible(g)) return gemm_tc_launch(L, g, ws, ws_floats);
+    gemm_simt_launch(L, g);
+    return true;
+}
+}  // namespace tt
+
+// run a GEMM with its split-K workspace bumped from the arena and released after
+static bool run_gemm(tt_ctx* c, const GemmArgs& g, int kind) {
+    const double es = g.in_bf16 ? 2.0 : 4.0;
+    ProfScope ps(c, kind, 2.0 * g.M * g.N * (double)g.K,
+                 es * ((double)g.M * g.K + (double)g.N * g.K) + (g.d_f32 ? 4.0 : es) * (double)g.M * g.N);
+    Launch L = launch_of(c);
+    size_t mark = c->off;
+    size_t wsf = gemm_workspace_floats(L, g);
+    float* ws = wsf ? (float*)arena_alloc(c, wsf * sizeof(float)) : nullptr;
+    bool ok = c->oom ? c->dry : gemm(L, g, ws, wsf);
+    c->off = mark;
+    return ok;
+}
+
+// ------------------------------------------------------------------ forward ops (record + launch)
+static int op_embed(tt_ctx* c, const void* wte, const void* wpe, float* dwte, float* dwpe,
+                    const int32_t* tok, int B, int T) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    int out = new_tensor(c, (long long)B * T, m.C, esize(m.dtype));
+    ProfScope ps(c, PK_EMBED_FWD, 0.0, 3.0 * B * T * m.C * esize(m.dtype) + 4.0 * B * T);
+    if (!c->oom) launch_embed_fwd(launch_of(c), bf, wte, wpe, tok, c->tensors[out].data, B, T, m.C, m.V);
+    Record r;
+    r.kind = R_EMBED;
+    r.out = out;
+    r.W = wte;
+    r.dW = dwte;
+    r.wpe = wpe;
+    r.dwpe = dwpe;
+    r.idx = tok;
+    r.B = B; r.T = T; r.N = m.C; r.V = m.V; r.maxT = m.maxT;
+    c->tape.push_back(r);
+    c->tensors[out].producer = (int)c->tape.size() - 1;
+    return out;
+}
+
+static int op_layernorm(tt_ctx* c, int x, const void* w, const void* b, float* dw, float* db) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    const int M = (int)c->tensors[x].rows, C = m.C;
+    int out = new_tensor(c, M, C, esize(m.dtype));
+    float* mean = (float*)arena_alloc(c, (size_t)M * 4);
+    float* rstd = (float*)arena_alloc(c, (size_t)M * 4);
+    ProfScope ps(c, PK_LN_FWD, 0.0, 2.0 * M * C * esize(m.dtype) + 8.0 * M);
+    if (!c->oom)
+        launch_layernorm_fwd(launch_of(c), bf, c->tensors[x].data, w, b, c->tensors[out].data, mean,
+                             rstd, M, C);
+    Record r;
+    r.kind = R_LN;
+    r.in = x; r.out = out; r.W = w; r.b = b; r.dW = dw; r.db = db;
+    r.mean = mean; r.rstd = rstd; r.M = M; r.N = C;
+    c->tape.push_back(r);
+    c->tensors[x].consumers++;
+    c->tensors[out].producer = (int)c->tape.size() - 1;
+    return out;
+}
+
+// y = x W^T + b (+ residual) or gelu(x W^T + b)
+static int op_linear(tt_ctx* c, int x, const void* W, const void* b, float* dW, float* db, int N,
+                     int res, bool gelu, int b_rows = 0, int n_store = 0) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    const size_t es = esize(m.dtype);
+    const int M = (int)c->tensors[x].rows, K = (int)c->tensors[x].cols;
+    int out = new_tensor(c, M, N, es);
+    void* pre = gelu ? arena_alloc(c, (size_t)M * N * es) : nullptr;
+    if (!c->oom) {
+        GemmArgs g;
+        g.A = c->tensors[x].data; g.lda = K; g.a_kmajor = true;
+        g.B = W; g.ldb = K; g.b_kmajor = true;
+        g.M = M; g.N = N; g.K = K;
+        g.b_rows = b_rows;
+        g.in_bf16 = bf;
+        g.D = c->tensors[out].data; g.ldd = N; g.d_f32 = !bf;
+        g.n_store = n_store;
+        g.epi = gelu ? EPI_GELU : EPI_STORE;
+        g.bias = b;
+        g.residual = res >= 0 ? c->tensors[res].data : nullptr;
+        g.aux = pre;
+        if (!run_gemm(c, g, PK_GEMM_FWD)) c->err = "linear forward: GEMM launch failed";
+    }
+    Record r;
+    r.kind = R_LINEAR;
+    r.in = x; r.out = out; r.res = res; r.pre = pre;
+    r.W = W; r.b = b; r.dW = dW; r.db = db;
+    r.M = M; r.K = K; r.N = N; r.b_rows = b_rows; r.n_store = n_store; r.gelu = gelu;
+    c->tape.push_back(r);
+    c->tensors[x].consumers++;
+    if (res >= 0) c->tensors[res].consumers++;
+    c->tensors[out].producer = (int)c->tape.size() - 1;
+    return out;
+}
+
+static int op_attention(tt_ctx* c, int qkv, int B, int T) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    const int M = B * T;
+    int out = new_tensor(c, M, m.C, esize(m.dtype));
+    float* lse = (float*)arena_alloc(c, (size_t)B * m.H * T * 4);
+    // causal: QK^T and PV over the T(T+1)/2 unmasked pairs
+    const double pairs = (double)B * m.H * T * (T + 1) / 2.0;
+    ProfScope ps(c, PK_ATTN_FWD, 4.0 * pairs * (m.C / m.H),
+                 (3.0 + 1.0) * M * m.C * esize(m.dtype) + 4.0 * B * m.H * T);
+    if (!c->oom)
+        launch_attention_fwd(launch_of(c), bf, c->tensors[qkv].data, c->tensors[out].data, lse, B, T,
+                             m.C, m.H);
+    Record r;
+    r.kind = R_ATTN;
+    r.in = qkv; r.out = out; r.lse = lse; r.B = B; r.T = T; r.H = m.H; r.N = m.C; r.M = M;
+    c->tape.push_back(r);
+    c->tensors[qkv].consumers++;
+    c->tensors[out].producer = (int)c->tape.size() - 1;
+    return out;
+}
+
+// Cross entropy, forward and backward fused: the logits are replaced by their
+// gradient in the same pass, so the logits tensor's gradient is its own buffer.
+static void op_xent(tt_ctx* c, int z, const int32_t* targets, int V) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    const int M = (int)c->tensors[z].rows, ld = (int)c->tensors[z].cols;
+    c->row_loss_dev = (float*)arena_alloc(c, (size_t)M * 4);
+    c->loss_dev = (float*)arena_alloc(c, 4);
+    ProfScope ps(c, PK_XENT, 0.0, 2.0 * M * ld * esize(m.dtype) + 8.0 * M);
+    if (!c->oom)
+        launch_xent(launch_of(c), bf, c->tensors[z].data, targets, c->row_loss_dev, c->loss_dev, M, V,
+                    ld, 1.0f / (float)M);
+    Record r;
+    r.kind = R_XENT;
+    r.in = z; r.M = M; r.N = V; r.idx = targets;
+    c->tape.push_back(r);
+    c->tensors[z].consumers++;
+    c->tensors[z].grad = c->tensors[z].data;
+}
+
+// ------------------------------------------------------------------ backward
+static bool first_write(tt_ctx* c, const float* p) {
+    return c->grad_written.insert(p).second;
+}
+
+// gradient buffer of tensor t for writing: returns (pointer, accumulate?)
+static void* grad_for_write(tt_ctx* c, int t, bool* accumulate) {
+    TapeTensor& x = c->tensors[t];
+    if (x.grad) { *accumulate = true; return x.grad; }
+    const size_t es = esize(c->cfg.dtype);
+    x.grad = arena_alloc(c, (size_t)(x.rows * x.cols) * es);
+    *accumulate = false;
+    return x.grad;
+}
+
+static tt_status backward_record(tt_ctx* c, const Record& r) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    Launch L = launch_of(c);
+    switch (r.kind) {
+    case R_XENT:
+        return TT_OK;  // fused into the forward pass
+    case R_LINEAR: {
+        TapeTensor& y = c->tensors[r.out];
+        if (!y.grad) return TT_OK;
+        if (r.gelu && !y.grad_is_pre)
+            return fail(c, TT_ERR, "tape: GELU output gradient was not produced by a linear input gradient");
+        const void* dy = y.grad;  // for a GELU layer this is already d/d(pre)
+        // residual input: the gradient passes through unchanged
+        if (r.res >= 0) {
+            TapeTensor& rt = c->tensors[r.res];
+            if (rt.grad) return fail(c, TT_ERR, "tape: residual gradient already allocated");
+            rt.grad = y.grad;
+        }
+        // input gradient dx = dy W (fused with GELU' when the input came from a GELU layer)
+        {
+            TapeTensor& xt = c->tensors[r.in];
+            bool acc = false;
+            const Record* prod = xt.producer >= 0 ? &c->tape[xt.producer] : nullptr;
+            const bool through_gelu = prod && prod->kind == R_LINEAR && prod->gelu && xt.consumers == 1;
+            void* dx = grad_for_write(c, r.in, &acc);
+            if (!c->oom) {
+                GemmArgs g;
+                g.A = dy; g.lda = r.N; g.a_kmajor = true;
+                g.B = r.W; g.ldb = r.K; g.b_kmajor = false;
+                g.M = r.M; g.N = r.K; g.K = r.N;
+                g.k_valid = r.b_rows ? r.b_rows : 0;  // tied head: rows of wte beyond V are zero
+                g.in_bf16 = bf;
+                g.D = dx; g.ldd = r.K; g.d_f32 = !bf;
+                g.accumulate = acc;
+                if (through_gelu) { g.epi = EPI_DGELU; g.aux = prod->pre; }
+                if (!run_gemm(c, g, PK_GEMM_DX)) return fail(c, TT_ERR_CUDA, "linear dx GEMM failed");
+            }
+            if (through_gelu) xt.grad_is_pre = true;
+        }
+        // weight and bias gradients (fp32, first write overwrites)
+        {
+            const bool accW = !first_write(c, r.dW);
+            GemmArgs g;
+            g.A = dy; g.lda = r.N; g.a_kmajor = false;
+            g.B = c->tensors[r.in].data; g.ldb = r.K; g.b_kmajor = false;
+            g.M = r.n_store ? std::min(r.n_store, r.b_rows ? r.b_rows : r.N) : r.N;
+            g.a_rows = g.M;
+            g.N = r.K; g.K = r.M;
+            g.in_bf16 = bf;
+            g.D = r.dW; g.ldd = r.K; g.d_f32 = true;
+            g.accumulate = accW;
+            if (!c->oom && !run_gemm(c, g, PK_GEMM_DW)) return fail(c, TT_ERR_CUDA, "linear dW GEMM failed");
+            if (r.db) {
+                if (!first_write(c, r.db)) return fail(c, TT_ERR, "tape: bias used twice");
+                size_t mark = c->off;
+                float* s = (float*)arena_alloc(c, colsum_scratch_floats(r.M, r.N) * 4);
+                ProfScope ps(c, PK_COLSUM, 0.0, (double)r.M * r.N * esize(m.dtype) + 4.0 * r.N);
+                if (!c->oom) launch_colsum(L, bf, dy, r.M, r.N, r.db, s);
+                c->off = mark;
+            }
+        }
+        return TT_OK;
+    }
+    case R_LN: {
+        TapeTensor& y = c->tensors[r.out];
+        if (!y.grad) return TT_OK;
+        bool acc = false;
+        void* dx = grad_for_write(c, r.in, &acc);
+        if (!first_write(c, r.dW) || !first_write(c, r.db))
+            return fail(c, TT_ERR, "tape: LayerNorm parameters used twice");
+        size_t mark = c->off;
+        float* s = (float*)arena_alloc(c, layernorm_bwd_scratch_floats(r.M, r.N) * 4);
+        ProfScope ps(c, PK_LN_BWD, 0.0, (acc ? 4.0 : 3.0) * r.M * r.N * esize(m.dtype) + 8.0 * r.M);
+        if (!c->oom)
+            launch_layernorm_bwd(L, bf, c->tensors[r.in].data, r.W, r.mean, r.rstd, y.grad, dx, r.dW,
+                                 r.db, r.M, r.N, acc, s);
+        c->off = mark;
+        return TT_OK;
+    }
+    case R_ATTN: {
+        TapeTensor& y = c->tensors[r.out];
+        if (!y.grad) return TT_OK;
+        bool acc = false;
+        void* dqkv = grad_for_write(c, r.in, &acc);
+        if (acc) return fail(c, TT_ERR, "tape: attention input gradient already allocated");
+        size_t mark = c->off;
+        float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(r.B, r.T, r.H) * 4);
+        // recompute QK^T, then dV, dP, dQ, dK: five products over the causal pairs
+        const double pairs = (double)r.B * r.H * r.T * (r.T + 1) / 2.0;
+        ProfScope ps(c, PK_ATTN_BWD, 10.0 * pairs * (r.N / r.H),
+                     (3.0 + 2.0 + 3.0) * r.M * r.N * esize(m.dtype) + 4.0 * r.B * r.H * r.T);
+        if (!c->oom)
+            launch_attention_bwd(L, bf, c->tensors[r.in].data, y.data, r.lse, y.grad, dqkv, r.B, r.T,
+                                 r.N, r.H, s);
+        c->off = mark;
+        return TT_OK;
+    }
+    case R_EMBED: {
+        TapeTensor& y = c->tensors[r.out];
+        if (!y.grad) return TT_OK;
+        if (first_write(c, r.dW) && !c->dry) {
+            if (cudaMemsetAsync(r.dW, 0, (size_t)r.V * r.N * 4, c->stream) != cudaSuccess)
+                return fail(c, TT_ERR_CUDA, "memset failed");
+        }
+        if (!first_write(c, r.dwpe)) return fail(c, TT_ERR, "tape: position table used twice");
+        size_t mark = c->off;
+        void* s = arena_alloc(c, embed_bwd_scratch_bytes(r.B * r.T));
+        ProfScope ps(c, PK_EMBED_BWD, 0.0,
+                     (double)r.B * r.T * r.N * (esize(m.dtype) + 8.0) + 4.0 * r.maxT * r.N);
+        if (!c->oom)
+            launch_embed_bwd(L, bf, y.grad, r.idx, r.dW, r.dwpe, r.B, r.T, r.N, r.V, r.maxT, s);
+        c->off = mark;
+        return TT_OK;
+    }
+    }
+    return TT_OK;
+}
+
+static tt_status tape_backward(tt_ctx* c) {
+    for (int i = (int)c->tape.size() - 1; i >= 0; i--) {
+        tt_status s = backward_record(c, c->tape[i]);
+        if (s != TT_OK) return s;
+    }
+    return TT_OK;
+}
+
+// ------------------------------------------------------------------ layout
+static bool cfg_ok(const tt_gpt2_config* m) {
+    if (!m || m->L < 0 || m->C <= 0 || m->H <= 0 || m->V <= 1 || m->maxT <= 0) return false;
+    if (m->C % m->H || m->C % 64 || m->C > 1024 || m->V >= 65535 * 16) return false;
+    if (m->dtype != TT_FP32 && m->dtype != TT_BF16) return false;
+    const int hd = m->C / m->H;
+    if (hd != 16 && hd != 32 && hd != 64) return false;
+    if (m->dtype == TT_BF16 && hd != 64) return false;
+    return true;
+}
+
+static int padded_vocab(int V) { return ((V + 127) / 128) * 128; }
+
+struct Offsets {
+    size_t wte, wpe, layers, per_layer, lnfw, lnfb, total;
+    size_t sub[12];
+};
+
+static Offsets offsets_of(const tt_gpt2_config* m) {
+    Offsets o{};
+    const size_t C = (size_t)m->C;
+    const size_t sizes[12] = {C, C, 3 * C * C, 3 * C, C * C, C, C, C, 4 * C * C, 4 * C, 4 * C * C, C};
+    o.wte = 0;
+    o.wpe = (size_t)m->V * C;
+    o.layers = o.wpe + (size_t)m->maxT * C;
+    size_t at = 0;
+    for (int i = 0; i < 12; i++) { o.sub[i] = at; at += sizes[i]; }
+    o.per_layer = at;
+    o.lnfw = o.layers + (size_t)m->L * at;
+    o.lnfb = o.lnfw + C;
+    o.total = o.lnfb + C;
+    return o;
+}
+
+// ------------------------------------------------------------------ the step
+static tt_status gpt2_forward_backward(tt_ctx* c, const void* params, float* grads,
+                                       const int32_t* tok, const int32_t* tgt, int B, int T) {
+    const tt_gpt2_config& m = c->cfg;
+    const size_t es = esize(m.dtype);
+    const Offsets o = offsets_of(&m);
+    auto P = [&](size_t off) -> const void* { return (const char*)params + off * es; };
+    auto G = [&](size_t off) -> float* { return grads + off; };
+    const int C = m.C;
+    const int Vp = padded_vocab(m.V);
+
+    int x = op_embed(c, P(o.wte), P(o.wpe), G(o.wte), G(o.wpe), tok, B, T);
+    for (int l = 0; l < m.L; l++) {
+        const size_t base = o.layers + (size_t)l * o.per_layer;
+        auto PL = [&](int i) { return P(base + o.sub[i]); };
+        auto GL = [&](int i) { return G(base + o.sub[i]); };
+        int h = op_layernorm(c, x, PL(0), PL(1), GL(0), GL(1));
+        int qkv = op_linear(c, h, PL(2), PL(3), GL(2), GL(3), 3 * C, -1, false);
+        int a = op_attention(c, qkv, B, T);
+        int x1 = op_linear(c, a, PL(4), PL(5), GL(4), GL(5), C, x, false);
+        int h2 = op_layernorm(c, x1, PL(6), PL(7), GL(6), GL(7));
+        int g = op_linear(c, h2, PL(8), PL(9), GL(8), GL(9), 4 * C, -1, true);
+        x = op_linear(c, g, PL(10), PL(11), GL(10), GL(11), C, x1, false);
+    }
+    int hf = op_layernorm(c, x, P(o.lnfw), P(o.lnfb), G(o.lnfw), G(o.lnfb));
+    // tied LM head: logits[M, Vp] = hf wte^T; wte rows >= V read as zero
+    int z = op_linear(c, hf, P(o.wte), nullptr, G(o.wte), nullptr, Vp, -1, false, m.V, Vp);
+    op_xent(c, z, tgt, m.V);
+    if (c->oom) return TT_ERR_ARENA_OOM;
+    return tape_backward(c);
+}
+
+static void begin_step(tt_ctx* c) {
+    c->tensors.clear();
+    c->tape.clear();
+    c->grad_written.clear();
+    c->oom = false;
+}
+
+static bool is_host_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
+}
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+tt_status tt_ctx_create(size_t arena_bytes, tt_ctx** out) {
+    if (!out) return TT_ERR_ARG;
+    *out = nullptr;
+    if (arena_bytes == 0) return TT_ERR_ARG;
+    tt_ctx* c = new tt_ctx();
+    c->cap = arena_bytes + ARENA_HEADER;
+    if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return TT_ERR_CUDA; }
+    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (cudaMalloc((void**)&c->arena, c->cap) != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return TT_ERR_CUDA;
+    }
+    if (cudaMemset(c->arena, 0, ARENA_HEADER) != cudaSuccess) {
+        cudaFree(c->arena);
+        delete c;
+        return TT_ERR_CUDA;
+    }
+    *out = c;
+    return TT_OK;
+}
+
+// The handle's small host shell is kept (poisoned) rather than freed, so that
+// a later call through a stale handle is detected instead of reading freed memory.
+void tt_ctx_destroy(tt_ctx* c) {
+    if (!live(c)) return;
+    c->magic = TT_DEAD;
+    cudaStreamSynchronize(c->stream);
+    cudaFree(c->arena);
+    c->arena = nullptr;
+    c->cap = 0;
+    std::vector<TapeTensor>().swap(c->tensors);
+    std::vector<Record>().swap(c->tape);
+    std::unordered_set<const float*>().swap(c->grad_written);
+    std::string().swap(c->err);
+    for (ProfEntry& e : c->prof) { cudaEventDestroy(e.e0); cudaEventDestroy(e.e1); }
+    for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+    std::vector<ProfEntry>().swap(c->prof);
+    std::vector<cudaEvent_t>().swap(c->event_pool);
+}
+
+tt_status tt_ctx_set_stream(tt_ctx* c, void* stream) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    c->stream = (cudaStream_t)stream;
+    return TT_OK;
+}
+
+tt_status tt_ctx_set_model(tt_ctx* c, const tt_gpt2_config* m) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!cfg_ok(m)) return fail(c, TT_ERR_ARG, "invalid model config");
+    c->cfg = *m;
+    c->has_model = true;
+    return TT_OK;
+}
+
+tt_status tt_ctx_set_gemm_backend(tt_ctx* c, int backend) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (backend != 0 && backend != 1) return fail(c, TT_ERR_ARG, "backend must be 0 or 1");
+    c->gemm_backend = backend;
+    return TT_OK;
+}
+
+tt_status tt_ctx_reset(tt_ctx* c) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    c->off = ARENA_HEADER;
+    begin_step(c);
+    c->loss_dev = c->row_loss_dev = nullptr;
+    if (cudaMemsetAsync(c->arena, 0, FLAG_COUNT * sizeof(int), c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
+    return TT_OK;
+}
+
+tt_status tt_ctx_sync(tt_ctx* c) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    int flags[FLAG_COUNT];
+    if (cudaMemcpyAsync(flags, c->arena, sizeof flags, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "sync: %s", cudaGetErrorString(cudaGetLastError()));
+    if (flags[FLAG_TIMEOUT]) return fail(c, TT_ERR_TIMEOUT, "a device-side wait timed out");
+    if (flags[FLAG_BAD_TOKEN]) return fail(c, TT_ERR_ARG, "token id out of range");
+    if (flags[FLAG_NONFINITE]) return fail(c, TT_ERR_NONFINITE, "non-finite loss");
+    return TT_OK;
+}
+
+tt_status tt_ctx_set_profiling(tt_ctx* c, int on) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    c->profiling = on != 0;
+    return TT_OK;
+}
+
+int tt_ctx_profile_read(tt_ctx* c, tt_op_profile* rows, int max_rows) {
+    if (!live(c)) return TT_ERR_STALE;
+    if (cudaStreamSynchronize(c->stream) != cudaSuccess) {
+        fail(c, TT_ERR_CUDA, "profile: %s", cudaGetErrorString(cudaGetLastError()));
+        return TT_ERR_CUDA;
+    }
+    tt_op_profile agg[PK_COUNT];
+    memset(agg, 0, sizeof agg);
+    for (const ProfEntry& e : c->prof) {
+        float ms = 0.0f;
+        cudaEventElapsedTime(&ms, e.e0, e.e1);
+        tt_op_profile& a = agg[e.kind];
+        a.calls++;
+        a.ms += ms;
+        a.flops += e.flops;
+        a.bytes += e.bytes;
+        c->event_pool.push_back(e.e0);
+        c->event_pool.push_back(e.e1);
+    }
+    c->prof.clear();
+    int n = 0;
+    for (int k = 0; k < PK_COUNT; k++) {
+        if (!agg[k].calls) continue;
+        if (rows && n < max_rows) {
+            rows[n] = agg[k];
+            snprintf(rows[n].name, sizeof rows[n].name, "%s", PROF_NAMES[k]);
+        }
+        n++;
+    }
+    cudaGetLastError();
+    return rows ? std::min(n, max_rows) : n;
+}
+
+size_t tt_ctx_arena_capacity(const tt_ctx* c) { return live(c) ? c->cap - ARENA_HEADER : 0; }
+size_t tt_ctx_arena_used(const tt_ctx* c) { return live(c) ? c->off - ARENA_HEADER : 0; }
+size_t tt_ctx_arena_high_water(const tt_ctx* c) { return live(c) ? c->high - ARENA_HEADER : 0; }
+uint64_t tt_ctx_launch_count(const tt_ctx* c) { return live(c) ? c->launches : 0; }
+
+const char* tt_last_error(const tt_ctx* c) {
+    if (!c) return "NULL context";
+    if (!live(c)) return "stale context";
+    return c->err.c_str();
+}
+
+size_t tt_gpt2_num_params(const tt_gpt2_config* m) {
+    if (!cfg_ok(m)) return 0;
+    return offsets_of(m).total;
+}
+
+tt_status tt_gpt2_param_offset(const tt_gpt2_config* m, int layer, int which, size_t* off,
+                               size_t* numel) {
+    if (!cfg_ok(m) || !off || !numel) return TT_ERR_ARG;
+    const Offsets o = offsets_of(m);
+    const size_t C = (size_t)m->C;
+    switch (which) {
+    case 0: *off = o.wte; *numel = (size_t)m->V * C; return TT_OK;
+    case 1: *off = o.wpe; *numel = (size_t)m->maxT * C; return TT_OK;
+    case 14: *off = o.lnfw; *numel = C; return TT_OK;
+    case 15: *off = o.lnfb; *numel = C; return TT_OK;
+    default: break;
+    }
+    if (which < 2 || which > 13 || layer < 0 || layer >= m->L) return TT_ERR_ARG;
+    const int i = which - 2;
+    *off = o.layers + (size_t)layer * o.per_layer + o.sub[i];
+    *numel = (i + 1 < 12 ? o.sub[i + 1] : o.per_layer) - o.sub[i];
+    return TT_OK;
+}
+
+size_t tt_gpt2_arena_bytes(const tt_gpt2_config* m, int B, int T) {
+    if (!cfg_ok(m) || B <= 0 || T <= 0 || T > m->maxT) return 0;
+    tt_ctx c;
+    c.cap = (size_t)-1 / 2;
+    c.cfg = *m;
+    c.has_model = true;
+    c.dry = true;
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        c.num_sms = sms;
+    else
+        cudaGetLastError();
+    const size_t M = (size_t)B * T;
+    arena_alloc(&c, M * 4);  // staged tokens (host inputs)
+    arena_alloc(&c, M * 4);  // staged targets
+    gpt2_forward_backward(&c, (const void*)(uintptr_t)0x1000, (float*)(uintptr_t)0x1000,
+                          (const int32_t*)(uintptr_t)0x1000, (const int32_t*)(uintptr_t)0x1000, B, T);
+    c.magic = TT_DEAD;
+    return c.high - ARENA_HEADER;
+}
+
+tt_status tt_gpt2_step(tt_ctx* c, const void* params, float* grads, const int32_t* tokens,
+                       const int32_t* targets, int B, int T, float* loss) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
+    if (!params || !grads || !tokens || !targets)
+        return fail(c, TT_ERR_ARG, "NULL parameter, gradient or token pointer");
+    if (B <= 0 || T <= 0 || T > c->cfg.maxT)
+        return fail(c, TT_ERR_ARG, "bad batch shape B=%d T=%d (maxT=%d)", B, T, c->cfg.maxT);
+    const size_t M = (size_t)B * T;
+    // exact plan first: nothing is launched if it does not fit
+    {
+        const size_t need = tt_gpt2_arena_bytes(&c->cfg, B, T);
+        const size_t at = (c->off + ARENA_ALIGN - 1) & ~(ARENA_ALIGN - 1);
+        if (need == 0 || at + need > c->cap)
+            return fail(c, TT_ERR_ARENA_OOM, "arena too small: step needs %zu bytes, %zu free", need,
+                        c->cap > at ? c->cap - at : (size_t)0);
+    }
+    begin_step(c);
+    // host token buffers are staged into the arena
+    const int32_t* tok = tokens;
+    const int32_t* tgt = targets;
+    int32_t* st_tok = (int32_t*)arena_alloc(c, M * 4);
+    int32_t* st_tgt = (int32_t*)arena_alloc(c, M * 4);
+    if (is_host_pointer(tokens)) {
+        if (cudaMemcpyAsync(st_tok, tokens, M * 4, cudaMemcpyHostToDevice, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "token copy failed");
+        tok = st_tok;
+    }
+    if (is_host_pointer(targets)) {
+        if (cudaMemcpyAsync(st_tgt, targets, M * 4, cudaMemcpyHostToDevice, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "target copy failed");
+        tgt = st_tgt;
+    }
+    tt_status s = gpt2_forward_backward(c, params, grads, tok, tgt, B, T);
+    if (s != TT_OK) {
+        if (s == TT_ERR_ARENA_OOM) return fail(c, s, "arena exhausted during the step");
+        return s;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    if (loss) {
+        if (cudaMemcpyAsync(loss, c->loss_dev, 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "loss copy failed");
+        return tt_ctx_sync(c);
+    }
+    return TT_OK;
+}
+
+tt_status tt_ctx_loss_device(const tt_ctx* c, const float** mean_loss, const float** row_losses) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!c->loss_dev) return TT_ERR_STATE;
+    if (mean_loss) *mean_loss = c->loss_dev;
+    if (row_losses) *row_losses = c->row_loss_dev;
+    return TT_OK;
+}
+
+tt_status tt_ctx_copy_row_losses(tt_ctx* c, float* dst, size_t n) {
+    if (!c || !dst) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!c->row_loss_dev) return fail(c, TT_ERR_STATE, "no step since the last reset");
+    if (!c->tensors.empty() && n > (size_t)c->tensors[0].rows)
+        return fail(c, TT_ERR_ARG, "n exceeds B*T");
+    if (cudaMemcpyAsync(dst, c->row_loss_dev, n * 4, cudaMemcpyDefault, c->stream) != cudaSuccess ||
+        cudaStreamSynchronize(c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "row loss copy: %s", cudaGetErrorString(cudaGetLastError()));
+    return TT_OK;
+}
+
+tt_status tt_adamw(tt_ctx* c, float* master, void* params_lowp, const float* grads, float* m,
+                   float* v, size_t n, float lr, float beta1, float beta2, float eps,
+                   float weight_decay, int step) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!master || !grads || !m || !v || step < 1)
+        return fail(c, TT_ERR_ARG, "adamw: NULL pointer or step < 1");
+    if (((uintptr_t)master | (uintptr_t)grads | (uintptr_t)m | (uintptr_t)v) & 15)
+        return fail(c, TT_ERR_ARG, "adamw: pointers must be 16-byte aligned");
+    if (params_lowp && ((uintptr_t)params_lowp & 7))
+        return fail(c, TT_ERR_ARG, "adamw: bf16 copy must be 8-byte aligned");
+    ProfScope ps(c, PK_ADAMW, 0.0, (double)n * (28.0 + (params_lowp ? 2.0 : 0.0)));
+    launch_adamw(launch_of(c), master, (__nv_bfloat16*)params_lowp, grads, m, v, n, lr, beta1, beta2,
+                 eps, weight_decay, step);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "adamw: %s", cudaGetErrorString(e));
+    return TT_OK;
+}
+
+tt_status tt_cast_f32_to_bf16(tt_ctx* c, const float* src, void* dst, size_t n) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!src || !dst) return fail(c, TT_ERR_ARG, "cast: NULL pointer");
+    launch_cast_bf16(launch_of(c), src, (__nv_bfloat16*)dst, n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "cast: %s", cudaGetErrorString(e));
+    return TT_OK;
+}
+
+// ------------------------------------------------------------------ op-level ABI
+#define TT_OP_PROLOGUE()                                  \
+    if (!c) return TT_ERR_ARG;                            \
+    if (!live(c)) return TT_ERR_STALE;                    \
+    if (dtype != TT_FP32 && dtype != TT_BF16) return fail(c, TT_ERR_ARG, "bad dtype");
+
+static tt_status op_epilogue(tt_ctx* c, const char* what) {
+    if (c->oom) { c->oom = false; return fail(c, TT_ERR_ARENA_OOM, "%s: scratch does not fit", what); }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return TT_OK;
+}
+
+tt_status tt_op_linear_fwd(tt_ctx* c, tt_dtype dtype, const void* x, const void* W, const void* b,
+                           const void* residual, void* y, void* pre, int M, int K, int N, int gelu) {
+    TT_OP_PROLOGUE();
+    if (!x || !W || !y || M <= 0 || K <= 0 || N <= 0 || (gelu && !pre))
+        return fail(c, TT_ERR_ARG, "linear_fwd: bad arguments");
+    GemmArgs g;
+    g.A = x; g.lda = K; g.a_kmajor = true;
+    g.B = W; g.ldb = K; g.b_kmajor = true;
+    g.M = M; g.N = N; g.K = K;
+    g.in_bf16 = dtype == TT_BF16;
+    g.D = y; g.ldd = N; g.d_f32 = dtype == TT_FP32;
+    g.epi = gelu ? EPI_GELU : EPI_STORE;
+    g.bias = b; g.residual = residual; g.aux = gelu ? pre : nullptr;
+    c->oom = false;
+    if (!run_gemm(c, g, PK_GEMM_FWD)) return fail(c, TT_ERR_CUDA, "linear_fwd: launch failed");
+    return op_epilogue(c, "linear_fwd");
+}
+
+tt_status tt_op_linear_bwd_dx(tt_ctx* c, tt_dtype dtype, const void* dy, const void* W,
+                              const void* pre, void* dx, int M, int K, int N, int accumulate) {
+    TT_OP_PROLOGUE();
+    if (!dy || !W || !dx || M <= 0 || K <= 0 || N <= 0)
+        return fail(c, TT_ERR_ARG, "linear_bwd_dx: bad arguments");
+    GemmArgs g;
+    g.A = dy; g.lda = N; g.a_kmajor = true;
+    g.B = W; g.ldb = K; g.b_kmajor = false;
+    g.M = M; g.N = K; g.K = N;
+    g.in_bf16 = dtype == TT_BF16;
+    g.D = dx; g.ldd = K; g.d_f32 = dtype == TT_FP32;
+    g.accumulate = accumulate != 0;
+    if (pre) { g.epi = EPI_DGELU; g.aux = const_cast<void*>(pre); }
+    c->oom = false;
+    if (!run_gemm(c, g, PK_GEMM_DX)) return fail(c, TT_ERR_CUDA, "linear_bwd_dx: launch failed");
+    return op_epilogue(c, "linear_bwd_dx");
+}
+
+tt_status tt_op_linear_bwd_dw(tt_ctx* c, tt_dtype dtype, const void* dy, const void* x, float* dW,
+                              float* db, int M, int K, int N) {
+    TT_OP_PROLOGUE();
+    if (!dy || !x || !dW || M <= 0 || K <= 0 || N <= 0)
+        return fail(c, TT_ERR_ARG, "linear_bwd_dw: bad arguments");
+    const bool bf = dtype == TT_BF16;
+    GemmArgs g;
+    g.A = dy; g.lda = N; g.a_kmajor = false;
+    g.B = x; g.ldb = K; g.b_kmajor = false;
+    g.M = N; g.N = K; g.K = M;
+    g.in_bf16 = bf;
+    g.D = dW; g.ldd = K; g.d_f32 = true;
+    c->oom = false;
+    if (!run_gemm(c, g, PK_GEMM_DW)) return fail(c, TT_ERR_CUDA, "linear_bwd_dw: launch failed");
+    if (db) {
+        size_t mark = c->off;
+        float* s = (float*)arena_alloc(c, colsum_scratch_floats(M, N) * 4);
+        if (!c->oom) launch_colsum(launch_of(c), bf, dy, M, N, db, s);
+        c->off = mark;
+    }
+    return op_epilogue(c, "linear_bwd_dw");
+}
+
+tt_status tt_op_attention_fwd(tt_ctx* c, tt_dtype dtype, const void* qkv, void* y, float* lse, int B,
+                              int T, int C, int H) {
+    TT_OP_PROLOGUE();
+    if (!qkv || !y || !lse || B <= 0 || T <= 0 || H <= 0 || C % H) return fail(c, TT_ERR_ARG, "attention_fwd: bad arguments");
+    const int hd = C / H;
+    if (hd != 16 && hd != 32 && hd != 64) return fail(c, TT_ERR_ARG, "attention: head dim must be 16, 32 or 64");
+    launch_attention_fwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, B, T, C, H);
+    return op_epilogue(c, "attention_fwd");
+}
+
+tt_status tt_op_attention_bwd(tt_ctx* c, tt_dtype dtype, const void* qkv, const void* y,
+                              const float* lse, const void* dy, void* dqkv, int B, int T, int C,
+                              int H) {
+    TT_OP_PROLOGUE();
+    if (!qkv || !y || !lse || !dy || !dqkv || B <= 0 || T <= 0 || H <= 0 || C % H)
+        return fail(c, TT_ERR_ARG, "attention_bwd: bad arguments");
+    const int hd = C / H;
+    if (hd != 16 && hd != 32 && hd != 64) return fail(c, TT_ERR_ARG, "attention: head dim must be 16, 32 or 64");
+    c->oom = false;
+    size_t mark = c->off;
+    float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(B, T, H) * 4);
+    if (!c->oom) launch_attention_bwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, dy, dqkv, B, T, C, H, s);
+    c->off = mark;
+    return op_epilogue(c, "attention_bwd");
+}
+
+tt_status tt_op_layernorm_fwd(tt_ctx* c, tt_dtype dtype, const void* x, const void* w, const void* b,
+                              void* y, float* mean, float* rstd, int M, int C) {
+    TT_OP_PROLOGUE();
+    if (!x || !w || !b || !y || !mean || !rstd || M <= 0 || C <= 0 || C % 32 || C > 1024)
+        return fail(c, TT_ERR_ARG, "layernorm_fwd: bad arguments");
+    launch_layernorm_fwd(launch_of(c), dtype == TT_BF16, x, w, b, y, mean, rstd, M, C);
+    return op_epilogue(c, "layernorm_fwd");
+}
+
+tt_status tt_op_layernorm_bwd(tt_ctx* c, tt_dtype dtype, const void* x, const void* w,
+                              const float* mean, const float* rstd, const void* dy, void* dx,
+                              float* dw, float* db, int M, int C, int accumulate) {
+    TT_OP_PROLOGUE();
+    if (!x || !w || !mean || !rstd || !dy || !dx || M <= 0 || C <= 0 || C % 32 || C > 1024)
+        return fail(c, TT_ERR_ARG, "layernorm_bwd: bad arguments");
+    c->oom = false;
+    size_t mark = c->off;
+    float* s = (float*)arena_alloc(c, layernorm_bwd_scratch_floats(M, C) * 4);
+    if (!c->oom)
+        launch_layernorm_bwd(launch_of(c), dtype == TT_BF16, x, w, mean, rstd, dy, dx, dw, db, M, C,
+                             accumulate != 0, s);
+    c->off = mark;
+    return op_epilogue(c, "layernorm_bwd");
+}
+
+tt_status tt_op_xent(tt_ctx* c, tt_dtype dtype, void* logits, const int32_t* targets,
+                     float* row_loss, float* mean_loss, int M, int V, int ld, float dscale) {
+    TT_OP_PROLOGUE();
+    if (!logits || !targets || !row_loss || M <= 0 || V <= 0 || ld < V)
+        return fail(c, TT_ERR_ARG, "xent: bad arguments");
+    launch_xent(launch_of(c), dtype == TT_BF16, logits, targets, row_loss, mean_loss, M, V, ld, dscale);
+    return op_epilogue(c, "xent");
+}
+
+tt_status tt_op_embed_fwd(tt_ctx* c, tt_dtype dtype, const void* wte, const void* wpe,
+                          const int32_t* tokens, void* x, int B, int T, int C, int V) {
+    TT_OP_PROLOGUE();
+    if (!wte || !wpe || !tokens || !x || B <= 0 || T <= 0 || C <= 0 || V <= 0)
+        return fail(c, TT_ERR_ARG, "embed_fwd: bad arguments");
+    launch_embed_fwd(launch_of(c), dtype == TT_BF16, wte, wpe, tokens, x, B, T, C, V);
+    return op_epilogue(c, "embed_fwd");
+}
+
+tt_status tt_op_embed_bwd(tt_ctx* c, tt_dtype dtype, const void* dx, const int32_t* tokens,
+                          float* dwte, float* dwpe, int B, int T, int C, int V, int maxT) {
+    TT_OP_PROLOGUE();
+    if (!dx || !tokens || !dwte || !dwpe || B <= 0 || T <= 0 || T > maxT || C <= 0 || C > 1024 ||
+        V <= 0 || V >= 65535 * 16)
+        return fail(c, TT_ERR_ARG, "embed_bwd: bad arguments");
+    c->oom = false;
+    size_t mark = c->off;
+    void* s = arena_alloc(c, embed_bwd_scratch_bytes(B * T));
+    if (!c->oom) launch_embed_bwd(launch_of(c), dtype == TT_BF16, dx, tokens, dwte, dwpe, B, T, C, V, maxT, s);
+    c->off = mark;
+    return op_epilogue(c, "embed_bwd");
+}
+
+}  // extern "C"

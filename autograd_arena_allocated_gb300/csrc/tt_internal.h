@@ -1,0 +1,120 @@
+// tt_internal.h -- shared declarations of the native runtime and its kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/tt.h"
+#include "../../include/tt_ops.h"
+
+namespace tt {
+
+// ------------------------------------------------------------ device flags
+// Error flags written by kernels (never a trap or fault); read back by the host.
+enum DeviceFlag : int {
+    FLAG_BAD_TOKEN = 0,  // a token/target id outside [0, V)
+    FLAG_TIMEOUT = 1,    // a bounded mbarrier wait gave up
+    FLAG_NONFINITE = 2,  // non-finite loss
+    FLAG_COUNT = 4
+};
+
+// ------------------------------------------------------------ launch context
+// What every kernel launcher needs: the stream, the flag buffer, and a counter
+// of launches (launch accounting for the benchmark).
+struct Launch {
+    cudaStream_t stream = nullptr;
+    int* flags = nullptr;  // device int[FLAG_COUNT]
+    uint64_t* launches = nullptr;
+    bool dry = false;      // plan only: allocate, launch nothing
+    int gemm_backend = 0;  // 0 auto, 1 SIMT only
+    int num_sms = 148;
+    void count() const { if (launches) ++*launches; }
+};
+
+// ------------------------------------------------------------ GEMM
+// Logical contraction D[m,n] = sum_k A(m,k) B(n,k) with
+//   A(m,k) = a_kmajor ? A[m*lda + k] : A[k*lda + m]
+//   B(n,k) = b_kmajor ? B[n*ldb + k] : B[k*ldb + n]
+// and an epilogue.  The three forms the step uses:
+//   FWD: A = x [M,K] (K-major), B = W [N,K] (K-major), D = y [M,N]
+//   DX : A = dy [M,N'] (K-major), B(n,k) = W[k,n] (MN-major), D = dx
+//   DW : A(n,m) = dy[m,n] (MN-major), B(k,m) = x[m,k] (MN-major), D = dW fp32
+enum EpiKind : int {
+    EPI_STORE = 0,   // D = acc (+ bias) (+ residual)
+    EPI_GELU = 1,    // aux = acc + bias (pre-activation), D = gelu(aux)
+    EPI_DGELU = 2,   // D = acc * gelu'(aux)
+};
+
+struct GemmArgs {
+    const void* A = nullptr; long long lda = 0; bool a_kmajor = true;
+    const void* B = nullptr; long long ldb = 0; bool b_kmajor = true;
+    int M = 0, N = 0, K = 0;
+    int a_rows = 0;          // valid extent of A's MN dimension (rows beyond read as 0); 0 = M
+    int b_rows = 0;          // valid extent of B's MN dimension (rows beyond read as 0); 0 = N
+    int k_valid = 0;         // valid extent of K (beyond reads as 0); 0 = K
+    bool in_bf16 = true;     // operand storage: bf16 or fp32
+    void* D = nullptr; long long ldd = 0; bool d_f32 = false;
+    int n_store = 0;         // columns >= n_store are not stored; 0 = N
+    int epi = EPI_STORE;
+    const void* bias = nullptr;      // [N], same storage type as operands
+    const void* residual = nullptr;  // [M, ldd] same type as D
+    void* aux = nullptr;             // EPI_GELU: out pre-activation; EPI_DGELU: in
+    bool accumulate = false;         // D += result
+};
+
+// Runs the GEMM; `workspace` (fp32, may be needed for split-K of the DW form)
+// is sized by gemm_workspace_floats.  Returns false on unsupported arguments.
+bool gemm(const Launch& L, const GemmArgs& g, float* workspace, size_t workspace_floats);
+size_t gemm_workspace_floats(const Launch& L, const GemmArgs& g);
+bool gemm_tc_eligible(const GemmArgs& g);
+bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t workspace_floats);
+size_t gemm_tc_workspace_floats(const Launch& L, const GemmArgs& g);
+void gemm_simt_launch(const Launch& L, const GemmArgs& g);
+
+// ------------------------------------------------------------ other kernels
+void launch_embed_fwd(const Launch& L, bool bf16, const void* wte, const void* wpe,
+                      const int32_t* tok, void* x, int B, int T, int C, int V);
+// scratch: int32 [4*M + 2] for the stable sort of positions by token id
+size_t embed_bwd_scratch_bytes(int M);
+void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t* tok,
+                      float* dwte, float* dwpe, int B, int T, int C, int V, int maxT,
+                      void* scratch);
+
+size_t layernorm_bwd_scratch_floats(int M, int C);
+void launch_layernorm_fwd(const Launch& L, bool bf16, const void* x, const void* w,
+                          const void* b, void* y, float* mean, float* rstd, int M, int C);
+void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void* w,
+                          const float* mean, const float* rstd, const void* dy, void* dx,
+                          float* dw, float* db, int M, int C, bool accumulate, float* scratch);
+
+void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* targets,
+                 float* row_loss, float* mean_loss, int M, int V, int ld, float dscale);
+
+size_t colsum_scratch_floats(int M, int N);
+void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, float* out,
+                   float* scratch);
+
+void launch_adamw(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g,
+                  float* m, float* v, size_t n, float lr, float b1, float b2, float eps,
+                  float wd, int step);
+void launch_cast_bf16(const Launch& L, const float* src, __nv_bfloat16* dst, size_t n);
+
+size_t attention_bwd_scratch_floats(int B, int T, int H);
+void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, float* lse,
+                          int B, int T, int C, int H);
+void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const void* y,
+                          const float* lse, const void* dy, void* dqkv, int B, int T, int C,
+                          int H, float* scratch);
+bool attention_mma_eligible(bool bf16, int C, int H);
+void launch_attention_fwd_mma(const Launch& L, const void* qkv, void* y, float* lse,
+                              int B, int T, int C, int H);
+void launch_attention_bwd_mma(const Launch& L, const void* qkv, const void* y,
+                              const float* lse, const void* dy, void* dqkv, int B, int T,
+                              int C, int H, float* scratch);
+
+}  // namespace tt

@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Training throughput of the GPT-2 step (forward + tape backward + AdamW).
+
+Default workload: GPT-2 124M (L=12, C=768, H=12, V=50257 tied head), B=32,
+T=1024, bf16 weights/activations with fp32 master weights, gradients and
+AdamW moments; synthetic Zipf(1.1) tokens and N(0, 0.02) init.  A step is
+tt_ctx_reset + tt_gpt2_step + tt_adamw over one resident batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank trains its
+own replica on its own GPU (weak scaling, no data-path collective); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+`--impl reference` times the oracle (plain double-precision CPU code) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "train tokens/sec (fwd+bwd+AdamW) GPT-2 124M on 1 GB300; MFU vs bf16 peak"
+UNIT = "tokens/s"
+
+
+def flops_per_token(sh, T):
+    """6 * matmul parameters + 12 * L * C * T (full, non-causal attention)."""
+    n_mm = sh.L * 12 * sh.C * sh.C + sh.V * sh.C
+    return 6 * n_mm + 12 * sh.L * sh.C * T
+
+
+def causal_flops_per_token(sh, T):
+    n_mm = sh.L * 12 * sh.C * sh.C + sh.V * sh.C
+    return 6 * n_mm + 6 * sh.L * sh.C * (T + 1)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from autograd_arena_allocated_gb300 import synth
+
+    oracle.set_threads(os.cpu_count() or 1)
+    w = synth.WORKLOADS[args.workload]
+    sh = w.shape
+    Bs, Ts = 1, args.ref_tokens
+    p = synth.init_params(sh).astype(np.float64)
+    tok, tgt = synth.token_stream(Bs, Ts, sh.V, w.tokens)
+    m = np.zeros_like(p)
+    v = np.zeros_like(p)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        _, g, _ = oracle.gpt2_step(sh, p, tok, tgt)
+        oracle.lib().or_adamw(oracle._d(p), oracle._d(g), oracle._d(m), oracle._d(v), p.size,
+                              w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, i + 1)
+        times.append(time.perf_counter() - t0)
+    timed = times[args.warmup:]
+    total = sum(timed)
+    value = Bs * Ts * len(timed) / total
+    sample = (f"B={Bs}, T={Ts} slice of the {w.name} workload per step (same architecture; "
+              f"the full B={w.B}, T={w.T} step is out of reach of the scalar oracle)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(timed),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Zipf(1.1) tokens, N(0,0.02) init)",
+        "config": config_of(w, world, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.get_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, world, args):
+    return {"workload": f"{w.name}: GPT-2 L={w.shape.L} C={w.shape.C} H={w.shape.H} "
+                        f"V={w.shape.V} (tied head), B={w.B} T={w.T} per GPU, {w.dtype}",
+            "global_batch": w.B * world, "seq_len": w.T, "parallelism": f"replicas x{world}",
+            "l2": "working set (~20 GB arena) far above the 129 MB L2; no flush needed",
+            "tokens": w.tokens}
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def cpu_baseline(w, tokens_target=64):
+    import numpy as np
+
+    import oracle
+    from autograd_arena_allocated_gb300 import synth
+
+    oracle.set_threads(os.cpu_count() or 1)
+    sh = w.shape
+    p = synth.init_params(sh).astype(np.float64)
+    tok, tgt = synth.token_stream(1, tokens_target, sh.V, w.tokens)
+    m = np.zeros_like(p)
+    v = np.zeros_like(p)
+    t0 = time.perf_counter()
+    _, g, _ = oracle.gpt2_step(sh, p, tok, tgt)
+    oracle.lib().or_adamw(oracle._d(p), oracle._d(g), oracle._d(m), oracle._d(v), p.size, w.lr,
+                          w.beta1, w.beta2, w.eps, w.weight_decay, 1)
+    dt = time.perf_counter() - t0
+    return {"value": tokens_target / dt, "unit": UNIT, "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": f"one step (fwd+bwd+AdamW over all {p.size} parameters) of the same "
+                      f"architecture on B=1, T={tokens_target}, double precision; {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2_124m_b32")
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import numpy as np
+    import torch
+
+    from autograd_arena_allocated_gb300 import api, synth
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    if rank == 0:
+        native_build.build()
+    if dist is not None:
+        dist.barrier()
+    native_build.build()  # no-op once built
+
+    w = synth.WORKLOADS[args.workload]
+    sh = w.shape
+    B, T = w.B, w.T
+    cfg = api.make_config(sh.L, sh.C, sh.H, sh.V, sh.maxT, w.dtype)
+    n = api.num_params(cfg)
+    peaks = load_peaks()
+
+    p = synth.init_params(sh)
+    tok, tgt = synth.token_stream(B, T, sh.V, w.tokens)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    master = torch.from_numpy(p).to(dev)
+    grads = torch.empty(n, device=dev)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    bf16 = w.dtype == "bf16"
+    lowp = torch.empty(n, device=dev, dtype=torch.bfloat16) if bf16 else None
+    tok_d = torch.from_numpy(tok).to(dev)
+    tgt_d = torch.from_numpy(tgt).to(dev)
+    ctx = api.Context(api.arena_bytes(cfg, B, T) + (64 << 20), stream=stream.cuda_stream)
+    ctx.set_model(cfg)
+    if bf16:
+        ctx.cast_bf16(master, lowp)
+    params = lowp if bf16 else master
+    hp = (w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    step_no = [0]
+
+    def train_step(tokens, targets, sync):
+        ctx.reset()
+        loss = ctx.step(params, grads, tokens, targets, B, T, sync=sync)
+        step_no[0] += 1
+        ctx.adamw(master, lowp, grads, m, v, *hp, step_no[0])
+        return loss
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # warm-up (also the first-use set-up of every kernel)
+    for _ in range(args.warmup):
+        train_step(tok_d, tgt_d, sync=False)
+    ctx.sync()
+
+    # ---------------- timed region: device-resident inputs
+    barrier()
+    l0 = ctx.launches
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            train_step(tok_d, tgt_d, sync=False)
+        e1.record(stream)
+        barrier()
+    launches = ctx.launches - l0  # kernels launched inside the timed region
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    ctx.sync()
+    ms_step = ms / args.steps
+    value = world * B * T * args.steps / (ms / 1e3)
+    fpt = flops_per_token(sh, T)
+    mfu = value / world * fpt / (peaks["bf16"] * 1e12)
+
+    # ---------------- per-op device times (a second pass with CUDA events per op)
+    ctx.set_profiling(True)
+    prof_steps = min(args.steps, 3)
+    for _ in range(prof_steps):
+        train_step(tok_d, tgt_d, sync=False)
+    prof = ctx.profile()
+    ctx.set_profiling(False)
+    total_ms = sum(r["ms"] for r in prof.values()) or 1.0
+    kernels = {k: {"share": r["ms"] / total_ms, "ms_per_step": r["ms"] / prof_steps,
+                   "launch_groups_per_step": r["calls"] // prof_steps}
+               for k, r in sorted(prof.items(), key=lambda kv: -kv[1]["ms"])}
+    top = max(prof, key=lambda k: prof[k]["ms"])
+    r = prof[top]
+    per_launch_ms = r["ms"] / r["calls"]
+    if top.startswith("gemm"):
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = r["flops"] / r["calls"] / (per_launch_ms * 1e-3) / 1e12
+        peak, peak_name = peaks["bf16_sustained"], "bf16_tflops_sustained"
+    elif top.startswith("attn") and not (sh.C // sh.H == 64 and bf16):
+        bound, unit = "alu", "TFLOP/s"
+        achieved = r["flops"] / r["calls"] / (per_launch_ms * 1e-3) / 1e12
+        peak, peak_name = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "fp32 FMA: 152 SM x 128 lanes x 2 x max clock"
+    elif top.startswith("attn"):
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = r["flops"] / r["calls"] / (per_launch_ms * 1e-3) / 1e12
+        peak, peak_name = peaks["bf16_sustained"], "bf16_tflops_sustained"
+    else:
+        bound, unit = "hbm", "GB/s"
+        achieved = r["bytes"] / r["calls"] / (per_launch_ms * 1e-3) / 1e9
+        peak, peak_name = peaks["hbm_gbs"], "hbm_gbs"
+    roofline = {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peaks['source']} {peak_name}",
+                "per_launch": {"ms": per_launch_ms, "flops": r["flops"] / r["calls"],
+                               "bytes": r["bytes"] / r["calls"]}}
+
+    # ---------------- end to end: pinned host buffers through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        tok_h = torch.from_numpy(tok).pin_memory()
+        tgt_h = torch.from_numpy(tgt).pin_memory()
+        train_step(tok_h, tgt_h, sync=True)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            train_step(tok_h, tgt_h, sync=True)  # H2D of the batch, D2H of the loss
+        barrier()
+        e2e_s = max_over_ranks(time.perf_counter() - t0)
+        e2e = {"value": world * B * T * args.steps / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4,
+               "ms_per_step": 1e3 * e2e_s / args.steps}
+
+    final_loss = ctx.step(params, grads, tok_d, tgt_d, B, T, sync=True) if rank == 0 else None
+
+    if rank == 0:
+        cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded Zipf(1.1) tokens, N(0,0.02) init, random weights)",
+            "config": config_of(w, world, args),
+            "mfu": mfu, "mfu_sustained": value / world * fpt / (peaks["bf16_sustained"] * 1e12),
+            "flops_per_token": fpt, "causal_flops_per_token": causal_flops_per_token(sh, T),
+            "roofline": roofline, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk.summary(), "loss": final_loss,
+            "arena_bytes": ctx.high_water,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

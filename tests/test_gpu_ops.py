@@ -1,0 +1,283 @@
+"""Per-kernel parity: each op of the C ABI (include/tt_ops.h) against the
+oracle on the same seeded inputs, at sizes that span several tiles with
+ragged tails.  Tolerances: fp32 mode ~1e-5 relative (fp32 accumulation);
+bf16 mode bounded by bf16 output rounding (2^-9 relative) plus fp32
+accumulation error, written per test."""
+import numpy as np
+import pytest
+import torch
+
+from autograd_arena_allocated_gb300 import api, synth
+from autograd_arena_allocated_gb300 import build as native_build
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    native_build.build()
+    c = api.Context(1 << 30)
+    yield c
+    c.close()
+
+
+_seed = [100]
+
+
+def rnd(*shape, scale=1.0):
+    _seed[0] += 1
+    n = int(np.prod(shape))
+    return (synth.normals(_seed[0], 0, n) * scale).astype(np.float32).reshape(shape)
+
+
+def to_dev(a, dt):
+    t = torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    return t.to(torch.bfloat16) if dt == "bf16" else t.float()
+
+
+def ovals(a, dt, oracle):
+    return oracle.bf16_values(a).reshape(a.shape) if dt == "bf16" else a.astype(np.float64)
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(got, ref, rtol, atol_frac, what=""):
+    """|got - ref| <= rtol*|ref| + atol_frac*rms(ref), element-wise."""
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), what
+    scale = np.sqrt(np.mean(ref ** 2)) + 1e-30
+    err = np.abs(got - ref)
+    bound = rtol * np.abs(ref) + atol_frac * scale
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} / {err.size} outside tolerance; worst at {i}: "
+                             f"got {got[i]} ref {ref[i]} (rms {scale})")
+
+
+TOL = {"fp32": (2e-5, 2e-6), "bf16": (8e-3, 4e-3)}
+
+
+# ----------------------------------------------------------------- linear
+@pytest.mark.parametrize("dt,backend", [("fp32", 1), ("bf16", 1), ("bf16", 0)])
+@pytest.mark.parametrize("M,K,N", [(200, 64, 96), (300, 192, 520), (512, 768, 2304), (129, 3072, 768)])
+@pytest.mark.parametrize("variant", ["plain", "bias_res", "gelu"])
+def test_linear_fwd(ctx, oracle, dt, backend, M, K, N, variant):
+    ctx.set_gemm_backend(backend)
+    x, W, b, r = rnd(M, K), rnd(N, K, scale=0.05), rnd(N, scale=0.1), rnd(M, N)
+    xd, Wd, bd, rd = (to_dev(a, dt) for a in (x, W, b, r))
+    y = torch.empty(M, N, device=DEV, dtype=xd.dtype)
+    pre = torch.empty_like(y) if variant == "gelu" else None
+    ctx.linear_fwd(dt, xd, Wd, bd if variant != "plain" else None,
+                   rd if variant == "bias_res" else None, y, pre, M, K, N, gelu=variant == "gelu")
+    torch.cuda.synchronize()
+    u = oracle.linear_fwd(ovals(x, dt, oracle), ovals(W, dt, oracle),
+                          ovals(b, dt, oracle) if variant != "plain" else None)
+    rtol, atol = TOL[dt]
+    if variant == "gelu":
+        assert_close(host(pre), u, rtol, atol, "pre-activation")
+        ref = oracle.gelu_fwd(u)
+    elif variant == "bias_res":
+        ref = u + ovals(r, dt, oracle)
+    else:
+        ref = u
+    assert_close(host(y), ref, rtol, atol, f"linear fwd {variant}")
+    ctx.set_gemm_backend(0)
+
+
+@pytest.mark.parametrize("dt,backend", [("fp32", 1), ("bf16", 1), ("bf16", 0)])
+@pytest.mark.parametrize("M,K,N", [(200, 64, 96), (300, 520, 192), (256, 768, 3072), (130, 3072, 768)])
+@pytest.mark.parametrize("variant", ["plain", "dgelu", "accumulate"])
+def test_linear_bwd_dx(ctx, oracle, dt, backend, M, K, N, variant):
+    ctx.set_gemm_backend(backend)
+    dy, W, pre, dx0 = rnd(M, N), rnd(N, K, scale=0.05), rnd(M, K), rnd(M, K)
+    dyd, Wd, pred = (to_dev(a, dt) for a in (dy, W, pre))
+    dx = to_dev(dx0, dt) if variant == "accumulate" else torch.empty(M, K, device=DEV, dtype=dyd.dtype)
+    ctx.linear_bwd_dx(dt, dyd, Wd, pred if variant == "dgelu" else None, dx, M, K, N,
+                      accumulate=variant == "accumulate")
+    torch.cuda.synchronize()
+    ref, _, _ = oracle.linear_bwd(np.zeros((M, K)), ovals(W, dt, oracle), ovals(dy, dt, oracle),
+                                  with_bias=False)
+    if variant == "dgelu":
+        ref = oracle.gelu_bwd(ovals(pre, dt, oracle), ref)
+    if variant == "accumulate":
+        ref = ref + ovals(dx0, dt, oracle)
+    rtol, atol = TOL[dt]
+    assert_close(host(dx), ref, rtol, atol, f"linear dx {variant}")
+    ctx.set_gemm_backend(0)
+
+
+@pytest.mark.parametrize("dt,backend", [("fp32", 1), ("bf16", 1), ("bf16", 0)])
+@pytest.mark.parametrize("M,K,N", [(200, 64, 96), (4096, 256, 192), (1000, 768, 2304), (2048, 3072, 768)])
+def test_linear_bwd_dw(ctx, oracle, dt, backend, M, K, N):
+    ctx.set_gemm_backend(backend)
+    dy, x = rnd(M, N), rnd(M, K)
+    dyd, xd = to_dev(dy, dt), to_dev(x, dt)
+    dW = torch.empty(N, K, device=DEV)
+    db = torch.empty(N, device=DEV)
+    ctx.linear_bwd_dw(dt, dyd, xd, dW, db, M, K, N)
+    torch.cuda.synchronize()
+    _, rW, rb = oracle.linear_bwd(ovals(x, dt, oracle), np.zeros((N, K)), ovals(dy, dt, oracle))
+    # fp32 outputs: only accumulation-order error (sums of M products)
+    assert_close(host(dW), rW, 1e-5, 2e-6, "dW")
+    assert_close(host(db), rb, 1e-5, 2e-6, "db")
+    # deterministic: a second call gives the same bits
+    dW2 = torch.empty_like(dW)
+    ctx.linear_bwd_dw(dt, dyd, xd, dW2, None, M, K, N)
+    torch.cuda.synchronize()
+    assert torch.equal(dW, dW2)
+    ctx.set_gemm_backend(0)
+
+
+# ----------------------------------------------------------------- attention
+@pytest.mark.parametrize("dt,B,T,C_,H", [("fp32", 2, 37, 64, 4), ("fp32", 1, 70, 64, 2),
+                                         ("bf16", 2, 100, 128, 2), ("bf16", 1, 257, 384, 6),
+                                         ("bf16", 3, 1, 128, 2)])
+def test_attention(ctx, oracle, dt, B, T, C_, H):
+    qkv, dy = rnd(B * T, 3 * C_), rnd(B * T, C_)
+    qd, dyd = to_dev(qkv, dt), to_dev(dy, dt)
+    y = torch.empty(B * T, C_, device=DEV, dtype=qd.dtype)
+    lse = torch.empty(B, H, T, device=DEV)
+    ctx.attention_fwd(dt, qd, y, lse, B, T, C_, H)
+    dqkv = torch.empty_like(qd)
+    ctx.attention_bwd(dt, qd, y, lse, dyd, dqkv, B, T, C_, H)
+    torch.cuda.synchronize()
+    q64 = ovals(qkv, dt, oracle)
+    ry, P = oracle.attention_fwd(q64, B, T, C_, H)
+    rtol, atol = TOL[dt]
+    assert_close(host(y), ry, rtol, atol, "attention y")
+    # the backward uses the GPU's own y (as the step does)
+    rd = oracle.attention_bwd(q64, P, ovals(dy, dt, oracle), B, T, C_, H)
+    assert_close(host(dqkv), rd, 4 * rtol, 2 * atol, "attention dqkv")
+
+
+# ----------------------------------------------------------------- layernorm
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("M,C_", [(300, 64), (130, 384), (257, 768), (64, 1024)])
+def test_layernorm(ctx, oracle, dt, M, C_):
+    x = rnd(M, C_) * 2 + 0.5
+    w, b, dy, dx0 = rnd(C_) * 0.2 + 1, rnd(C_, scale=0.1), rnd(M, C_), rnd(M, C_)
+    xd, wd, bd, dyd = (to_dev(a, dt) for a in (x, w, b, dy))
+    y = torch.empty_like(xd)
+    mean = torch.empty(M, device=DEV)
+    rstd = torch.empty(M, device=DEV)
+    ctx.layernorm_fwd(dt, xd, wd, bd, y, mean, rstd, M, C_)
+    dx = to_dev(dx0, dt)
+    dw = torch.empty(C_, device=DEV)
+    db = torch.empty(C_, device=DEV)
+    ctx.layernorm_bwd(dt, xd, wd, mean, rstd, dyd, dx, dw, db, M, C_, accumulate=True)
+    torch.cuda.synchronize()
+    x64, w64, b64, dy64 = (ovals(a, dt, oracle) for a in (x, w, b, dy))
+    ry, rmean, rrstd = oracle.layernorm_fwd(x64, w64, b64)
+    rtol, atol = TOL[dt]
+    assert_close(host(y), ry, rtol, atol, "ln y")
+    assert_close(host(mean), rmean, 1e-5, 1e-6, "ln mean")
+    assert_close(host(rstd), rrstd, 1e-5, 1e-6, "ln rstd")
+    rdx, rdw, rdb = oracle.layernorm_bwd(x64, w64, rmean, rrstd, dy64)
+    assert_close(host(dx), rdx + ovals(dx0, dt, oracle), rtol, atol, "ln dx (accumulated)")
+    assert_close(host(dw), rdw, 1e-4, 1e-5, "ln dw")
+    assert_close(host(db), rdb, 1e-4, 1e-5, "ln db")
+
+
+# ----------------------------------------------------------------- cross entropy
+@pytest.mark.parametrize("dt,M,V,ld", [("fp32", 37, 65, 128), ("bf16", 37, 65, 128),
+                                       ("fp32", 5, 256, 256), ("bf16", 9, 50257, 50304)])
+def test_xent(ctx, oracle, dt, M, V, ld):
+    z = rnd(M, ld, scale=3.0)
+    tgt = synth.token_stream(1, M, V, "zipf", seed=7)[0].reshape(M)
+    zd = to_dev(z, dt)
+    td = torch.from_numpy(tgt).to(DEV)
+    rl = torch.empty(M, device=DEV)
+    ml = torch.empty(1, device=DEV)
+    ctx.xent(dt, zd, td, rl, ml, M, V, ld, 1.0 / M)
+    torch.cuda.synchronize()
+    z64 = ovals(z, dt, oracle)[:, :V].copy()
+    loss, rrl, rdz = oracle.xent(z64, tgt, want_grad=True)
+    assert_close(host(rl), rrl, 2e-6, 1e-6, "row loss")
+    assert abs(ml.item() - loss) <= 2e-6 * abs(loss)
+    g = host(zd)
+    rtol, atol = TOL[dt]
+    assert_close(g[:, :V], rdz, rtol, atol, "dlogits")
+    assert np.all(g[:, V:] == 0.0)
+
+
+def test_xent_uniform_logits_is_log_v(ctx):
+    import math
+    M, V, ld = 4, 50257, 50304
+    z = torch.zeros(M, ld, device=DEV, dtype=torch.bfloat16)
+    td = torch.tensor([0, 1, V - 1, 77], dtype=torch.int32, device=DEV)
+    rl = torch.empty(M, device=DEV)
+    ml = torch.empty(1, device=DEV)
+    ctx.xent("bf16", z, td, rl, ml, M, V, ld, 1.0 / M)
+    torch.cuda.synchronize()
+    assert abs(ml.item() - math.log(V)) < 2e-6 * math.log(V)
+
+
+# ----------------------------------------------------------------- embedding
+@pytest.mark.parametrize("dt,B,T,C_,V,maxT", [("fp32", 3, 50, 64, 100, 64),
+                                              ("bf16", 4, 128, 768, 50257, 1024),
+                                              ("bf16", 2, 33, 384, 65, 256)])
+def test_embedding(ctx, oracle, dt, B, T, C_, V, maxT):
+    wte, wpe = rnd(V, C_, scale=0.02), rnd(maxT, C_, scale=0.02)
+    tok = synth.token_stream(B, T, V, "zipf", seed=3)[0]
+    dx = rnd(B * T, C_)
+    base = rnd(V, C_)  # dwte is accumulated into
+    wted, wped, dxd = to_dev(wte, dt), to_dev(wpe, dt), to_dev(dx, dt)
+    td = torch.from_numpy(tok).to(DEV)
+    x = torch.empty(B * T, C_, device=DEV, dtype=wted.dtype)
+    ctx.embed_fwd(dt, wted, wped, td, x, B, T, C_, V)
+    dwte = torch.from_numpy(base).to(DEV)
+    dwpe = torch.full((maxT, C_), 7.0, device=DEV)
+    ctx.embed_bwd(dt, dxd, td, dwte, dwpe, B, T, C_, V, maxT)
+    torch.cuda.synchronize()
+    rx = oracle.embed_fwd(ovals(wte, dt, oracle), ovals(wpe, dt, oracle), tok, B, T)
+    rtol, atol = TOL[dt]
+    assert_close(host(x), rx, rtol, atol, "embedding x")
+    rwte, rwpe = oracle.embed_bwd(ovals(dx, dt, oracle), tok, B, T, V, maxT)
+    assert_close(host(dwte), rwte + base, 1e-5, 1e-6, "dwte")
+    assert_close(host(dwpe), rwpe, 1e-5, 1e-6, "dwpe")
+    # deterministic
+    dwte2 = torch.from_numpy(base).to(DEV)
+    ctx.embed_bwd(dt, dxd, td, dwte2, dwpe, B, T, C_, V, maxT)
+    torch.cuda.synchronize()
+    assert torch.equal(dwte, dwte2)
+
+
+def test_embedding_bad_token_sets_flag(ctx):
+    ctx.reset()
+    wte = torch.zeros(10, 64, device=DEV)
+    wpe = torch.zeros(4, 64, device=DEV)
+    tok = torch.tensor([1, 2, 10, 3], dtype=torch.int32, device=DEV)
+    x = torch.empty(4, 64, device=DEV)
+    ctx.embed_fwd("fp32", wte, wpe, tok, x, 1, 4, 64, 10)
+    with pytest.raises(api.TTError, match="TT_ERR_ARG"):
+        ctx.sync()
+    ctx.reset()
+    ctx.sync()
+
+
+# ----------------------------------------------------------------- adamw / cast
+@pytest.mark.parametrize("n", [1, 7, 1001, 1 << 16])
+def test_adamw_and_cast(ctx, oracle, n):
+    p0, g, m0, v0 = rnd(n), rnd(n), rnd(n, scale=0.1), np.abs(rnd(n, scale=0.1))
+    P, G, Mm, Vv = (torch.from_numpy(a.copy()).to(DEV) for a in (p0, g, m0, v0))
+    low = torch.empty(n, device=DEV, dtype=torch.bfloat16)
+    args = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    ctx.adamw(P, low, G, Mm, Vv, step=3, **args)
+    torch.cuda.synchronize()
+    rp, rm, rv = oracle.adamw(p0, g, m0, v0, args["lr"], args["beta1"], args["beta2"], args["eps"],
+                              args["weight_decay"], 3)
+    assert_close(host(P), rp, 1e-6, 1e-7, "master")
+    assert_close(host(Mm), rm, 1e-6, 1e-7, "m")
+    assert_close(host(Vv), rv, 1e-6, 1e-7, "v")
+    # the bf16 copy is the nearest bf16 of the updated fp32 master
+    assert np.array_equal(host(low), oracle.bf16_values(P.cpu().numpy()))
+    cast = torch.empty(n, device=DEV, dtype=torch.bfloat16)
+    ctx.cast_bf16(G, cast)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(cast), oracle.bf16_values(g))
