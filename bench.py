@@ -351,7 +351,8 @@ def main():
                "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4,
                "ms_per_step": 1e3 * e2e_s / args.steps}
 
-    final_loss = ctx.step(params, grads, tok_d, tgt_d, B, T, sync=True) if rank == 0 else None
+    ctx.reset()
+    final_loss = ctx.step(params, grads, tok_d, tgt_d, B, T, sync=True)
 
     if rank == 0:
         cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w)

@@ -76,7 +76,7 @@ def tensor_slices(cfg, L):
     return out
 
 
-def compare_grads(cfg, L, g, rg, rel_l2, min_cos=None, T=None, maxT=None):
+def compare_grads(cfg, L, g, rg, rel_l2, min_cos=None, T=None, maxT=None, label=""):
     worst = []
     for name, off, n in tensor_slices(cfg, L):
         a, b = g[off:off + n], rg[off:off + n]
@@ -91,7 +91,10 @@ def compare_grads(cfg, L, g, rg, rel_l2, min_cos=None, T=None, maxT=None):
         assert err <= rel_l2, f"{name}: rel-L2 {err:.3e} > {rel_l2}"
         if min_cos is not None:
             assert cos >= min_cos, f"{name}: cosine {cos:.6f} < {min_cos}"
-    return max(worst)
+    w = max(worst)
+    print(f"[{label}] worst gradient rel-L2 {w[0]:.3e} ({w[1]}), min cosine "
+          f"{min(c for _, _, c in worst):.6f}")
+    return w
 
 
 @pytest.fixture(scope="module")
@@ -112,7 +115,8 @@ def test_tiny_fp32_step_matches_oracle(ctx, oracle):
     rl, rg, _ = oracle.gpt2_step(sh, p.astype(np.float64), tok, tgt)
     assert abs(loss - rl) <= 1e-5 * abs(rl), (loss, rl)
     g = run.grads.cpu().numpy().astype(np.float64)
-    compare_grads(run.cfg, sh.L, g, rg, 1e-4)
+    compare_grads(run.cfg, sh.L, g, rg, 1e-4, label="tiny fp32")
+    print(f"[tiny fp32] loss {loss:.7f} oracle {rl:.7f} rel {abs(loss - rl) / rl:.2e}")
     # AdamW on the master (fp32 mode trains the master directly)
     lr, b1, b2, eps, wd = w.lr, w.beta1, w.beta2, w.eps, w.weight_decay
     ctx.adamw(run.master, None, run.grads, run.m, run.v, lr, b1, b2, eps, wd, 1)
@@ -137,41 +141,69 @@ def test_tiny_fp32_short_sequences(ctx, oracle):
 
 
 # ----------------------------------------------------------------- bf16 mode
-def _bf16_parity(ctx, oracle, sh, B, T, kind, jitter):
+def _bf16_parity(ctx, oracle, sh, B, T, kind, jitter, label):
     p, tok, tgt = make_inputs(sh, B, T, kind, jitter=jitter)
     run = Run(ctx, sh, "bf16", p)
     loss = run.step(tok, tgt)
     po = oracle_params(oracle, p, "bf16")
     rl, rg, _ = oracle.gpt2_step(sh, po, tok, tgt)
+    print(f"[{label}] loss {loss:.6f} oracle {rl:.6f} rel {abs(loss - rl) / rl:.2e}")
     assert abs(loss - rl) <= 2e-3 * abs(rl), (loss, rl)
     g = run.grads.cpu().numpy().astype(np.float64)
-    compare_grads(run.cfg, sh.L, g, rg, 2e-2, min_cos=0.999, T=T, maxT=sh.maxT)
+    compare_grads(run.cfg, sh.L, g, rg, 2e-2, min_cos=0.999, T=T, maxT=sh.maxT, label=label)
     return run, p, rg
 
 
 def test_char_bf16_step_matches_oracle(ctx, oracle):
     w = synth.WORKLOADS["char_bf16"]
-    run, p, rg = _bf16_parity(ctx, oracle, w.shape, 4, 128, "zipf", jitter=0.05)
-    # AdamW-updated parameters vs the oracle's update of the oracle's gradient
+    run, p, rg = _bf16_parity(ctx, oracle, w.shape, 4, 128, "zipf", jitter=0.05, label="char bf16")
     lr, b1, b2, eps, wd = w.lr, w.beta1, w.beta2, w.eps, w.weight_decay
-    ctx.adamw(run.master, run.lowp, run.grads, run.m, run.v, lr, b1, b2, eps, wd, 1)
-    torch.cuda.synchronize()
     rp, _, _ = oracle.adamw(p.astype(np.float64), rg, np.zeros(p.size), np.zeros(p.size), lr, b1, b2,
                             eps, wd, 1)
+    rel = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))
+    # (1) AdamW-updated parameters from identical inputs (the oracle's gradient
+    #     given to the GPU's tt_adamw): the fp32 master within 1e-3 (it is at
+    #     ~1e-7); the bf16 compute copy is exactly the nearest bf16 of the
+    #     master (its distance to the exact update is bf16 rounding, ~2e-3)
+    g_or = torch.from_numpy(rg.astype(np.float32)).to(DEV)
+    master = torch.from_numpy(p).to(DEV)
+    low = torch.empty_like(run.lowp)
+    ctx.adamw(master, low, g_or, torch.zeros_like(master), torch.zeros_like(master), lr, b1, b2,
+              eps, wd, 1)
+    torch.cuda.synchronize()
+    e_master = rel(master.cpu().numpy().astype(np.float64), rp)
+    e_low = rel(low.float().cpu().numpy().astype(np.float64), rp)
+    print(f"[char bf16] AdamW from identical inputs: master rel-L2 {e_master:.2e}, bf16 copy {e_low:.2e}")
+    assert e_master <= 1e-6
+    assert np.array_equal(low.float().cpu().numpy().astype(np.float64),
+                          oracle.bf16_values(master.cpu().numpy()))
+    # (2) end to end: the update of the GPU's own bf16-mode gradient.  At step 1
+    #     Adam moves every element by ~lr*sign(g), so the few components whose
+    #     sign the bf16 gradient gets wrong (|g| near zero) move by 2*lr.
+    ctx.adamw(run.master, run.lowp, run.grads, run.m, run.v, lr, b1, b2, eps, wd, 1)
+    torch.cuda.synchronize()
     got = run.master.cpu().numpy().astype(np.float64)
-    assert np.linalg.norm(got - rp) / np.linalg.norm(rp) <= 1e-3
+    e2e = rel(got, rp)
+    g = run.grads.cpu().numpy()
+    flips = float(np.mean(np.sign(g) != np.sign(rg)))
+    print(f"[char bf16] AdamW after the bf16 step: params rel-L2 {e2e:.2e}, "
+          f"gradient sign disagreements {100 * flips:.3f}%")
+    assert e2e <= 2 * lr * math.sqrt(flips) * math.sqrt(p.size) / np.linalg.norm(rp) + 1e-3
     assert np.array_equal(run.lowp.float().cpu().numpy().astype(np.float64),
                           oracle.bf16_values(run.master.cpu().numpy()))
 
 
 def test_gpt2_124m_bf16_reduced_batch(ctx, oracle):
     """GPT-2 124M architecture at B=1, T=64 (the oracle's reduced size)."""
-    _bf16_parity(ctx, oracle, synth.GPT2_124M, 1, 64, "zipf", jitter=0.0)
+    _bf16_parity(ctx, oracle, synth.GPT2_124M, 1, 64, "zipf", jitter=0.0, label="124M B=1 T=64")
 
 
 def _sampled_sequences(ctx, oracle, w, seqs):
     sh = w.shape
     p, tok, tgt = make_inputs(sh, w.B, w.T, w.tokens)
+    cfg = api.make_config(sh.L, sh.C, sh.H, sh.V, sh.maxT, "bf16")
+    big = api.Context(api.arena_bytes(cfg, w.B, w.T))
+    ctx = big
     run = Run(ctx, sh, "bf16", p)
     loss = run.step(tok, tgt)
     rl_gpu = torch.empty(w.B * w.T, device=DEV)
@@ -184,8 +216,12 @@ def _sampled_sequences(ctx, oracle, w, seqs):
         _, _, rl = oracle.gpt2_step(sh, po, tok[b:b + 1], tgt[b:b + 1], want_grads=False,
                                     want_row_loss=True)
         err = np.abs(rl_gpu[b] - rl)
+        print(f"[{w.name}] sequence {b}: per-position loss max abs err {np.max(err):.2e}, "
+              f"mean abs err {np.mean(err):.2e} (mean loss {np.mean(rl):.4f})")
         assert np.max(err) <= 2e-2 and np.mean(err) <= 2e-3 * np.mean(rl), (b, np.max(err))
-    return run
+    g = run.grads.clone()
+    big.close()
+    return g
 
 
 def test_char_bf16_full_batch_sampled(ctx, oracle):
@@ -194,8 +230,7 @@ def test_char_bf16_full_batch_sampled(ctx, oracle):
 
 def test_gpt2_124m_full_batch_sampled(ctx, oracle):
     """The benchmark's workload (B=32, T=1024): one whole sequence sampled."""
-    run = _sampled_sequences(ctx, oracle, synth.WORKLOADS["gpt2_124m_b32"], [31])
-    g = run.grads
+    g = _sampled_sequences(ctx, oracle, synth.WORKLOADS["gpt2_124m_b32"], [31])
     assert torch.isfinite(g).all()
 
 
