@@ -70,6 +70,7 @@ SIGNATURES = {
     "tt_op_xent": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _f]),
     "tt_op_embed_fwd": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i]),
     "tt_op_embed_bwd": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i]),
+    "tt_linear_bwd_dw_noalloc": (_st, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i]),
 }
 
 _lib = None

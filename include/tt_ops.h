@@ -91,6 +91,47 @@ tt_status tt_op_embed_fwd(tt_ctx* ctx, tt_dtype dtype, const void* wte, const vo
 tt_status tt_op_embed_bwd(tt_ctx* ctx, tt_dtype dtype, const void* dx, const int32_t* tokens,
                           float* dwte, float* dwpe, int B, int T, int C, int V, int maxT);
 
+/* ------------------------------------------------------ allocation-free call
+ * The pages have no counterpart to this entry point.  It serves callers of
+ * this library that cannot allocate device memory: a program whose GPU memory
+ * is owned by another allocator (for example a framework's caching allocator
+ * or a server that budgets all memory when it starts) must not have a library
+ * call cudaMalloc behind its back, and such a caller cannot create a tt_ctx
+ * either, because a context's arena is one cudaMalloc.
+ *
+ * tt_linear_bwd_dw_noalloc computes the same weight and bias gradients as
+ * tt_op_linear_bwd_dw in bf16 mode (tensor cores, deterministic split-K):
+ *   dW[N,K] = dy^T x (fp32, overwritten),  db[N] = column sums of dy (fp32,
+ *   overwritten; db may be NULL),  dy [M,N] and x [M,K] bf16 row-major,
+ *   16-byte aligned, N and K multiples of 8.
+ * It takes a stream (a cudaStream_t; NULL = legacy default stream) instead
+ * of a context and allocates nothing -- no cudaMalloc, no cudaFree, no
+ * allocating library routine.  Its scratch is one fixed array of
+ * TT_NOALLOC_SCRATCH_BYTES (32 MiB + 256 B) of device memory inside this
+ * library, held by every GPU that loads the library until the process exits:
+ * 256 B of device flags, TT_NOALLOC_SPLIT_FLOATS floats of split-K partial
+ * sums (always enough on GPUs with up to 192 SMs) and TT_NOALLOC_BIAS_FLOATS
+ * floats of bias partial sums.
+ * Returns TT_ERR_ARG for a NULL pointer, a non-positive size, operands the
+ * tensor-core path cannot take, or when db != NULL and the bias partial sums,
+ * ceil(M / 256) * N floats, exceed TT_NOALLOC_BIAS_FLOATS (for M = 32768 that
+ * allows N <= 16384); TT_ERR_CUDA if a CUDA call fails.  It returns before the
+ * GPU finishes; a device-side wait that times out leaves dW undefined and is
+ * not reported by this call.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture begins.  Every call shares the
+ * one array and it keeps the last call's contents: nothing in it needs to
+ * start at zero except the flags, which each call clears on its stream, since
+ * every scratch element a call reads is written earlier in that call.  Calls
+ * that overlap on the GPU (on different streams, or from threads without
+ * ordering between them) race on the array: issue them on one stream. */
+#define TT_NOALLOC_SPLIT_FLOATS 6291456u
+#define TT_NOALLOC_BIAS_FLOATS 2097152u
+#define TT_NOALLOC_SCRATCH_BYTES (256u + 4u * (TT_NOALLOC_SPLIT_FLOATS + TT_NOALLOC_BIAS_FLOATS))
+tt_status tt_linear_bwd_dw_noalloc(void* stream, const void* dy, const void* x, float* dW,
+                                   float* db, int M, int K, int N);
+
 #ifdef __cplusplus
 }
 #endif
