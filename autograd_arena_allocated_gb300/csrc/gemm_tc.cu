@@ -3,11 +3,13 @@
 // operands staged by TMA (cp.async.bulk.tensor, 128-byte swizzle) through an
 // mbarrier ring, accumulators read back with tcgen05.ld for a fused epilogue.
 //
-// Persistent, warp-specialised CTA (192 threads, one CTA per SM):
+// Persistent, warp-specialised CTA (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM allocator + MMA issuer (one elected lane)
-//   warps 2..5  epilogue: TMEM -> registers -> bias / GELU / GELU' /
-//               residual -> global (warp w reads TMEM lanes 32*(w%4)..+31)
+//   warps 2..9  epilogue: TMEM -> registers -> bias / GELU / GELU' /
+//               residual -> global.  Warp w reads TMEM lanes 32*(w%4)..+31;
+//               warps 2..5 take the left half of the tile's columns, 6..9
+//               the right half.
 // The accumulator is double-buffered in TMEM (2 x BN fp32 columns), so the
 // epilogue of tile i overlaps the main loop of tile i+1.
 //
@@ -32,7 +34,8 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one 128B-swizzle row
 constexpr int UMMA_K = 16;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
+constexpr int EPI_WARPS = 8;
 constexpr int MN_BOX = 64;                  // MN extent of one MN-major TMA box
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB: 64 k-rows x 128 bytes
 
@@ -189,13 +192,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// tanh by the hardware approximation (max relative error about 2^-11, far
+// below the bf16 rounding of the epilogue's outputs)
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float gelu_tanh(float u) {
     const float k = 0.7978845608028654f, a = 0.044715f;
-    return 0.5f * u * (1.0f + tanhf(k * (u + a * u * u * u)));
+    return 0.5f * u * (1.0f + tanh_hw(k * (u + a * u * u * u)));
 }
 __device__ __forceinline__ float dgelu_tanh(float u) {
     const float k = 0.7978845608028654f, a = 0.044715f;
-    float tau = tanhf(k * (u + a * u * u * u));
+    const float tau = tanh_hw(k * (u + a * u * u * u));
     return 0.5f * (1.0f + tau) + 0.5f * u * (1.0f - tau * tau) * k * (1.0f + 3.0f * a * u * u);
 }
 
@@ -276,7 +286,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4 * 32);
+            mbar_init(&tempty[a], EPI_WARPS * 32);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -385,7 +395,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     } else {
         // ---------------------------------------------------------- epilogue
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
+        constexpr int CHUNKS = BN / 32 / 2;  // 32-column chunks per half
         int acc = 0;
         uint32_t acc_phase = 0;
         const bool d_vec = p.d_f32 ? ((p.ldd & 3) == 0) : ((p.ldd & 7) == 0);
@@ -398,7 +410,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int m = m0 + row;
             const bool row_ok = m < p.M;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; c++) {
+            for (int c = half * CHUNKS; c < (half + 1) * CHUNKS; c++) {
                 uint32_t r[32];
                 __syncwarp();
                 tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);

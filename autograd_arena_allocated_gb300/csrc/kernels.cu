@@ -187,7 +187,9 @@ __global__ void k_embed_wpe(const T* __restrict__ dx, int B, int T_, int C, int 
     dwpe[i] = s;
 }
 
-size_t embed_bwd_scratch_bytes(int M) { return (size_t)4 * M * sizeof(int32_t) + 256; }
+size_t embed_bwd_scratch_bytes(int M, int C) {
+    return (size_t)4 * M * sizeof(int32_t) + 256 + embed_chunk_scratch_floats(M, C) * sizeof(float);
+}
 
 void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t* tok,
                       float* dwte, float* dwpe, int B, int T, int C, int V, int maxT,
@@ -207,14 +209,17 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
     L.count();
     k_sort_positions<<<1, SORT_THREADS, SORT_RADIX * SORT_THREADS * sizeof(int), L.stream>>>(
         tok, M, V, passes, s, s + M, s + 2 * M, s + 3 * M);
-    int threads = (C + 7) / 8;
-    threads = ((threads + 31) / 32) * 32;
-    L.count();
-    if (bf16)
-        k_embed_segsum<__nv_bfloat16><<<M, threads, 0, L.stream>>>(
-            (const __nv_bfloat16*)dx, s, s + M, M, C, V, dwte);
-    else
-        k_embed_segsum<float><<<M, threads, 0, L.stream>>>((const float*)dx, s, s + M, M, C, V, dwte);
+    float* chunk_scratch = (float*)((char*)scratch + (((size_t)4 * M * sizeof(int32_t) + 255) & ~(size_t)255));
+    if (!launch_embed_chunks(L, bf16, dx, s, s + M, M, C, V, dwte, chunk_scratch)) {
+        int threads = (C + 7) / 8;
+        threads = ((threads + 31) / 32) * 32;
+        L.count();
+        if (bf16)
+            k_embed_segsum<__nv_bfloat16><<<M, threads, 0, L.stream>>>(
+                (const __nv_bfloat16*)dx, s, s + M, M, C, V, dwte);
+        else
+            k_embed_segsum<float><<<M, threads, 0, L.stream>>>((const float*)dx, s, s + M, M, C, V, dwte);
+    }
     long long n = (long long)maxT * C;
     L.count();
     if (bf16)
@@ -263,6 +268,7 @@ __global__ void k_layernorm_fwd(const T* __restrict__ x, const T* __restrict__ w
 void launch_layernorm_fwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const void* b, void* y, float* mean, float* rstd, int M, int C) {
     if (L.dry) return;
+    if (bf16 && launch_ln_fwd_bf16(L, x, w, b, y, mean, rstd, M, C)) return;
     const int warps = 8;
     L.count();
     if (bf16)
@@ -351,13 +357,17 @@ __global__ void k_sum_partials(const float* __restrict__ part, int nblk, int C,
 }
 
 size_t layernorm_bwd_scratch_floats(int M, int C) {
-    return (size_t)((M + LN_ROWS - 1) / LN_ROWS) * 2 * C + 64;
+    size_t a = (size_t)((M + LN_ROWS - 1) / LN_ROWS) * 2 * C + 64;
+    size_t b = ln_bwd_bf16_scratch_floats(C);
+    return a > b ? a : b;
 }
 
 void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const float* mean, const float* rstd, const void* dy, void* dx,
                           float* dw, float* db, int M, int C, bool accumulate, float* scratch) {
     if (L.dry) return;
+    if (bf16 && launch_ln_bwd_bf16(L, x, w, mean, rstd, dy, dx, dw, db, M, C, accumulate, scratch))
+        return;
     const int nblk = (M + LN_ROWS - 1) / LN_ROWS;
     const size_t smem = (size_t)LN_BWD_WARPS * 2 * C * sizeof(float);
     static bool attr = false;
@@ -463,6 +473,13 @@ __global__ void k_mean_loss(const float* __restrict__ row_loss, int M, float* __
 void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* targets,
                  float* row_loss, float* mean_loss, int M, int V, int ld_, float dscale) {
     if (L.dry) return;
+    if (bf16 && launch_xent_bf16(L, logits, targets, row_loss, M, V, ld_, dscale)) {
+        if (mean_loss) {
+            L.count();
+            k_mean_loss<<<1, 1024, 0, L.stream>>>(row_loss, M, mean_loss, L.flags);
+        }
+        return;
+    }
     L.count();
     if (bf16)
         k_xent<__nv_bfloat16><<<M, XENT_THREADS, 0, L.stream>>>(
@@ -507,6 +524,11 @@ void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, floa
                    float* scratch) {
     if (L.dry) return;
     int nchunk = (M + COLSUM_ROWS - 1) / COLSUM_ROWS;
+    if (bf16 && launch_colsum_bf16(L, x, M, N, scratch)) {
+        L.count();
+        k_colsum_final<<<blocks_for(N, 256), 256, 0, L.stream>>>(scratch, nchunk, N, out);
+        return;
+    }
     dim3 grid(blocks_for(N, 128), nchunk);
     L.count();
     if (bf16)

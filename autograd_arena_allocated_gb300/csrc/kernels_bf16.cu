@@ -1,0 +1,495 @@
+// kernels_bf16.cu -- the memory-bound kernels of the bf16 step, written for
+// HBM bandwidth: 16-byte vector loads and stores (8 bf16), rows held in
+// registers between passes, grids sized from the SM count, and every
+// reduction in a fixed order (no floating-point atomics).
+//   LayerNorm forward / backward  (one warp per row)
+//   fused cross entropy           (one 1024-thread CTA per row, row in registers)
+//   column sums (bias gradients)  (8 columns per thread)
+//   embedding-gradient scatter    (fixed 64-row chunks of the token-sorted
+//                                  positions, then chunk partials in order)
+#include "tt_internal.h"
+
+#include <math.h>
+
+namespace tt {
+
+typedef __nv_bfloat16 bf16;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pk2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    return make_uint4(pk2(f[0], f[1]), pk2(f[2], f[3]), pk2(f[4], f[5]), pk2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float wsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ================================================================== LayerNorm
+constexpr int LNV_WARPS = 8;
+
+template <int NV>
+__global__ void __launch_bounds__(LNV_WARPS * 32)
+k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16* __restrict__ b,
+              bf16* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, int M, int C) {
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * LNV_WARPS + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const int nvec = C >> 3;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * C);
+    float v[NV][8];
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int vi = lane + 32 * i;
+        if (vi < nvec) {
+            unpack8(xr[vi], v[i]);
+#pragma unroll
+            for (int e = 0; e < 8; e++) s += v[i][e];
+        }
+    }
+    const float mu = wsum(s) / C;
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; i++)
+        if (lane + 32 * i < nvec)
+#pragma unroll
+            for (int e = 0; e < 8; e++) { const float d = v[i][e] - mu; q += d * d; }
+    const float rs = rsqrtf(wsum(q) / C + 1e-5f);
+    uint4* yr = reinterpret_cast<uint4*>(y + row * C);
+    const uint4* wr = reinterpret_cast<const uint4*>(w);
+    const uint4* br = reinterpret_cast<const uint4*>(b);
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int vi = lane + 32 * i;
+        if (vi < nvec) {
+            float wf[8], bfv[8], o[8];
+            unpack8(wr[vi], wf);
+            unpack8(br[vi], bfv);
+#pragma unroll
+            for (int e = 0; e < 8; e++) o[e] = (v[i][e] - mu) * rs * wf[e] + bfv[e];
+            yr[vi] = pack8(o);
+        }
+    }
+    if (lane == 0) { mean[row] = mu; rstd[row] = rs; }
+}
+
+// Backward: a fixed grid of G blocks; warp j of block g takes rows
+// g*8 + j, + 8G, + 16G, ...; each warp accumulates its dw/db partials in its
+// own slice of shared memory (each lane owns its columns: no atomics), the
+// block combines its warps in warp order, and k_ln_partials adds the G block
+// rows in block order.
+template <int NV>
+__global__ void __launch_bounds__(LNV_WARPS * 32, 2)
+k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
+              const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
+              float* __restrict__ part, int M, int C, int accumulate) {
+    extern __shared__ float s_part[];  // [LNV_WARPS][2C]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nvec = C >> 3;
+    float* pw = s_part + warp * 2 * C;
+    float* pb = pw + C;
+    float wv[NV][8];
+    const uint4* wr = reinterpret_cast<const uint4*>(w);
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int vi = lane + 32 * i;
+        if (vi < nvec) {
+            unpack8(wr[vi], wv[i]);
+#pragma unroll
+            for (int e = 0; e < 8; e++) { pw[vi * 8 + e] = 0.0f; pb[vi * 8 + e] = 0.0f; }
+        }
+    }
+    for (long long row = (long long)blockIdx.x * LNV_WARPS + warp; row < M;
+         row += (long long)gridDim.x * LNV_WARPS) {
+        const uint4* xr = reinterpret_cast<const uint4*>(x + row * C);
+        const uint4* dr = reinterpret_cast<const uint4*>(dy + row * C);
+        const float mu = mean[row], rs = rstd[row];
+        float xh[NV][8], g[NV][8];
+        float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
+                float xf[8], df[8];
+                unpack8(xr[vi], xf);
+                unpack8(dr[vi], df);
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    xh[i][e] = (xf[e] - mu) * rs;
+                    g[i][e] = df[e] * wv[i][e];
+                    sg += g[i][e];
+                    sgx += g[i][e] * xh[i][e];
+                    pw[vi * 8 + e] += df[e] * xh[i][e];
+                    pb[vi * 8 + e] += df[e];
+                }
+            }
+        }
+        const float mg = wsum(sg) / C, mgx = wsum(sgx) / C;
+        uint4* xo = reinterpret_cast<uint4*>(dx + row * C);
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) o[e] = rs * (g[i][e] - mg - xh[i][e] * mgx);
+                if (accumulate) {
+                    float old[8];
+                    unpack8(xo[vi], old);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) o[e] += old[e];
+                }
+                xo[vi] = pack8(o);
+            }
+        }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < LNV_WARPS; k++) s += s_part[k * 2 * C + c];
+        part[(long long)blockIdx.x * 2 * C + c] = s;
+    }
+}
+
+// out_a[c] = sum_g part[g][c], out_b[c] = sum_g part[g][C + c] in block order;
+__global__ void k_ln_partials(const float* __restrict__ part, int G, int C, float* __restrict__ out_a,
+                              float* __restrict__ out_b) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= 2 * C) return;
+    float s = 0.0f;
+    for (int g = 0; g < G; g++) s += part[(long long)g * 2 * C + c];
+    if (c < C) { if (out_a) out_a[c] = s; }
+    else if (out_b) out_b[c - C] = s;
+}
+
+constexpr int LN_BWD_MAX_BLOCKS = 1024;
+
+static int ln_bwd_blocks(const Launch& L, int M) {
+    int g = 2 * (L.num_sms > 0 ? L.num_sms : 148);
+    if (g > LN_BWD_MAX_BLOCKS) g = LN_BWD_MAX_BLOCKS;
+    const int need = (M + LNV_WARPS - 1) / LNV_WARPS;
+    return need < g ? need : g;
+}
+
+size_t ln_bwd_bf16_scratch_floats(int C) { return (size_t)LN_BWD_MAX_BLOCKS * 2 * C + 64; }
+
+bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const void* b, void* y,
+                        float* mean, float* rstd, int M, int C) {
+    if (C % 8 || C > 1024) return false;
+    if (L.dry) return true;
+    const unsigned grid = (unsigned)((M + LNV_WARPS - 1) / LNV_WARPS);
+    const int nv = (C / 8 + 31) / 32;
+    L.count();
+#define LNF(NV) k_ln_fwd_bf16<NV><<<grid, LNV_WARPS * 32, 0, L.stream>>>( \
+        (const bf16*)x, (const bf16*)w, (const bf16*)b, (bf16*)y, mean, rstd, M, C)
+    if (nv == 1) LNF(1); else if (nv == 2) LNF(2); else if (nv == 3) LNF(3); else LNF(4);
+#undef LNF
+    return true;
+}
+
+bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
+                        const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
+                        int C, bool accumulate, float* scratch) {
+    if (C % 8 || C > 1024) return false;
+    if (L.dry) return true;
+    const int G = ln_bwd_blocks(L, M);
+    const int nv = (C / 8 + 31) / 32;
+    const size_t smem = (size_t)LNV_WARPS * 2 * C * sizeof(float);
+    static bool attr = false;
+    if (!attr) {
+        const int mx = LNV_WARPS * 2 * 1024 * (int)sizeof(float);
+        cudaFuncSetAttribute(k_ln_bwd_bf16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        cudaFuncSetAttribute(k_ln_bwd_bf16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        cudaFuncSetAttribute(k_ln_bwd_bf16<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        cudaFuncSetAttribute(k_ln_bwd_bf16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        attr = true;
+    }
+    L.count();
+#define LNB(NV) k_ln_bwd_bf16<NV><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
+        (const bf16*)x, (const bf16*)w, mean, rstd, (const bf16*)dy, (bf16*)dx, scratch, M, C, \
+        accumulate ? 1 : 0)
+    if (nv == 1) LNB(1); else if (nv == 2) LNB(2); else if (nv == 3) LNB(3); else LNB(4);
+#undef LNB
+    L.count();
+    k_ln_partials<<<(2 * C + 255) / 256, 256, 0, L.stream>>>(scratch, G, C, dw, db);
+    return true;
+}
+
+// ================================================================== cross entropy
+constexpr float XV_LOG2E = 1.4426950408889634f;
+
+// One CTA per row, two passes over the row: pass 1 keeps a per-thread
+// online (max, sum of exp) over 8-value vectors; after the block combine,
+// pass 2 re-reads the row (it is still in L2) and overwrites it with the
+// gradient.  Few registers, so several rows are in flight per SM.
+constexpr int XS_THREADS = 512;
+
+__device__ __forceinline__ void online_merge2(float& m, float& s, float m2, float s2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) { m = m2; s = s2; return; }
+    if (m2 > m) { s = s * exp2f((m - m2) * XV_LOG2E) + s2; m = m2; }
+    else s += s2 * exp2f((m2 - m) * XV_LOG2E);
+}
+
+__global__ void __launch_bounds__(XS_THREADS)
+k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict__ row_loss,
+            int V, int ld, float dscale, int* flags) {
+    __shared__ float sm_m[XS_THREADS / 32], sm_s[XS_THREADS / 32];
+    const long long row = blockIdx.x;
+    uint4* zr = reinterpret_cast<uint4*>(z + row * (long long)ld);
+    const int nvec = ld >> 3;
+    const int vfull = V >> 3;  // vectors with all 8 columns < V
+    float m = -INFINITY, s = 0.0f;
+    for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
+        float f[8];
+        unpack8(zr[vi], f);
+        const int valid = vi < vfull ? 8 : max(0, V - vi * 8);
+        float m8 = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 8; e++)
+            if (e < valid) m8 = fmaxf(m8, f[e]);
+        if (valid == 0) continue;
+        if (m8 > m) {
+            s = (m == -INFINITY) ? 0.0f : s * exp2f((m - m8) * XV_LOG2E);
+            m = m8;
+        }
+        const float ml = m * XV_LOG2E;
+#pragma unroll
+        for (int e = 0; e < 8; e++)
+            if (e < valid) s += exp2f(f[e] * XV_LOG2E - ml);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        online_merge2(m, s, m2, s2);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) { sm_m[warp] = m; sm_s[warp] = s; }
+    __syncthreads();
+    float M_ = sm_m[0], S_ = sm_s[0];
+    for (int k = 1; k < XS_THREADS / 32; k++) online_merge2(M_, S_, sm_m[k], sm_s[k]);
+    const float lse = M_ + logf(S_);
+    const float lsel = lse * XV_LOG2E;  // in base-2 units
+    const int tgt = targets[row];
+    if (!(tgt >= 0 && tgt < V) && threadIdx.x == 0) {
+        atomicOr(&flags[FLAG_BAD_TOKEN], 1);
+        row_loss[row] = 0.0f;
+    }
+    for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
+        float f[8], o[8];
+        unpack8(zr[vi], f);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int col = vi * 8 + e;
+            float gval = 0.0f;
+            if (col < V) {
+                gval = exp2f(f[e] * XV_LOG2E - lsel);
+                if (col == tgt) {
+                    row_loss[row] = lse - f[e];
+                    gval -= 1.0f;
+                }
+                gval *= dscale;
+            }
+            o[e] = gval;
+        }
+        zr[vi] = pack8(o);
+    }
+}
+
+bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
+                      int V, int ld, float dscale) {
+    if (ld % 8 || ((uintptr_t)logits & 15) || ld < 2048) return false;
+    if (L.dry) return true;
+    L.count();
+    k_xent_bf16<<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
+                                                 L.flags);
+    return true;
+}
+
+// ================================================================== column sums
+constexpr int CS_ROWS = 256;  // rows per partial (the same chunking as the generic kernel)
+
+// block: 32 lanes x 8 columns = 256 columns, 8 warps split the 256 rows of
+// one partial (warp w takes rows w, w+8, ...); warps combine in warp order
+__global__ void __launch_bounds__(256)
+k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part) {
+    __shared__ float sm[8][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n8 = blockIdx.x * 256 + lane * 8;
+    const long long r0 = (long long)blockIdx.y * CS_ROWS;
+    const long long r1 = min((long long)M, r0 + CS_ROWS);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (n8 < N) {
+        for (long long r = r0 + warp; r < r1; r += 8) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4*>(x + r * N + n8), f);
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[e] += f[e];
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e++) sm[warp][lane * 8 + e] = acc[e];
+    __syncthreads();
+    const int col = blockIdx.x * 256 + threadIdx.x;
+    if (col < N) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; w++) t += sm[w][threadIdx.x];
+        part[(long long)blockIdx.y * N + col] = t;
+    }
+}
+
+bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part) {
+    if (N % 8 || ((uintptr_t)x & 15) || ((uintptr_t)part & 15)) return false;
+    if (L.dry) return true;
+    dim3 grid((N + 255) / 256, (M + CS_ROWS - 1) / CS_ROWS);
+    L.count();
+    k_colsum_bf16<<<grid, 256, 0, L.stream>>>((const bf16*)x, M, N, part);
+    return true;
+}
+
+// ================================================================== embedding gradient
+// After the stable sort, positions with equal token id form runs.  Chunk c
+// (sorted indices [64c, 64c+64)) sums each run piece it holds in sorted order:
+// a run wholly inside the chunk goes straight to dwte; the piece of a run
+// that began in an earlier chunk goes to first[c]; the piece of a run that
+// continues into the next chunk goes to last[c].  The chunk where such a run
+// begins then adds last[c] + first[c+1] + ... in chunk order.
+constexpr int EB_CHUNK = 64;
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* f);
+template <>
+__device__ __forceinline__ void load8<bf16>(const bf16* p, float* f) {
+    unpack8(*reinterpret_cast<const uint4*>(p), f);
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float* f) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void store8(float* p, const float* f) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+__device__ __forceinline__ void add8(float* p, const float* f) {
+    float4 a = reinterpret_cast<float4*>(p)[0], b = reinterpret_cast<float4*>(p)[1];
+    a.x += f[0]; a.y += f[1]; a.z += f[2]; a.w += f[3];
+    b.x += f[4]; b.y += f[5]; b.z += f[6]; b.w += f[7];
+    reinterpret_cast<float4*>(p)[0] = a;
+    reinterpret_cast<float4*>(p)[1] = b;
+}
+
+// thread t owns columns [8t, 8t+8)
+template <typename T>
+__global__ void k_embed_chunks(const T* __restrict__ dx, const int32_t* __restrict__ keys,
+                               const int32_t* __restrict__ vals, int M, int C, int V,
+                               float* __restrict__ dwte, float* __restrict__ first,
+                               float* __restrict__ last) {
+    const int c = blockIdx.x;
+    const int col = threadIdx.x * 8;
+    if (col >= C) return;
+    const int i0 = c * EB_CHUNK, i1 = min(M, i0 + EB_CHUNK);
+    const bool continues_in = i0 > 0 && keys[i0 - 1] == keys[i0];
+    const bool continues_out = i1 < M && keys[i1] == keys[i1 - 1];
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int run_key = keys[i0], run_start = i0;
+    for (int i = i0; i <= i1; i++) {
+        const int k = i < i1 ? keys[i] : -1;
+        if (k != run_key) {
+            // close the run piece [run_start, i)
+            if (run_key < V) {
+                const bool began_before = run_start == i0 && continues_in;
+                const bool goes_on = i == i1 && continues_out;
+                if (began_before) store8(first + (long long)c * C + col, acc);
+                else if (goes_on) store8(last + (long long)c * C + col, acc);
+                else add8(dwte + (long long)run_key * C + col, acc);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[e] = 0.0f;
+            run_key = k;
+            run_start = i;
+            if (i == i1) break;
+        }
+        if (k < V) {
+            float f[8];
+            load8(dx + (long long)vals[i] * C + col, f);
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[e] += f[e];
+        }
+    }
+}
+
+template <typename T>
+__global__ void k_embed_gather(const int32_t* __restrict__ keys, int M, int C, int V,
+                               float* __restrict__ dwte, const float* __restrict__ first,
+                               const float* __restrict__ last) {
+    const int c = blockIdx.x;
+    const int col = threadIdx.x * 8;
+    if (col >= C) return;
+    const int i0 = c * EB_CHUNK, i1 = min(M, i0 + EB_CHUNK);
+    if (!(i1 < M && keys[i1] == keys[i1 - 1])) return;  // last run does not continue
+    const int key = keys[i1 - 1];
+    if (key >= V) return;
+    // owner only if the run begins in this chunk
+    if (keys[i0] == key && i0 > 0 && keys[i0 - 1] == key) return;
+    float acc[8], f[8];
+    const float* p = last + (long long)c * C + col;
+#pragma unroll
+    for (int e = 0; e < 8; e++) acc[e] = p[e];
+    for (int cc = c + 1; cc * EB_CHUNK < M; cc++) {
+        const float* q = first + (long long)cc * C + col;
+#pragma unroll
+        for (int e = 0; e < 8; e++) f[e] = q[e];
+#pragma unroll
+        for (int e = 0; e < 8; e++) acc[e] += f[e];
+        const int j1 = min(M, (cc + 1) * EB_CHUNK);
+        if (!(j1 < M && keys[j1] == key)) break;  // the run ends in chunk cc
+    }
+    add8(dwte + (long long)key * C + col, acc);
+}
+
+size_t embed_chunk_scratch_floats(int M, int C) {
+    return (size_t)2 * ((M + EB_CHUNK - 1) / EB_CHUNK) * C + 64;
+}
+
+bool launch_embed_chunks(const Launch& L, bool is_bf16, const void* dx, const int32_t* keys,
+                         const int32_t* vals, int M, int C, int V, float* dwte, float* scratch) {
+    if (C % 8 || C > 8 * 1024) return false;
+    if (L.dry) return true;
+    const int nchunk = (M + EB_CHUNK - 1) / EB_CHUNK;
+    float* first = scratch;
+    float* last = scratch + (size_t)nchunk * C;
+    const int threads = ((C / 8 + 31) / 32) * 32;
+    L.count();
+    if (is_bf16)
+        k_embed_chunks<bf16><<<nchunk, threads, 0, L.stream>>>((const bf16*)dx, keys, vals, M, C, V,
+                                                               dwte, first, last);
+    else
+        k_embed_chunks<float><<<nchunk, threads, 0, L.stream>>>((const float*)dx, keys, vals, M, C, V,
+                                                                dwte, first, last);
+    L.count();
+    k_embed_gather<float><<<nchunk, threads, 0, L.stream>>>(keys, M, C, V, dwte, first, last);
+    return true;
+}
+
+}  // namespace tt

@@ -454,7 +454,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
         }
         if (!first_write(c, r.dwpe)) return fail(c, TT_ERR, "tape: position table used twice");
         size_t mark = c->off;
-        void* s = arena_alloc(c, embed_bwd_scratch_bytes(r.B * r.T));
+        void* s = arena_alloc(c, embed_bwd_scratch_bytes(r.B * r.T, r.N));
         ProfScope ps(c, PK_EMBED_BWD, 0.0,
                      (double)r.B * r.T * r.N * (esize(m.dtype) + 8.0) + 4.0 * r.maxT * r.N);
         if (!c->oom)
@@ -922,7 +922,11 @@ tt_status tt_op_attention_fwd(tt_ctx* c, tt_dtype dtype, const void* qkv, void* 
     if (!qkv || !y || !lse || B <= 0 || T <= 0 || H <= 0 || C % H) return fail(c, TT_ERR_ARG, "attention_fwd: bad arguments");
     const int hd = C / H;
     if (hd != 16 && hd != 32 && hd != 64) return fail(c, TT_ERR_ARG, "attention: head dim must be 16, 32 or 64");
-    launch_attention_fwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, B, T, C, H);
+    {
+        const double pairs = (double)B * H * T * (T + 1) / 2.0;
+        ProfScope ps(c, PK_ATTN_FWD, 4.0 * pairs * hd, 4.0 * B * T * C * (dtype == TT_BF16 ? 2 : 4));
+        launch_attention_fwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, B, T, C, H);
+    }
     return op_epilogue(c, "attention_fwd");
 }
 
@@ -937,7 +941,11 @@ tt_status tt_op_attention_bwd(tt_ctx* c, tt_dtype dtype, const void* qkv, const 
     c->oom = false;
     size_t mark = c->off;
     float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(B, T, H) * 4);
-    if (!c->oom) launch_attention_bwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, dy, dqkv, B, T, C, H, s);
+    if (!c->oom) {
+        const double pairs = (double)B * H * T * (T + 1) / 2.0;
+        ProfScope ps(c, PK_ATTN_BWD, 10.0 * pairs * hd, 8.0 * B * T * C * (dtype == TT_BF16 ? 2 : 4));
+        launch_attention_bwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, dy, dqkv, B, T, C, H, s);
+    }
     c->off = mark;
     return op_epilogue(c, "attention_bwd");
 }
@@ -947,7 +955,10 @@ tt_status tt_op_layernorm_fwd(tt_ctx* c, tt_dtype dtype, const void* x, const vo
     TT_OP_PROLOGUE();
     if (!x || !w || !b || !y || !mean || !rstd || M <= 0 || C <= 0 || C % 32 || C > 1024)
         return fail(c, TT_ERR_ARG, "layernorm_fwd: bad arguments");
-    launch_layernorm_fwd(launch_of(c), dtype == TT_BF16, x, w, b, y, mean, rstd, M, C);
+    {
+        ProfScope ps(c, PK_LN_FWD, 0.0, 2.0 * M * C * (dtype == TT_BF16 ? 2 : 4) + 8.0 * M);
+        launch_layernorm_fwd(launch_of(c), dtype == TT_BF16, x, w, b, y, mean, rstd, M, C);
+    }
     return op_epilogue(c, "layernorm_fwd");
 }
 
@@ -960,9 +971,11 @@ tt_status tt_op_layernorm_bwd(tt_ctx* c, tt_dtype dtype, const void* x, const vo
     c->oom = false;
     size_t mark = c->off;
     float* s = (float*)arena_alloc(c, layernorm_bwd_scratch_floats(M, C) * 4);
-    if (!c->oom)
+    if (!c->oom) {
+        ProfScope ps(c, PK_LN_BWD, 0.0, (accumulate ? 4.0 : 3.0) * M * C * (dtype == TT_BF16 ? 2 : 4) + 8.0 * M);
         launch_layernorm_bwd(launch_of(c), dtype == TT_BF16, x, w, mean, rstd, dy, dx, dw, db, M, C,
                              accumulate != 0, s);
+    }
     c->off = mark;
     return op_epilogue(c, "layernorm_bwd");
 }
@@ -972,7 +985,10 @@ tt_status tt_op_xent(tt_ctx* c, tt_dtype dtype, void* logits, const int32_t* tar
     TT_OP_PROLOGUE();
     if (!logits || !targets || !row_loss || M <= 0 || V <= 0 || ld < V)
         return fail(c, TT_ERR_ARG, "xent: bad arguments");
-    launch_xent(launch_of(c), dtype == TT_BF16, logits, targets, row_loss, mean_loss, M, V, ld, dscale);
+    {
+        ProfScope ps(c, PK_XENT, 0.0, 2.0 * M * ld * (dtype == TT_BF16 ? 2 : 4) + 8.0 * M);
+        launch_xent(launch_of(c), dtype == TT_BF16, logits, targets, row_loss, mean_loss, M, V, ld, dscale);
+    }
     return op_epilogue(c, "xent");
 }
 
@@ -993,8 +1009,11 @@ tt_status tt_op_embed_bwd(tt_ctx* c, tt_dtype dtype, const void* dx, const int32
         return fail(c, TT_ERR_ARG, "embed_bwd: bad arguments");
     c->oom = false;
     size_t mark = c->off;
-    void* s = arena_alloc(c, embed_bwd_scratch_bytes(B * T));
-    if (!c->oom) launch_embed_bwd(launch_of(c), dtype == TT_BF16, dx, tokens, dwte, dwpe, B, T, C, V, maxT, s);
+    void* s = arena_alloc(c, embed_bwd_scratch_bytes(B * T, C));
+    if (!c->oom) {
+        ProfScope ps(c, PK_EMBED_BWD, 0.0, (double)B * T * C * ((dtype == TT_BF16 ? 2 : 4) + 8.0) + 4.0 * maxT * C);
+        launch_embed_bwd(launch_of(c), dtype == TT_BF16, dx, tokens, dwte, dwpe, B, T, C, V, maxT, s);
+    }
     c->off = mark;
     return op_epilogue(c, "embed_bwd");
 }

@@ -79,8 +79,8 @@ void gemm_simt_launch(const Launch& L, const GemmArgs& g);
 // ------------------------------------------------------------ other kernels
 void launch_embed_fwd(const Launch& L, bool bf16, const void* wte, const void* wpe,
                       const int32_t* tok, void* x, int B, int T, int C, int V);
-// scratch: int32 [4*M + 2] for the stable sort of positions by token id
-size_t embed_bwd_scratch_bytes(int M);
+// scratch: the stable sort of positions by token id plus chunk partial sums
+size_t embed_bwd_scratch_bytes(int M, int C);
 void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t* tok,
                       float* dwte, float* dwpe, int B, int T, int C, int V, int maxT,
                       void* scratch);
@@ -110,6 +110,20 @@ void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, 
 void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const void* y,
                           const float* lse, const void* dy, void* dqkv, int B, int T, int C,
                           int H, float* scratch);
+// bandwidth-oriented bf16 kernels (kernels_bf16.cu); false = shape not taken
+bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const void* b, void* y,
+                        float* mean, float* rstd, int M, int C);
+bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
+                        const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
+                        int C, bool accumulate, float* scratch);
+size_t ln_bwd_bf16_scratch_floats(int C);
+bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
+                      int V, int ld, float dscale);
+bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part);
+size_t embed_chunk_scratch_floats(int M, int C);
+bool launch_embed_chunks(const Launch& L, bool bf16, const void* dx, const int32_t* keys,
+                         const int32_t* vals, int M, int C, int V, float* dwte, float* scratch);
+
 bool attention_mma_eligible(bool bf16, int C, int H);
 void launch_attention_fwd_mma(const Launch& L, const void* qkv, void* y, float* lse,
                               int B, int T, int C, int H);

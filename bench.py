@@ -193,6 +193,129 @@ def cpu_baseline(w, tokens_target=64):
                       f"architecture on B=1, T={tokens_target}, double precision; {dt:.1f} s"}
 
 
+# ------------------------------------------------------------------ single-op mode
+OP_SHAPES = {
+    # name: (description, shape) at the 124M workload's sizes (M = B*T = 32768 tokens)
+    "gemm_fwd": "FC forward: x[32768,768] W[3072,768]^T + b, GELU epilogue",
+    "gemm_dx": "FC-proj input gradient: dy[32768,768] W[768,3072], GELU' epilogue",
+    "gemm_dw": "FC weight gradient: dy[32768,3072]^T x[32768,768] (fp32 out)",
+    "gemm_lm": "tied LM head: hf[32768,768] wte[50257,768]^T -> logits[32768,50304]",
+    "attn_fwd": "causal attention forward, B=32 T=1024 H=12 hd=64",
+    "attn_bwd": "causal attention backward, B=32 T=1024 H=12 hd=64",
+    "ln_fwd": "LayerNorm forward [32768,768]",
+    "ln_bwd": "LayerNorm backward [32768,768], accumulating dx",
+    "xent": "fused cross entropy over [32768,50304] logits",
+    "embed_bwd": "embedding-gradient scatter, 32768 Zipf tokens, C=768",
+    "adamw": "AdamW over 124,439,808 parameters",
+}
+
+
+def run_op(args):
+    """Runs one kernel group `--reps` times through the C ABI (for profiling)."""
+    import torch
+
+    from autograd_arena_allocated_gb300 import api, synth
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    dev = "cuda"
+    bf = torch.bfloat16
+    M, C, V, Vp, B, T, H = 32768, 768, 50257, 50304, 32, 1024, 12
+
+    def rnd(*shape, dtype=bf, scale=1.0):
+        g = torch.Generator(device=dev).manual_seed(0)
+        return (torch.randn(*shape, device=dev, generator=g) * scale).to(dtype)
+
+    ctx = api.Context(8 << 30)
+    op = args.op
+    if op == "gemm_fwd":
+        x, W, b = rnd(M, C), rnd(4 * C, C, scale=0.02), rnd(4 * C)
+        y, pre = torch.empty(M, 4 * C, device=dev, dtype=bf), torch.empty(M, 4 * C, device=dev, dtype=bf)
+        fn = lambda: ctx.linear_fwd("bf16", x, W, b, None, y, pre, M, C, 4 * C, gelu=True)
+        flops = 2.0 * M * C * 4 * C
+    elif op == "gemm_dx":
+        dy, W, pre = rnd(M, C), rnd(C, 4 * C, scale=0.02), rnd(M, 4 * C)
+        dx = torch.empty(M, 4 * C, device=dev, dtype=bf)
+        fn = lambda: ctx.linear_bwd_dx("bf16", dy, W, pre, dx, M, 4 * C, C)
+        flops = 2.0 * M * C * 4 * C
+    elif op == "gemm_dw":
+        dy, x = rnd(M, 4 * C), rnd(M, C)
+        dW = torch.empty(4 * C, C, device=dev)
+        fn = lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", dy, x, dW, None, M, C, 4 * C))
+        flops = 2.0 * M * C * 4 * C
+    elif op == "gemm_lm":
+        x, W = rnd(M, C), rnd(V, C, scale=0.02)
+        y = torch.empty(M, Vp, device=dev, dtype=bf)
+        from autograd_arena_allocated_gb300._native import lib
+        fn = lambda: ctx.linear_fwd("bf16", x, W, None, None, y, None, M, C, Vp)
+        flops = 2.0 * M * C * Vp
+    elif op in ("attn_fwd", "attn_bwd"):
+        qkv, dy = rnd(M, 3 * C), rnd(M, C)
+        y = torch.empty(M, C, device=dev, dtype=bf)
+        lse = torch.empty(B, H, T, device=dev)
+        dqkv = torch.empty_like(qkv)
+        ctx.attention_fwd("bf16", qkv, y, lse, B, T, C, H)
+        pairs = B * H * T * (T + 1) / 2
+        if op == "attn_fwd":
+            fn = lambda: ctx.attention_fwd("bf16", qkv, y, lse, B, T, C, H)
+            flops = 4.0 * pairs * 64
+        else:
+            fn = lambda: (ctx.reset(), ctx.attention_bwd("bf16", qkv, y, lse, dy, dqkv, B, T, C, H))
+            flops = 10.0 * pairs * 64
+    elif op in ("ln_fwd", "ln_bwd"):
+        x, w, b, dy = rnd(M, C), rnd(C), rnd(C), rnd(M, C)
+        y, dx = torch.empty_like(x), rnd(M, C)
+        mean, rstd = torch.empty(M, device=dev), torch.empty(M, device=dev)
+        dw, db = torch.empty(C, device=dev), torch.empty(C, device=dev)
+        ctx.layernorm_fwd("bf16", x, w, b, y, mean, rstd, M, C)
+        if op == "ln_fwd":
+            fn = lambda: ctx.layernorm_fwd("bf16", x, w, b, y, mean, rstd, M, C)
+        else:
+            fn = lambda: (ctx.reset(), ctx.layernorm_bwd("bf16", x, w, mean, rstd, dy, dx, dw, db, M, C,
+                                                         accumulate=True))
+        flops = 0.0
+    elif op == "xent":
+        z = rnd(M, Vp)
+        tok, tgt = synth.token_stream(B, T, V, "zipf")
+        td = torch.from_numpy(tgt.reshape(-1)).to(dev)
+        rl, ml = torch.empty(M, device=dev), torch.empty(1, device=dev)
+        fn = lambda: ctx.xent("bf16", z, td, rl, ml, M, V, Vp, 1.0 / M)
+        flops = 0.0
+    elif op == "embed_bwd":
+        dx = rnd(M, C)
+        tok, _ = synth.token_stream(B, T, V, "zipf")
+        td = torch.from_numpy(tok.reshape(-1)).to(dev)
+        dwte, dwpe = torch.zeros(V, C, device=dev), torch.empty(T, C, device=dev)
+        fn = lambda: (ctx.reset(), ctx.embed_bwd("bf16", dx, td, dwte, dwpe, B, T, C, V, T))
+        flops = 0.0
+    elif op == "adamw":
+        n = 124_439_808
+        p_, g_, m_, v_ = (torch.zeros(n, device=dev) for _ in range(4))
+        low = torch.empty(n, device=dev, dtype=bf)
+        fn = lambda: ctx.adamw(p_, low, g_, m_, v_, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+        flops = 0.0
+    else:
+        raise SystemExit(f"unknown op {op}; choose from {sorted(OP_SHAPES)}")
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ctx.set_profiling(True)
+    for _ in range(args.reps):
+        fn()
+    prof = ctx.profile()
+    ctx.set_profiling(False)
+    out = {"op": op, "what": OP_SHAPES[op], "reps": args.reps, "groups": {}}
+    for k, r in prof.items():
+        per = r["ms"] / r["calls"]
+        out["groups"][k] = {"ms_per_call": per, "calls": r["calls"],
+                            "tflops": r["flops"] / r["calls"] / (per * 1e-3) / 1e12,
+                            "gbps": r["bytes"] / r["calls"] / (per * 1e-3) / 1e9}
+    print(json.dumps(out), flush=True)
+    ctx.close()
+    return 0
+
+
 # ------------------------------------------------------------------ our arm
 def main():
     ap = argparse.ArgumentParser()
@@ -204,7 +327,12 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default=None, help="run one kernel group: " + ", ".join(OP_SHAPES))
+    ap.add_argument("--reps", type=int, default=5)
     args = ap.parse_args()
+    if args.op:
+        args.warmup = max(1, args.warmup)
+        return run_op(args)
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     world, rank, local = dist_setup()
 

@@ -218,7 +218,10 @@ def _sampled_sequences(ctx, oracle, w, seqs):
         err = np.abs(rl_gpu[b] - rl)
         print(f"[{w.name}] sequence {b}: per-position loss max abs err {np.max(err):.2e}, "
               f"mean abs err {np.mean(err):.2e} (mean loss {np.mean(rl):.4f})")
-        assert np.max(err) <= 2e-2 and np.mean(err) <= 2e-3 * np.mean(rl), (b, np.max(err))
+        # the spec's bf16 loss bound (2e-3 relative) on the sequence's mean loss;
+        # single positions within 5e-3 relative
+        assert abs(np.mean(rl_gpu[b]) - np.mean(rl)) <= 2e-3 * np.mean(rl)
+        assert np.max(err) <= 5e-3 * np.mean(rl) and np.mean(err) <= 2e-3 * np.mean(rl), (b, np.max(err))
     g = run.grads.clone()
     big.close()
     return g
