@@ -31,7 +31,8 @@ def sources():
 
 
 def _deps_mtime():
-    files = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    files = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                         if f.endswith(".h") or f.endswith(".cuh")]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return max(os.path.getmtime(f) for f in files)
 

@@ -868,6 +868,7 @@ static void attn_bwd_simt(const Launch& L, const void* qkv, const void* y, const
 void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, float* lse,
                           int B, int T, int C, int H) {
     if (L.dry) return;
+    if (attention_tc_eligible(bf16, C, H) && launch_attention_fwd_tc(L, qkv, y, lse, B, T, C, H)) return;
     if (attention_mma_eligible(bf16, C, H)) {
         launch_attention_fwd_mma(L, qkv, y, lse, B, T, C, H);
         return;
@@ -880,6 +881,9 @@ void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const voi
                           const float* lse, const void* dy, void* dqkv, int B, int T, int C,
                           int H, float* scratch) {
     if (L.dry) return;
+    if (attention_tc_eligible(bf16, C, H) &&
+        launch_attention_bwd_tc(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch))
+        return;
     if (attention_mma_eligible(bf16, C, H)) {
         launch_attention_bwd_mma(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch);
         return;

@@ -124,6 +124,13 @@ size_t embed_chunk_scratch_floats(int M, int C);
 bool launch_embed_chunks(const Launch& L, bool bf16, const void* dx, const int32_t* keys,
                          const int32_t* vals, int M, int C, int V, float* dwte, float* scratch);
 
+// tcgen05 attention (attn_tc.cu); false = not taken (then the mma.sync path runs)
+bool attention_tc_eligible(bool bf16, int C, int H);
+bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T,
+                             int C, int H);
+bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
+                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt);
+
 bool attention_mma_eligible(bool bf16, int C, int H);
 void launch_attention_fwd_mma(const Launch& L, const void* qkv, void* y, float* lse,
                               int B, int T, int C, int H);
