@@ -27,6 +27,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cstring>
 #include <mutex>
 
 namespace tt {
@@ -47,13 +48,15 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int BAR_BYTES = 1024;                 // barriers, padded to keep staging aligned
+    static constexpr int STAGING_BYTES = EPI_WARPS * 2 * 2048;  // 2 x [32 rows x 64 B] per epilogue warp
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + STAGING_BYTES + 1024;
 };
 
 struct Params {
     int M, N, K;
     int m_tiles, n_tiles, tiles;
+    int n_fast;  // tile order: n-tiles fastest (B stays in L2, A streams once) or m-tiles fastest
     int kb_total, kb_per_split, splits, units;
     void* D;
     long long ldd;
@@ -63,6 +66,7 @@ struct Params {
     __nv_bfloat16* aux;
     float* ws;  // split-K partials [splits][M][N]
     int* flags;
+    int tma_store;  // bf16 outputs leave through shared memory and TMA stores
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -88,6 +92,35 @@ __device__ __forceinline__ float dgelu_tanh(float u) {
     const float tau = tanh_hw(k * (u + a * u * u * u));
     return 0.5f * (1.0f + tau) + 0.5f * u * (1.0f - tau * tau) * k * (1.0f + 3.0f * a * u * u);
 }
+
+// One warp's 32 x 32 bf16 staging tile (row = lane, 64 bytes per row) in the
+// layout of a TMA SWIZZLE_64B box: the 16-byte chunk c of row r sits at
+// c ^ ((r >> 1) & 3).  Row writes from the 32 lanes are bank-conflict free.
+__device__ __forceinline__ void stage_row32(uint8_t* buf, int r, const float* v) {
+    uint8_t* rowp = buf + r * 64;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        uint4 w;
+        w.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
+        w.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
+        w.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
+        w.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4)) = w;
+    }
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     (uint64_t)map),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Load 32 consecutive bf16 (64 bytes) as floats; vector path when aligned.
 __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, int valid, bool vec, float* v) {
@@ -138,10 +171,14 @@ __device__ __forceinline__ void store32_f32(float* p, int valid, bool vec, const
     }
 }
 
+__device__ __forceinline__ int tile_m(const Params& p, int t) { return p.n_fast ? t / p.n_tiles : t % p.m_tiles; }
+__device__ __forceinline__ int tile_n(const Params& p, int t) { return p.n_fast ? t % p.n_tiles : t / p.m_tiles; }
+
 // ------------------------------------------------------------------ the kernel
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
           const Params p) {
     using CF = Cfg<BN>;
     constexpr int S = CF::STAGES;
@@ -172,6 +209,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+        if (p.tma_store) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmD) : "memory");
+            if (p.epi == EPI_GELU) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
+        }
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -193,8 +234,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             bool ok = true;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 const int tile = u / p.splits, split = u - tile * p.splits;
-                const int m0 = (tile % p.m_tiles) * BM;
-                const int n0 = (tile / p.m_tiles) * BN;
+                const int m0 = tile_m(p, tile) * BM;
+                const int n0 = tile_n(p, tile) * BN;
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 for (int kb = kb0; kb < kb1; kb++) {
@@ -281,10 +322,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         int acc = 0;
         uint32_t acc_phase = 0;
         const bool d_vec = p.d_f32 ? ((p.ldd & 3) == 0) : ((p.ldd & 7) == 0);
+        uint8_t* stg = smem + S * CF::STAGE_BYTES + CF::BAR_BYTES + (warp - 2) * 2 * 2048;
+        int sbuf = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const int tile = u / p.splits, split = u - tile * p.splits;
-            const int m0 = (tile % p.m_tiles) * BM;
-            const int n0 = (tile / p.m_tiles) * BN;
+            const int m0 = tile_m(p, tile) * BM;
+            const int n0 = tile_n(p, tile) * BN;
             if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.flags)) break;
             tc_fence_after();
             const int m = m0 + row;
@@ -296,7 +339,59 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
                 const int n = n0 + c * 32;
                 const int valid = min(32, p.n_store - n);
-                if (!row_ok || valid <= 0) continue;
+                if (valid <= 0) continue;  // uniform across the warp
+                if (p.tma_store) {
+                    // bf16 result through shared memory and TMA; rows >= M and
+                    // columns >= n_store are clipped by the tensor map
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+                    const long long o = (long long)m * p.ldd + n;
+                    if (p.bias) {
+                        float b[32];
+                        load32_bf16(p.bias + n, valid, true, b);
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] += b[j];
+                    }
+                    const bool gelu = p.epi == EPI_GELU;
+                    if (lane == 0) {
+                        if (gelu) bulk_wait_read<0>(); else bulk_wait_read<1>();
+                    }
+                    __syncwarp();
+                    if (gelu) {
+                        stage_row32(stg, lane, v);  // pre-activation
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] = gelu_tanh(v[j]);
+                    } else if (p.epi == EPI_DGELU) {
+                        float u_[32];
+                        if (row_ok) load32_bf16(p.aux + o, valid, d_vec, u_);
+                        else {
+#pragma unroll
+                            for (int j = 0; j < 32; j++) u_[j] = 0.0f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(u_[j]);
+                    }
+                    if (p.residual && row_ok) {
+                        float rr[32];
+                        load32_bf16(p.residual + o, valid, d_vec, rr);
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] += rr[j];
+                    }
+                    uint8_t* dbuf = gelu ? stg + 2048 : stg + sbuf * 2048;
+                    stage_row32(dbuf, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int y = m0 + quarter * 32;
+                        if (gelu) tma_store_2d(&tmX, smem_u32(stg), n, y);
+                        tma_store_2d(&tmD, smem_u32(dbuf), n, y);
+                        bulk_commit();
+                    }
+                    sbuf ^= 1;
+                    continue;
+                }
+                if (!row_ok) continue;
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
@@ -351,6 +446,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_arrive(&tempty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        if (p.tma_store && lane == 0) bulk_wait_all();  // staged stores done before exit
     }
 
     tc_fence_before();
@@ -395,7 +491,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, long long inner, long lo
 
 // 2-D bf16 map: inner extent, outer extent, row pitch in elements, box.
 static bool make_map(CUtensorMap* map, const void* base, long long inner, long long outer,
-                     long long pitch, int box_inner, int box_outer) {
+                     long long pitch, int box_inner, int box_outer,
+                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
@@ -403,7 +500,7 @@ static bool make_map(CUtensorMap* map, const void* base, long long inner, long l
     cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -429,6 +526,11 @@ static Plan make_plan(const Launch& L, const GemmArgs& g) {
     p.m_tiles = (g.M + BM - 1) / BM;
     p.n_tiles = (g.N + pl.BN - 1) / pl.BN;
     p.tiles = p.m_tiles * p.n_tiles;
+    // consecutive CTAs share the B operand's tiles when n is fastest; that is the
+    // better order whenever B (the weight, for the forward and input-gradient
+    // forms) is small next to the 129 MB L2, since A is then read from DRAM once
+    const double b_bytes = 2.0 * (double)g.N * (double)g.K;
+    p.n_fast = (b_bytes <= 24.0 * 1024 * 1024) ? 1 : 0;
     p.kb_total = (g.K + BK - 1) / BK;
     p.splits = 1;
     const int sms = L.num_sms > 0 ? L.num_sms : 148;
@@ -479,7 +581,7 @@ size_t gemm_tc_workspace_floats(const Launch& L, const GemmArgs& g) {
 
 template <int BN, bool A_MN, bool B_MN>
 static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma,
-                      const CUtensorMap& mb) {
+                      const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& mx) {
     auto kern = tc::k_gemm_tc<BN, A_MN, B_MN>;
     static bool attr_done = false;  // one flag per instantiation
     if (!attr_done) {
@@ -489,7 +591,7 @@ static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma
         attr_done = true;
     }
     L.count();
-    kern<<<pl.grid, tc::THREADS, tc::Cfg<BN>::SMEM_BYTES, L.stream>>>(ma, mb, pl.p);
+    kern<<<pl.grid, tc::THREADS, tc::Cfg<BN>::SMEM_BYTES, L.stream>>>(ma, mb, md, mx, pl.p);
     return true;
 }
 
@@ -513,15 +615,28 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
     if (!b_mn) ok = tc::make_map(&mb, g.B, kval, b_rows, g.ldb, tc::BK, pl.BN);
     else ok = tc::make_map(&mb, g.B, b_rows, kval, g.ldb, tc::MN_BOX, tc::BK);
     if (!ok) return false;
+    // bf16 outputs: TMA stores (box 32 x 32, 64-byte swizzle) when the rows allow
+    CUtensorMap md, mx;
+    memset(&md, 0, sizeof md);
+    memset(&mx, 0, sizeof mx);
+    pl.p.tma_store = 0;
+    if (!g.d_f32 && !g.accumulate && (g.ldd % 8) == 0 && ((uintptr_t)g.D & 15) == 0 &&
+        (g.epi != EPI_GELU || ((uintptr_t)g.aux & 15) == 0)) {
+        const int ns = g.n_store ? g.n_store : g.N;
+        bool ok2 = tc::make_map(&md, g.D, ns, g.M, g.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (ok2 && g.epi == EPI_GELU)
+            ok2 = tc::make_map(&mx, g.aux, ns, g.M, g.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+        pl.p.tma_store = ok2 ? 1 : 0;
+    }
     bool launched;
     if (pl.BN == 256) {
-        if (!a_mn && !b_mn) launched = launch_tc<256, false, false>(L, pl, ma, mb);
-        else if (!a_mn) launched = launch_tc<256, false, true>(L, pl, ma, mb);
-        else launched = launch_tc<256, true, true>(L, pl, ma, mb);
+        if (!a_mn && !b_mn) launched = launch_tc<256, false, false>(L, pl, ma, mb, md, mx);
+        else if (!a_mn) launched = launch_tc<256, false, true>(L, pl, ma, mb, md, mx);
+        else launched = launch_tc<256, true, true>(L, pl, ma, mb, md, mx);
     } else {
-        if (!a_mn && !b_mn) launched = launch_tc<128, false, false>(L, pl, ma, mb);
-        else if (!a_mn) launched = launch_tc<128, false, true>(L, pl, ma, mb);
-        else launched = launch_tc<128, true, true>(L, pl, ma, mb);
+        if (!a_mn && !b_mn) launched = launch_tc<128, false, false>(L, pl, ma, mb, md, mx);
+        else if (!a_mn) launched = launch_tc<128, false, true>(L, pl, ma, mb, md, mx);
+        else launched = launch_tc<128, true, true>(L, pl, ma, mb, md, mx);
     }
     if (!launched) return false;
     if (pl.p.splits > 1) {

@@ -525,8 +525,7 @@ void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, floa
     if (L.dry) return;
     int nchunk = (M + COLSUM_ROWS - 1) / COLSUM_ROWS;
     if (bf16 && launch_colsum_bf16(L, x, M, N, scratch)) {
-        L.count();
-        k_colsum_final<<<blocks_for(N, 256), 256, 0, L.stream>>>(scratch, nchunk, N, out);
+        launch_sum_rows(L, scratch, nchunk, N, N, out, nullptr);
         return;
     }
     dim3 grid(blocks_for(N, 128), nchunk);

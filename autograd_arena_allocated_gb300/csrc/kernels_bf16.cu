@@ -94,63 +94,82 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
 // block combines its warps in warp order, and k_ln_partials adds the G block
 // rows in block order.
 template <int NV>
-__global__ void __launch_bounds__(LNV_WARPS * 32, 2)
+__global__ void __launch_bounds__(LNV_WARPS * 32, 3)
 k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
               const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
               float* __restrict__ part, int M, int C, int accumulate) {
-    extern __shared__ float s_part[];  // [LNV_WARPS][2C]
+    extern __shared__ float s_part[];  // [LNV_WARPS][2C] per-warp dw/db partials, then w
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvec = C >> 3;
     float* pw = s_part + warp * 2 * C;
     float* pb = pw + C;
-    float wv[NV][8];
-    const uint4* wr = reinterpret_cast<const uint4*>(w);
+    float* sw = s_part + LNV_WARPS * 2 * C;  // gamma as floats
+    for (int c = threadIdx.x; c < C; c += blockDim.x) sw[c] = __bfloat162float(w[c]);
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int vi = lane + 32 * i;
-        if (vi < nvec) {
-            unpack8(wr[vi], wv[i]);
+        if (vi < nvec)
 #pragma unroll
             for (int e = 0; e < 8; e++) { pw[vi * 8 + e] = 0.0f; pb[vi * 8 + e] = 0.0f; }
-        }
     }
+    __syncthreads();
     for (long long row = (long long)blockIdx.x * LNV_WARPS + warp; row < M;
          row += (long long)gridDim.x * LNV_WARPS) {
         const uint4* xr = reinterpret_cast<const uint4*>(x + row * C);
         const uint4* dr = reinterpret_cast<const uint4*>(dy + row * C);
         const float mu = mean[row], rs = rstd[row];
-        float xh[NV][8], g[NV][8];
+        // pass 1: the two row sums, and this row's dw/db contributions
+        uint4 xv[NV], dv[NV];
         float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) { xv[i] = xr[vi]; dv[i] = dr[vi]; }
+        }
 #pragma unroll
         for (int i = 0; i < NV; i++) {
             const int vi = lane + 32 * i;
             if (vi < nvec) {
                 float xf[8], df[8];
-                unpack8(xr[vi], xf);
-                unpack8(dr[vi], df);
+                unpack8(xv[i], xf);
+                unpack8(dv[i], df);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
-                    xh[i][e] = (xf[e] - mu) * rs;
-                    g[i][e] = df[e] * wv[i][e];
-                    sg += g[i][e];
-                    sgx += g[i][e] * xh[i][e];
-                    pw[vi * 8 + e] += df[e] * xh[i][e];
+                    const float xh = (xf[e] - mu) * rs;
+                    const float g = df[e] * sw[vi * 8 + e];
+                    sg += g;
+                    sgx += g * xh;
+                    pw[vi * 8 + e] += df[e] * xh;
                     pb[vi * 8 + e] += df[e];
                 }
             }
         }
         const float mg = wsum(sg) / C, mgx = wsum(sgx) / C;
+        // pass 2: dx from the same registers
         uint4* xo = reinterpret_cast<uint4*>(dx + row * C);
+        uint4 ov[NV];
+        if (accumulate) {
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                const int vi = lane + 32 * i;
+                if (vi < nvec) ov[i] = xo[vi];
+            }
+        }
 #pragma unroll
         for (int i = 0; i < NV; i++) {
             const int vi = lane + 32 * i;
             if (vi < nvec) {
-                float o[8];
+                float xf[8], df[8], o[8];
+                unpack8(xv[i], xf);
+                unpack8(dv[i], df);
 #pragma unroll
-                for (int e = 0; e < 8; e++) o[e] = rs * (g[i][e] - mg - xh[i][e] * mgx);
+                for (int e = 0; e < 8; e++) {
+                    const float xh = (xf[e] - mu) * rs;
+                    o[e] = rs * (df[e] * sw[vi * 8 + e] - mg - xh * mgx);
+                }
                 if (accumulate) {
                     float old[8];
-                    unpack8(xo[vi], old);
+                    unpack8(ov[i], old);
 #pragma unroll
                     for (int e = 0; e < 8; e++) o[e] += old[e];
                 }
@@ -167,21 +186,41 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
     }
 }
 
-// out_a[c] = sum_g part[g][c], out_b[c] = sum_g part[g][C + c] in block order;
-__global__ void k_ln_partials(const float* __restrict__ part, int G, int C, float* __restrict__ out_a,
-                              float* __restrict__ out_b) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= 2 * C) return;
+// out[c] = sum_g part[g][c] over the G partial rows, in a fixed order: block
+// = 32 columns x 8 warps; warp w adds rows w, w+8, ...; the 8 warp sums are
+// then added in warp order.  (Used for the LayerNorm dw/db partials, with
+// out_a taking columns [0, C) and out_b columns [C, 2C), and for bias sums.)
+__global__ void __launch_bounds__(256)
+k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* __restrict__ out_a,
+           float* __restrict__ out_b) {
+    __shared__ float sm[8][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
     float s = 0.0f;
-    for (int g = 0; g < G; g++) s += part[(long long)g * 2 * C + c];
-    if (c < C) { if (out_a) out_a[c] = s; }
-    else if (out_b) out_b[c - C] = s;
+    if (c < ncols)
+        for (int g = warp; g < G; g += 8) s += part[(long long)g * ncols + c];
+    sm[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && c < ncols) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; w++) t += sm[w][lane];
+        if (c < split) { if (out_a) out_a[c] = t; }
+        else if (out_b) out_b[c - split] = t;
+    }
+}
+
+void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int split, float* out_a,
+                     float* out_b) {
+    if (L.dry) return;
+    L.count();
+    k_sum_rows<<<(ncols + 31) / 32, 256, 0, L.stream>>>(part, G, ncols, split, out_a, out_b);
 }
 
 constexpr int LN_BWD_MAX_BLOCKS = 1024;
 
 static int ln_bwd_blocks(const Launch& L, int M) {
-    int g = 2 * (L.num_sms > 0 ? L.num_sms : 148);
+    int g = 3 * (L.num_sms > 0 ? L.num_sms : 148);
     if (g > LN_BWD_MAX_BLOCKS) g = LN_BWD_MAX_BLOCKS;
     const int need = (M + LNV_WARPS - 1) / LNV_WARPS;
     return need < g ? need : g;
@@ -210,10 +249,10 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     if (L.dry) return true;
     const int G = ln_bwd_blocks(L, M);
     const int nv = (C / 8 + 31) / 32;
-    const size_t smem = (size_t)LNV_WARPS * 2 * C * sizeof(float);
+    const size_t smem = (size_t)(LNV_WARPS * 2 + 1) * C * sizeof(float);
     static bool attr = false;
     if (!attr) {
-        const int mx = LNV_WARPS * 2 * 1024 * (int)sizeof(float);
+        const int mx = (LNV_WARPS * 2 + 1) * 1024 * (int)sizeof(float);
         cudaFuncSetAttribute(k_ln_bwd_bf16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
@@ -227,87 +266,108 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     if (nv == 1) LNB(1); else if (nv == 2) LNB(2); else if (nv == 3) LNB(3); else LNB(4);
 #undef LNB
     L.count();
-    k_ln_partials<<<(2 * C + 255) / 256, 256, 0, L.stream>>>(scratch, G, C, dw, db);
+    k_sum_rows<<<(2 * C + 31) / 32, 256, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db);
     return true;
 }
 
 // ================================================================== cross entropy
 constexpr float XV_LOG2E = 1.4426950408889634f;
 
-// One CTA per row, two passes over the row: pass 1 keeps a per-thread
-// online (max, sum of exp) over 8-value vectors; after the block combine,
-// pass 2 re-reads the row (it is still in L2) and overwrites it with the
-// gradient.  Few registers, so several rows are in flight per SM.
+// One CTA per row, three passes over the row (the first from HBM, the others
+// from L2): (1) the row max, on packed bf16 pairs; (2) the sum of
+// 2^((z - max) log2 e); (3) the gradient, written in place.  Few registers, so
+// several rows are in flight per SM; exponentials use the single hardware
+// instruction ex2.approx (relative error ~2^-22).
 constexpr int XS_THREADS = 512;
 
-__device__ __forceinline__ void online_merge2(float& m, float& s, float m2, float s2) {
-    if (m2 == -INFINITY) return;
-    if (m == -INFINITY) { m = m2; s = s2; return; }
-    if (m2 > m) { s = s * exp2f((m - m2) * XV_LOG2E) + s2; m = m2; }
-    else s += s2 * exp2f((m2 - m) * XV_LOG2E);
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __global__ void __launch_bounds__(XS_THREADS)
 k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict__ row_loss,
             int V, int ld, float dscale, int* flags) {
-    __shared__ float sm_m[XS_THREADS / 32], sm_s[XS_THREADS / 32];
+    __shared__ float sm[XS_THREADS / 32];
     const long long row = blockIdx.x;
     uint4* zr = reinterpret_cast<uint4*>(z + row * (long long)ld);
     const int nvec = ld >> 3;
-    const int vfull = V >> 3;  // vectors with all 8 columns < V
-    float m = -INFINITY, s = 0.0f;
+    const int vfull = V >> 3;  // vectors whose 8 columns are all < V
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // pass 1: max
+    __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+    float mx = -INFINITY;
+    for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
+        const uint4 u = zr[vi];
+        if (vi < vfull) {
+            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.x));
+            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.y));
+            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.z));
+            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.w));
+        } else {
+            float f[8];
+            unpack8(u, f);
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (vi * 8 + e < V) mx = fmaxf(mx, f[e]);
+        }
+    }
+    mx = fmaxf(mx, fmaxf(__low2float(m2), __high2float(m2)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) sm[warp] = mx;
+    __syncthreads();
+    mx = sm[0];
+#pragma unroll
+    for (int k = 1; k < XS_THREADS / 32; k++) mx = fmaxf(mx, sm[k]);
+    const float ml = mx * XV_LOG2E;
+    // pass 2: sum of exponentials
+    float s = 0.0f;
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
         float f[8];
         unpack8(zr[vi], f);
-        const int valid = vi < vfull ? 8 : max(0, V - vi * 8);
-        float m8 = -INFINITY;
+        if (vi < vfull) {
 #pragma unroll
-        for (int e = 0; e < 8; e++)
-            if (e < valid) m8 = fmaxf(m8, f[e]);
-        if (valid == 0) continue;
-        if (m8 > m) {
-            s = (m == -INFINITY) ? 0.0f : s * exp2f((m - m8) * XV_LOG2E);
-            m = m8;
+            for (int e = 0; e < 8; e++) s += ex2f(fmaf(f[e], XV_LOG2E, -ml));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (vi * 8 + e < V) s += ex2f(fmaf(f[e], XV_LOG2E, -ml));
         }
-        const float ml = m * XV_LOG2E;
-#pragma unroll
-        for (int e = 0; e < 8; e++)
-            if (e < valid) s += exp2f(f[e] * XV_LOG2E - ml);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        online_merge2(m, s, m2, s2);
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) { sm_m[warp] = m; sm_s[warp] = s; }
+    s = wsum(s);
+    __syncthreads();  // everyone has read sm[] above
+    if (lane == 0) sm[warp] = s;
     __syncthreads();
-    float M_ = sm_m[0], S_ = sm_s[0];
-    for (int k = 1; k < XS_THREADS / 32; k++) online_merge2(M_, S_, sm_m[k], sm_s[k]);
-    const float lse = M_ + logf(S_);
-    const float lsel = lse * XV_LOG2E;  // in base-2 units
+    float S_ = 0.0f;
+#pragma unroll
+    for (int k = 0; k < XS_THREADS / 32; k++) S_ += sm[k];  // same order in every thread
+    const float lse = mx + logf(S_);
+    const float lsel = lse * XV_LOG2E;
     const int tgt = targets[row];
-    if (!(tgt >= 0 && tgt < V) && threadIdx.x == 0) {
+    const bool ok = tgt >= 0 && tgt < V;
+    if (!ok && threadIdx.x == 0) {
         atomicOr(&flags[FLAG_BAD_TOKEN], 1);
         row_loss[row] = 0.0f;
     }
+    const int tv = ok ? (tgt >> 3) : -1;
+    // pass 3: gradient, in place
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
         float f[8], o[8];
         unpack8(zr[vi], f);
+        if (vi < vfull) {
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-            const int col = vi * 8 + e;
-            float gval = 0.0f;
-            if (col < V) {
-                gval = exp2f(f[e] * XV_LOG2E - lsel);
-                if (col == tgt) {
-                    row_loss[row] = lse - f[e];
-                    gval -= 1.0f;
-                }
-                gval *= dscale;
-            }
-            o[e] = gval;
+            for (int e = 0; e < 8; e++) o[e] = ex2f(fmaf(f[e], XV_LOG2E, -lsel)) * dscale;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                o[e] = (vi * 8 + e < V) ? ex2f(fmaf(f[e], XV_LOG2E, -lsel)) * dscale : 0.0f;
+        }
+        if (vi == tv) {
+            const int e = tgt & 7;
+            row_loss[row] = lse - f[e];
+            o[e] -= dscale;
         }
         zr[vi] = pack8(o);
     }

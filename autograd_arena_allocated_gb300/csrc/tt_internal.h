@@ -120,6 +120,9 @@ size_t ln_bwd_bf16_scratch_floats(int C);
 bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
                       int V, int ld, float dscale);
 bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part);
+// out[c] = sum of the G rows of part[G][ncols] (fixed order); columns >= split go to out_b
+void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int split, float* out_a,
+                     float* out_b);
 size_t embed_chunk_scratch_floats(int M, int C);
 bool launch_embed_chunks(const Launch& L, bool bf16, const void* dx, const int32_t* keys,
                          const int32_t* vals, int M, int C, int V, float* dwte, float* scratch);
