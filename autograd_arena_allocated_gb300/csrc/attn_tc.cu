@@ -1,21 +1,29 @@
 // attn_tc.cu -- causal self-attention on the 5th-generation tensor cores
 // (tcgen05, bf16 in, fp32 accumulate in tensor memory), head dim 64.
 //
-// Forward, one CTA per (batch, head, 128-query tile), 192 threads:
-//   warp 0      TMA: the Q tile once, K and V tiles of 128 keys (K double
-//               buffered) from the packed [B*T, 3C] qkv buffer
-//   warp 1      TMEM allocation and the MMAs: S = Q K^T (M=128, N=128, K=64)
-//               into TMEM, then O_j = P_j V_j (M=128, N=64, K=128)
-//   warps 2..5  one thread per query row: reads its row of S from TMEM,
-//               applies the causal mask, keeps the running max and sum (base-2
-//               exponentials), writes P_j as bf16 into shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads, and folds
-//               O_j into an fp32 accumulator in registers, rescaled whenever
-//               the running max moves.  Finally y = O / l and the row's
-//               log-sum-exp are written.
-// About 97 KB of shared memory and 256 TMEM columns per CTA: two CTAs share
-// an SM, so one CTA's softmax overlaps the other's MMAs.  Every wait is
-// bounded (FLAG_TIMEOUT), as in the GEMM.
+// Every kernel streams 64-wide blocks of the other sequence past a
+// 128-row tile, so that the score block (128 x 64 fp32) needs only 64 TMEM
+// columns and several CTAs fit on one SM; each CTA has 192 threads:
+//   warp 0      TMA (128-byte-swizzled tiles straight from the packed
+//               [B*T, 3C] qkv buffer and the [B*T, C] output gradient)
+//   warp 1      TMEM allocation and the MMAs (one elected lane)
+//   warps 2..5  one thread per tile row: reads its row of the score block
+//               from TMEM, does the elementwise work in fp32, and writes the
+//               bf16 operand of the next MMA into shared memory in the
+//               128-byte-swizzled K-major layout the MMA reads.
+//
+// Forward (one CTA per 128 queries, 3 CTAs/SM): S = Q K_j^T; online softmax
+//   in base 2; P_j to shared memory; O += P_j V_j accumulates in TMEM (V read
+//   as an MN-major operand), rescaled in place only when the row max grows by
+//   more than 2^8; finally y = O / l and the row's log-sum-exp.
+// Backward, deterministic (no atomics):
+//   dQ kernel (one CTA per 128 queries, 2 CTAs/SM): D = rowsum(dO o O);
+//     S = Q K_j^T, dP = dO V_j^T; dS = P o (dP - D) with P from the saved
+//     log-sum-exp; dQ += dS K_j accumulates in TMEM.
+//   dK/dV kernel (one CTA per 128 keys, 2 CTAs/SM): S^T = K Q_j^T,
+//     dP^T = V dO_j^T; P^T and dS^T; dV += P^T dO_j, dK += dS^T Q_j in TMEM
+//     (Q_j and dO_j, loaded K-major, are read again as MN-major operands).
+// Every wait is bounded (FLAG_TIMEOUT), as in the GEMM.
 #include "tt_internal.h"
 #include "tc_ptx.cuh"
 
@@ -28,59 +36,69 @@ using namespace tc;
 typedef __nv_bfloat16 bf16;
 
 constexpr int D = 64;
-constexpr int BQ = 128;
-constexpr int BKV = 128;
+constexpr int BQ = 128;  // rows of the CTA's tile
+constexpr int BN = 64;   // width of the streamed blocks
 constexpr int THREADS = 192;
-constexpr int TILE = 128 * 128;  // 128 rows x 128 bytes
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int T128 = 128 * 128;  // 128 rows x 128 bytes
+constexpr int T64 = 64 * 128;    // 64 rows x 128 bytes
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
-
-// forward shared-memory map (offsets from a 1024-aligned base)
-constexpr int F_Q = 0;
-constexpr int F_K = F_Q + TILE;      // 2 stages
-constexpr int F_V = F_K + 2 * TILE;  // 1 stage
-constexpr int F_P = F_V + TILE;      // 2 swizzle atoms (keys 0-63, 64-127)
-constexpr int F_BAR = F_P + 2 * TILE;
-constexpr int F_SMEM = F_BAR + 256 + 1024;
+constexpr float SL2 = 0.125f * LOG2E;  // 1/sqrt(64), base-2 units
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
-// Store 32 bf16 values (keys k0..k0+31 of row r) into a K-major, 128-byte
-// swizzled operand made of 64-key atoms of [128 rows x 128 B].
-__device__ __forceinline__ void store_row32(uint8_t* base, int r, int k0, const uint32_t (&w)[16]) {
-    uint8_t* atom = base + (k0 >> 6) * TILE + r * 128;
-    const int c0 = (k0 & 63) >> 3;  // first 16-byte chunk
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int phys = (c0 + i) ^ (r & 7);
-        *reinterpret_cast<uint4*>(atom + phys * 16) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    }
-}
-
-// 2^x by the single hardware instruction (relative error ~2^-22; inputs here
-// are at most 0, results feed bf16 operands or fp32 sums)
+// 2^x by the single hardware instruction (relative error ~2^-22)
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-// backward kernels: warps 0 (TMA) and 1 (MMA) plus 8 elementwise warps; warp
-// w handles TMEM lanes 32*(w%4).. and column half (w-2)/4 of its rows
-constexpr int THREADS_B = 320;
-
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// ------------------------------------------------------------------ forward
+// 32 bf16 values (columns k0..k0+31, k0 in {0, 32}) of row r of a K-major,
+// 128-byte-swizzled [128 rows x 64 columns] operand (16-byte chunk c of row r
+// at c ^ (r mod 8)).  Rows of 32 consecutive lanes: conflict-free.
+__device__ __forceinline__ void store_row32(uint8_t* base, int r, int k0, const uint32_t (&w)[16]) {
+    uint8_t* row = base + r * 128;
+    const int c0 = k0 >> 3;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        *reinterpret_cast<uint4*>(row + (((c0 + i) ^ (r & 7)) << 4)) =
+            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+__device__ __forceinline__ void store_out64(bf16* dst, const float* v, float scale) {
+    uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        o[i] = make_uint4(pack_bf2(v[8 * i] * scale, v[8 * i + 1] * scale),
+                          pack_bf2(v[8 * i + 2] * scale, v[8 * i + 3] * scale),
+                          pack_bf2(v[8 * i + 4] * scale, v[8 * i + 5] * scale),
+                          pack_bf2(v[8 * i + 6] * scale, v[8 * i + 7] * scale));
+}
+
+__device__ __forceinline__ void init_done() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// ================================================================== forward
+constexpr int F_Q = 0;
+constexpr int F_K = F_Q + T128;     // 2 stages
+constexpr int F_V = F_K + 2 * T64;  // 1 stage
+constexpr int F_P = F_V + T64;      // P: [128 x 64] bf16
+constexpr int F_BAR = F_P + T128;
+constexpr int F_SMEM = F_BAR + 256 + 1024;
+constexpr uint32_t F_TMEM = 128;    // S: cols 0..63, O_j: 64..127
+
 __global__ void __launch_bounds__(THREADS)
-k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, float* __restrict__ lse,
-              int T, int C, int H, int* flags) {
+k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + F_BAR);
@@ -99,7 +117,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, floa
     const int nqt = gridDim.x;
     const int qt = nqt - 1 - (int)blockIdx.x;  // longest rows first
     const int b = blockIdx.y / H, h = blockIdx.y % H;
-    const int nkv = qt + 1;
+    const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -116,10 +134,9 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, floa
         mbar_init(p_full, 128);
         mbar_init(o_full, 1);
         *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm) : "memory");
+        init_done();
     }
-    if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
+    if (warp == 1) tmem_alloc(tmem_holder, F_TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -128,19 +145,19 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, floa
     if (warp == 0) {
         if (lane == 0) {
             const int xq = h * D, xk = C + h * D, xv = 2 * C + h * D;
-            mbar_expect_tx(q_full, TILE);
-            tma_load_2d(smem_u32(sm + F_Q), &tm, q_full, xq, row0 + qt * BQ);
+            mbar_expect_tx(q_full, T128);
+            tma_load_2d(smem_u32(sm + F_Q), &tq, q_full, xq, row0 + qt * BQ);
             int issued_k = 0, issued_v = 0;
             bool ok = true;
             for (int j = 0; j < nkv && ok; j++) {
                 const int st = j & 1;
-                if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags)) { ok = false; break; }
-                mbar_expect_tx(&k_full[st], TILE);
-                tma_load_2d(smem_u32(sm + F_K + st * TILE), &tm, &k_full[st], xk, row0 + j * BKV);
+                if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x100 + 1)) { ok = false; break; }
+                mbar_expect_tx(&k_full[st], T64);
+                tma_load_2d(smem_u32(sm + F_K + st * T64), &tk, &k_full[st], xk, row0 + j * BN);
                 ++issued_k;
-                if (!mbar_wait(v_empty, (j & 1) ^ 1, abort_flag, flags)) { ok = false; break; }
-                mbar_expect_tx(v_full, TILE);
-                tma_load_2d(smem_u32(sm + F_V), &tm, v_full, xv, row0 + j * BKV);
+                if (!mbar_wait(v_empty, (j & 1) ^ 1, abort_flag, flags, 0x100 + 2)) { ok = false; break; }
+                mbar_expect_tx(v_full, T64);
+                tma_load_2d(smem_u32(sm + F_V), &tk, v_full, xv, row0 + j * BN);
                 ++issued_v;
             }
             if (!ok) {  // let issued copies land before the CTA exits
@@ -154,29 +171,35 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, floa
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16(BQ, BKV, false, false);
+            constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_O = idesc_bf16(BQ, D, false, true);
             const uint32_t sq = smem_u32(sm + F_Q), sp = smem_u32(sm + F_P), sv = smem_u32(sm + F_V);
-            bool ok = mbar_wait(q_full, 0, abort_flag, flags);
-            for (int j = 0; j < nkv && ok; j++) {
+            bool ok = mbar_wait(q_full, 0, abort_flag, flags, 0x100 + 3);
+            // S_{j+1} is issued as soon as the row threads hold S_j in registers,
+            // so that it overlaps the softmax of block j
+            auto issue_s = [&](int j) -> bool {
                 const int st = j & 1;
-                if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, flags)) break;
-                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags)) break;
+                if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, flags, 0x100 + 4)) return false;
+                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x100 + 5)) return false;
                 tc_fence_after();
-                const uint32_t sk = smem_u32(sm + F_K + st * TILE);
+                const uint32_t sk = smem_u32(sm + F_K + st * T64);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID_S,
-                              k > 0 ? 1u : 0u);
+                    umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(s_full);
                 umma_commit(&k_empty[st]);
-                if (!mbar_wait(p_full, j & 1, abort_flag, flags)) break;
-                if (!mbar_wait(v_full, j & 1, abort_flag, flags)) break;
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; j < nkv && ok; j++) {
+                if (j + 1 < nkv && !issue_s(j + 1)) break;
+                if (!mbar_wait(p_full, j & 1, abort_flag, flags, 0x100 + 6)) break;
+                if (!mbar_wait(v_full, j & 1, abort_flag, flags, 0x100 + 7)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < BKV / 16; k++)
-                    umma_bf16(tmem + BKV, sdesc(sp + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                              sdesc(sv + k * 2048, TILE, 1024), ID_O, k > 0 ? 1u : 0u);
+                for (int k = 0; k < BN / 16; k++)
+                    umma_bf16(tmem + BN, sdesc(sp + 32 * k, 16, 1024), sdesc(sv + k * 2048, T64, 1024), ID_O,
+                              (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(o_full);
                 umma_commit(v_empty);
             }
@@ -186,91 +209,100 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, floa
         const int r = quarter * 32 + lane;
         const int q = qt * BQ + r;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sl2 = 0.125f * LOG2E;  // 1/sqrt(64) in base-2 units
-        float m = -INFINITY, l = 0.0f, corr_prev = 1.0f;
-        float o[D];
-#pragma unroll
-        for (int d = 0; d < D; d++) o[d] = 0.0f;
+        // O accumulates in TMEM (the P.V MMAs add into it); P is taken relative
+        // to a reference max m that is raised -- and O, l rescaled in place --
+        // only when the row max exceeds it by more than 8 (P <= 2^8 otherwise)
+        float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; j++) {
-            if (!mbar_wait(s_full, j & 1, abort_flag, flags)) { ok = false; break; }
+            if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x100 + 8)) { ok = false; break; }
             tc_fence_after();
-            const bool diag = (j == qt);
-            const int kq = q - j * BKV;  // keys with column index > kq are masked (diagonal block)
-            // pass 1: row max of the raw scores (the scale is positive)
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < 4; c++) {
-                uint32_t w[32];
-                tmem_ld32(tl + c * 32, w);
-                if (!diag) {
-#pragma unroll
-                    for (int e = 0; e < 32; e++) mx = fmaxf(mx, __uint_as_float(w[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; e++)
-                        if (c * 32 + e <= kq) mx = fmaxf(mx, __uint_as_float(w[e]));
-                }
-            }
-            const float mn = fmaxf(m, mx * sl2);
-            const float corr = ex2(m - mn);
-            m = mn;
-            // fold O_{j-1} (its MMA has finished reading P once o_full flips)
-            if (j > 0) {
-                if (!mbar_wait(o_full, (j - 1) & 1, abort_flag, flags)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t w[32];
-                tmem_ld32(tl + BKV, w);
-#pragma unroll
-                for (int d = 0; d < 32; d++) o[d] = fmaf(o[d], corr_prev, __uint_as_float(w[d]));
-                tmem_ld32(tl + BKV + 32, w);
-#pragma unroll
-                for (int d = 0; d < 32; d++) o[32 + d] = fmaf(o[32 + d], corr_prev, __uint_as_float(w[d]));
-            }
-            corr_prev = corr;
-            // pass 2: P = 2^(s*scale - m) as bf16 into shared memory
-            float rs = 0.0f;
-#pragma unroll 1
-            for (int c = 0; c < 4; c++) {
-                uint32_t w[32], pk[16];
-                tmem_ld32(tl + c * 32, w);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2(fmaf(__uint_as_float(w[e]), sl2, -m));
-                    float p1 = ex2(fmaf(__uint_as_float(w[e + 1]), sl2, -m));
-                    if (diag) {
-                        if (c * 32 + e > kq) p0 = 0.0f;
-                        if (c * 32 + e + 1 > kq) p1 = 0.0f;
-                    }
-                    rs += p0 + p1;
-                    pk[e >> 1] = pack_bf2(p0, p1);
-                }
-                store_row32(sm + F_P, r, c * 32, pk);
-            }
-            l = fmaf(l, corr, rs);
+            const bool diag = (j >= 2 * qt);
+            const int kq = q - j * BN;  // on the diagonal, key columns > kq are masked
+            uint32_t w0[32], w1[32];
+            tmem_ld32(tl, w0);
+            tmem_ld32(tl + 32, w1);
             tc_fence_before();
-            mbar_arrive(s_free);
+            mbar_arrive(s_free);  // S is in registers: the next S may be computed
+            float mx = -INFINITY;
+            if (!diag) {
+#pragma unroll
+                for (int e = 0; e < 32; e++) mx = fmaxf(mx, fmaxf(__uint_as_float(w0[e]), __uint_as_float(w1[e])));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    if (e <= kq) mx = fmaxf(mx, __uint_as_float(w0[e]));
+                    if (32 + e <= kq) mx = fmaxf(mx, __uint_as_float(w1[e]));
+                }
+            }
+            const float mn = fmaxf(m, mx * SL2);
+            if (j > 0) {
+                // P_{j-1} V_{j-1} is complete: P's buffer is free and O is current
+                if (!mbar_wait_warp(o_full, (j - 1) & 1, abort_flag, flags, 0x100 + 9)) { ok = false; break; }
+                tc_fence_after();
+                // warp-uniform decision: the TMEM loads and stores are warp-collective
+                if (__any_sync(0xffffffffu, mn > m + 8.0f)) {
+                    const float corr = ex2(m - mn);
+                    uint32_t v[32];
+                    tmem_ld32(tl + BN, v);
+#pragma unroll
+                    for (int d = 0; d < 32; d++) v[d] = __float_as_uint(__uint_as_float(v[d]) * corr);
+                    tmem_st32(tl + BN, v);
+                    tmem_ld32(tl + BN + 32, v);
+#pragma unroll
+                    for (int d = 0; d < 32; d++) v[d] = __float_as_uint(__uint_as_float(v[d]) * corr);
+                    tmem_st32(tl + BN + 32, v);
+                    tmem_st_wait();
+                    l *= corr;
+                    m = mn;
+                }
+            } else {
+                m = mn;
+            }
+            // P = 2^(s*scale - m) as bf16 into shared memory
+            float rs = 0.0f;
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float p0 = ex2(fmaf(__uint_as_float(w0[e]), SL2, -m));
+                float p1 = ex2(fmaf(__uint_as_float(w0[e + 1]), SL2, -m));
+                if (diag) {
+                    if (e > kq) p0 = 0.0f;
+                    if (e + 1 > kq) p1 = 0.0f;
+                }
+                rs += p0 + p1;
+                pk[e >> 1] = pack_bf2(p0, p1);
+            }
+            store_row32(sm + F_P, r, 0, pk);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float p0 = ex2(fmaf(__uint_as_float(w1[e]), SL2, -m));
+                float p1 = ex2(fmaf(__uint_as_float(w1[e + 1]), SL2, -m));
+                if (diag) {
+                    if (32 + e > kq) p0 = 0.0f;
+                    if (33 + e > kq) p1 = 0.0f;
+                }
+                rs += p0 + p1;
+                pk[e >> 1] = pack_bf2(p0, p1);
+            }
+            store_row32(sm + F_P, r, 32, pk);
+            l += rs;
+            tc_fence_before();  // orders the TMEM stores of a rescale before the next MMA
             fence_proxy_async_smem();
             mbar_arrive(p_full);
         }
-        if (ok && mbar_wait(o_full, (nkv - 1) & 1, abort_flag, flags)) {
+        if (ok && mbar_wait_warp(o_full, (nkv - 1) & 1, abort_flag, flags, 0x100 + 10)) {
             tc_fence_after();
-            uint32_t w[32];
-            tmem_ld32(tl + BKV, w);
+            float o[D];
+            uint32_t v[32];
+            tmem_ld32(tl + BN, v);
 #pragma unroll
-            for (int d = 0; d < 32; d++) o[d] = fmaf(o[d], corr_prev, __uint_as_float(w[d]));
-            tmem_ld32(tl + BKV + 32, w);
+            for (int d = 0; d < 32; d++) o[d] = __uint_as_float(v[d]);
+            tmem_ld32(tl + BN + 32, v);
 #pragma unroll
-            for (int d = 0; d < 32; d++) o[32 + d] = fmaf(o[32 + d], corr_prev, __uint_as_float(w[d]));
+            for (int d = 0; d < 32; d++) o[32 + d] = __uint_as_float(v[d]);
             if (q < T) {
-                const float inv = 1.0f / l;
-                uint4* yr = reinterpret_cast<uint4*>(y + (long long)(row0 + q) * C + h * D);
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                    yr[i] = make_uint4(pack_bf2(o[8 * i] * inv, o[8 * i + 1] * inv),
-                                       pack_bf2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                                       pack_bf2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                                       pack_bf2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+                store_out64(y + (long long)(row0 + q) * C + h * D, o, 1.0f / l);
                 lse[((long long)b * H + h) * T + q] = (m + log2f(l)) * LN2;
             }
         }
@@ -278,29 +310,24 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ y, floa
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem, F_TMEM);
 }
 
-// ------------------------------------------------------------------ backward
-// dQ kernel shared-memory map.  One CTA per (batch, head, 128-query tile):
-//   S = Q K_j^T and dP = dO V_j^T into TMEM; query-row threads form
-//   dS = P o (dP - D) (P from the saved log-sum-exp) as bf16 in shared
-//   memory; dQ += dS K_j accumulates in TMEM (K_j read as an MN-major B).
-// The row threads first compute D = rowsum(dO o O) for their query and store
-// it for the dK/dV kernel, which runs after this one.
+// ================================================================== backward: dQ
 constexpr int Q_Q = 0;
-constexpr int Q_O = Q_Q + TILE;       // dO tile
-constexpr int Q_K = Q_O + TILE;       // 2 stages
-constexpr int Q_V = Q_K + 2 * TILE;   // 2 stages
-constexpr int Q_S = Q_V + 2 * TILE;   // dS, 2 atoms
-constexpr int Q_BAR = Q_S + 2 * TILE;
+constexpr int Q_O = Q_Q + T128;     // dO tile
+constexpr int Q_K = Q_O + T128;     // 2 stages
+constexpr int Q_V = Q_K + 2 * T64;  // 2 stages
+constexpr int Q_S = Q_V + 2 * T64;  // dS: [128 x 64] bf16
+constexpr int Q_BAR = Q_S + T128;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
-constexpr uint32_t BWD_TMEM_COLS = 512;
+constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191
 
-__global__ void __launch_bounds__(THREADS_B, 1)
-k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo,
-                 const bf16* __restrict__ y, const float* __restrict__ lse, float* __restrict__ Dlt,
-                 bf16* __restrict__ dqkv, int T, int C, int H, int* flags) {
+__global__ void __launch_bounds__(THREADS)
+k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
+                 const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
+                 int T, int C, int H, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
@@ -318,7 +345,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant_
     const int nqt = gridDim.x;
     const int qt = nqt - 1 - (int)blockIdx.x;
     const int b = blockIdx.y / H, h = blockIdx.y % H;
-    const int nkv = qt + 1;
+    const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -329,14 +356,14 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant_
         mbar_init(&kv_empty[0], 1);
         mbar_init(&kv_empty[1], 1);
         mbar_init(s_full, 1);
-        mbar_init(s_free, 256);
-        mbar_init(ds_full, 256);
+        mbar_init(s_free, 128);
+        mbar_init(ds_full, 128);
         mbar_init(ds_free, 1);
         mbar_init(acc_full, 1);
         *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        init_done();
     }
-    if (warp == 1) tmem_alloc(tmem_holder, BWD_TMEM_COLS);
+    if (warp == 1) tmem_alloc(tmem_holder, Q_TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -345,17 +372,17 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant_
     if (warp == 0) {
         if (lane == 0) {
             const int xq = h * D, xk = C + h * D, xv = 2 * C + h * D;
-            mbar_expect_tx(qo_full, 2 * TILE);
-            tma_load_2d(smem_u32(sm + Q_Q), &tmq, qo_full, xq, row0 + qt * BQ);
-            tma_load_2d(smem_u32(sm + Q_O), &tmo, qo_full, h * D, row0 + qt * BQ);
+            mbar_expect_tx(qo_full, 2 * T128);
+            tma_load_2d(smem_u32(sm + Q_Q), &tq, qo_full, xq, row0 + qt * BQ);
+            tma_load_2d(smem_u32(sm + Q_O), &to, qo_full, h * D, row0 + qt * BQ);
             int issued = 0;
             bool ok = true;
             for (int j = 0; j < nkv; j++) {
                 const int st = j & 1;
-                if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags)) { ok = false; break; }
-                mbar_expect_tx(&kv_full[st], 2 * TILE);
-                tma_load_2d(smem_u32(sm + Q_K + st * TILE), &tmq, &kv_full[st], xk, row0 + j * BKV);
-                tma_load_2d(smem_u32(sm + Q_V + st * TILE), &tmq, &kv_full[st], xv, row0 + j * BKV);
+                if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x200 + 1)) { ok = false; break; }
+                mbar_expect_tx(&kv_full[st], 2 * T64);
+                tma_load_2d(smem_u32(sm + Q_K + st * T64), &tk, &kv_full[st], xk, row0 + j * BN);
+                tma_load_2d(smem_u32(sm + Q_V + st * T64), &tk, &kv_full[st], xv, row0 + j * BN);
                 ++issued;
             }
             if (!ok) {
@@ -367,30 +394,29 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant_
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16(BQ, BKV, false, false);
+            constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_Q = idesc_bf16(BQ, D, false, true);
             const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O), sds = smem_u32(sm + Q_S);
-            bool ok = mbar_wait(qo_full, 0, abort_flag, flags);
+            bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2);
             for (int j = 0; j < nkv && ok; j++) {
                 const int st = j & 1;
-                if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, flags)) { ok = false; break; }
-                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags)) { ok = false; break; }
+                if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, flags, 0x200 + 3)) { ok = false; break; }
+                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 4)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sk = smem_u32(sm + Q_K + st * TILE), sv = smem_u32(sm + Q_V + st * TILE);
+                const uint32_t sk = smem_u32(sm + Q_K + st * T64), sv = smem_u32(sm + Q_V + st * T64);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID_S, k > 0);
+                    umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem + BKV, sdesc(so + 32 * k, 16, 1024), sdesc(sv + 32 * k, 16, 1024), ID_S,
-                              k > 0);
+                    umma_bf16(tmem + BN, sdesc(so + 32 * k, 16, 1024), sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(s_full);
-                if (!mbar_wait(ds_full, j & 1, abort_flag, flags)) { ok = false; break; }
+                if (!mbar_wait(ds_full, j & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < BKV / 16; k++)
-                    umma_bf16(tmem + 2 * BKV, sdesc(sds + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                              sdesc(sk + k * 2048, TILE, 1024), ID_Q, (j > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < BN / 16; k++)
+                    umma_bf16(tmem + 2 * BN, sdesc(sds + 32 * k, 16, 1024), sdesc(sk + k * 2048, T64, 1024),
+                              ID_Q, (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(&kv_empty[st]);
                 umma_commit(ds_free);
             }
@@ -398,19 +424,17 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant_
         }
     } else {
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int q = qt * BQ + r;
         const bool qv = q < T;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sl2 = 0.125f * LOG2E;
         const long long bh = (long long)b * H + h;
+        bool ok = mbar_wait_warp(qo_full, 0, abort_flag, flags, 0x200 + 6);
         // D = rowsum(dO o O) for this query (dO row from the swizzled tile)
-        if (!mbar_wait(qo_full, 0, abort_flag, flags)) goto rows_done;
-        {
-            float Dq = 0.0f;
+        float Dq = 0.0f;
+        if (ok && qv) {
             const uint8_t* orow = sm + Q_O + r * 128;
-            const uint4* yr = reinterpret_cast<const uint4*>(y + (long long)(row0 + (qv ? q : 0)) * C + h * D);
+            const uint4* yr = reinterpret_cast<const uint4*>(y + (long long)(row0 + q) * C + h * D);
 #pragma unroll
             for (int c = 0; c < 8; c++) {
                 const uint4 a = *reinterpret_cast<const uint4*>(orow + ((c ^ (r & 7)) * 16));
@@ -422,80 +446,72 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant_
                     Dq = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), Dq);
                 }
             }
-            if (!qv) Dq = 0.0f;
-            if (qv && half == 0) Dlt[bh * T + q] = Dq;
-            const float Lq = qv ? lse[bh * T + q] * LOG2E : 0.0f;
-            for (int j = 0; j < nkv; j++) {
-                if (!mbar_wait(s_full, j & 1, abort_flag, flags)) goto rows_done;
-                if (!mbar_wait(ds_free, (j & 1) ^ 1, abort_flag, flags)) goto rows_done;
-                tc_fence_after();
-                const bool diag = (j == qt);
-                const int kq = q - j * BKV;  // key columns > kq are masked on the diagonal
-#pragma unroll 1
-                for (int c = 2 * half; c < 2 * half + 2; c++) {
-                    uint32_t sw[32], pw[32], pk[16];
-                    tmem_ld32(tl + c * 32, sw);
-                    tmem_ld32(tl + BKV + c * 32, pw);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float d0 = ex2(fmaf(__uint_as_float(sw[e]), sl2, -Lq)) * (__uint_as_float(pw[e]) - Dq);
-                        float d1 = ex2(fmaf(__uint_as_float(sw[e + 1]), sl2, -Lq)) * (__uint_as_float(pw[e + 1]) - Dq);
-                        if (diag) {
-                            if (c * 32 + e > kq) d0 = 0.0f;
-                            if (c * 32 + e + 1 > kq) d1 = 0.0f;
-                        }
-                        pk[e >> 1] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
-                    }
-                    store_row32(sm + Q_S, r, c * 32, pk);
-                }
-                tc_fence_before();
-                mbar_arrive(s_free);
-                fence_proxy_async_smem();
-                mbar_arrive(ds_full);
-            }
-            if (!mbar_wait(acc_full, 0, abort_flag, flags)) goto rows_done;
-            tc_fence_after();
-            {
-                uint32_t w0[32];
-                tmem_ld32(tl + 2 * BKV + 32 * half, w0);
-                if (qv) {
-                    uint4* o = reinterpret_cast<uint4*>(dqkv + (long long)(row0 + q) * 3 * C + h * D + 32 * half);
-                    const float sc = 0.125f;
-#pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        o[i] = make_uint4(pack_bf2(__uint_as_float(w0[8 * i]) * sc, __uint_as_float(w0[8 * i + 1]) * sc),
-                                          pack_bf2(__uint_as_float(w0[8 * i + 2]) * sc, __uint_as_float(w0[8 * i + 3]) * sc),
-                                          pack_bf2(__uint_as_float(w0[8 * i + 4]) * sc, __uint_as_float(w0[8 * i + 5]) * sc),
-                                          pack_bf2(__uint_as_float(w0[8 * i + 6]) * sc, __uint_as_float(w0[8 * i + 7]) * sc));
-                }
-            }
+            Dlt[bh * T + q] = Dq;
         }
-    rows_done:;
+        const float Lq = qv ? lse[bh * T + q] * LOG2E : 0.0f;
+        for (int j = 0; j < nkv && ok; j++) {
+            if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x200 + 7)) { ok = false; break; }
+            if (!mbar_wait_warp(ds_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 8)) { ok = false; break; }
+            tc_fence_after();
+            const bool diag = (j >= 2 * qt);
+            const int kq = q - j * BN;
+#pragma unroll 1
+            for (int c = 0; c < 2; c++) {
+                uint32_t sw[32], pw[32], pk[16];
+                tmem_ld32(tl + c * 32, sw);
+                tmem_ld32(tl + BN + c * 32, pw);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float d0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -Lq)) * (__uint_as_float(pw[e]) - Dq);
+                    float d1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -Lq)) * (__uint_as_float(pw[e + 1]) - Dq);
+                    if (diag) {
+                        if (c * 32 + e > kq) d0 = 0.0f;
+                        if (c * 32 + e + 1 > kq) d1 = 0.0f;
+                    }
+                    pk[e >> 1] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
+                }
+                store_row32(sm + Q_S, r, c * 32, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(s_free);
+            fence_proxy_async_smem();
+            mbar_arrive(ds_full);
+        }
+        if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x200 + 9)) {
+            tc_fence_after();
+            float acc[64];
+            uint32_t w[32];
+            tmem_ld32(tl + 2 * BN, w);
+#pragma unroll
+            for (int d = 0; d < 32; d++) acc[d] = __uint_as_float(w[d]);
+            tmem_ld32(tl + 2 * BN + 32, w);
+#pragma unroll
+            for (int d = 0; d < 32; d++) acc[32 + d] = __uint_as_float(w[d]);
+            if (qv) store_out64(dqkv + (long long)(row0 + q) * 3 * C + h * D, acc, 0.125f);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, BWD_TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem, Q_TMEM);
 }
 
-// dK/dV kernel shared-memory map.  One CTA per (batch, head, 128-key tile),
-// looping over the query tiles at or after it:
-//   S^T = K Q_j^T and dP^T = V dO_j^T into TMEM; key-row threads form P^T
-//   and dS^T = P^T o (dP^T - D) as bf16 in shared memory; dV += P^T dO_j and
-//   dK += dS^T Q_j accumulate in TMEM (Q_j and dO_j read as MN-major B).
+// ================================================================== backward: dK, dV
 constexpr int K_K = 0;
-constexpr int K_V = K_K + TILE;
-constexpr int K_Q = K_V + TILE;        // 2 stages
-constexpr int K_O = K_Q + 2 * TILE;    // 2 stages
-constexpr int K_P = K_O + 2 * TILE;    // P^T, 2 atoms
-constexpr int K_S = K_P + 2 * TILE;    // dS^T, 2 atoms
-constexpr int K_BAR = K_S + 2 * TILE;
+constexpr int K_V = K_K + T128;
+constexpr int K_Q = K_V + T128;     // 2 stages
+constexpr int K_O = K_Q + 2 * T64;  // 2 stages
+constexpr int K_P = K_O + 2 * T64;  // P^T: [128 keys x 64 queries]
+constexpr int K_S = K_P + T128;     // dS^T
+constexpr int K_BAR = K_S + T128;
 constexpr int K_SMEM = K_BAR + 256 + 1024;
+constexpr uint32_t K_TMEM = 256;    // S^T 0..63, dP^T 64..127, dV 128..191, dK 192..255
 
-__global__ void __launch_bounds__(THREADS_B, 1)
-k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo,
-                   const float* __restrict__ lse, const float* __restrict__ Dlt,
-                   bf16* __restrict__ dqkv, int T, int C, int H, int* flags) {
+__global__ void __launch_bounds__(THREADS)
+k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
+                   const float* __restrict__ Dlt, bf16* __restrict__ dqkv, int T, int C, int H,
+                   int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + K_BAR);
@@ -510,11 +526,12 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     uint32_t* tmem_holder = (uint32_t*)(bars + 10);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    const int nt = gridDim.x;
-    const int kt = (int)blockIdx.x;   // key tile; tile kt loops over nt - kt query tiles
+    const int kt = (int)blockIdx.x;  // key tile; low tiles see the most query blocks
     const int b = blockIdx.y / H, h = blockIdx.y % H;
     const int row0 = b * T;
-    const int nq = nt - kt;
+    const int nqb = (T + BN - 1) / BN;
+    const int j0 = 2 * kt;
+    const int nq = nqb - j0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -524,14 +541,14 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         mbar_init(&qo_empty[0], 1);
         mbar_init(&qo_empty[1], 1);
         mbar_init(st_full, 1);
-        mbar_init(st_free, 256);
-        mbar_init(ps_full, 256);
+        mbar_init(st_free, 128);
+        mbar_init(ps_full, 128);
         mbar_init(ps_free, 1);
         mbar_init(acc_full, 1);
         *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        init_done();
     }
-    if (warp == 1) tmem_alloc(tmem_holder, BWD_TMEM_COLS);
+    if (warp == 1) tmem_alloc(tmem_holder, K_TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -540,17 +557,17 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (warp == 0) {
         if (lane == 0) {
             const int xq = h * D, xk = C + h * D, xv = 2 * C + h * D;
-            mbar_expect_tx(kv_full, 2 * TILE);
-            tma_load_2d(smem_u32(sm + K_K), &tmq, kv_full, xk, row0 + kt * BKV);
-            tma_load_2d(smem_u32(sm + K_V), &tmq, kv_full, xv, row0 + kt * BKV);
+            mbar_expect_tx(kv_full, 2 * T128);
+            tma_load_2d(smem_u32(sm + K_K), &tq, kv_full, xk, row0 + kt * BQ);
+            tma_load_2d(smem_u32(sm + K_V), &tq, kv_full, xv, row0 + kt * BQ);
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < nq; i++) {
-                const int st = i & 1, j = kt + i;
-                if (!mbar_wait(&qo_empty[st], ((i >> 1) & 1) ^ 1, abort_flag, flags)) { ok = false; break; }
-                mbar_expect_tx(&qo_full[st], 2 * TILE);
-                tma_load_2d(smem_u32(sm + K_Q + st * TILE), &tmq, &qo_full[st], xq, row0 + j * BQ);
-                tma_load_2d(smem_u32(sm + K_O + st * TILE), &tmo, &qo_full[st], h * D, row0 + j * BQ);
+                const int st = i & 1, j = j0 + i;
+                if (!mbar_wait(&qo_empty[st], ((i >> 1) & 1) ^ 1, abort_flag, flags, 0x300 + 1)) { ok = false; break; }
+                mbar_expect_tx(&qo_full[st], 2 * T64);
+                tma_load_2d(smem_u32(sm + K_Q + st * T64), &tk, &qo_full[st], xq, row0 + j * BN);
+                tma_load_2d(smem_u32(sm + K_O + st * T64), &to, &qo_full[st], h * D, row0 + j * BN);
                 ++issued;
             }
             if (!ok) {
@@ -562,34 +579,33 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16(BKV, BQ, false, false);
-            constexpr uint32_t ID_A = idesc_bf16(BKV, D, false, true);
+            constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
+            constexpr uint32_t ID_A = idesc_bf16(BQ, D, false, true);
             const uint32_t sk = smem_u32(sm + K_K), sv = smem_u32(sm + K_V);
             const uint32_t sp = smem_u32(sm + K_P), sds = smem_u32(sm + K_S);
-            bool ok = mbar_wait(kv_full, 0, abort_flag, flags);
+            bool ok = mbar_wait(kv_full, 0, abort_flag, flags, 0x300 + 2);
             for (int i = 0; i < nq && ok; i++) {
                 const int st = i & 1;
-                if (!mbar_wait(&qo_full[st], (i >> 1) & 1, abort_flag, flags)) { ok = false; break; }
-                if (!mbar_wait(st_free, (i & 1) ^ 1, abort_flag, flags)) { ok = false; break; }
+                if (!mbar_wait(&qo_full[st], (i >> 1) & 1, abort_flag, flags, 0x300 + 3)) { ok = false; break; }
+                if (!mbar_wait(st_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 4)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sq = smem_u32(sm + K_Q + st * TILE), so = smem_u32(sm + K_O + st * TILE);
+                const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem, sdesc(sk + 32 * k, 16, 1024), sdesc(sq + 32 * k, 16, 1024), ID_S, k > 0);
+                    umma_bf16(tmem, sdesc(sk + 32 * k, 16, 1024), sdesc(sq + 32 * k, 16, 1024), ID, k > 0);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem + BQ, sdesc(sv + 32 * k, 16, 1024), sdesc(so + 32 * k, 16, 1024), ID_S,
-                              k > 0);
+                    umma_bf16(tmem + BN, sdesc(sv + 32 * k, 16, 1024), sdesc(so + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(st_full);
-                if (!mbar_wait(ps_full, i & 1, abort_flag, flags)) { ok = false; break; }
+                if (!mbar_wait(ps_full, i & 1, abort_flag, flags, 0x300 + 5)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < BQ / 16; k++) {
+                for (int k = 0; k < BN / 16; k++) {
                     const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
-                    umma_bf16(tmem + 2 * BQ, sdesc(sp + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                              sdesc(so + k * 2048, TILE, 1024), ID_A, acc);
-                    umma_bf16(tmem + 2 * BQ + D, sdesc(sds + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                              sdesc(sq + k * 2048, TILE, 1024), ID_A, acc);
+                    umma_bf16(tmem + 2 * BN, sdesc(sp + 32 * k, 16, 1024), sdesc(so + k * 2048, T64, 1024),
+                              ID_A, acc);
+                    umma_bf16(tmem + 3 * BN, sdesc(sds + 32 * k, 16, 1024), sdesc(sq + k * 2048, T64, 1024),
+                              ID_A, acc);
                 }
                 umma_commit(&qo_empty[st]);
                 umma_commit(ps_free);
@@ -598,36 +614,35 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         }
     } else {
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
-        const int key = kt * BKV + r;
+        const int key = kt * BQ + r;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sl2 = 0.125f * LOG2E;
         const long long bh = (long long)b * H + h;
         const float* lrow = lse + bh * T;
         const float* drow = Dlt + bh * T;
+        bool ok = true;
         for (int i = 0; i < nq; i++) {
-            const int j = kt + i;
-            if (!mbar_wait(st_full, i & 1, abort_flag, flags)) break;
-            if (!mbar_wait(ps_free, (i & 1) ^ 1, abort_flag, flags)) break;
+            const int j = j0 + i;
+            if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6)) { ok = false; break; }
+            if (!mbar_wait_warp(ps_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 7)) { ok = false; break; }
             tc_fence_after();
-            const bool diag = (i == 0);
+            const bool diag = (i < 2);  // query blocks that overlap this key tile
 #pragma unroll 1
-            for (int c = 2 * half; c < 2 * half + 2; c++) {
+            for (int c = 0; c < 2; c++) {
                 // the chunk's 32 queries: lane l fetches query q0 + l, then broadcasts
-                const int q0 = j * BQ + c * 32;
+                const int q0 = j * BN + c * 32;
                 const bool lv = q0 + lane < T;
                 const float Ll = lv ? __ldg(lrow + q0 + lane) * LOG2E : INFINITY;
                 const float Dl = lv ? __ldg(drow + q0 + lane) : 0.0f;
                 uint32_t sw[32], dw[32], pk[16], dk[16];
                 tmem_ld32(tl + c * 32, sw);
-                tmem_ld32(tl + BQ + c * 32, dw);
+                tmem_ld32(tl + BN + c * 32, dw);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float L0 = __shfl_sync(0xffffffffu, Ll, e), L1 = __shfl_sync(0xffffffffu, Ll, e + 1);
                     const float D0 = __shfl_sync(0xffffffffu, Dl, e), D1 = __shfl_sync(0xffffffffu, Dl, e + 1);
-                    float p0 = ex2(fmaf(__uint_as_float(sw[e]), sl2, -L0));
-                    float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), sl2, -L1));
+                    float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L0));
+                    float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L1));
                     if (diag) {
                         if (q0 + e < key) p0 = 0.0f;
                         if (q0 + e + 1 < key) p1 = 0.0f;
@@ -643,33 +658,31 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constan
             fence_proxy_async_smem();
             mbar_arrive(ps_full);
         }
-        if (mbar_wait(acc_full, 0, abort_flag, flags)) {
+        if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x300 + 8)) {
             tc_fence_after();
-            // half 0 writes dV, half 1 writes dK (scaled by 1/sqrt(64))
-            uint32_t w0[32], w1[32];
-            tmem_ld32(tl + 2 * BQ + D * half, w0);
-            tmem_ld32(tl + 2 * BQ + D * half + 32, w1);
-            if (key < T) {
-                const float sc = half ? 0.125f : 1.0f;
-                uint4* o = reinterpret_cast<uint4*>(dqkv + (long long)(row0 + key) * 3 * C + (half ? C : 2 * C) + h * D);
+            float acc[64];
+            uint32_t w[32];
+            bf16* base = dqkv + (long long)(row0 + key) * 3 * C + h * D;
+            tmem_ld32(tl + 2 * BN, w);
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    o[i] = make_uint4(pack_bf2(__uint_as_float(w0[8 * i]) * sc, __uint_as_float(w0[8 * i + 1]) * sc),
-                                      pack_bf2(__uint_as_float(w0[8 * i + 2]) * sc, __uint_as_float(w0[8 * i + 3]) * sc),
-                                      pack_bf2(__uint_as_float(w0[8 * i + 4]) * sc, __uint_as_float(w0[8 * i + 5]) * sc),
-                                      pack_bf2(__uint_as_float(w0[8 * i + 6]) * sc, __uint_as_float(w0[8 * i + 7]) * sc));
-                    o[4 + i] = make_uint4(pack_bf2(__uint_as_float(w1[8 * i]) * sc, __uint_as_float(w1[8 * i + 1]) * sc),
-                                          pack_bf2(__uint_as_float(w1[8 * i + 2]) * sc, __uint_as_float(w1[8 * i + 3]) * sc),
-                                          pack_bf2(__uint_as_float(w1[8 * i + 4]) * sc, __uint_as_float(w1[8 * i + 5]) * sc),
-                                          pack_bf2(__uint_as_float(w1[8 * i + 6]) * sc, __uint_as_float(w1[8 * i + 7]) * sc));
-                }
-            }
+            for (int d = 0; d < 32; d++) acc[d] = __uint_as_float(w[d]);
+            tmem_ld32(tl + 2 * BN + 32, w);
+#pragma unroll
+            for (int d = 0; d < 32; d++) acc[32 + d] = __uint_as_float(w[d]);
+            if (key < T) store_out64(base + 2 * C, acc, 1.0f);  // dV
+            tmem_ld32(tl + 3 * BN, w);
+#pragma unroll
+            for (int d = 0; d < 32; d++) acc[d] = __uint_as_float(w[d]);
+            tmem_ld32(tl + 3 * BN + 32, w);
+#pragma unroll
+            for (int d = 0; d < 32; d++) acc[32 + d] = __uint_as_float(w[d]);
+            if (key < T) store_out64(base + C, acc, 0.125f);  // dK, times 1/sqrt(64)
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, BWD_TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem, K_TMEM);
 }
 
 }  // namespace fa5
@@ -678,51 +691,53 @@ bool attention_tc_eligible(bool bf16, int C, int H) {
     return bf16 && H > 0 && C % H == 0 && C / H == fa5::D && C % 8 == 0;
 }
 
+static bool attn_set_smem() {
+    static int done = 0;  // 1 ok, -1 failed
+    if (!done) {
+        done = (cudaFuncSetAttribute(fa5::k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     fa5::F_SMEM) == cudaSuccess &&
+                cudaFuncSetAttribute(fa5::k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     fa5::Q_SMEM) == cudaSuccess &&
+                cudaFuncSetAttribute(fa5::k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     fa5::K_SMEM) == cudaSuccess)
+                   ? 1
+                   : -1;
+    }
+    return done == 1;
+}
+
 bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T,
                              int C, int H) {
     if (L.dry) return true;
-    CUtensorMap tm;
-    if (!tc::make_tmap_bf16(&tm, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(fa5::k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 fa5::F_SMEM) != cudaSuccess)
-            return false;
-        attr = true;
-    }
+    CUtensorMap tq, tk;
+    if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
+    if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
+    if (!attn_set_smem()) return false;
     dim3 grid((T + fa5::BQ - 1) / fa5::BQ, B * H);
     L.count();
-    fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tm, (fa5::bf16*)y, lse, T, C, H,
-                                                                     L.flags);
+    fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C,
+                                                                     H, L.flags);
     return true;
 }
-
-}  // namespace tt
-
-namespace tt {
 
 bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
                              const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt) {
     if (L.dry) return true;
-    CUtensorMap tmq, tmo;
-    if (!tc::make_tmap_bf16(&tmq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
-    if (!tc::make_tmap_bf16(&tmo, dy, (long long)C, (long long)B * T, (long long)C, fa5::D, fa5::BQ)) return false;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(fa5::k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 fa5::Q_SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(fa5::k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 fa5::K_SMEM) != cudaSuccess)
-            return false;
-        attr = true;
-    }
+    CUtensorMap tq, tk, to128, to64;
+    if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
+    if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
+    if (!tc::make_tmap_bf16(&to128, dy, (long long)C, (long long)B * T, (long long)C, fa5::D, fa5::BQ))
+        return false;
+    if (!tc::make_tmap_bf16(&to64, dy, (long long)C, (long long)B * T, (long long)C, fa5::D, fa5::BN))
+        return false;
+    if (!attn_set_smem()) return false;
     dim3 grid((T + fa5::BQ - 1) / fa5::BQ, B * H);
     L.count();
-    fa5::k_attn_bwd_dq_tc<<<grid, fa5::THREADS_B, fa5::Q_SMEM, L.stream>>>(
-        tmq, tmo, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);
+    fa5::k_attn_bwd_dq_tc<<<grid, fa5::THREADS, fa5::Q_SMEM, L.stream>>>(
+        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);
     L.count();
-    fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::THREADS_B, fa5::K_SMEM, L.stream>>>(
-        tmq, tmo, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);
+    fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::THREADS, fa5::K_SMEM, L.stream>>>(
+        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);
     return true;
 }
 

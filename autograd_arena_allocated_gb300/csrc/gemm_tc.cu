@@ -239,7 +239,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags)) { ok = false; break; }
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 1)) { ok = false; break; }
                     mbar_expect_tx(&full[stage], CF::STAGE_BYTES);
                     const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
                     const uint32_t sb = sa + CF::A_BYTES;
@@ -288,11 +288,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 (void)tile;
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags)) { ok = false; break; }
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags, 0x400 + 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.flags)) { ok = false; break; }
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.flags, 0x400 + 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
                     const uint32_t sb = sa + CF::A_BYTES;
@@ -328,7 +328,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int tile = u / p.splits, split = u - tile * p.splits;
             const int m0 = tile_m(p, tile) * BM;
             const int n0 = tile_n(p, tile) * BN;
-            if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.flags)) break;
+            if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
             tc_fence_after();
             const int m = m0 + row;
             const bool row_ok = m < p.M;

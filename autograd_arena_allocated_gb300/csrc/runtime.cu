@@ -642,7 +642,8 @@ tt_status tt_ctx_sync(tt_ctx* c) {
     if (cudaMemcpyAsync(flags, c->arena, sizeof flags, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
         cudaStreamSynchronize(c->stream) != cudaSuccess)
         return fail(c, TT_ERR_CUDA, "sync: %s", cudaGetErrorString(cudaGetLastError()));
-    if (flags[FLAG_TIMEOUT]) return fail(c, TT_ERR_TIMEOUT, "a device-side wait timed out");
+    if (flags[FLAG_TIMEOUT])
+        return fail(c, TT_ERR_TIMEOUT, "a device-side wait timed out (site 0x%x)", (unsigned)flags[FLAG_SITE]);
     if (flags[FLAG_BAD_TOKEN]) return fail(c, TT_ERR_ARG, "token id out of range");
     if (flags[FLAG_NONFINITE]) return fail(c, TT_ERR_NONFINITE, "non-finite loss");
     return TT_OK;

@@ -20,6 +20,7 @@ enum DeviceFlag : int {
     FLAG_BAD_TOKEN = 0,  // a token/target id outside [0, V)
     FLAG_TIMEOUT = 1,    // a bounded mbarrier wait gave up
     FLAG_NONFINITE = 2,  // non-finite loss
+    FLAG_SITE = 3,       // which bounded wait gave up first (kernel-specific code)
     FLAG_COUNT = 4
 };
 

@@ -111,6 +111,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ distributed
+def stage(msg):
+    """Progress marker on stderr (the result line is the only stdout output)."""
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -404,11 +409,13 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    stage("warm-up")
     # warm-up (also the first-use set-up of every kernel)
     for _ in range(args.warmup):
         train_step(tok_d, tgt_d, sync=False)
     ctx.sync()
 
+    stage("timed region")
     # ---------------- timed region: device-resident inputs
     barrier()
     l0 = ctx.launches
@@ -427,6 +434,7 @@ def main():
     fpt = flops_per_token(sh, T)
     mfu = value / world * fpt / (peaks["bf16"] * 1e12)
 
+    stage("per-op timing pass")
     # ---------------- per-op device times (a second pass with CUDA events per op)
     ctx.set_profiling(True)
     prof_steps = min(args.steps, 3)
@@ -463,6 +471,7 @@ def main():
                 "per_launch": {"ms": per_launch_ms, "flops": r["flops"] / r["calls"],
                                "bytes": r["bytes"] / r["calls"]}}
 
+    stage("end-to-end pass")
     # ---------------- end to end: pinned host buffers through the C ABI
     e2e = None
     if not args.no_e2e:
@@ -479,10 +488,12 @@ def main():
                "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4,
                "ms_per_step": 1e3 * e2e_s / args.steps}
 
+    stage("final loss")
     ctx.reset()
     final_loss = ctx.step(params, grads, tok_d, tgt_d, B, T, sync=True)
 
     if rank == 0:
+        stage("cpu baseline")
         cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -162,6 +162,37 @@ def test_attention(ctx, oracle, dt, B, T, C_, H):
         assert rel(host(dqkv), rd) < 1e-2
 
 
+@pytest.mark.parametrize("T", [384, 1000])
+def test_attention_growing_max(ctx, oracle, T):
+    """Score rows whose maximum keeps rising along the keys (odd rows) beside
+    rows whose maximum is the first key (even rows), so that the online
+    softmax's running maximum is raised many times for some rows of a warp and
+    never for their neighbours; the scores span ~30 in log2 units."""
+    B, C_, H = 1, 128, 2
+    D = C_ // H
+    qkv = rnd(B * T, 3 * C_, scale=0.5)
+    sign = np.where(np.arange(T) % 2 == 1, 1.0, -1.0).astype(np.float32)
+    ramp = (24.0 * np.arange(T) / T).astype(np.float32)
+    for h in range(H):
+        qkv[:, h * D] = 6.0 * sign                # q . e0
+        qkv[:, C_ + h * D] = ramp                 # k . e0 grows with the key position
+    dy = rnd(B * T, C_)
+    qd, dyd = to_dev(qkv, "bf16"), to_dev(dy, "bf16")
+    y = torch.empty(B * T, C_, device=DEV, dtype=qd.dtype)
+    lse = torch.empty(B, H, T, device=DEV)
+    ctx.attention_fwd("bf16", qd, y, lse, B, T, C_, H)
+    dqkv = torch.empty_like(qd)
+    ctx.attention_bwd("bf16", qd, y, lse, dyd, dqkv, B, T, C_, H)
+    torch.cuda.synchronize()
+    q64 = ovals(qkv, "bf16", oracle)
+    ry, P = oracle.attention_fwd(q64, B, T, C_, H)
+    assert_close(host(y), ry, 8e-3, 3e-2, "attention y")
+    rd = oracle.attention_bwd(q64, P, ovals(dy, "bf16", oracle), B, T, C_, H)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel(host(y), ry) < 5e-3
+    assert rel(host(dqkv), rd) < 1e-2
+
+
 # ----------------------------------------------------------------- layernorm
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 @pytest.mark.parametrize("M,C_", [(300, 64), (130, 384), (257, 768), (64, 1024)])
