@@ -117,10 +117,10 @@ def stage(msg):
 
 
 def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+    from autograd_arena_allocated_gb300.replicas import rank_env
+
+    r = rank_env()
+    return r.world, r.rank, r.local
 
 
 # ------------------------------------------------------------------ reference arm
@@ -349,6 +349,7 @@ def main():
 
     from autograd_arena_allocated_gb300 import api, synth
     from autograd_arena_allocated_gb300 import build as native_build
+    from autograd_arena_allocated_gb300.replicas import Group, job_throughput, token_seed
 
     if world > 1:
         import torch.distributed as dist
@@ -371,7 +372,8 @@ def main():
     peaks = load_peaks()
 
     p = synth.init_params(sh)
-    tok, tgt = synth.token_stream(B, T, sh.V, w.tokens)
+    # each replica trains on its own token stream (rank 0: the single-GPU stream)
+    tok, tgt = synth.token_stream(B, T, sh.V, w.tokens, seed=token_seed(synth.TOKEN_SEED, rank))
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
     master = torch.from_numpy(p).to(dev)
@@ -397,17 +399,8 @@ def main():
         ctx.adamw(master, lowp, grads, m, v, *hp, step_no[0])
         return loss
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    group = Group(dist, device=dev, sync=torch.cuda.synchronize)
+    barrier, max_over_ranks = group.barrier, group.max
 
     stage("warm-up")
     # warm-up (also the first-use set-up of every kernel)
@@ -430,7 +423,7 @@ def main():
     ms = max_over_ranks(e0.elapsed_time(e1))
     ctx.sync()
     ms_step = ms / args.steps
-    value = world * B * T * args.steps / (ms / 1e3)
+    value = job_throughput(world, B * T, args.steps, ms / 1e3)
     fpt = flops_per_token(sh, T)
     mfu = value / world * fpt / (peaks["bf16"] * 1e12)
 
@@ -484,7 +477,7 @@ def main():
             train_step(tok_h, tgt_h, sync=True)  # H2D of the batch, D2H of the loss
         barrier()
         e2e_s = max_over_ranks(time.perf_counter() - t0)
-        e2e = {"value": world * B * T * args.steps / e2e_s, "unit": UNIT,
+        e2e = {"value": job_throughput(world, B * T, args.steps, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4,
                "ms_per_step": 1e3 * e2e_s / args.steps}
 
