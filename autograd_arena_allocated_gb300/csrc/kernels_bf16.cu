@@ -3,7 +3,7 @@
 // registers between passes, grids sized from the SM count, and every
 // reduction in a fixed order (no floating-point atomics).
 //   LayerNorm forward / backward  (one warp per row)
-//   fused cross entropy           (one 1024-thread CTA per row, row in registers)
+//   fused cross entropy           (one 512-thread CTA per row, three passes)
 //   column sums (bias gradients)  (8 columns per thread)
 //   embedding-gradient scatter    (fixed 64-row chunks of the token-sorted
 //                                  positions, then chunk partials in order)
