@@ -72,78 +72,114 @@ void launch_embed_fwd(const Launch& L, bool bf16, const void* wte, const void* w
             (const float*)wte, (const float*)wpe, tok, (float*)x, T, C, V, total, L.flags);
 }
 
-// Stable LSD radix sort of positions by token id in ONE thread block (4-bit
-// digits).  Thread j owns the contiguous chunk [j*per, (j+1)*per) of the
-// input; counts are scanned digit-major then thread-minor, which keeps equal
-// keys in input (position) order.
-constexpr int SORT_THREADS = 1024;
-constexpr int SORT_RADIX = 16;
+// Stable LSD radix sort of positions by token id, 8-bit digits, across the
+// whole GPU.  Each pass is three launches over tiles of RS_TILE consecutive
+// elements: per-tile digit counts; one exclusive scan of the counts in
+// digit-major, tile-minor order; a scatter in which every element's place is
+// its digit's scanned base for the tile plus its rank among the tile's
+// earlier elements of the same digit -- so equal keys keep input (position)
+// order, and the result is the same however the hardware schedules it.
+// Pass 0 reads the token ids themselves (an id outside [0, V) gets key V and
+// sorts last); the values are the positions.
+constexpr int RS_THREADS = 256;
+constexpr int RS_ROUNDS = 4;
+constexpr int RS_TILE = RS_THREADS * RS_ROUNDS;
+constexpr int RS_BINS = 256;
 
-__global__ void __launch_bounds__(SORT_THREADS)
-k_sort_positions(const int32_t* __restrict__ tok, int M, int V, int passes,
-                 int32_t* keysA, int32_t* valsA, int32_t* keysB, int32_t* valsB) {
-    extern __shared__ int s_cnt[];  // [SORT_RADIX][SORT_THREADS]
-    __shared__ int s_tot[SORT_THREADS];
-    const int tid = threadIdx.x;
-    const int per = (M + SORT_THREADS - 1) / SORT_THREADS;
-    const int lo = min(M, tid * per), hi = min(M, lo + per);
-    for (int i = lo; i < hi; i++) {
-        int id = tok[i];
-        keysA[i] = (id < 0 || id >= V) ? V : id;  // bad ids sort last and are skipped
-        valsA[i] = i;
+__device__ __forceinline__ int rs_key(const int32_t* __restrict__ in, int from_tok, int V, int i) {
+    const int k = in[i];
+    return from_tok ? ((k < 0 || k >= V) ? V : k) : k;
+}
+
+__global__ void __launch_bounds__(RS_THREADS)
+k_rs_hist(const int32_t* __restrict__ in, int from_tok, int V, int M, int shift, int G, int* __restrict__ hist) {
+    __shared__ int s_h[RS_BINS];
+    s_h[threadIdx.x] = 0;
+    __syncthreads();
+    const long long i0 = (long long)blockIdx.x * RS_TILE;
+#pragma unroll
+    for (int r = 0; r < RS_ROUNDS; r++) {
+        const long long i = i0 + r * RS_THREADS + threadIdx.x;
+        if (i < M) atomicAdd(&s_h[(rs_key(in, from_tok, V, (int)i) >> shift) & (RS_BINS - 1)], 1);
     }
     __syncthreads();
-    int32_t *ki = keysA, *vi = valsA, *ko = keysB, *vo = valsB;
-    for (int p = 0; p < passes; p++) {
-        const int shift = 4 * p;
-        int cnt[SORT_RADIX];
+    hist[(long long)threadIdx.x * G + blockIdx.x] = s_h[threadIdx.x];
+}
+
+// exclusive scan of n ints in place, one block of 1024 threads: thread t
+// takes a contiguous run of ceil(n/1024) entries
+__global__ void __launch_bounds__(1024) k_rs_scan(int* __restrict__ a, int n) {
+    __shared__ int s_w[32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int per = (n + 1023) / 1024;
+    const int lo = min(n, t * per), hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; i++) sum += a[i];
+    int incl = sum;
 #pragma unroll
-        for (int d = 0; d < SORT_RADIX; d++) cnt[d] = 0;
-        for (int i = lo; i < hi; i++) cnt[(ki[i] >> shift) & 15]++;
-#pragma unroll
-        for (int d = 0; d < SORT_RADIX; d++) s_cnt[d * SORT_THREADS + tid] = cnt[d];
-        __syncthreads();
-        // exclusive scan of the 16*1024 counts in digit-major order:
-        // thread j scans the 16 consecutive entries [16j, 16j+16)
-        int loc[SORT_RADIX];
-        int run = 0;
-#pragma unroll
-        for (int d = 0; d < SORT_RADIX; d++) {
-            loc[d] = run;
-            run += s_cnt[tid * SORT_RADIX + d];
-        }
-        s_tot[tid] = run;
-        __syncthreads();
-        // block-wide exclusive scan of s_tot (Hillis-Steele over 1024 entries)
-        for (int off = 1; off < SORT_THREADS; off <<= 1) {
-            int v = (tid >= off) ? s_tot[tid - off] : 0;
-            __syncthreads();
-            s_tot[tid] += v;
-            __syncthreads();
-        }
-        int base = s_tot[tid] - run;
-#pragma unroll
-        for (int d = 0; d < SORT_RADIX; d++) s_cnt[tid * SORT_RADIX + d] = base + loc[d];
-        __syncthreads();
-#pragma unroll
-        for (int d = 0; d < SORT_RADIX; d++) cnt[d] = s_cnt[d * SORT_THREADS + tid];
-        for (int i = lo; i < hi; i++) {
-            int k = ki[i];
-            int d = (k >> shift) & 15;
-            int pos = cnt[d]++;
-            ko[pos] = k;
-            vo[pos] = vi[i];
-        }
-        __syncthreads();
-        int32_t* t;
-        t = ki; ki = ko; ko = t;
-        t = vi; vi = vo; vo = t;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
     }
-    // make sure the sorted result ends in buffer A
-    if (ki != keysA) {
-        for (int i = lo; i < hi; i++) { keysA[i] = ki[i]; valsA[i] = vi[i]; }
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_w[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
+        }
+        s_w[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - sum + (warp > 0 ? s_w[warp - 1] : 0);
+    for (int i = lo; i < hi; i++) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
     }
 }
+
+__global__ void __launch_bounds__(RS_THREADS)
+k_rs_scatter(const int32_t* __restrict__ kin, const int32_t* __restrict__ vin, int from_tok, int V, int M,
+             int shift, int G, const int* __restrict__ scan, int32_t* __restrict__ kout,
+             int32_t* __restrict__ vout) {
+    __shared__ int s_base[RS_BINS];
+    __shared__ int s_wc[RS_THREADS / 32][RS_BINS];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    s_base[t] = scan[(long long)t * G + blockIdx.x];
+    const long long i0 = (long long)blockIdx.x * RS_TILE;
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll 1
+    for (int r = 0; r < RS_ROUNDS; r++) {
+#pragma unroll
+        for (int w = 0; w < RS_THREADS / 32; w++) s_wc[w][t] = 0;
+        const long long i = i0 + r * RS_THREADS + t;  // index order = round, warp, lane
+        const bool ok = i < M;
+        const int key = ok ? rs_key(kin, from_tok, V, (int)i) : 0;
+        const int val = ok ? (from_tok ? (int)i : vin[i]) : 0;
+        const int d = ok ? (key >> shift) & (RS_BINS - 1) : RS_BINS;
+        __syncthreads();
+        const unsigned same = __match_any_sync(0xffffffffu, d);
+        const int rank = __popc(same & lt);
+        if (ok && rank == 0) s_wc[warp][d] = __popc(same);
+        __syncthreads();
+        if (ok) {
+            int pos = s_base[d] + rank;
+            for (int w = 0; w < warp; w++) pos += s_wc[w][d];
+            kout[pos] = key;
+            vout[pos] = val;
+        }
+        __syncthreads();
+        int add = 0;
+#pragma unroll
+        for (int w = 0; w < RS_THREADS / 32; w++) add += s_wc[w][t];
+        s_base[t] += add;  // the tile's later rounds come after this one
+    }
+}
+
+static int rs_tiles(int M) { return (M + RS_TILE - 1) / RS_TILE; }
 
 // One block per sorted index; the block at the start of a run of equal
 // token ids sums that run's rows of dx in increasing position order and adds
@@ -187,8 +223,13 @@ __global__ void k_embed_wpe(const T* __restrict__ dx, int B, int T_, int C, int 
     dwpe[i] = s;
 }
 
+// scratch: keys/values A and B [M] each, the digit counts [256 x tiles], then
+// the chunk partial sums of the segmented reduction
+static size_t rs_ints(int M) { return (size_t)4 * M + (size_t)RS_BINS * rs_tiles(M); }
+
 size_t embed_bwd_scratch_bytes(int M, int C) {
-    return (size_t)4 * M * sizeof(int32_t) + 256 + embed_chunk_scratch_floats(M, C) * sizeof(float);
+    return ((rs_ints(M) * sizeof(int32_t) + 255) & ~(size_t)255) +
+           embed_chunk_scratch_floats(M, C) * sizeof(float);
 }
 
 void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t* tok,
@@ -199,17 +240,27 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
     int32_t* s = (int32_t*)scratch;
     int bits = 1;
     while ((1 << bits) <= V) bits++;  // keys take values 0..V
-    int passes = (bits + 3) / 4;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_sort_positions, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SORT_RADIX * SORT_THREADS * (int)sizeof(int));
-        attr = true;
+    const int passes = (bits + 7) / 8;
+    const int G = rs_tiles(M);
+    int32_t *kA = s, *vA = s + M, *kB = s + 2 * M, *vB = s + 3 * M;
+    int* hist = s + 4 * (size_t)M;
+    // the last pass must write buffer A
+    int32_t* ko = (passes & 1) ? kA : kB;
+    int32_t* vo = (passes & 1) ? vA : vB;
+    const int32_t *ki = tok, *vi = nullptr;
+    for (int p = 0; p < passes; p++) {
+        const int from_tok = p == 0;
+        L.count();
+        k_rs_hist<<<G, RS_THREADS, 0, L.stream>>>(ki, from_tok, V, M, 8 * p, G, hist);
+        L.count();
+        k_rs_scan<<<1, 1024, 0, L.stream>>>(hist, RS_BINS * G);
+        L.count();
+        k_rs_scatter<<<G, RS_THREADS, 0, L.stream>>>(ki, vi, from_tok, V, M, 8 * p, G, hist, ko, vo);
+        ki = ko; vi = vo;
+        ko = (ko == kA) ? kB : kA;
+        vo = (vo == vA) ? vB : vA;
     }
-    L.count();
-    k_sort_positions<<<1, SORT_THREADS, SORT_RADIX * SORT_THREADS * sizeof(int), L.stream>>>(
-        tok, M, V, passes, s, s + M, s + 2 * M, s + 3 * M);
-    float* chunk_scratch = (float*)((char*)scratch + (((size_t)4 * M * sizeof(int32_t) + 255) & ~(size_t)255));
+    float* chunk_scratch = (float*)((char*)scratch + ((rs_ints(M) * sizeof(int32_t) + 255) & ~(size_t)255));
     if (!launch_embed_chunks(L, bf16, dx, s, s + M, M, C, V, dwte, chunk_scratch)) {
         int threads = (C + 7) / 8;
         threads = ((threads + 31) / 32) * 32;

@@ -89,83 +89,79 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
 }
 
 // Backward: a fixed grid of G blocks; warp j of block g takes rows
-// g*8 + j, + 8G, + 16G, ...; each warp accumulates its dw/db partials in its
-// own slice of shared memory (each lane owns its columns: no atomics), the
-// block combines its warps in warp order, and k_ln_partials adds the G block
-// rows in block order.
+// g*8 + j, + 8G, + 16G, ...  Lane l owns columns 8(l + 32i) .. +7, so it keeps
+// the dw/db partial sums of those columns (and gamma) in registers across its
+// rows; at the end the block adds its warps' partials in warp order through
+// shared memory and writes one partial row, and k_sum_rows adds the G block
+// rows in block order (no atomics anywhere).
 template <int NV>
-__global__ void __launch_bounds__(LNV_WARPS * 32, 3)
+__global__ void __launch_bounds__(LNV_WARPS * 32, 2)
 k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
               const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
               float* __restrict__ part, int M, int C, int accumulate) {
-    extern __shared__ float s_part[];  // [LNV_WARPS][2C] per-warp dw/db partials, then w
+    extern __shared__ float s_part[];  // [LNV_WARPS][2C]: each warp's dw | db partials
+    __shared__ uint4 s_gamma[128];        // gamma, 8 bf16 per entry (C <= 1024)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvec = C >> 3;
-    float* pw = s_part + warp * 2 * C;
-    float* pb = pw + C;
-    float* sw = s_part + LNV_WARPS * 2 * C;  // gamma as floats
-    for (int c = threadIdx.x; c < C; c += blockDim.x) sw[c] = __bfloat162float(w[c]);
+    const float inv_c = 1.0f / (float)C;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) s_gamma[v] = reinterpret_cast<const uint4*>(w)[v];
+    float aw[NV][8], ab[NV][8];
 #pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int vi = lane + 32 * i;
-        if (vi < nvec)
+    for (int i = 0; i < NV; i++)
 #pragma unroll
-            for (int e = 0; e < 8; e++) { pw[vi * 8 + e] = 0.0f; pb[vi * 8 + e] = 0.0f; }
-    }
+        for (int e = 0; e < 8; e++) { aw[i][e] = 0.0f; ab[i][e] = 0.0f; }
     __syncthreads();
     for (long long row = (long long)blockIdx.x * LNV_WARPS + warp; row < M;
          row += (long long)gridDim.x * LNV_WARPS) {
         const uint4* xr = reinterpret_cast<const uint4*>(x + row * C);
         const uint4* dr = reinterpret_cast<const uint4*>(dy + row * C);
+        uint4* xo = reinterpret_cast<uint4*>(dx + row * C);
+        // every load of the row is issued before any arithmetic
+        uint4 xv[NV], dv[NV], ov[NV];
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
+                xv[i] = xr[vi];
+                dv[i] = dr[vi];
+                if (accumulate) ov[i] = xo[vi];
+            }
+        }
         const float mu = mean[row], rs = rstd[row];
         // pass 1: the two row sums, and this row's dw/db contributions
-        uint4 xv[NV], dv[NV];
         float sg = 0.0f, sgx = 0.0f;
 #pragma unroll
         for (int i = 0; i < NV; i++) {
-            const int vi = lane + 32 * i;
-            if (vi < nvec) { xv[i] = xr[vi]; dv[i] = dr[vi]; }
-        }
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            const int vi = lane + 32 * i;
-            if (vi < nvec) {
-                float xf[8], df[8];
+            if (lane + 32 * i < nvec) {
+                float xf[8], df[8], wf[8];
                 unpack8(xv[i], xf);
                 unpack8(dv[i], df);
+                unpack8(s_gamma[lane + 32 * i], wf);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const float xh = (xf[e] - mu) * rs;
-                    const float g = df[e] * sw[vi * 8 + e];
+                    const float g = df[e] * wf[e];
                     sg += g;
                     sgx += g * xh;
-                    pw[vi * 8 + e] += df[e] * xh;
-                    pb[vi * 8 + e] += df[e];
+                    aw[i][e] = fmaf(df[e], xh, aw[i][e]);
+                    ab[i][e] += df[e];
                 }
             }
         }
-        const float mg = wsum(sg) / C, mgx = wsum(sgx) / C;
+        const float mg = wsum(sg) * inv_c, mgx = wsum(sgx) * inv_c;
         // pass 2: dx from the same registers
-        uint4* xo = reinterpret_cast<uint4*>(dx + row * C);
-        uint4 ov[NV];
-        if (accumulate) {
-#pragma unroll
-            for (int i = 0; i < NV; i++) {
-                const int vi = lane + 32 * i;
-                if (vi < nvec) ov[i] = xo[vi];
-            }
-        }
 #pragma unroll
         for (int i = 0; i < NV; i++) {
             const int vi = lane + 32 * i;
             if (vi < nvec) {
-                float xf[8], df[8], o[8];
+                float xf[8], df[8], wf[8], o[8];
                 unpack8(xv[i], xf);
                 unpack8(dv[i], df);
+                unpack8(s_gamma[vi], wf);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const float xh = (xf[e] - mu) * rs;
-                    o[e] = rs * (df[e] * sw[vi * 8 + e] - mg - xh * mgx);
+                    o[e] = rs * (df[e] * wf[e] - mg - xh * mgx);
                 }
                 if (accumulate) {
                     float old[8];
@@ -175,6 +171,20 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
                 }
                 xo[vi] = pack8(o);
             }
+        }
+    }
+    // the block's partials: warps in warp order
+    float* pw = s_part + warp * 2 * C;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int vi = lane + 32 * i;
+        if (vi < nvec) {
+            float4* dwp = reinterpret_cast<float4*>(pw + vi * 8);
+            float4* dbp = reinterpret_cast<float4*>(pw + C + vi * 8);
+            dwp[0] = make_float4(aw[i][0], aw[i][1], aw[i][2], aw[i][3]);
+            dwp[1] = make_float4(aw[i][4], aw[i][5], aw[i][6], aw[i][7]);
+            dbp[0] = make_float4(ab[i][0], ab[i][1], ab[i][2], ab[i][3]);
+            dbp[1] = make_float4(ab[i][4], ab[i][5], ab[i][6], ab[i][7]);
         }
     }
     __syncthreads();
@@ -219,8 +229,22 @@ void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int s
 
 constexpr int LN_BWD_MAX_BLOCKS = 1024;
 
+// G = the blocks that are resident at once (SMs x blocks per SM), so that
+// every block runs its rows in one wave; fewer when M is small.
+template <int NV>
 static int ln_bwd_blocks(const Launch& L, int M) {
-    int g = 3 * (L.num_sms > 0 ? L.num_sms : 148);
+    static int per_sm[5] = {0, 0, 0, 0, 0};
+    if (!per_sm[NV]) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_ln_bwd_bf16<NV>, LNV_WARPS * 32,
+                                                          (LNV_WARPS * 2) * 1024 * sizeof(float)) !=
+                cudaSuccess || b < 1) {
+            cudaGetLastError();
+            b = 1;
+        }
+        per_sm[NV] = b;
+    }
+    int g = per_sm[NV] * (L.num_sms > 0 ? L.num_sms : 148);
     if (g > LN_BWD_MAX_BLOCKS) g = LN_BWD_MAX_BLOCKS;
     const int need = (M + LNV_WARPS - 1) / LNV_WARPS;
     return need < g ? need : g;
@@ -247,12 +271,11 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
                         int C, bool accumulate, float* scratch) {
     if (C % 8 || C > 1024) return false;
     if (L.dry) return true;
-    const int G = ln_bwd_blocks(L, M);
     const int nv = (C / 8 + 31) / 32;
-    const size_t smem = (size_t)(LNV_WARPS * 2 + 1) * C * sizeof(float);
+    const size_t smem = (size_t)(LNV_WARPS * 2) * C * sizeof(float);
     static bool attr = false;
     if (!attr) {
-        const int mx = (LNV_WARPS * 2 + 1) * 1024 * (int)sizeof(float);
+        const int mx = (LNV_WARPS * 2) * 1024 * (int)sizeof(float);
         cudaFuncSetAttribute(k_ln_bwd_bf16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
@@ -260,10 +283,12 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
         attr = true;
     }
     L.count();
-#define LNB(NV) k_ln_bwd_bf16<NV><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
+    int G = 0;
+#define LNB(NV) G = ln_bwd_blocks<NV>(L, M); \
+    k_ln_bwd_bf16<NV><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
         (const bf16*)x, (const bf16*)w, mean, rstd, (const bf16*)dy, (bf16*)dx, scratch, M, C, \
         accumulate ? 1 : 0)
-    if (nv == 1) LNB(1); else if (nv == 2) LNB(2); else if (nv == 3) LNB(3); else LNB(4);
+    if (nv == 1) { LNB(1); } else if (nv == 2) { LNB(2); } else if (nv == 3) { LNB(3); } else { LNB(4); }
 #undef LNB
     L.count();
     k_sum_rows<<<(2 * C + 31) / 32, 256, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db);
@@ -397,7 +422,22 @@ k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part
     const long long r1 = min((long long)M, r0 + CS_ROWS);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (n8 < N) {
-        for (long long r = r0 + warp; r < r1; r += 8) {
+        // rows r0 + warp + 8j in increasing j; 8 loads in flight per thread
+        constexpr int U = 8;
+        long long r = r0 + warp;
+        for (; r + 8 * (U - 1) < r1; r += 8 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) v[u] = *reinterpret_cast<const uint4*>(x + (r + 8 * u) * N + n8);
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                float f[8];
+                unpack8(v[u], f);
+#pragma unroll
+                for (int e = 0; e < 8; e++) acc[e] += f[e];
+            }
+        }
+        for (; r < r1; r += 8) {
             float f[8];
             unpack8(*reinterpret_cast<const uint4*>(x + r * N + n8), f);
 #pragma unroll
