@@ -12,14 +12,20 @@
 //               bf16 operand of the next MMA into shared memory in the
 //               128-byte-swizzled K-major layout the MMA reads.
 //
+// In every kernel the MMA warp issues the next block's score MMAs as soon as
+// the row threads have copied the current scores from TMEM to registers, and
+// the row threads compute the next MMA operand in registers before they wait
+// for its shared-memory buffer, so the tensor pipe and the elementwise work
+// overlap instead of taking turns.
+//
 // Forward (one CTA per 128 queries, 3 CTAs/SM): S = Q K_j^T; online softmax
-//   in base 2; P_j to shared memory; O += P_j V_j accumulates in TMEM (V read
-//   as an MN-major operand), rescaled in place only when the row max grows by
-//   more than 2^8; finally y = O / l and the row's log-sum-exp.
+//   in base 2; P_j to shared memory (two buffers); O += P_j V_j accumulates in
+//   TMEM (V read as an MN-major operand), rescaled in place only when the row
+//   max grows by more than 2^8; finally y = O / l and the row's log-sum-exp.
 // Backward, deterministic (no atomics):
 //   dQ kernel (one CTA per 128 queries, 2 CTAs/SM): D = rowsum(dO o O);
 //     S = Q K_j^T, dP = dO V_j^T; dS = P o (dP - D) with P from the saved
-//     log-sum-exp; dQ += dS K_j accumulates in TMEM.
+//     log-sum-exp (two dS buffers); dQ += dS K_j accumulates in TMEM.
 //   dK/dV kernel (one CTA per 128 keys, 2 CTAs/SM): S^T = K Q_j^T,
 //     dP^T = V dO_j^T; P^T and dS^T; dV += P^T dO_j, dK += dS^T Q_j in TMEM
 //     (Q_j and dO_j, loaded K-major, are read again as MN-major operands).
@@ -88,15 +94,20 @@ __device__ __forceinline__ void init_done() {
 }
 
 // ================================================================== forward
+// The softmax warps never wait for the P.V product of the previous block in
+// the common case: P is double-buffered in shared memory (buffer j & 1, with
+// its own full / consumed barriers), the exponentials of block j are
+// computed in registers while P_{j-1} V_{j-1} runs, and the warps wait for
+// the previous product only when the row maximum forces a rescale of O.
 constexpr int F_Q = 0;
 constexpr int F_K = F_Q + T128;     // 2 stages
 constexpr int F_V = F_K + 2 * T64;  // 1 stage
-constexpr int F_P = F_V + T64;      // P: [128 x 64] bf16
-constexpr int F_BAR = F_P + T128;
+constexpr int F_P = F_V + T64;      // P: 2 x [128 x 64] bf16
+constexpr int F_BAR = F_P + 2 * T128;
 constexpr int F_SMEM = F_BAR + 256 + 1024;
-constexpr uint32_t F_TMEM = 128;    // S: cols 0..63, O_j: 64..127
+constexpr uint32_t F_TMEM = 128;    // S: cols 0..63, O: 64..127
 
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 3)
 k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -109,9 +120,9 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     uint64_t* v_empty = bars + 6;
     uint64_t* s_full = bars + 7;
     uint64_t* s_free = bars + 8;
-    uint64_t* p_full = bars + 9;
-    uint64_t* o_full = bars + 10;
-    uint32_t* tmem_holder = (uint32_t*)(bars + 11);
+    uint64_t* p_full = bars + 9;   // [2]: P buffer written
+    uint64_t* o_full = bars + 11;  // [2]: P.V of a block in buffer s done (buffer s consumed)
+    uint32_t* tmem_holder = (uint32_t*)(bars + 13);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int nqt = gridDim.x;
@@ -131,8 +142,10 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(v_empty, 1);
         mbar_init(s_full, 1);
         mbar_init(s_free, 128);
-        mbar_init(p_full, 128);
-        mbar_init(o_full, 1);
+        mbar_init(&p_full[0], 128);
+        mbar_init(&p_full[1], 128);
+        mbar_init(&o_full[0], 1);
+        mbar_init(&o_full[1], 1);
         *abort_flag = 0;
         init_done();
     }
@@ -173,7 +186,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         if (lane == 0) {
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_O = idesc_bf16(BQ, D, false, true);
-            const uint32_t sq = smem_u32(sm + F_Q), sp = smem_u32(sm + F_P), sv = smem_u32(sm + F_V);
+            const uint32_t sq = smem_u32(sm + F_Q), sv = smem_u32(sm + F_V);
             bool ok = mbar_wait(q_full, 0, abort_flag, flags, 0x100 + 3);
             // S_{j+1} is issued as soon as the row threads hold S_j in registers,
             // so that it overlaps the softmax of block j
@@ -193,14 +206,16 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if (ok) ok = issue_s(0);
             for (int j = 0; j < nkv && ok; j++) {
                 if (j + 1 < nkv && !issue_s(j + 1)) break;
-                if (!mbar_wait(p_full, j & 1, abort_flag, flags, 0x100 + 6)) break;
+                const int pb = j & 1;
+                if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, flags, 0x100 + 6)) break;
                 if (!mbar_wait(v_full, j & 1, abort_flag, flags, 0x100 + 7)) break;
                 tc_fence_after();
+                const uint32_t sp = smem_u32(sm + F_P + pb * T128);
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++)
                     umma_bf16(tmem + BN, sdesc(sp + 32 * k, 16, 1024), sdesc(sv + k * 2048, T64, 1024), ID_O,
                               (j > 0 || k > 0) ? 1u : 0u);
-                umma_commit(o_full);
+                umma_commit(&o_full[pb]);
                 umma_commit(v_empty);
             }
         }
@@ -209,9 +224,10 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const int r = quarter * 32 + lane;
         const int q = qt * BQ + r;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        // O accumulates in TMEM (the P.V MMAs add into it); P is taken relative
-        // to a reference max m that is raised -- and O, l rescaled in place --
-        // only when the row max exceeds it by more than 8 (P <= 2^8 otherwise)
+        // P is taken relative to a reference max m that is raised -- and O, l
+        // rescaled in place -- only when some row of the warp exceeds it by
+        // more than 8 (P <= 2^8 otherwise); the decision is a warp vote since
+        // the TMEM loads and stores of O are warp-collective
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; j++) {
@@ -236,62 +252,72 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 }
             }
             const float mn = fmaxf(m, mx * SL2);
-            if (j > 0) {
-                // P_{j-1} V_{j-1} is complete: P's buffer is free and O is current
-                if (!mbar_wait_warp(o_full, (j - 1) & 1, abort_flag, flags, 0x100 + 9)) { ok = false; break; }
-                tc_fence_after();
-                // warp-uniform decision: the TMEM loads and stores are warp-collective
-                if (__any_sync(0xffffffffu, mn > m + 8.0f)) {
-                    const float corr = ex2(m - mn);
-                    uint32_t v[32];
-                    tmem_ld32(tl + BN, v);
-#pragma unroll
-                    for (int d = 0; d < 32; d++) v[d] = __float_as_uint(__uint_as_float(v[d]) * corr);
-                    tmem_st32(tl + BN, v);
-                    tmem_ld32(tl + BN + 32, v);
-#pragma unroll
-                    for (int d = 0; d < 32; d++) v[d] = __float_as_uint(__uint_as_float(v[d]) * corr);
-                    tmem_st32(tl + BN + 32, v);
-                    tmem_st_wait();
-                    l *= corr;
-                    m = mn;
-                }
-            } else {
-                m = mn;
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, mn > m + 8.0f);
+            const float m_old = m;
+            if (j == 0 || rescale) m = mn;
+            const int pb = j & 1;
+            // buffer pb was last read by P_{j-2} V_{j-2} (long done, as a rule)
+            if (j >= 2 && !mbar_wait_warp(&o_full[pb], ((j - 2) >> 1) & 1, abort_flag, flags, 0x100 + 9)) {
+                ok = false;
+                break;
             }
-            // P = 2^(s*scale - m) as bf16 into shared memory
+            // P = 2^(s*scale - m) as bf16, each 32-column half straight to shared memory
+            uint8_t* pbuf = sm + F_P + pb * T128;
             float rs = 0.0f;
-            uint32_t pk[16];
+            {
+                uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                float p0 = ex2(fmaf(__uint_as_float(w0[e]), SL2, -m));
-                float p1 = ex2(fmaf(__uint_as_float(w0[e + 1]), SL2, -m));
-                if (diag) {
-                    if (e > kq) p0 = 0.0f;
-                    if (e + 1 > kq) p1 = 0.0f;
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = ex2(fmaf(__uint_as_float(w0[e]), SL2, -m));
+                    float p1 = ex2(fmaf(__uint_as_float(w0[e + 1]), SL2, -m));
+                    if (diag) {
+                        if (e > kq) p0 = 0.0f;
+                        if (e + 1 > kq) p1 = 0.0f;
+                    }
+                    rs += p0 + p1;
+                    pk[e >> 1] = pack_bf2(p0, p1);
                 }
-                rs += p0 + p1;
-                pk[e >> 1] = pack_bf2(p0, p1);
-            }
-            store_row32(sm + F_P, r, 0, pk);
+                store_row32(pbuf, r, 0, pk);
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                float p0 = ex2(fmaf(__uint_as_float(w1[e]), SL2, -m));
-                float p1 = ex2(fmaf(__uint_as_float(w1[e + 1]), SL2, -m));
-                if (diag) {
-                    if (32 + e > kq) p0 = 0.0f;
-                    if (33 + e > kq) p1 = 0.0f;
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = ex2(fmaf(__uint_as_float(w1[e]), SL2, -m));
+                    float p1 = ex2(fmaf(__uint_as_float(w1[e + 1]), SL2, -m));
+                    if (diag) {
+                        if (32 + e > kq) p0 = 0.0f;
+                        if (33 + e > kq) p1 = 0.0f;
+                    }
+                    rs += p0 + p1;
+                    pk[e >> 1] = pack_bf2(p0, p1);
                 }
-                rs += p0 + p1;
-                pk[e >> 1] = pack_bf2(p0, p1);
+                store_row32(pbuf, r, 32, pk);
             }
-            store_row32(sm + F_P, r, 32, pk);
+            if (rescale) {
+                // O must hold P_{j-1} V_{j-1} before it is scaled
+                if (!mbar_wait_warp(&o_full[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag, flags, 0x100 + 10)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float corr = ex2(m_old - m);
+                uint32_t v[32];
+                tmem_ld32(tl + BN, v);
+#pragma unroll
+                for (int d = 0; d < 32; d++) v[d] = __float_as_uint(__uint_as_float(v[d]) * corr);
+                tmem_st32(tl + BN, v);
+                tmem_ld32(tl + BN + 32, v);
+#pragma unroll
+                for (int d = 0; d < 32; d++) v[d] = __float_as_uint(__uint_as_float(v[d]) * corr);
+                tmem_st32(tl + BN + 32, v);
+                tmem_st_wait();
+                l *= corr;
+            }
             l += rs;
             tc_fence_before();  // orders the TMEM stores of a rescale before the next MMA
             fence_proxy_async_smem();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[pb]);
         }
-        if (ok && mbar_wait_warp(o_full, (nkv - 1) & 1, abort_flag, flags, 0x100 + 10)) {
+        const int jl = nkv - 1;
+        if (ok && mbar_wait_warp(&o_full[jl & 1], (jl >> 1) & 1, abort_flag, flags, 0x100 + 11)) {
             tc_fence_after();
             float o[D];
             uint32_t v[32];
@@ -318,8 +344,8 @@ constexpr int Q_Q = 0;
 constexpr int Q_O = Q_Q + T128;     // dO tile
 constexpr int Q_K = Q_O + T128;     // 2 stages
 constexpr int Q_V = Q_K + 2 * T64;  // 2 stages
-constexpr int Q_S = Q_V + 2 * T64;  // dS: [128 x 64] bf16
-constexpr int Q_BAR = Q_S + T128;
+constexpr int Q_S = Q_V + 2 * T64;  // dS: 2 x [128 x 64] bf16
+constexpr int Q_BAR = Q_S + 2 * T128;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
 constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191
 
@@ -336,10 +362,10 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint64_t* kv_empty = bars + 3;  // [2]
     uint64_t* s_full = bars + 5;
     uint64_t* s_free = bars + 6;
-    uint64_t* ds_full = bars + 7;
-    uint64_t* ds_free = bars + 8;
-    uint64_t* acc_full = bars + 9;
-    uint32_t* tmem_holder = (uint32_t*)(bars + 10);
+    uint64_t* ds_full = bars + 7;   // [2]: dS buffer written
+    uint64_t* ds_free = bars + 9;   // [2]: dS buffer consumed by its dQ MMA
+    uint64_t* acc_full = bars + 11;
+    uint32_t* tmem_holder = (uint32_t*)(bars + 12);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int nqt = gridDim.x;
@@ -357,8 +383,10 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&kv_empty[1], 1);
         mbar_init(s_full, 1);
         mbar_init(s_free, 128);
-        mbar_init(ds_full, 128);
-        mbar_init(ds_free, 1);
+        mbar_init(&ds_full[0], 128);
+        mbar_init(&ds_full[1], 128);
+        mbar_init(&ds_free[0], 1);
+        mbar_init(&ds_free[1], 1);
         mbar_init(acc_full, 1);
         *abort_flag = 0;
         init_done();
@@ -396,12 +424,14 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         if (lane == 0) {
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_Q = idesc_bf16(BQ, D, false, true);
-            const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O), sds = smem_u32(sm + Q_S);
+            const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O);
             bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2);
-            for (int j = 0; j < nkv && ok; j++) {
+            // S_{j+1} and dP_{j+1} are issued as soon as the row threads hold
+            // S_j and dP_j in registers, overlapping their elementwise work
+            auto issue_sdp = [&](int j) -> bool {
                 const int st = j & 1;
-                if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, flags, 0x200 + 3)) { ok = false; break; }
-                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 4)) { ok = false; break; }
+                if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, flags, 0x200 + 3)) return false;
+                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 4)) return false;
                 tc_fence_after();
                 const uint32_t sk = smem_u32(sm + Q_K + st * T64), sv = smem_u32(sm + Q_V + st * T64);
 #pragma unroll
@@ -411,14 +441,21 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int k = 0; k < D / 16; k++)
                     umma_bf16(tmem + BN, sdesc(so + 32 * k, 16, 1024), sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(s_full);
-                if (!mbar_wait(ds_full, j & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
+                return true;
+            };
+            if (ok) ok = issue_sdp(0);
+            for (int j = 0; j < nkv && ok; j++) {
+                if (j + 1 < nkv && !issue_sdp(j + 1)) { ok = false; break; }
+                const int db = j & 1;
+                if (!mbar_wait(&ds_full[db], (j >> 1) & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t sk = smem_u32(sm + Q_K + db * T64), sds = smem_u32(sm + Q_S + db * T128);
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++)
                     umma_bf16(tmem + 2 * BN, sdesc(sds + 32 * k, 16, 1024), sdesc(sk + k * 2048, T64, 1024),
                               ID_Q, (j > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&kv_empty[st]);
-                umma_commit(ds_free);
+                umma_commit(&kv_empty[db]);
+                umma_commit(&ds_free[db]);
             }
             if (ok) umma_commit(acc_full);
         }
@@ -451,13 +488,14 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const float Lq = qv ? lse[bh * T + q] * LOG2E : 0.0f;
         for (int j = 0; j < nkv && ok; j++) {
             if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x200 + 7)) { ok = false; break; }
-            if (!mbar_wait_warp(ds_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 8)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (j >= 2 * qt);
             const int kq = q - j * BN;
-#pragma unroll 1
+            // dS = P o (dP - D), packed bf16 in registers
+            uint32_t pk[32];
+#pragma unroll
             for (int c = 0; c < 2; c++) {
-                uint32_t sw[32], pw[32], pk[16];
+                uint32_t sw[32], pw[32];
                 tmem_ld32(tl + c * 32, sw);
                 tmem_ld32(tl + BN + c * 32, pw);
 #pragma unroll
@@ -468,14 +506,26 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         if (c * 32 + e > kq) d0 = 0.0f;
                         if (c * 32 + e + 1 > kq) d1 = 0.0f;
                     }
-                    pk[e >> 1] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
+                    pk[c * 16 + (e >> 1)] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
                 }
-                store_row32(sm + Q_S, r, c * 32, pk);
             }
             tc_fence_before();
-            mbar_arrive(s_free);
+            mbar_arrive(s_free);  // S and dP are consumed: the next pair may be computed
+            const int db = j & 1;
+            // buffer db was last read by the dQ MMA of block j - 2
+            if (j >= 2 && !mbar_wait_warp(&ds_free[db], ((j - 2) >> 1) & 1, abort_flag, flags, 0x200 + 8)) {
+                ok = false;
+                break;
+            }
+            uint32_t half[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) half[i] = pk[i];
+            store_row32(sm + Q_S + db * T128, r, 0, half);
+#pragma unroll
+            for (int i = 0; i < 16; i++) half[i] = pk[16 + i];
+            store_row32(sm + Q_S + db * T128, r, 32, half);
             fence_proxy_async_smem();
-            mbar_arrive(ds_full);
+            mbar_arrive(&ds_full[db]);
         }
         if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x200 + 9)) {
             tc_fence_after();
@@ -584,10 +634,12 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const uint32_t sk = smem_u32(sm + K_K), sv = smem_u32(sm + K_V);
             const uint32_t sp = smem_u32(sm + K_P), sds = smem_u32(sm + K_S);
             bool ok = mbar_wait(kv_full, 0, abort_flag, flags, 0x300 + 2);
-            for (int i = 0; i < nq && ok; i++) {
+            // S^T_{i+1} and dP^T_{i+1} are issued as soon as the row threads
+            // hold S^T_i and dP^T_i in registers
+            auto issue_st = [&](int i) -> bool {
                 const int st = i & 1;
-                if (!mbar_wait(&qo_full[st], (i >> 1) & 1, abort_flag, flags, 0x300 + 3)) { ok = false; break; }
-                if (!mbar_wait(st_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 4)) { ok = false; break; }
+                if (!mbar_wait(&qo_full[st], (i >> 1) & 1, abort_flag, flags, 0x300 + 3)) return false;
+                if (!mbar_wait(st_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 4)) return false;
                 tc_fence_after();
                 const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
 #pragma unroll
@@ -597,8 +649,15 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 for (int k = 0; k < D / 16; k++)
                     umma_bf16(tmem + BN, sdesc(sv + 32 * k, 16, 1024), sdesc(so + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(st_full);
+                return true;
+            };
+            if (ok) ok = issue_st(0);
+            for (int i = 0; i < nq && ok; i++) {
+                if (i + 1 < nq && !issue_st(i + 1)) { ok = false; break; }
+                const int st = i & 1;
                 if (!mbar_wait(ps_full, i & 1, abort_flag, flags, 0x300 + 5)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++) {
                     const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
@@ -623,38 +682,54 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
         bool ok = true;
         for (int i = 0; i < nq; i++) {
             const int j = j0 + i;
+            // the block's 64 queries: lane l holds the log-sum-exp and D of
+            // queries j*64 + l and j*64 + 32 + l (fetched before the wait)
+            float Ll[2], Dl[2];
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+                const int qq = j * BN + c * 32 + lane;
+                Ll[c] = qq < T ? __ldg(lrow + qq) * LOG2E : INFINITY;
+                Dl[c] = qq < T ? __ldg(drow + qq) : 0.0f;
+            }
             if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6)) { ok = false; break; }
-            if (!mbar_wait_warp(ps_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 7)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (i < 2);  // query blocks that overlap this key tile
-#pragma unroll 1
+            uint32_t pk[32], dk[32];
+#pragma unroll
             for (int c = 0; c < 2; c++) {
-                // the chunk's 32 queries: lane l fetches query q0 + l, then broadcasts
                 const int q0 = j * BN + c * 32;
-                const bool lv = q0 + lane < T;
-                const float Ll = lv ? __ldg(lrow + q0 + lane) * LOG2E : INFINITY;
-                const float Dl = lv ? __ldg(drow + q0 + lane) : 0.0f;
-                uint32_t sw[32], dw[32], pk[16], dk[16];
+                uint32_t sw[32], dw[32];
                 tmem_ld32(tl + c * 32, sw);
                 tmem_ld32(tl + BN + c * 32, dw);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float L0 = __shfl_sync(0xffffffffu, Ll, e), L1 = __shfl_sync(0xffffffffu, Ll, e + 1);
-                    const float D0 = __shfl_sync(0xffffffffu, Dl, e), D1 = __shfl_sync(0xffffffffu, Dl, e + 1);
+                    const float L0 = __shfl_sync(0xffffffffu, Ll[c], e), L1 = __shfl_sync(0xffffffffu, Ll[c], e + 1);
+                    const float D0 = __shfl_sync(0xffffffffu, Dl[c], e), D1 = __shfl_sync(0xffffffffu, Dl[c], e + 1);
                     float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L0));
                     float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L1));
                     if (diag) {
                         if (q0 + e < key) p0 = 0.0f;
                         if (q0 + e + 1 < key) p1 = 0.0f;
                     }
-                    pk[e >> 1] = pack_bf2(p0, p1);
-                    dk[e >> 1] = pack_bf2(p0 * (__uint_as_float(dw[e]) - D0), p1 * (__uint_as_float(dw[e + 1]) - D1));
+                    pk[c * 16 + (e >> 1)] = pack_bf2(p0, p1);
+                    dk[c * 16 + (e >> 1)] =
+                        pack_bf2(p0 * (__uint_as_float(dw[e]) - D0), p1 * (__uint_as_float(dw[e + 1]) - D1));
                 }
-                store_row32(sm + K_P, r, c * 32, pk);
-                store_row32(sm + K_S, r, c * 32, dk);
             }
             tc_fence_before();
-            mbar_arrive(st_free);
+            mbar_arrive(st_free);  // S^T and dP^T are consumed
+            // P^T and dS^T buffers: read by the dV / dK MMAs of block i - 1
+            if (!mbar_wait_warp(ps_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 7)) { ok = false; break; }
+            uint32_t half[16];
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+#pragma unroll
+                for (int t = 0; t < 16; t++) half[t] = pk[c * 16 + t];
+                store_row32(sm + K_P, r, c * 32, half);
+#pragma unroll
+                for (int t = 0; t < 16; t++) half[t] = dk[c * 16 + t];
+                store_row32(sm + K_S, r, c * 32, half);
+            }
             fence_proxy_async_smem();
             mbar_arrive(ps_full);
         }
