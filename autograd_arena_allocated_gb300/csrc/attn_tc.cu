@@ -160,18 +160,25 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const int xq = h * D, xk = C + h * D, xv = 2 * C + h * D;
             mbar_expect_tx(q_full, T128);
             tma_load_2d(smem_u32(sm + F_Q), &tq, q_full, xq, row0 + qt * BQ);
+            // K runs two blocks ahead of V: K_{j+2} needs only S_j done, while
+            // V_{j+1} has to wait for P_j V_j (V has one buffer)
             int issued_k = 0, issued_v = 0;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; j++) {
+            auto load_k = [&](int j) -> bool {
                 const int st = j & 1;
-                if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x100 + 1)) { ok = false; break; }
+                if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x100 + 1)) return false;
                 mbar_expect_tx(&k_full[st], T64);
                 tma_load_2d(smem_u32(sm + F_K + st * T64), &tk, &k_full[st], xk, row0 + j * BN);
                 ++issued_k;
+                return true;
+            };
+            ok = load_k(0) && (nkv < 2 || load_k(1));
+            for (int j = 0; j < nkv && ok; j++) {
                 if (!mbar_wait(v_empty, (j & 1) ^ 1, abort_flag, flags, 0x100 + 2)) { ok = false; break; }
                 mbar_expect_tx(v_full, T64);
                 tma_load_2d(smem_u32(sm + F_V), &tk, v_full, xv, row0 + j * BN);
                 ++issued_v;
+                if (j + 2 < nkv && !load_k(j + 2)) { ok = false; break; }
             }
             if (!ok) {  // let issued copies land before the CTA exits
                 const long long t0 = clock64();
@@ -236,21 +243,29 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const bool diag = (j >= 2 * qt);
             const int kq = q - j * BN;  // on the diagonal, key columns > kq are masked
             uint32_t w0[32], w1[32];
-            tmem_ld32(tl, w0);
-            tmem_ld32(tl + 32, w1);
+            tmem_ld32x2(tl, w0, tl + 32, w1);
             tc_fence_before();
             mbar_arrive(s_free);  // S is in registers: the next S may be computed
-            float mx = -INFINITY;
+            // row max over four independent chains (max is exact in any order)
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (!diag) {
 #pragma unroll
-                for (int e = 0; e < 32; e++) mx = fmaxf(mx, fmaxf(__uint_as_float(w0[e]), __uint_as_float(w1[e])));
+                for (int e = 0; e < 32; e += 2) {
+                    mq[0] = fmaxf(mq[0], __uint_as_float(w0[e]));
+                    mq[1] = fmaxf(mq[1], __uint_as_float(w0[e + 1]));
+                    mq[2] = fmaxf(mq[2], __uint_as_float(w1[e]));
+                    mq[3] = fmaxf(mq[3], __uint_as_float(w1[e + 1]));
+                }
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    if (e <= kq) mx = fmaxf(mx, __uint_as_float(w0[e]));
-                    if (32 + e <= kq) mx = fmaxf(mx, __uint_as_float(w1[e]));
+                for (int e = 0; e < 32; e += 2) {
+                    if (e <= kq) mq[0] = fmaxf(mq[0], __uint_as_float(w0[e]));
+                    if (e + 1 <= kq) mq[1] = fmaxf(mq[1], __uint_as_float(w0[e + 1]));
+                    if (32 + e <= kq) mq[2] = fmaxf(mq[2], __uint_as_float(w1[e]));
+                    if (33 + e <= kq) mq[3] = fmaxf(mq[3], __uint_as_float(w1[e + 1]));
                 }
             }
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             const float mn = fmaxf(m, mx * SL2);
             const bool rescale = j > 0 && __any_sync(0xffffffffu, mn > m + 8.0f);
             const float m_old = m;
@@ -263,7 +278,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             }
             // P = 2^(s*scale - m) as bf16, each 32-column half straight to shared memory
             uint8_t* pbuf = sm + F_P + pb * T128;
-            float rs = 0.0f;
+            float rs0 = 0.0f, rs1 = 0.0f;  // two independent chains
             {
                 uint32_t pk[16];
 #pragma unroll
@@ -274,7 +289,8 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                         if (e > kq) p0 = 0.0f;
                         if (e + 1 > kq) p1 = 0.0f;
                     }
-                    rs += p0 + p1;
+                    rs0 += p0;
+                    rs1 += p1;
                     pk[e >> 1] = pack_bf2(p0, p1);
                 }
                 store_row32(pbuf, r, 0, pk);
@@ -286,11 +302,13 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                         if (32 + e > kq) p0 = 0.0f;
                         if (33 + e > kq) p1 = 0.0f;
                     }
-                    rs += p0 + p1;
+                    rs0 += p0;
+                    rs1 += p1;
                     pk[e >> 1] = pack_bf2(p0, p1);
                 }
                 store_row32(pbuf, r, 32, pk);
             }
+            const float rs = rs0 + rs1;
             if (rescale) {
                 // O must hold P_{j-1} V_{j-1} before it is scaled
                 if (!mbar_wait_warp(&o_full[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag, flags, 0x100 + 10)) {
@@ -496,8 +514,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
             for (int c = 0; c < 2; c++) {
                 uint32_t sw[32], pw[32];
-                tmem_ld32(tl + c * 32, sw);
-                tmem_ld32(tl + BN + c * 32, pw);
+                tmem_ld32x2(tl + c * 32, sw, tl + BN + c * 32, pw);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float d0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -Lq)) * (__uint_as_float(pw[e]) - Dq);
@@ -699,8 +716,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int c = 0; c < 2; c++) {
                 const int q0 = j * BN + c * 32;
                 uint32_t sw[32], dw[32];
-                tmem_ld32(tl + c * 32, sw);
-                tmem_ld32(tl + BN + c * 32, dw);
+                tmem_ld32x2(tl + c * 32, sw, tl + BN + c * 32, dw);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float L0 = __shfl_sync(0xffffffffu, Ll[c], e), L1 = __shfl_sync(0xffffffffu, Ll[c], e + 1);

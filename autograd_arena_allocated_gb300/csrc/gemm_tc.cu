@@ -322,6 +322,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         int acc = 0;
         uint32_t acc_phase = 0;
         const bool d_vec = p.d_f32 ? ((p.ldd & 3) == 0) : ((p.ldd & 7) == 0);
+        // vector accesses also need 16-byte aligned base pointers
+        const bool aux_vec = d_vec && ((uintptr_t)p.aux & 15) == 0;
+        const bool res_vec = d_vec && ((uintptr_t)p.residual & 15) == 0;
+        const bool out_vec = d_vec && ((uintptr_t)p.D & 15) == 0;
         uint8_t* stg = smem + S * CF::STAGE_BYTES + CF::BAR_BYTES + (warp - 2) * 2 * 2048;
         int sbuf = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
@@ -364,7 +368,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         for (int j = 0; j < 32; j++) v[j] = gelu_tanh(v[j]);
                     } else if (p.epi == EPI_DGELU) {
                         float u_[32];
-                        if (row_ok) load32_bf16(p.aux + o, valid, d_vec, u_);
+                        if (row_ok) load32_bf16(p.aux + o, valid, aux_vec, u_);
                         else {
 #pragma unroll
                             for (int j = 0; j < 32; j++) u_[j] = 0.0f;
@@ -374,7 +378,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     }
                     if (p.residual && row_ok) {
                         float rr[32];
-                        load32_bf16(p.residual + o, valid, d_vec, rr);
+                        load32_bf16(p.residual + o, valid, res_vec, rr);
 #pragma unroll
                         for (int j = 0; j < 32; j++) v[j] += rr[j];
                     }
@@ -408,7 +412,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         for (int j = 0; j < 32; j++)
                             if (j < valid) v[j] += d[j];
                     }
-                    store32_f32(d, valid, d_vec, v);
+                    store32_f32(d, valid, out_vec, v);
                     continue;
                 }
                 if (p.bias) {
@@ -418,29 +422,29 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     for (int j = 0; j < 32; j++) v[j] += b[j];
                 }
                 if (p.epi == EPI_GELU) {
-                    store32_bf16(p.aux + o, valid, d_vec, v);
+                    store32_bf16(p.aux + o, valid, aux_vec, v);
 #pragma unroll
                     for (int j = 0; j < 32; j++) v[j] = gelu_tanh(v[j]);
                 } else if (p.epi == EPI_DGELU) {
                     float u_[32];
-                    load32_bf16(p.aux + o, valid, d_vec, u_);
+                    load32_bf16(p.aux + o, valid, aux_vec, u_);
 #pragma unroll
                     for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(u_[j]);
                 }
                 if (p.residual) {
                     float rr[32];
-                    load32_bf16(p.residual + o, valid, d_vec, rr);
+                    load32_bf16(p.residual + o, valid, res_vec, rr);
 #pragma unroll
                     for (int j = 0; j < 32; j++) v[j] += rr[j];
                 }
                 __nv_bfloat16* d = (__nv_bfloat16*)p.D + o;
                 if (p.accumulate) {
                     float old[32];
-                    load32_bf16(d, valid, d_vec, old);
+                    load32_bf16(d, valid, out_vec, old);
 #pragma unroll
                     for (int j = 0; j < 32; j++) v[j] += old[j];
                 }
-                store32_bf16(d, valid, d_vec, v);
+                store32_bf16(d, valid, out_vec, v);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
