@@ -360,9 +360,10 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 // ================================================================== backward: dQ
 constexpr int Q_Q = 0;
 constexpr int Q_O = Q_Q + T128;     // dO tile
-constexpr int Q_K = Q_O + T128;     // 2 stages
-constexpr int Q_V = Q_K + 2 * T64;  // 2 stages
-constexpr int Q_S = Q_V + 2 * T64;  // dS: 2 x [128 x 64] bf16
+constexpr int Q_KST = 3;             // K stages: K_j is held until dQ_j
+constexpr int Q_K = Q_O + T128;
+constexpr int Q_V = Q_K + Q_KST * T64;  // 2 stages: V_j is free once dP_j is done
+constexpr int Q_S = Q_V + 2 * T64;      // dS: 2 x [128 x 64] bf16
 constexpr int Q_BAR = Q_S + 2 * T128;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
 constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191
@@ -376,14 +377,16 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
     uint64_t* qo_full = bars + 0;
-    uint64_t* kv_full = bars + 1;   // [2]
-    uint64_t* kv_empty = bars + 3;  // [2]
-    uint64_t* s_full = bars + 5;
-    uint64_t* s_free = bars + 6;
-    uint64_t* ds_full = bars + 7;   // [2]: dS buffer written
-    uint64_t* ds_free = bars + 9;   // [2]: dS buffer consumed by its dQ MMA
-    uint64_t* acc_full = bars + 11;
-    uint32_t* tmem_holder = (uint32_t*)(bars + 12);
+    uint64_t* k_full = bars + 1;    // [3]
+    uint64_t* k_empty = bars + 4;   // [3]
+    uint64_t* v_full = bars + 7;    // [2]
+    uint64_t* v_empty = bars + 9;   // [2]
+    uint64_t* s_full = bars + 11;
+    uint64_t* s_free = bars + 12;
+    uint64_t* ds_full = bars + 13;  // [2]: dS buffer written
+    uint64_t* ds_free = bars + 15;  // [2]: dS buffer consumed by its dQ MMA
+    uint64_t* acc_full = bars + 17;
+    uint32_t* tmem_holder = (uint32_t*)(bars + 18);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int nqt = gridDim.x;
@@ -395,10 +398,14 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
     if (threadIdx.x == 0) {
         mbar_init(qo_full, 1);
-        mbar_init(&kv_full[0], 1);
-        mbar_init(&kv_full[1], 1);
-        mbar_init(&kv_empty[0], 1);
-        mbar_init(&kv_empty[1], 1);
+        for (int i = 0; i < Q_KST; i++) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
         mbar_init(s_full, 1);
         mbar_init(s_free, 128);
         mbar_init(&ds_full[0], 128);
@@ -421,21 +428,27 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_expect_tx(qo_full, 2 * T128);
             tma_load_2d(smem_u32(sm + Q_Q), &tq, qo_full, xq, row0 + qt * BQ);
             tma_load_2d(smem_u32(sm + Q_O), &to, qo_full, h * D, row0 + qt * BQ);
-            int issued = 0;
+            int issued_k = 0, issued_v = 0;
             bool ok = true;
             for (int j = 0; j < nkv; j++) {
-                const int st = j & 1;
-                if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x200 + 1)) { ok = false; break; }
-                mbar_expect_tx(&kv_full[st], 2 * T64);
-                tma_load_2d(smem_u32(sm + Q_K + st * T64), &tk, &kv_full[st], xk, row0 + j * BN);
-                tma_load_2d(smem_u32(sm + Q_V + st * T64), &tk, &kv_full[st], xv, row0 + j * BN);
-                ++issued;
+                const int ks = j % Q_KST, kr = j / Q_KST;
+                if (!mbar_wait(&k_empty[ks], (kr & 1) ^ 1, abort_flag, flags, 0x200 + 1)) { ok = false; break; }
+                mbar_expect_tx(&k_full[ks], T64);
+                tma_load_2d(smem_u32(sm + Q_K + ks * T64), &tk, &k_full[ks], xk, row0 + j * BN);
+                ++issued_k;
+                const int vs = j & 1;
+                if (!mbar_wait(&v_empty[vs], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x200 + 10)) { ok = false; break; }
+                mbar_expect_tx(&v_full[vs], T64);
+                tma_load_2d(smem_u32(sm + Q_V + vs * T64), &tk, &v_full[vs], xv, row0 + j * BN);
+                ++issued_v;
             }
-            if (!ok) {
+            if (!ok) {  // let issued copies land before the CTA exits
                 const long long t0 = clock64();
                 while (!mbar_try_wait(qo_full, 0) && clock64() - t0 < WAIT_CYCLES) {}
-                for (int j = (issued > 2 ? issued - 2 : 0); j < issued; j++)
-                    while (!mbar_try_wait(&kv_full[j & 1], (j >> 1) & 1) && clock64() - t0 < 2 * WAIT_CYCLES) {}
+                for (int j = (issued_k > Q_KST ? issued_k - Q_KST : 0); j < issued_k; j++)
+                    while (!mbar_try_wait(&k_full[j % Q_KST], (j / Q_KST) & 1) && clock64() - t0 < 2 * WAIT_CYCLES) {}
+                for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; j++)
+                    while (!mbar_try_wait(&v_full[j & 1], (j >> 1) & 1) && clock64() - t0 < 3 * WAIT_CYCLES) {}
             }
         }
     } else if (warp == 1) {
@@ -447,11 +460,12 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // S_{j+1} and dP_{j+1} are issued as soon as the row threads hold
             // S_j and dP_j in registers, overlapping their elementwise work
             auto issue_sdp = [&](int j) -> bool {
-                const int st = j & 1;
-                if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, flags, 0x200 + 3)) return false;
+                const int ks = j % Q_KST, vs = j & 1;
+                if (!mbar_wait(&k_full[ks], (j / Q_KST) & 1, abort_flag, flags, 0x200 + 3)) return false;
+                if (!mbar_wait(&v_full[vs], (j >> 1) & 1, abort_flag, flags, 0x200 + 11)) return false;
                 if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 4)) return false;
                 tc_fence_after();
-                const uint32_t sk = smem_u32(sm + Q_K + st * T64), sv = smem_u32(sm + Q_V + st * T64);
+                const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sv = smem_u32(sm + Q_V + vs * T64);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
                     umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
@@ -459,20 +473,21 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int k = 0; k < D / 16; k++)
                     umma_bf16(tmem + BN, sdesc(so + 32 * k, 16, 1024), sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(s_full);
+                umma_commit(&v_empty[vs]);  // V_j is no longer needed
                 return true;
             };
             if (ok) ok = issue_sdp(0);
             for (int j = 0; j < nkv && ok; j++) {
                 if (j + 1 < nkv && !issue_sdp(j + 1)) { ok = false; break; }
-                const int db = j & 1;
+                const int db = j & 1, ks = j % Q_KST;
                 if (!mbar_wait(&ds_full[db], (j >> 1) & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sk = smem_u32(sm + Q_K + db * T64), sds = smem_u32(sm + Q_S + db * T128);
+                const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sds = smem_u32(sm + Q_S + db * T128);
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++)
                     umma_bf16(tmem + 2 * BN, sdesc(sds + 32 * k, 16, 1024), sdesc(sk + k * 2048, T64, 1024),
                               ID_Q, (j > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&kv_empty[db]);
+                umma_commit(&k_empty[ks]);
                 umma_commit(&ds_free[db]);
             }
             if (ok) umma_commit(acc_full);
@@ -570,7 +585,8 @@ constexpr int K_Q = K_V + T128;     // 2 stages
 constexpr int K_O = K_Q + 2 * T64;  // 2 stages
 constexpr int K_P = K_O + 2 * T64;  // P^T: [128 keys x 64 queries]
 constexpr int K_S = K_P + T128;     // dS^T
-constexpr int K_BAR = K_S + T128;
+constexpr int K_LD = K_S + T128;    // per row warp: log-sum-exp and D of the block's 64 queries
+constexpr int K_BAR = K_LD + 4 * 128 * 4;
 constexpr int K_SMEM = K_BAR + 256 + 1024;
 constexpr uint32_t K_TMEM = 256;    // S^T 0..63, dP^T 64..127, dV 128..191, dK 192..255
 
@@ -697,17 +713,30 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const float* lrow = lse + bh * T;
         const float* drow = Dlt + bh * T;
         bool ok = true;
-        for (int i = 0; i < nq; i++) {
-            const int j = j0 + i;
-            // the block's 64 queries: lane l holds the log-sum-exp and D of
-            // queries j*64 + l and j*64 + 32 + l (fetched before the wait)
-            float Ll[2], Dl[2];
+        // The log-sum-exp (base 2) and D of query block i are fetched one block
+        // ahead into registers (lane l: queries 64i + l and 64i + 32 + l), then
+        // placed in this warp's slice of shared memory, from which every lane
+        // reads them as broadcasts.
+        float* sl = reinterpret_cast<float*>(sm + K_LD) + quarter * 128;  // [64 L | 64 D]
+        float Ln[2], Dn[2];
+        auto fetch = [&](int i) {
 #pragma unroll
             for (int c = 0; c < 2; c++) {
-                const int qq = j * BN + c * 32 + lane;
-                Ll[c] = qq < T ? __ldg(lrow + qq) * LOG2E : INFINITY;
-                Dl[c] = qq < T ? __ldg(drow + qq) : 0.0f;
+                const int qq = (j0 + i) * BN + c * 32 + lane;
+                Ln[c] = qq < T ? __ldg(lrow + qq) * LOG2E : INFINITY;
+                Dn[c] = qq < T ? __ldg(drow + qq) : 0.0f;
             }
+        };
+        fetch(0);
+        for (int i = 0; i < nq; i++) {
+            const int j = j0 + i;
+            __syncwarp();  // the previous block's reads of the slice are done
+            sl[lane] = Ln[0];
+            sl[32 + lane] = Ln[1];
+            sl[64 + lane] = Dn[0];
+            sl[96 + lane] = Dn[1];
+            __syncwarp();
+            if (i + 1 < nq) fetch(i + 1);
             if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (i < 2);  // query blocks that overlap this key tile
@@ -718,18 +747,25 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 uint32_t sw[32], dw[32];
                 tmem_ld32x2(tl + c * 32, sw, tl + BN + c * 32, dw);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float L0 = __shfl_sync(0xffffffffu, Ll[c], e), L1 = __shfl_sync(0xffffffffu, Ll[c], e + 1);
-                    const float D0 = __shfl_sync(0xffffffffu, Dl[c], e), D1 = __shfl_sync(0xffffffffu, Dl[c], e + 1);
-                    float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L0));
-                    float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L1));
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 L4 = *reinterpret_cast<const float4*>(sl + c * 32 + e);
+                    const float4 D4 = *reinterpret_cast<const float4*>(sl + 64 + c * 32 + e);
+                    float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L4.x));
+                    float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L4.y));
+                    float p2 = ex2(fmaf(__uint_as_float(sw[e + 2]), SL2, -L4.z));
+                    float p3 = ex2(fmaf(__uint_as_float(sw[e + 3]), SL2, -L4.w));
                     if (diag) {
                         if (q0 + e < key) p0 = 0.0f;
                         if (q0 + e + 1 < key) p1 = 0.0f;
+                        if (q0 + e + 2 < key) p2 = 0.0f;
+                        if (q0 + e + 3 < key) p3 = 0.0f;
                     }
                     pk[c * 16 + (e >> 1)] = pack_bf2(p0, p1);
+                    pk[c * 16 + (e >> 1) + 1] = pack_bf2(p2, p3);
                     dk[c * 16 + (e >> 1)] =
-                        pack_bf2(p0 * (__uint_as_float(dw[e]) - D0), p1 * (__uint_as_float(dw[e + 1]) - D1));
+                        pack_bf2(p0 * (__uint_as_float(dw[e]) - D4.x), p1 * (__uint_as_float(dw[e + 1]) - D4.y));
+                    dk[c * 16 + (e >> 1) + 1] =
+                        pack_bf2(p2 * (__uint_as_float(dw[e + 2]) - D4.z), p3 * (__uint_as_float(dw[e + 3]) - D4.w));
                 }
             }
             tc_fence_before();
