@@ -366,7 +366,8 @@ constexpr int Q_V = Q_K + Q_KST * T64;  // 2 stages: V_j is free once dP_j is do
 constexpr int Q_S = Q_V + 2 * T64;      // dS: 2 x [128 x 64] bf16
 constexpr int Q_BAR = Q_S + 2 * T128;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
-constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191
+constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191, Q 192..223, dO 224..255
+constexpr uint32_t Q_TQ = 192, Q_TO = 224;
 
 __global__ void __launch_bounds__(THREADS)
 k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -386,7 +387,8 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint64_t* ds_full = bars + 13;  // [2]: dS buffer written
     uint64_t* ds_free = bars + 15;  // [2]: dS buffer consumed by its dQ MMA
     uint64_t* acc_full = bars + 17;
-    uint32_t* tmem_holder = (uint32_t*)(bars + 18);
+    uint64_t* qo_tm = bars + 18;    // Q and dO copied into TMEM
+    uint32_t* tmem_holder = (uint32_t*)(bars + 19);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int nqt = gridDim.x;
@@ -413,6 +415,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(&ds_free[0], 1);
         mbar_init(&ds_free[1], 1);
         mbar_init(acc_full, 1);
+        mbar_init(qo_tm, 128);
         *abort_flag = 0;
         init_done();
     }
@@ -455,8 +458,9 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         if (lane == 0) {
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_Q = idesc_bf16(BQ, D, false, true);
-            const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O);
-            bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2);
+            // Q and dO, fixed for the CTA, are A operands read from TMEM
+            bool ok = mbar_wait(qo_tm, 0, abort_flag, flags, 0x200 + 2);
+            tc_fence_after();
             // S_{j+1} and dP_{j+1} are issued as soon as the row threads hold
             // S_j and dP_j in registers, overlapping their elementwise work
             auto issue_sdp = [&](int j) -> bool {
@@ -468,10 +472,10 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sv = smem_u32(sm + Q_V + vs * T64);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
+                    umma_bf16_ts(tmem, tmem + Q_TQ + 8 * k, sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
-                    umma_bf16(tmem + BN, sdesc(so + 32 * k, 16, 1024), sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
+                    umma_bf16_ts(tmem + BN, tmem + Q_TO + 8 * k, sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
                 umma_commit(s_full);
                 umma_commit(&v_empty[vs]);  // V_j is no longer needed
                 return true;
@@ -500,24 +504,44 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
         const long long bh = (long long)b * H + h;
         bool ok = mbar_wait_warp(qo_full, 0, abort_flag, flags, 0x200 + 6);
-        // D = rowsum(dO o O) for this query (dO row from the swizzled tile)
+        // Copy this row of Q and of dO from the swizzled tiles into TMEM (the A
+        // operands of S and dP), and form D = rowsum(dO o O) from the dO row.
         float Dq = 0.0f;
-        if (ok && qv) {
+        if (ok) {
+            const uint8_t* qrow = sm + Q_Q + r * 128;
             const uint8_t* orow = sm + Q_O + r * 128;
-            const uint4* yr = reinterpret_cast<const uint4*>(y + (long long)(row0 + q) * C + h * D);
+            uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 8; c++) {
-                const uint4 a = *reinterpret_cast<const uint4*>(orow + ((c ^ (r & 7)) * 16));
-                const uint4 bb = yr[c];
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    Dq = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), Dq);
-                    Dq = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), Dq);
-                }
+                const uint4 a = *reinterpret_cast<const uint4*>(qrow + ((c ^ (r & 7)) << 4));
+                w[4 * c] = a.x; w[4 * c + 1] = a.y; w[4 * c + 2] = a.z; w[4 * c + 3] = a.w;
             }
-            Dlt[bh * T + q] = Dq;
+            tmem_st32(tl + Q_TQ, w);
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                const uint4 a = *reinterpret_cast<const uint4*>(orow + ((c ^ (r & 7)) << 4));
+                w[4 * c] = a.x; w[4 * c + 1] = a.y; w[4 * c + 2] = a.z; w[4 * c + 3] = a.w;
+            }
+            tmem_st32(tl + Q_TO, w);
+            tmem_st_wait();
+            if (qv) {
+                const uint4* yr = reinterpret_cast<const uint4*>(y + (long long)(row0 + q) * C + h * D);
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint4 bb = yr[c];
+                    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t aw = w[4 * c + i];
+                        Dq = fmaf(__uint_as_float(aw << 16), __uint_as_float(bw[i] << 16), Dq);
+                        Dq = fmaf(__uint_as_float(aw & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), Dq);
+                    }
+                }
+                Dlt[bh * T + q] = Dq;
+            }
         }
+        tc_fence_before();
+        mbar_arrive(qo_tm);
         const float Lq = qv ? lse[bh * T + q] * LOG2E : 0.0f;
         for (int j = 0; j < nkv && ok; j++) {
             if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x200 + 7)) { ok = false; break; }
