@@ -470,12 +470,13 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 4)) return false;
                 tc_fence_after();
                 const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sv = smem_u32(sm + Q_V + vs * T64);
+                // the S and dP chains are independent: interleaved, so the tensor
+                // pipe overlaps them
 #pragma unroll
-                for (int k = 0; k < D / 16; k++)
+                for (int k = 0; k < D / 16; k++) {
                     umma_bf16_ts(tmem, tmem + Q_TQ + 8 * k, sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
-#pragma unroll
-                for (int k = 0; k < D / 16; k++)
                     umma_bf16_ts(tmem + BN, tmem + Q_TO + 8 * k, sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
+                }
                 umma_commit(s_full);
                 umma_commit(&v_empty[vs]);  // V_j is no longer needed
                 return true;
@@ -700,11 +701,10 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 tc_fence_after();
                 const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
 #pragma unroll
-                for (int k = 0; k < D / 16; k++)
+                for (int k = 0; k < D / 16; k++) {  // two independent chains, interleaved
                     umma_bf16(tmem, sdesc(sk + 32 * k, 16, 1024), sdesc(sq + 32 * k, 16, 1024), ID, k > 0);
-#pragma unroll
-                for (int k = 0; k < D / 16; k++)
                     umma_bf16(tmem + BN, sdesc(sv + 32 * k, 16, 1024), sdesc(so + 32 * k, 16, 1024), ID, k > 0);
+                }
                 umma_commit(st_full);
                 return true;
             };

@@ -67,6 +67,7 @@ struct Params {
     float* ws;  // split-K partials [splits][M][N]
     int* flags;
     int tma_store;  // bf16 outputs leave through shared memory and TMA stores
+    int ext_tma;    // the extra epilogue operand (GELU' input or residual) arrives by TMA loads
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -106,6 +107,20 @@ __device__ __forceinline__ void stage_row32(uint8_t* buf, int r, const float* v)
         w.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
         w.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
         *reinterpret_cast<uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4)) = w;
+    }
+}
+
+// Row r of a [32 rows x 32 bf16] buffer in the same 64-byte-swizzled layout
+// (as a TMA load with SWIZZLE_64B leaves it), as floats.
+__device__ __forceinline__ void load_row32(const uint8_t* buf, int r, float* v) {
+    const uint8_t* rowp = buf + r * 64;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4));
+        v[8 * c + 0] = bf_lo(w.x); v[8 * c + 1] = bf_hi(w.x);
+        v[8 * c + 2] = bf_lo(w.y); v[8 * c + 3] = bf_hi(w.y);
+        v[8 * c + 4] = bf_lo(w.z); v[8 * c + 5] = bf_hi(w.z);
+        v[8 * c + 6] = bf_lo(w.w); v[8 * c + 7] = bf_hi(w.w);
     }
 }
 
@@ -192,6 +207,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     uint64_t* tempty = tfull + 2;  // [2]
     uint32_t* tmem_base_holder = (uint32_t*)(tempty + 2);
     volatile int* abort_flag = (volatile int*)(tmem_base_holder + 1);
+    // two per epilogue warp: the extra operand's tile has landed in staging buffer 0 / 1
+    uint64_t* ebar = (uint64_t*)(smem + S * CF::STAGE_BYTES + 512);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -205,13 +222,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], EPI_WARPS * 32);
         }
+        for (int e = 0; e < 2 * EPI_WARPS; e++) mbar_init(&ebar[e], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
         if (p.tma_store) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmD) : "memory");
-            if (p.epi == EPI_GELU) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
+            if (p.epi == EPI_GELU || p.ext_tma) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
         }
     }
     if (warp == 1) {
@@ -328,7 +346,97 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const bool out_vec = d_vec && ((uintptr_t)p.D & 15) == 0;
         uint8_t* stg = smem + S * CF::STAGE_BYTES + CF::BAR_BYTES + (warp - 2) * 2 * 2048;
         int sbuf = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        if (p.ext_tma) {
+            // bf16 result through shared memory and TMA stores, with the extra
+            // operand (GELU' input, or residual) of each 32 x 32 chunk TMA-loaded
+            // into the warp's staging buffer one chunk ahead.  A thread reads its
+            // row, writes its result row over it, and lane 0 stores the buffer.
+            // Every chunk is valid here (n_store is a multiple of BN).
+            const int ew = warp - 2;
+            uint64_t* eb = ebar + 2 * ew;
+            uint32_t eph = 0u, pending = 0u;  // bit b: phase of ebar b / a load into buffer b in flight
+            const int y_off = quarter * 32;
+            auto issue_ext = [&](int b, int n, int y) {
+                if (lane == 0) {
+                    mbar_expect_tx(&eb[b], 2048);
+                    tma_load_2d(smem_u32(stg + b * 2048), &tmX, &eb[b], n, y);
+                }
+                pending |= 1u << b;
+            };
+            int k = 0;  // chunk counter of this warp; buffer k & 1
+            if (blockIdx.x < p.units) {
+                const int t0 = (int)blockIdx.x / p.splits;
+                issue_ext(0, tile_n(p, t0) * BN + half * CHUNKS * 32, tile_m(p, t0) * BM + y_off);
+            }
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                const int tile = u / p.splits;
+                const int m0 = tile_m(p, tile) * BM;
+                const int n0 = tile_n(p, tile) * BN;
+                if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int i = 0; i < CHUNKS; i++, k++) {
+                    const int c = half * CHUNKS + i;
+                    const int n = n0 + c * 32;
+                    const int b = k & 1;
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                    // the next chunk's operand goes to the other buffer once that
+                    // buffer's last store has been read out
+                    int nn = -1, ny = 0;
+                    if (i + 1 < CHUNKS) {
+                        nn = n + 32;
+                        ny = m0 + y_off;
+                    } else if (u + (int)gridDim.x < p.units) {
+                        const int t2 = (u + (int)gridDim.x) / p.splits;
+                        nn = tile_n(p, t2) * BN + half * CHUNKS * 32;
+                        ny = tile_m(p, t2) * BM + y_off;
+                    }
+                    if (nn >= 0) {
+                        if (lane == 0) bulk_wait_read<0>();
+                        __syncwarp();
+                        issue_ext(b ^ 1, nn, ny);
+                    }
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+                    if (p.bias) {
+                        float bb[32];
+                        load32_bf16(p.bias + n, 32, true, bb);
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] += bb[j];
+                    }
+                    if (!mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 5)) { ok = false; break; }
+                    eph ^= 1u << b;
+                    pending &= ~(1u << b);
+                    float e[32];
+                    load_row32(stg + b * 2048, lane, e);
+                    if (p.epi == EPI_DGELU) {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(e[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] += e[j];
+                    }
+                    stage_row32(stg + b * 2048, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmD, smem_u32(stg + b * 2048), n, m0 + y_off);
+                        bulk_commit();
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            // a load still in flight must land before the CTA's shared memory goes away
+            for (int b = 0; b < 2; b++)
+                if ((pending >> b) & 1u) mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 6);
+        }
+        for (int u = blockIdx.x; u < p.units && !p.ext_tma; u += gridDim.x) {
             const int tile = u / p.splits, split = u - tile * p.splits;
             const int m0 = tile_m(p, tile) * BM;
             const int n0 = tile_n(p, tile) * BN;
@@ -631,6 +739,12 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
         if (ok2 && g.epi == EPI_GELU)
             ok2 = tc::make_map(&mx, g.aux, ns, g.M, g.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         pl.p.tma_store = ok2 ? 1 : 0;
+        // the extra operand of the GELU' or residual epilogue by TMA loads, same
+        // box and layout as the stores (needs whole chunks: n_store % BN == 0)
+        const void* ext = g.epi == EPI_DGELU ? g.aux : (g.epi == EPI_STORE ? g.residual : nullptr);
+        if (ok2 && ext && (ns % pl.BN) == 0 && ((uintptr_t)ext & 15) == 0 &&
+            tc::make_map(&mx, ext, ns, g.M, g.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            pl.p.ext_tma = 1;
     }
     bool launched;
     if (pl.BN == 256) {

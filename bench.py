@@ -212,7 +212,69 @@ OP_SHAPES = {
     "xent": "fused cross entropy over [32768,50304] logits",
     "embed_bwd": "embedding-gradient scatter, 32768 Zipf tokens, C=768",
     "adamw": "AdamW over 124,439,808 parameters",
+    "gemm_shapes": "every GEMM of one 124M step (12 per-layer forms + the LM head), one row each",
 }
+
+
+def run_gemm_shapes(args):
+    """Times every distinct GEMM of the 124M step (CUDA events, `--reps` calls each)."""
+    import torch
+
+    from autograd_arena_allocated_gb300 import api
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    dev, bf = "cuda", torch.bfloat16
+    M, C, Vp, V = 32768, 768, 50304, 50257
+
+    def rnd(*shape, scale=1.0):
+        g = torch.Generator(device=dev).manual_seed(0)
+        return (torch.randn(*shape, device=dev, generator=g) * scale).to(bf)
+
+    def timed(label, flops, fn):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.reps
+        print(json.dumps({"gemm": label, "us": round(ms * 1e3, 1),
+                          "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}), flush=True)
+
+    ctx = api.Context(4 << 30)
+    # the four linear layers of a block: (name, N out, K in, GELU epilogue, residual epilogue)
+    layers = [("qkv", 3 * C, C, False, False), ("proj", C, C, False, True),
+              ("fc", 4 * C, C, True, False), ("fcproj", C, 4 * C, False, True)]
+    for name, N, K, gelu, res in layers:
+        x, W, b = rnd(M, K), rnd(N, K, scale=0.02), rnd(N)
+        r = rnd(M, N) if res else None
+        y = torch.empty(M, N, device=dev, dtype=bf)
+        pre = torch.empty(M, N, device=dev, dtype=bf) if gelu else None
+        dy = rnd(M, N)
+        dx = torch.empty(M, K, device=dev, dtype=bf)
+        upre = rnd(M, K) if name == "fcproj" else None  # its input came through the FC GELU
+        dW, db = torch.empty(N, K, device=dev), torch.empty(N, device=dev)
+        f = 2.0 * M * N * K
+        timed(f"fwd {name}", f, lambda: ctx.linear_fwd("bf16", x, W, b, r, y, pre, M, K, N, gelu=gelu))
+        timed(f"dx {name}", f, lambda: ctx.linear_bwd_dx("bf16", dy, W, upre, dx, M, K, N))
+        timed(f"dw {name}", f, lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", dy, x, dW, db, M, K, N)))
+        del x, W, b, r, y, pre, dy, dx, upre, dW, db
+    # tied LM head: logits [M, Vp] = hf wte^T (rows >= V of wte read as zero)
+    # the op takes W as [N, K] = [Vp, C]: the pad rows V..Vp-1 are zero
+    hf, wte = rnd(M, C), rnd(Vp, C, scale=0.02)
+    wte[V:].zero_()
+    z = rnd(M, Vp)
+    dhf = torch.empty(M, C, device=dev, dtype=bf)
+    f = 2.0 * M * Vp * C
+    timed("fwd lm", f, lambda: ctx.linear_fwd("bf16", hf, wte, None, None, z, None, M, C, Vp))
+    timed("dx lm", f, lambda: ctx.linear_bwd_dx("bf16", z, wte, None, dhf, M, C, Vp))
+    ctx.close()
+    return 0
 
 
 def run_op(args):
@@ -250,9 +312,10 @@ def run_op(args):
         fn = lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", dy, x, dW, None, M, C, 4 * C))
         flops = 2.0 * M * C * 4 * C
     elif op == "gemm_lm":
-        x, W = rnd(M, C), rnd(V, C, scale=0.02)
+        # the op takes W as [N, K] = [Vp, C]: the pad rows V..Vp-1 are zero
+        x, W = rnd(M, C), rnd(Vp, C, scale=0.02)
+        W[V:].zero_()
         y = torch.empty(M, Vp, device=dev, dtype=bf)
-        from autograd_arena_allocated_gb300._native import lib
         fn = lambda: ctx.linear_fwd("bf16", x, W, None, None, y, None, M, C, Vp)
         flops = 2.0 * M * C * Vp
     elif op in ("attn_fwd", "attn_bwd"):
@@ -337,7 +400,7 @@ def main():
     args = ap.parse_args()
     if args.op:
         args.warmup = max(1, args.warmup)
-        return run_op(args)
+        return run_gemm_shapes(args) if args.op == "gemm_shapes" else run_op(args)
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     world, rank, local = dist_setup()
 
