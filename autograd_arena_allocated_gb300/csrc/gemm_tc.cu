@@ -638,11 +638,11 @@ static Plan make_plan(const Launch& L, const GemmArgs& g) {
     p.m_tiles = (g.M + BM - 1) / BM;
     p.n_tiles = (g.N + pl.BN - 1) / pl.BN;
     p.tiles = p.m_tiles * p.n_tiles;
-    // consecutive CTAs share the B operand's tiles when n is fastest; that is the
-    // better order whenever B (the weight, for the forward and input-gradient
-    // forms) is small next to the 129 MB L2, since A is then read from DRAM once
-    const double b_bytes = 2.0 * (double)g.N * (double)g.K;
-    p.n_fast = (b_bytes <= 24.0 * 1024 * 1024) ? 1 : 0;
+    // Tile order.  With n fastest, the CTAs running at the same time share A's
+    // row blocks, so A is read from DRAM once and B is re-read, wave after wave,
+    // from L2; with m fastest it is the other way round.  The larger operand is
+    // the one to stream once: A when M >= N (A holds M x K elements, B N x K).
+    p.n_fast = (g.M >= g.N) ? 1 : 0;
     p.kb_total = (g.K + BK - 1) / BK;
     p.splits = 1;
     const int sms = L.num_sms > 0 ? L.num_sms : 148;

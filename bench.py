@@ -273,6 +273,8 @@ def run_gemm_shapes(args):
     f = 2.0 * M * Vp * C
     timed("fwd lm", f, lambda: ctx.linear_fwd("bf16", hf, wte, None, None, z, None, M, C, Vp))
     timed("dx lm", f, lambda: ctx.linear_bwd_dx("bf16", z, wte, None, dhf, M, C, Vp))
+    dwte = torch.empty(Vp, C, device=dev)
+    timed("dw lm", f, lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", z, hf, dwte, None, M, C, Vp)))
     ctx.close()
     return 0
 
