@@ -216,6 +216,55 @@ OP_SHAPES = {
 }
 
 
+# DRAM bytes per launch group of each op kind (dram__bytes_read.sum +
+# dram__bytes_write.sum summed over the kind's kernels in one ncu capture of a
+# whole step of the workload, divided by the kind's launch groups per step),
+# valid only for the kernel sources whose digest is recorded: once any kernel
+# source differs, the roofline reports no traffic.
+MEASURED_TRAFFIC = {
+    "workload": "gpt2_124m_b32",
+    "sources": "f4b416334175f2a6",
+    "bytes_per_launch_group": {
+        "gemm_fwd": 346837065,
+        "gemm_dx": 297013467,
+        "gemm_dw": 294037765,
+        "attn_fwd": 179071061,
+        "attn_bwd": 560962261,
+        "xent": 6538611968,
+        "colsum": 114272165,
+        "ln_fwd": 54037279,
+        "ln_bwd": 170579395,
+        "adamw": 3671939072,
+        "embed_fwd": 12884224,
+        "embed_bwd": 124953344,
+    },
+}
+
+
+def kernel_sources_digest():
+    """Digest of the native sources (kernels, their headers and the C ABI)."""
+    import hashlib
+
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "autograd_arena_allocated_gb300", "csrc")
+    inc = os.path.join(root, "include")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    files += sorted(os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, kind):
+    t = MEASURED_TRAFFIC
+    if t["workload"] != workload or not t["sources"] or t["sources"] != kernel_sources_digest():
+        return None
+    return t["bytes_per_launch_group"].get(kind)
+
+
 def run_gemm_shapes(args):
     """Times every distinct GEMM of the 124M step (CUDA events, `--reps` calls each)."""
     import torch
@@ -524,7 +573,8 @@ def main():
         achieved = r["bytes"] / r["calls"] / (per_launch_ms * 1e-3) / 1e9
         peak, peak_name = peaks["hbm_gbs"], "hbm_gbs"
     roofline = {"kernel": top, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, top),
+                "traffic_unit": "bytes per launch group (ncu DRAM read + write)",
                 "peak_source": f"{peaks['source']} {peak_name}",
                 "per_launch": {"ms": per_launch_ms, "flops": r["flops"] / r["calls"],
                                "bytes": r["bytes"] / r["calls"]}}
