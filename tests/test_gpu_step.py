@@ -227,6 +227,20 @@ def _sampled_sequences(ctx, oracle, w, seqs):
     return g
 
 
+def test_gpt2_350m_bf16_reduced_batch(ctx, oracle):
+    """GPT-2 medium (L=24, C=1024, H=16) at B=1, T=64: every gradient tensor."""
+    _bf16_parity(ctx, oracle, synth.GPT2_350M, 1, 64, "zipf", jitter=0.0, label="350M B=1 T=64")
+
+
+def test_gpt2_124m_b8_full_batch_sampled(ctx, oracle):
+    _sampled_sequences(ctx, oracle, synth.WORKLOADS["gpt2_124m_b8"], [0, 7])
+
+
+def test_gpt2_350m_b8_full_batch_sampled(ctx, oracle):
+    g = _sampled_sequences(ctx, oracle, synth.WORKLOADS["gpt2_350m_b8"], [5])
+    assert torch.isfinite(g).all()
+
+
 def test_char_bf16_full_batch_sampled(ctx, oracle):
     _sampled_sequences(ctx, oracle, synth.WORKLOADS["char_bf16"], [0, 37, 63])
 
