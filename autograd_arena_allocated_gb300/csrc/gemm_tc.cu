@@ -43,11 +43,11 @@ constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB: 64 k-rows x 128 bytes
 
 template <int BN>
 struct Cfg {
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STAGES = (BN >= 192) ? 4 : 6;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // two accumulators, power of two
     static constexpr int BAR_BYTES = 1024;                 // barriers, padded to keep staging aligned
     static constexpr int STAGING_BYTES = EPI_WARPS * 2 * 2048;  // 2 x [32 rows x 64 B] per epilogue warp
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + STAGING_BYTES + 1024;
@@ -628,9 +628,9 @@ struct Plan {
     int grid;
 };
 
-static Plan make_plan(const Launch& L, const GemmArgs& g) {
+static Plan plan_for(const Launch& L, const GemmArgs& g, int BN) {
     Plan pl{};
-    pl.BN = (g.N <= 128) ? 128 : 256;
+    pl.BN = BN;
     Params& p = pl.p;
     p.M = g.M;
     p.N = g.N;
@@ -658,6 +658,11 @@ static Plan make_plan(const Launch& L, const GemmArgs& g) {
     p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
     p.units = p.tiles * p.splits;
     pl.grid = p.units < sms ? p.units : sms;
+    return pl;
+}
+
+static Plan finish_plan(const Launch& L, const GemmArgs& g, Plan pl) {
+    Params& p = pl.p;
     p.D = g.D;
     p.ldd = g.ldd;
     p.d_f32 = g.d_f32 ? 1 : 0;
@@ -671,6 +676,32 @@ static Plan make_plan(const Launch& L, const GemmArgs& g) {
     p.flags = L.flags;
     return pl;
 }
+
+// Tile width: 128 for narrow outputs, else 256.  The weight-gradient form
+// (both operands MN-major, few output tiles, split K) may take 192 instead
+// when that needs clearly fewer tile-times (waves of the persistent grid x
+// width x k-blocks per unit): its tiles then fill more of the SMs (for the
+// [2304, 768] QKV weight, 144 units instead of 108).  N = 192 MMAs run at a
+// lower rate per FLOP than N = 256, which outweighs the better wave fill of
+// the other forms.
+static Plan make_plan(const Launch& L, const GemmArgs& g) {
+    if (g.N <= 128) return finish_plan(L, g, plan_for(L, g, 128));
+    if (g.a_kmajor || g.b_kmajor) return finish_plan(L, g, plan_for(L, g, 256));
+    const int sms = L.num_sms > 0 ? L.num_sms : 148;
+    Plan best{};
+    double best_cost = 0.0;
+    for (int bn : {256, 192}) {
+        Plan c = plan_for(L, g, bn);
+        const double waves = (double)((c.p.units + sms - 1) / sms);
+        const double cost = waves * bn * (double)c.p.kb_per_split;
+        if (bn == 256 || cost < 0.92 * best_cost) {  // 192 must win clearly
+            best = c;
+            best_cost = cost;
+        }
+    }
+    return finish_plan(L, g, best);
+}
+
 
 }  // namespace tc
 
@@ -751,6 +782,8 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
         if (!a_mn && !b_mn) launched = launch_tc<256, false, false>(L, pl, ma, mb, md, mx);
         else if (!a_mn) launched = launch_tc<256, false, true>(L, pl, ma, mb, md, mx);
         else launched = launch_tc<256, true, true>(L, pl, ma, mb, md, mx);
+    } else if (pl.BN == 192) {  // weight-gradient form only
+        launched = (a_mn && b_mn) && launch_tc<192, true, true>(L, pl, ma, mb, md, mx);
     } else {
         if (!a_mn && !b_mn) launched = launch_tc<128, false, false>(L, pl, ma, mb, md, mx);
         else if (!a_mn) launched = launch_tc<128, false, true>(L, pl, ma, mb, md, mx);

@@ -207,8 +207,18 @@ k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* _
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
     float s = 0.0f;
-    if (c < ncols)
-        for (int g = warp; g < G; g += 8) s += part[(long long)g * ncols + c];
+    if (c < ncols) {
+        // rows warp, warp + 8, ... added in that order; eight loads in flight
+        int g = warp;
+        for (; g + 56 < G; g += 64) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) v[u] = part[(long long)(g + 8 * u) * ncols + c];
+#pragma unroll
+            for (int u = 0; u < 8; u++) s += v[u];
+        }
+        for (; g < G; g += 8) s += part[(long long)g * ncols + c];
+    }
     sm[warp][lane] = s;
     __syncthreads();
     if (warp == 0 && c < ncols) {
