@@ -48,6 +48,7 @@ def lib():
             "or_embed_bwd": (None, [dp, ip, i, i, i, dp, dp]),
             "or_adamw": (None, [dp, dp, dp, dp, sz, d, d, d, d, d, i]),
             "or_gpt2_step": (d, [i, i, i, i, i, dp, ip, ip, i, i, dp, dp]),
+            "or_gpt2_logits_last": (i, [i, i, i, i, i, dp, ip, i, i, dp]),
             "or_val_reset": (None, []),
             "or_val_leaf": (i, [d]),
             "or_val_add": (i, [i, i]),
@@ -235,6 +236,19 @@ def gpt2_step(shape, params, tokens, targets, want_grads=True, want_row_loss=Fal
     loss = lib().or_gpt2_step(shape.L, shape.C, shape.H, shape.V, shape.maxT, _d(P),
                               _i(tokens), _i(targets), B, T, _d(G), _d(rl))
     return float(loss), G, rl
+
+
+def gpt2_logits_last(shape, params, tokens):
+    """Logits of each sequence's last position, float64 [B, V] (forward only)."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, T = tokens.shape
+    P = f64(params)
+    out = np.zeros((B, shape.V))
+    rc = lib().or_gpt2_logits_last(shape.L, shape.C, shape.H, shape.V, shape.maxT, _d(P), _i(tokens),
+                                   B, T, _d(out))
+    if rc != 0:
+        raise ValueError("bad arguments to or_gpt2_logits_last")
+    return out
 
 
 # ---------------------------------------------------------------- scalar tape

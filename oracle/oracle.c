@@ -674,6 +674,53 @@ static void tp_free(otape* tp) {
 /* GPT-2 training step ([TT] 三.6 model, 三.7 loop steps 2-3)               */
 /* ------------------------------------------------------------------------ */
 
+/* The model's forward ([TT] 三.6) on the tape: embedding, L pre-LN blocks,
+ * final LayerNorm and the tied LM head.  Parameter tensors point straight into
+ * the flat vectors (and their gradients into G, when given).  Returns the
+ * logits [B*T, V]. */
+static otensor* tp_gpt2_forward(otape* tp, const or_config* cfg, const or_layout* o,
+                                const double* params, double* G, const int* tokens, int B, int T) {
+    const int L = cfg->L, C = cfg->C, H = cfg->H, V = cfg->V, maxT = cfg->maxT;
+    const int M = B * T;
+#define PARAM(off, n) ot_wrap(tp, (double*)params + (off), G ? G + (off) : NULL, (n))
+    size_t Cz = (size_t)C;
+    otensor* wte = PARAM(o->wte, (size_t)V * Cz);
+    otensor* wpe = PARAM(o->wpe, (size_t)maxT * Cz);
+    otensor* x = tp_embed(tp, wte, wpe, tokens, B, T, C);
+    for (int l = 0; l < L; l++) {
+        size_t base = o->layers_begin + (size_t)l * o->layer_stride;
+        otensor* ln1w = PARAM(base + o->ln1w, Cz);
+        otensor* ln1b = PARAM(base + o->ln1b, Cz);
+        otensor* qkvw = PARAM(base + o->qkvw, 3 * Cz * Cz);
+        otensor* qkvb = PARAM(base + o->qkvb, 3 * Cz);
+        otensor* projw = PARAM(base + o->projw, Cz * Cz);
+        otensor* projb = PARAM(base + o->projb, Cz);
+        otensor* ln2w = PARAM(base + o->ln2w, Cz);
+        otensor* ln2b = PARAM(base + o->ln2b, Cz);
+        otensor* fcw = PARAM(base + o->fcw, 4 * Cz * Cz);
+        otensor* fcb = PARAM(base + o->fcb, 4 * Cz);
+        otensor* fpw = PARAM(base + o->fpw, 4 * Cz * Cz);
+        otensor* fpb = PARAM(base + o->fpb, Cz);
+        /* pre-LN block: LN -> attention -> residual -> LN -> MLP -> residual */
+        otensor* h = tp_layernorm(tp, x, ln1w, ln1b, M, C);
+        otensor* qkv = tp_linear(tp, h, qkvw, qkvb, M, C, 3 * C);
+        otensor* a = tp_attention(tp, qkv, B, T, C, H);
+        otensor* p = tp_linear(tp, a, projw, projb, M, C, C);
+        otensor* x1 = tp_add(tp, x, p);
+        otensor* h2 = tp_layernorm(tp, x1, ln2w, ln2b, M, C);
+        otensor* u = tp_linear(tp, h2, fcw, fcb, M, C, 4 * C);
+        otensor* g = tp_gelu(tp, u);
+        otensor* f = tp_linear(tp, g, fpw, fpb, M, 4 * C, C);
+        x = tp_add(tp, x1, f);
+    }
+    otensor* lnfw = PARAM(o->lnfw, Cz);
+    otensor* lnfb = PARAM(o->lnfb, Cz);
+    otensor* hf = tp_layernorm(tp, x, lnfw, lnfb, M, C);
+    /* tied LM head: logits = hf * wte^T */
+    return tp_linear(tp, hf, wte, NULL, M, C, V);
+#undef PARAM
+}
+
 /* Forward + backward of one batch.  params: flat [num_params] in the fixed
  * layout; grads (optional): overwritten with d(mean loss)/d(params);
  * row_loss (optional): [B*T] per-position losses.  Returns the mean loss,
@@ -686,54 +733,35 @@ OR_EXPORT double or_gpt2_step(int L, int C, int H, int V, int maxT,
         if (tokens[i] < 0 || tokens[i] >= V || targets[i] < 0 || targets[i] >= V) return NAN;
     or_config cfg = {L, C, H, V, maxT};
     or_layout o = or_make_layout(&cfg);
-    int M = B * T;
     otape tp;
     memset(&tp, 0, sizeof(tp));
     double* G = grads;
     if (G) memset(G, 0, sizeof(double) * o.total);
-    /* parameter tensors point straight into the flat vectors */
-#define PARAM(off, n) ot_wrap(&tp, (double*)params + (off), G ? G + (off) : NULL, (n))
-    size_t Cz = (size_t)C;
-    otensor* wte = PARAM(o.wte, (size_t)V * Cz);
-    otensor* wpe = PARAM(o.wpe, (size_t)maxT * Cz);
-    otensor* x = tp_embed(&tp, wte, wpe, tokens, B, T, C);
-    for (int l = 0; l < L; l++) {
-        size_t base = o.layers_begin + (size_t)l * o.layer_stride;
-        otensor* ln1w = PARAM(base + o.ln1w, Cz);
-        otensor* ln1b = PARAM(base + o.ln1b, Cz);
-        otensor* qkvw = PARAM(base + o.qkvw, 3 * Cz * Cz);
-        otensor* qkvb = PARAM(base + o.qkvb, 3 * Cz);
-        otensor* projw = PARAM(base + o.projw, Cz * Cz);
-        otensor* projb = PARAM(base + o.projb, Cz);
-        otensor* ln2w = PARAM(base + o.ln2w, Cz);
-        otensor* ln2b = PARAM(base + o.ln2b, Cz);
-        otensor* fcw = PARAM(base + o.fcw, 4 * Cz * Cz);
-        otensor* fcb = PARAM(base + o.fcb, 4 * Cz);
-        otensor* fpw = PARAM(base + o.fpw, 4 * Cz * Cz);
-        otensor* fpb = PARAM(base + o.fpb, Cz);
-        /* pre-LN block: LN -> attention -> residual -> LN -> MLP -> residual */
-        otensor* h = tp_layernorm(&tp, x, ln1w, ln1b, M, C);
-        otensor* qkv = tp_linear(&tp, h, qkvw, qkvb, M, C, 3 * C);
-        otensor* a = tp_attention(&tp, qkv, B, T, C, H);
-        otensor* p = tp_linear(&tp, a, projw, projb, M, C, C);
-        otensor* x1 = tp_add(&tp, x, p);
-        otensor* h2 = tp_layernorm(&tp, x1, ln2w, ln2b, M, C);
-        otensor* u = tp_linear(&tp, h2, fcw, fcb, M, C, 4 * C);
-        otensor* g = tp_gelu(&tp, u);
-        otensor* f = tp_linear(&tp, g, fpw, fpb, M, 4 * C, C);
-        x = tp_add(&tp, x1, f);
-    }
-    otensor* lnfw = PARAM(o.lnfw, Cz);
-    otensor* lnfb = PARAM(o.lnfb, Cz);
-    otensor* hf = tp_layernorm(&tp, x, lnfw, lnfb, M, C);
-    /* tied LM head: logits = hf * wte^T */
-    otensor* z = tp_linear(&tp, hf, wte, NULL, M, C, V);
-    otensor* loss = tp_xent(&tp, z, targets, M, V, row_loss);
-#undef PARAM
+    otensor* z = tp_gpt2_forward(&tp, &cfg, &o, params, G, tokens, B, T);
+    otensor* loss = tp_xent(&tp, z, targets, B * T, V, row_loss);
     double lv = loss->v[0];
     if (G) tp_backward(&tp, loss);
     tp_free(&tp);
     return lv;
+}
+
+/* The logits of each sequence's last position, [B][V] (the distribution the
+ * next token is drawn from when generating; [TT] 八.3 generates text after
+ * training).  Returns 0, or -1 on bad arguments. */
+OR_EXPORT int or_gpt2_logits_last(int L, int C, int H, int V, int maxT, const double* params,
+                                  const int* tokens, int B, int T, double* logits_last) {
+    if (B <= 0 || T <= 0 || T > maxT || C % H != 0 || !logits_last) return -1;
+    for (size_t i = 0; i < (size_t)B * T; i++)
+        if (tokens[i] < 0 || tokens[i] >= V) return -1;
+    or_config cfg = {L, C, H, V, maxT};
+    or_layout o = or_make_layout(&cfg);
+    otape tp;
+    memset(&tp, 0, sizeof(tp));
+    otensor* z = tp_gpt2_forward(&tp, &cfg, &o, params, NULL, tokens, B, T);
+    for (int b = 0; b < B; b++)
+        memcpy(logits_last + (size_t)b * V, z->v + ((size_t)b * T + (T - 1)) * V, sizeof(double) * (size_t)V);
+    tp_free(&tp);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -216,3 +216,39 @@ def test_thread_count_does_not_change_results(oracle):
     oracle.set_threads(n0)
     assert l1 == l2
     np.testing.assert_array_equal(g1, g2)
+
+
+def test_last_position_logits_agree_with_the_step(oracle):
+    """or_gpt2_logits_last against the pinned step: for every prefix length t,
+    log-sum-exp(z) - z[target] of the last-position logits of tokens[:, :t] is
+    the step's per-position loss at position t - 1 of the full sequence (which
+    also pins causality: later tokens do not change earlier positions)."""
+    sh = Shape(2, 32, 4, 97, 16)
+    B, T = 2, 9
+    p, tok, tgt = _inputs(sh, B, T)
+    p = p + 0.05 * synth.normals(7, 0, p.size)  # no constant tensors
+    _, _, rl = oracle.gpt2_step(sh, p, tok, tgt, want_grads=False, want_row_loss=True)
+    rl = rl.reshape(B, T)
+    for t in range(1, T + 1):
+        z = oracle.gpt2_logits_last(sh, p, tok[:, :t])
+        assert z.shape == (B, sh.V)
+        zmax = z.max(axis=1, keepdims=True)
+        lse = zmax[:, 0] + np.log(np.exp(z - zmax).sum(axis=1))
+        ce = lse - z[np.arange(B), tgt[:, t - 1]]
+        np.testing.assert_allclose(ce, rl[:, t - 1], rtol=1e-12, atol=1e-13)
+
+
+def test_last_position_logits_zero_embedding_and_bad_arguments(oracle):
+    sh = Shape(1, 16, 2, 33, 8)
+    p, tok, _ = _inputs(sh, 2, 5)
+    off, n = oracle.param_offset(sh.L, sh.C, sh.H, sh.V, sh.maxT, 0, 0)
+    p[off:off + n] = 0.0  # tied head: logits = hf wte^T = 0
+    assert np.all(oracle.gpt2_logits_last(sh, p, tok) == 0.0)
+    bad = tok.copy()
+    bad[0, 0] = sh.V
+    try:
+        oracle.gpt2_logits_last(sh, p, bad)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("an out-of-range token must be rejected")
