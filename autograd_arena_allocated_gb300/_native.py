@@ -58,6 +58,9 @@ SIGNATURES = {
     "tt_ctx_copy_row_losses": (_st, [_vp, _vp, _sz]),
     "tt_adamw": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _i]),
     "tt_cast_f32_to_bf16": (_st, [_vp, _vp, _vp, _sz]),
+    "tt_gpt2_eval": (_st, [_vp, _vp, _vp, _vp, _i, _i, C.POINTER(C.c_float)]),
+    "tt_gpt2_generate_arena_bytes": (_sz, [_vp, _i, _i, _i]),
+    "tt_gpt2_generate": (_st, [_vp, _vp, _vp, _i, _i, _i, _vp]),
     # tt_ops.h
     "tt_ctx_set_gemm_backend": (_st, [_vp, _i]),
     "tt_op_linear_fwd": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i]),

@@ -47,6 +47,11 @@ def param_offset(cfg: GPT2Config, layer: int, which: int):
     return int(off.value), int(n.value)
 
 
+def generate_arena_bytes(cfg, B: int, T_prompt: int, n_new: int) -> int:
+    """Exact arena bytes of tt_gpt2_generate."""
+    return int(lib().tt_gpt2_generate_arena_bytes(C.byref(cfg), int(B), int(T_prompt), int(n_new)))
+
+
 def arena_bytes(cfg: GPT2Config, B: int, T: int) -> int:
     return int(lib().tt_gpt2_arena_bytes(C.byref(cfg), B, T))
 
@@ -143,6 +148,19 @@ class Context:
                                        _ptr(targets), int(B), int(T),
                                        C.byref(loss) if sync else None))
         return float(loss.value) if sync else None
+
+    def eval(self, params, tokens, targets, B: int, T: int) -> float:
+        """tt_gpt2_eval: forward and mean loss only (synchronizes)."""
+        loss = C.c_float()
+        self._check(lib().tt_gpt2_eval(self.h, _ptr(params), _ptr(tokens), _ptr(targets), int(B), int(T),
+                                       C.byref(loss)))
+        return float(loss.value)
+
+    def generate(self, params, prompt, B: int, T_prompt: int, n_new: int, out):
+        """tt_gpt2_generate: greedy tokens; out [B, T_prompt + n_new] int32 (host or device)."""
+        self._check(lib().tt_gpt2_generate(self.h, _ptr(params), _ptr(prompt), int(B), int(T_prompt), int(n_new),
+                                           _ptr(out)))
+        return out
 
     def loss_device(self):
         """(mean_loss_ptr, row_losses_ptr) device addresses of the last step."""

@@ -509,13 +509,16 @@ static Offsets offsets_of(const tt_gpt2_config* m) {
 }
 
 // ------------------------------------------------------------------ the step
-static tt_status gpt2_forward_backward(tt_ctx* c, const void* params, float* grads,
-                                       const int32_t* tok, const int32_t* tgt, int B, int T) {
+// The model's forward on the tape (tinytorch 三.6): returns the logits tensor
+// [B*T, Vp].  grads may be NULL (no backward will follow); qkv, when given,
+// receives each layer's qkv tensor.
+static int gpt2_forward(tt_ctx* c, const void* params, float* grads, const int32_t* tok, int B, int T,
+                        std::vector<int>* qkv_of_layer = nullptr) {
     const tt_gpt2_config& m = c->cfg;
     const size_t es = esize(m.dtype);
     const Offsets o = offsets_of(&m);
     auto P = [&](size_t off) -> const void* { return (const char*)params + off * es; };
-    auto G = [&](size_t off) -> float* { return grads + off; };
+    auto G = [&](size_t off) -> float* { return grads ? grads + off : nullptr; };
     const int C = m.C;
     const int Vp = padded_vocab(m.V);
 
@@ -526,6 +529,7 @@ static tt_status gpt2_forward_backward(tt_ctx* c, const void* params, float* gra
         auto GL = [&](int i) { return G(base + o.sub[i]); };
         int h = op_layernorm(c, x, PL(0), PL(1), GL(0), GL(1));
         int qkv = op_linear(c, h, PL(2), PL(3), GL(2), GL(3), 3 * C, -1, false);
+        if (qkv_of_layer) qkv_of_layer->push_back(qkv);
         int a = op_attention(c, qkv, B, T);
         int x1 = op_linear(c, a, PL(4), PL(5), GL(4), GL(5), C, x, false);
         int h2 = op_layernorm(c, x1, PL(6), PL(7), GL(6), GL(7));
@@ -534,10 +538,116 @@ static tt_status gpt2_forward_backward(tt_ctx* c, const void* params, float* gra
     }
     int hf = op_layernorm(c, x, P(o.lnfw), P(o.lnfb), G(o.lnfw), G(o.lnfb));
     // tied LM head: logits[M, Vp] = hf wte^T; wte rows >= V read as zero
-    int z = op_linear(c, hf, P(o.wte), nullptr, G(o.wte), nullptr, Vp, -1, false, m.V, Vp);
-    op_xent(c, z, tgt, m.V);
+    return op_linear(c, hf, P(o.wte), nullptr, G(o.wte), nullptr, Vp, -1, false, m.V, Vp);
+}
+
+static tt_status gpt2_forward_backward(tt_ctx* c, const void* params, float* grads,
+                                       const int32_t* tok, const int32_t* tgt, int B, int T) {
+    int z = gpt2_forward(c, params, grads, tok, B, T);
+    op_xent(c, z, tgt, c->cfg.V);
     if (c->oom) return TT_ERR_ARENA_OOM;
     return tape_backward(c);
+}
+
+// ------------------------------------------------------------------ greedy generation
+// Prefill: the forward over the prompt, whose qkv tensors fill the key/value
+// cache, and the greedy token after the prompt.  Then one decode step per new
+// token: the newest token through every layer (its key and value appended to
+// the cache, its query against keys 0..pos) and the greedy choice from its
+// logits.  Tokens live in a device buffer [B, Tp + n_new]; nothing returns to
+// the host until the end.  Each decode step's tensors are released after it.
+static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* prompt_dev, int B, int Tp, int n_new,
+                               int32_t* tokbuf) {
+    const tt_gpt2_config& m = c->cfg;
+    const bool bf = m.dtype == TT_BF16;
+    const size_t es = esize(m.dtype);
+    const Offsets o = offsets_of(&m);
+    auto P = [&](size_t off) -> const void* { return (const char*)params + off * es; };
+    const int C = m.C, Vp = padded_vocab(m.V), Ttot = Tp + n_new;
+    Launch L = launch_of(c);
+    // the cache: per layer [B, maxT, 2C]
+    const size_t layer_cache = (size_t)B * m.maxT * 2 * C * es;
+    char* cache = (char*)arena_alloc(c, layer_cache * (size_t)m.L);
+    // prefill
+    std::vector<int> qkv_ids;
+    int z = gpt2_forward(c, params, nullptr, prompt_dev, B, Tp, &qkv_ids);
+    if (c->oom) return TT_ERR_ARENA_OOM;
+    for (int l = 0; l < m.L; l++)
+        if (!launch_kv_fill(L, bf, c->tensors[qkv_ids[l]].data, cache + layer_cache * l, B, Tp, C, 0, m.maxT))
+            return fail(c, TT_ERR_ARG, "generate: sequence longer than maxT");
+    launch_argmax(L, bf, (const char*)c->tensors[z].data + (size_t)(Tp - 1) * Vp * es, (long long)Tp * Vp, B, m.V,
+                  tokbuf, Ttot, Tp);
+    // decode steps: the token at pos (just chosen) gives the one at pos + 1
+    const size_t mark = c->off;
+    for (int pos = Tp; pos < Ttot - 1; pos++) {
+        c->off = mark;
+        auto buf = [&](int cols) { return arena_alloc(c, (size_t)B * cols * es); };
+        void* x = buf(C);
+        launch_embed_at(L, bf, P(o.wte), P(o.wpe), tokbuf, Ttot, pos, x, B, C, m.V);
+        for (int l = 0; l < m.L; l++) {
+            const size_t base = o.layers + (size_t)l * o.per_layer;
+            auto PL = [&](int i) { return P(base + o.sub[i]); };
+            void* h = buf(C);
+            float* mean = (float*)arena_alloc(c, (size_t)B * 4);
+            float* rstd = (float*)arena_alloc(c, (size_t)B * 4);
+            void* qkv = buf(3 * C);
+            void* a = buf(C);
+            void* x1 = buf(C);
+            void* h2 = buf(C);
+            void* u = buf(4 * C);
+            void* g = buf(4 * C);
+            void* x2 = buf(C);
+            if (c->oom) return TT_ERR_ARENA_OOM;
+            auto linear = [&](const void* in, int K, const void* W, const void* bias, int N, void* out,
+                              const void* res, void* pre) -> bool {
+                // a few rows: the weight-streaming skinny GEMM
+                if (launch_gemm_skinny(L, bf, in, W, bias, res, out, pre, B, N, K, N, N, pre != nullptr))
+                    return true;
+                GemmArgs ga;
+                ga.A = in; ga.lda = K; ga.a_kmajor = true;
+                ga.B = W; ga.ldb = K; ga.b_kmajor = true;
+                ga.M = B; ga.N = N; ga.K = K;
+                ga.in_bf16 = bf;
+                ga.D = out; ga.ldd = N; ga.d_f32 = !bf;
+                ga.epi = pre ? EPI_GELU : EPI_STORE;
+                ga.bias = bias;
+                ga.residual = res;
+                ga.aux = pre;
+                return run_gemm(c, ga, PK_GEMM_FWD);
+            };
+            launch_layernorm_fwd(L, bf, x, PL(0), PL(1), h, mean, rstd, B, C);
+            if (!linear(h, C, PL(2), PL(3), 3 * C, qkv, nullptr, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            launch_kv_fill(L, bf, qkv, cache + layer_cache * l, B, 1, C, pos, m.maxT);
+            if (!launch_decode_attn(L, bf, qkv, cache + layer_cache * l, a, B, m.H, C, pos, m.maxT))
+                return fail(c, TT_ERR_ARG, "generate: attention shape not supported");
+            if (!linear(a, C, PL(4), PL(5), C, x1, x, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            launch_layernorm_fwd(L, bf, x1, PL(6), PL(7), h2, mean, rstd, B, C);
+            if (!linear(h2, C, PL(8), PL(9), 4 * C, g, nullptr, u)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            if (!linear(g, 4 * C, PL(10), PL(11), C, x2, x1, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            x = x2;
+        }
+        void* hf = buf(C);
+        float* mean = (float*)arena_alloc(c, (size_t)B * 4);
+        float* rstd = (float*)arena_alloc(c, (size_t)B * 4);
+        void* zl = buf(Vp);
+        if (c->oom) return TT_ERR_ARENA_OOM;
+        launch_layernorm_fwd(L, bf, x, P(o.lnfw), P(o.lnfb), hf, mean, rstd, B, C);
+        // tied LM head over the V real rows of wte (argmax reads only those columns)
+        if (launch_gemm_skinny(L, bf, hf, P(o.wte), nullptr, nullptr, zl, nullptr, B, m.V, C, Vp, m.V, false)) {
+            launch_argmax(L, bf, zl, Vp, B, m.V, tokbuf, Ttot, pos + 1);
+            continue;
+        }
+        GemmArgs ga;
+        ga.A = hf; ga.lda = C; ga.a_kmajor = true;
+        ga.B = P(o.wte); ga.ldb = C; ga.b_kmajor = true;
+        ga.M = B; ga.N = Vp; ga.K = C;
+        ga.b_rows = m.V;
+        ga.in_bf16 = bf;
+        ga.D = zl; ga.ldd = Vp; ga.d_f32 = !bf;
+        if (!run_gemm(c, ga, PK_GEMM_FWD)) return fail(c, TT_ERR_CUDA, "generate: LM head GEMM");
+        launch_argmax(L, bf, zl, Vp, B, m.V, tokbuf, Ttot, pos + 1);
+    }
+    return TT_OK;
 }
 
 static void begin_step(tt_ctx* c) {
@@ -793,6 +903,113 @@ tt_status tt_gpt2_step(tt_ctx* c, const void* params, float* grads, const int32_
         return tt_ctx_sync(c);
     }
     return TT_OK;
+}
+
+// Token inputs may be host or device buffers; host ones are staged into the arena.
+static const int32_t* stage_tokens(tt_ctx* c, const int32_t* tokens, size_t n, tt_status* st) {
+    int32_t* dst = (int32_t*)arena_alloc(c, n * 4);
+    *st = TT_OK;
+    if (c->oom || c->dry || !is_host_pointer(tokens)) return c->dry ? dst : tokens;
+    if (cudaMemcpyAsync(dst, tokens, n * 4, cudaMemcpyHostToDevice, c->stream) != cudaSuccess) {
+        *st = fail(c, TT_ERR_CUDA, "token copy failed");
+        return nullptr;
+    }
+    return dst;
+}
+
+tt_status tt_gpt2_eval(tt_ctx* c, const void* params, const int32_t* tokens, const int32_t* targets, int B, int T,
+                       float* loss) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
+    if (!params || !tokens || !targets) return fail(c, TT_ERR_ARG, "NULL parameter or token pointer");
+    if (B <= 0 || T <= 0 || T > c->cfg.maxT)
+        return fail(c, TT_ERR_ARG, "bad batch shape B=%d T=%d (maxT=%d)", B, T, c->cfg.maxT);
+    {
+        const size_t need = tt_gpt2_arena_bytes(&c->cfg, B, T);
+        const size_t at = (c->off + ARENA_ALIGN - 1) & ~(ARENA_ALIGN - 1);
+        if (need == 0 || at + need > c->cap)
+            return fail(c, TT_ERR_ARENA_OOM, "arena too small: evaluation needs %zu bytes, %zu free", need,
+                        c->cap > at ? c->cap - at : (size_t)0);
+    }
+    begin_step(c);
+    const size_t M = (size_t)B * T;
+    tt_status st;
+    const int32_t* tok = stage_tokens(c, tokens, M, &st);
+    if (st != TT_OK) return st;
+    const int32_t* tgt = stage_tokens(c, targets, M, &st);
+    if (st != TT_OK) return st;
+    int z = gpt2_forward(c, params, nullptr, tok, B, T);
+    op_xent(c, z, tgt, c->cfg.V);
+    if (c->oom) return fail(c, TT_ERR_ARENA_OOM, "arena exhausted during evaluation");
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    if (loss) {
+        if (cudaMemcpyAsync(loss, c->loss_dev, 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "loss copy failed");
+        return tt_ctx_sync(c);
+    }
+    return TT_OK;
+}
+
+size_t tt_gpt2_generate_arena_bytes(const tt_gpt2_config* m, int B, int T_prompt, int n_new) {
+    if (!cfg_ok(m) || B <= 0 || T_prompt <= 0 || n_new < 0 || T_prompt + n_new > m->maxT) return 0;
+    tt_ctx c;
+    c.cap = (size_t)-1 / 2;
+    c.cfg = *m;
+    c.has_model = true;
+    c.dry = true;
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        c.num_sms = sms;
+    else
+        cudaGetLastError();
+    arena_alloc(&c, (size_t)B * T_prompt * 4);              // staged prompt
+    arena_alloc(&c, (size_t)B * (T_prompt + n_new) * 4);    // token buffer
+    if (n_new > 0)
+        gpt2_generate(&c, (const void*)(uintptr_t)0x1000, (const int32_t*)(uintptr_t)0x1000, B, T_prompt, n_new,
+                      (int32_t*)(uintptr_t)0x1000);
+    c.magic = TT_DEAD;
+    return c.high - ARENA_HEADER;
+}
+
+tt_status tt_gpt2_generate(tt_ctx* c, const void* params, const int32_t* prompt, int B, int T_prompt, int n_new,
+                           int32_t* out) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
+    if (!params || !prompt || !out) return fail(c, TT_ERR_ARG, "NULL parameter, prompt or output pointer");
+    if (B <= 0 || T_prompt <= 0 || n_new < 0 || T_prompt + n_new > c->cfg.maxT)
+        return fail(c, TT_ERR_ARG, "bad generation shape B=%d prompt=%d new=%d (maxT=%d)", B, T_prompt, n_new,
+                    c->cfg.maxT);
+    {
+        const size_t need = tt_gpt2_generate_arena_bytes(&c->cfg, B, T_prompt, n_new);
+        const size_t at = (c->off + ARENA_ALIGN - 1) & ~(ARENA_ALIGN - 1);
+        if (need == 0 || at + need > c->cap)
+            return fail(c, TT_ERR_ARENA_OOM, "arena too small: generation needs %zu bytes, %zu free", need,
+                        c->cap > at ? c->cap - at : (size_t)0);
+    }
+    begin_step(c);
+    const int Ttot = T_prompt + n_new;
+    tt_status st;
+    const int32_t* pr = stage_tokens(c, prompt, (size_t)B * T_prompt, &st);
+    if (st != TT_OK) return st;
+    int32_t* tokbuf = (int32_t*)arena_alloc(c, (size_t)B * Ttot * 4);
+    if (c->oom) return fail(c, TT_ERR_ARENA_OOM, "arena exhausted during generation");
+    // the prompt opens each row of the token buffer
+    if (cudaMemcpy2DAsync(tokbuf, (size_t)Ttot * 4, pr, (size_t)T_prompt * 4, (size_t)T_prompt * 4, (size_t)B,
+                          cudaMemcpyDeviceToDevice, c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "prompt copy failed");
+    if (n_new > 0) {
+        st = gpt2_generate(c, params, pr, B, T_prompt, n_new, tokbuf);
+        if (st != TT_OK) return st == TT_ERR_ARENA_OOM ? fail(c, st, "arena exhausted during generation") : st;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    if (cudaMemcpyAsync(out, tokbuf, (size_t)B * Ttot * 4, cudaMemcpyDefault, c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "token copy failed");
+    return tt_ctx_sync(c);
 }
 
 tt_status tt_ctx_loss_device(const tt_ctx* c, const float** mean_loss, const float** row_losses) {

@@ -135,6 +135,19 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
 bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
                              const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt);
 
+// decoding with a key/value cache (decode.cu); cache per layer [B, maxT, 2C]
+bool launch_kv_fill(const Launch& L, bool bf16, const void* qkv, void* cache, int B, int Tn, int C, int t0,
+                    int maxT);
+void launch_embed_at(const Launch& L, bool bf16, const void* wte, const void* wpe, const int32_t* tok,
+                     int ld_tok, int pos, void* x, int B, int C, int V);
+bool launch_decode_attn(const Launch& L, bool bf16, const void* qkv, const void* cache, void* y, int B, int H,
+                        int C, int pos, int maxT);
+void launch_argmax(const Launch& L, bool bf16, const void* z, long long row_stride, int rows, int V, int32_t* out,
+                   int ld_out, int col);
+// decode-step linear layers (M <= 16 rows); false = shape not taken
+bool launch_gemm_skinny(const Launch& L, bool bf16, const void* A, const void* W, const void* bias, const void* res,
+                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu);
+
 bool attention_mma_eligible(bool bf16, int C, int H);
 void launch_attention_fwd_mma(const Launch& L, const void* qkv, void* y, float* lse,
                               int B, int T, int C, int H);

@@ -213,6 +213,9 @@ OP_SHAPES = {
     "embed_bwd": "embedding-gradient scatter, 32768 Zipf tokens, C=768",
     "adamw": "AdamW over 124,439,808 parameters",
     "gemm_shapes": "every GEMM of one 124M step (12 per-layer forms + the LM head), one row each",
+    "eval": "forward-only evaluation loss (tt_gpt2_eval), 124M, B=32 T=1024, bf16",
+    "generate": "greedy generation with the key/value cache (tt_gpt2_generate), 124M bf16, B=8, "
+                "64-token prompts, 448 new tokens",
 }
 
 
@@ -324,6 +327,55 @@ def run_gemm_shapes(args):
     timed("dx lm", f, lambda: ctx.linear_bwd_dx("bf16", z, wte, None, dhf, M, C, Vp))
     dwte = torch.empty(Vp, C, device=dev)
     timed("dw lm", f, lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", z, hf, dwte, None, M, C, Vp)))
+    ctx.close()
+    return 0
+
+
+def run_inference(args):
+    """Times tt_gpt2_eval or tt_gpt2_generate (CUDA events around `--reps` calls)."""
+    import numpy as np
+    import torch
+
+    from autograd_arena_allocated_gb300 import api, synth
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    w = synth.WORKLOADS["gpt2_124m_b32"]
+    sh = w.shape
+    cfg = api.make_config(sh.L, sh.C, sh.H, sh.V, sh.maxT, "bf16")
+    p = synth.init_params(sh)
+    master = torch.from_numpy(p).to("cuda")
+    params = torch.empty(p.size, device="cuda", dtype=torch.bfloat16)
+    if args.op == "eval":
+        B, T = w.B, w.T
+        tok, tgt = synth.token_stream(B, T, sh.V, w.tokens)
+        td, gd = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+        ctx = api.Context(api.arena_bytes(cfg, B, T) + (64 << 20))
+        fn = lambda: (ctx.reset(), ctx.eval(params, td, gd, B, T))
+        tokens_per_call = B * T
+    else:
+        B, Tp, n_new = 8, 64, 448
+        prompt, _ = synth.token_stream(B, Tp, sh.V, w.tokens, seed=5)
+        pd = torch.from_numpy(prompt).cuda()
+        out = torch.empty(B, Tp + n_new, dtype=torch.int32, device="cuda")
+        ctx = api.Context(api.generate_arena_bytes(cfg, B, Tp, n_new) + (64 << 20))
+        fn = lambda: (ctx.reset(), ctx.generate(params, pd, B, Tp, n_new, out))
+        tokens_per_call = B * n_new
+    ctx.set_model(cfg)
+    ctx.cast_bf16(master, params)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.reps
+    print(json.dumps({"op": args.op, "what": OP_SHAPES[args.op], "ms_per_call": ms,
+                      "tokens_per_s": tokens_per_call / (ms * 1e-3)}), flush=True)
     ctx.close()
     return 0
 
@@ -451,6 +503,8 @@ def main():
     args = ap.parse_args()
     if args.op:
         args.warmup = max(1, args.warmup)
+        if args.op in ("eval", "generate"):
+            return run_inference(args)
         return run_gemm_shapes(args) if args.op == "gemm_shapes" else run_op(args)
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     world, rank, local = dist_setup()

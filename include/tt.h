@@ -193,6 +193,39 @@ tt_status tt_adamw(tt_ctx* ctx, float* master, void* params_lowp, const float* g
  * Used to make the bf16 parameter copy of a freshly initialized master. */
 tt_status tt_cast_f32_to_bf16(tt_ctx* ctx, const float* src, void* dst, size_t n);
 
+/* ------------------------------------------------------------- inference */
+
+/* The forward pass and the mean cross entropy only, no gradients: the
+ * validation loss the tinytorch page's training loop evaluates every 40 steps
+ * (三.7, 八.3).  Arguments as for tt_gpt2_step without grads; the arena needs
+ * at most tt_gpt2_arena_bytes(cfg, B, T).  The logits buffer of the arena is
+ * overwritten by the fused cross entropy, as in the step.  The arena is NOT
+ * reset by this call. */
+tt_status tt_gpt2_eval(tt_ctx* ctx, const void* params, const int32_t* tokens,
+                       const int32_t* targets, int B, int T, float* loss);
+
+/* Exact number of arena bytes tt_gpt2_generate needs (the same allocation
+ * sequence, run without launching); 0 for invalid arguments. */
+size_t tt_gpt2_generate_arena_bytes(const tt_gpt2_config* cfg, int B, int T_prompt, int n_new);
+
+/* Greedy generation with a key/value cache (tinytorch 八.3 generates text
+ * after training; the Forge page, 性能瓶颈与未来路线图, names the key/value
+ * cache: each new token's query against the cached keys of the earlier
+ * positions, instead of recomputing every position).
+ *   prompt  int32 [B, T_prompt] row-major, device or host memory; ids in [0, V).
+ *   out     int32 [B, T_prompt + n_new] row-major, device or host memory:
+ *           receives the prompt followed by n_new tokens, each the first index
+ *           of the largest logit given everything before it (greedy).
+ *   T_prompt >= 1, n_new >= 0, T_prompt + n_new <= maxT.
+ * The prompt runs through the training forward once (prefill), which fills a
+ * per-layer cache [B, maxT, 2C] in the arena; every further token is one
+ * decode step on the device.  The call synchronizes the stream.  Errors:
+ * TT_ERR_ARG for bad shapes, NULL pointers or a prompt id out of range;
+ * TT_ERR_ARENA_OOM from the host plan before anything is launched.  The
+ * arena is NOT reset by this call. */
+tt_status tt_gpt2_generate(tt_ctx* ctx, const void* params, const int32_t* prompt, int B,
+                           int T_prompt, int n_new, int32_t* out);
+
 #ifdef __cplusplus
 }
 #endif
