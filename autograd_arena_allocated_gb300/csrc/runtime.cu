@@ -555,7 +555,10 @@ static tt_status gpt2_forward_backward(tt_ctx* c, const void* params, float* gra
 // token: the newest token through every layer (its key and value appended to
 // the cache, its query against keys 0..pos) and the greedy choice from its
 // logits.  Tokens live in a device buffer [B, Tp + n_new]; nothing returns to
-// the host until the end.  Each decode step's tensors are released after it.
+// the host until the end.  The decode kernels read the position from device
+// memory and the step advances it, so every step launches the same kernels
+// with the same arguments: the first step runs eagerly and the rest replay it
+// as a CUDA graph.
 static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* prompt_dev, int B, int Tp, int n_new,
                                int32_t* tokbuf) {
     const tt_gpt2_config& m = c->cfg;
@@ -564,10 +567,29 @@ static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* pro
     const Offsets o = offsets_of(&m);
     auto P = [&](size_t off) -> const void* { return (const char*)params + off * es; };
     const int C = m.C, Vp = padded_vocab(m.V), Ttot = Tp + n_new;
+    const int max_keys = Ttot - 1;  // keys seen by the last decode step
     Launch L = launch_of(c);
     // the cache: per layer [B, maxT, 2C]
     const size_t layer_cache = (size_t)B * m.maxT * 2 * C * es;
     char* cache = (char*)arena_alloc(c, layer_cache * (size_t)m.L);
+    int* pos_dev = (int*)arena_alloc(c, sizeof(int));
+    int* counters = (int*)arena_alloc(c, (size_t)B * m.H * sizeof(int));
+    float* part = (float*)arena_alloc(c, decode_attn_scratch_floats(B, m.H, max_keys) * sizeof(float));
+    const int nct = skinny_pick_ctas(m.V);
+    auto* keys = (unsigned long long*)arena_alloc(c, (size_t)B * nct * sizeof(unsigned long long));
+    // one set of decode-step tensors, reused by every layer and step
+    auto buf = [&](int cols) { return arena_alloc(c, (size_t)B * cols * es); };
+    void* xa = buf(C);
+    void* xb = buf(C);
+    void* h = buf(C);
+    void* qkv = buf(3 * C);
+    void* att = buf(C);
+    void* x1 = buf(C);
+    void* u = buf(4 * C);
+    void* g = buf(4 * C);
+    void* zl = buf(Vp);
+    float* mean = (float*)arena_alloc(c, (size_t)B * 4);
+    float* rstd = (float*)arena_alloc(c, (size_t)B * 4);
     // prefill
     std::vector<int> qkv_ids;
     int z = gpt2_forward(c, params, nullptr, prompt_dev, B, Tp, &qkv_ids);
@@ -576,76 +598,117 @@ static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* pro
         if (!launch_kv_fill(L, bf, c->tensors[qkv_ids[l]].data, cache + layer_cache * l, B, Tp, C, 0, m.maxT))
             return fail(c, TT_ERR_ARG, "generate: sequence longer than maxT");
     launch_argmax(L, bf, (const char*)c->tensors[z].data + (size_t)(Tp - 1) * Vp * es, (long long)Tp * Vp, B, m.V,
-                  tokbuf, Ttot, Tp);
-    // decode steps: the token at pos (just chosen) gives the one at pos + 1
+                  tokbuf, Ttot, Tp, nullptr);
+    const int n_steps = n_new - 1;
+    if (n_steps <= 0) return TT_OK;
+    if (!L.dry && cudaMemsetAsync(counters, 0, (size_t)B * m.H * sizeof(int), c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "generate: counter reset failed");
+    launch_set_int(L, pos_dev, Tp);
+
+    // one decode step: the token at *pos_dev gives the one at *pos_dev + 1
     const size_t mark = c->off;
-    for (int pos = Tp; pos < Ttot - 1; pos++) {
+    auto step = [&]() -> tt_status {
         c->off = mark;
-        auto buf = [&](int cols) { return arena_alloc(c, (size_t)B * cols * es); };
-        void* x = buf(C);
-        launch_embed_at(L, bf, P(o.wte), P(o.wpe), tokbuf, Ttot, pos, x, B, C, m.V);
+        const Launch S = launch_of(c);
+        auto linear = [&](const void* in, int K, const void* W, const void* bias, int N, void* out, const void* res,
+                          void* pre) -> bool {
+            // a few rows: the weight-streaming skinny GEMM
+            if (launch_gemm_skinny(S, bf, in, W, bias, res, out, pre, B, N, K, N, N, pre != nullptr, nullptr))
+                return true;
+            GemmArgs ga;
+            ga.A = in; ga.lda = K; ga.a_kmajor = true;
+            ga.B = W; ga.ldb = K; ga.b_kmajor = true;
+            ga.M = B; ga.N = N; ga.K = K;
+            ga.in_bf16 = bf;
+            ga.D = out; ga.ldd = N; ga.d_f32 = !bf;
+            ga.epi = pre ? EPI_GELU : EPI_STORE;
+            ga.bias = bias;
+            ga.residual = res;
+            ga.aux = pre;
+            return run_gemm(c, ga, PK_GEMM_FWD);
+        };
+        void* x = xa;
+        void* x2 = xb;
+        launch_embed_at(S, bf, P(o.wte), P(o.wpe), tokbuf, Ttot, pos_dev, x, B, C, m.V);
         for (int l = 0; l < m.L; l++) {
             const size_t base = o.layers + (size_t)l * o.per_layer;
             auto PL = [&](int i) { return P(base + o.sub[i]); };
-            void* h = buf(C);
-            float* mean = (float*)arena_alloc(c, (size_t)B * 4);
-            float* rstd = (float*)arena_alloc(c, (size_t)B * 4);
-            void* qkv = buf(3 * C);
-            void* a = buf(C);
-            void* x1 = buf(C);
-            void* h2 = buf(C);
-            void* u = buf(4 * C);
-            void* g = buf(4 * C);
-            void* x2 = buf(C);
-            if (c->oom) return TT_ERR_ARENA_OOM;
-            auto linear = [&](const void* in, int K, const void* W, const void* bias, int N, void* out,
-                              const void* res, void* pre) -> bool {
-                // a few rows: the weight-streaming skinny GEMM
-                if (launch_gemm_skinny(L, bf, in, W, bias, res, out, pre, B, N, K, N, N, pre != nullptr))
-                    return true;
-                GemmArgs ga;
-                ga.A = in; ga.lda = K; ga.a_kmajor = true;
-                ga.B = W; ga.ldb = K; ga.b_kmajor = true;
-                ga.M = B; ga.N = N; ga.K = K;
-                ga.in_bf16 = bf;
-                ga.D = out; ga.ldd = N; ga.d_f32 = !bf;
-                ga.epi = pre ? EPI_GELU : EPI_STORE;
-                ga.bias = bias;
-                ga.residual = res;
-                ga.aux = pre;
-                return run_gemm(c, ga, PK_GEMM_FWD);
-            };
-            launch_layernorm_fwd(L, bf, x, PL(0), PL(1), h, mean, rstd, B, C);
+            launch_layernorm_fwd(S, bf, x, PL(0), PL(1), h, mean, rstd, B, C);
             if (!linear(h, C, PL(2), PL(3), 3 * C, qkv, nullptr, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
-            launch_kv_fill(L, bf, qkv, cache + layer_cache * l, B, 1, C, pos, m.maxT);
-            if (!launch_decode_attn(L, bf, qkv, cache + layer_cache * l, a, B, m.H, C, pos, m.maxT))
+            if (!launch_decode_attn(S, bf, qkv, cache + layer_cache * l, att, B, m.H, C, pos_dev, max_keys, m.maxT,
+                                    part, counters))
                 return fail(c, TT_ERR_ARG, "generate: attention shape not supported");
-            if (!linear(a, C, PL(4), PL(5), C, x1, x, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
-            launch_layernorm_fwd(L, bf, x1, PL(6), PL(7), h2, mean, rstd, B, C);
-            if (!linear(h2, C, PL(8), PL(9), 4 * C, g, nullptr, u)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            if (!linear(att, C, PL(4), PL(5), C, x1, x, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            launch_layernorm_fwd(S, bf, x1, PL(6), PL(7), h, mean, rstd, B, C);
+            if (!linear(h, C, PL(8), PL(9), 4 * C, g, nullptr, u)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
             if (!linear(g, 4 * C, PL(10), PL(11), C, x2, x1, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
-            x = x2;
+            std::swap(x, x2);
         }
-        void* hf = buf(C);
-        float* mean = (float*)arena_alloc(c, (size_t)B * 4);
-        float* rstd = (float*)arena_alloc(c, (size_t)B * 4);
-        void* zl = buf(Vp);
-        if (c->oom) return TT_ERR_ARENA_OOM;
-        launch_layernorm_fwd(L, bf, x, P(o.lnfw), P(o.lnfb), hf, mean, rstd, B, C);
-        // tied LM head over the V real rows of wte (argmax reads only those columns)
-        if (launch_gemm_skinny(L, bf, hf, P(o.wte), nullptr, nullptr, zl, nullptr, B, m.V, C, Vp, m.V, false)) {
-            launch_argmax(L, bf, zl, Vp, B, m.V, tokbuf, Ttot, pos + 1);
-            continue;
+        launch_layernorm_fwd(S, bf, x, P(o.lnfw), P(o.lnfb), h, mean, rstd, B, C);
+        // tied LM head over the V real rows of wte, which also advances the position
+        if (bf && launch_gemm_skinny_pick(S, h, P(o.wte), B, m.V, C, keys, pos_dev)) {
+            launch_pick(S, keys, nct, B, tokbuf, Ttot, pos_dev);
+            return TT_OK;
         }
-        GemmArgs ga;
-        ga.A = hf; ga.lda = C; ga.a_kmajor = true;
-        ga.B = P(o.wte); ga.ldb = C; ga.b_kmajor = true;
-        ga.M = B; ga.N = Vp; ga.K = C;
-        ga.b_rows = m.V;
-        ga.in_bf16 = bf;
-        ga.D = zl; ga.ldd = Vp; ga.d_f32 = !bf;
-        if (!run_gemm(c, ga, PK_GEMM_FWD)) return fail(c, TT_ERR_CUDA, "generate: LM head GEMM");
-        launch_argmax(L, bf, zl, Vp, B, m.V, tokbuf, Ttot, pos + 1);
+        if (!launch_gemm_skinny(S, bf, h, P(o.wte), nullptr, nullptr, zl, nullptr, B, m.V, C, Vp, m.V, false,
+                                pos_dev)) {
+            GemmArgs ga;
+            ga.A = h; ga.lda = C; ga.a_kmajor = true;
+            ga.B = P(o.wte); ga.ldb = C; ga.b_kmajor = true;
+            ga.M = B; ga.N = Vp; ga.K = C;
+            ga.b_rows = m.V;
+            ga.in_bf16 = bf;
+            ga.D = zl; ga.ldd = Vp; ga.d_f32 = !bf;
+            if (!run_gemm(c, ga, PK_GEMM_FWD)) return fail(c, TT_ERR_CUDA, "generate: LM head GEMM");
+            launch_add_int(S, pos_dev, 1);
+        }
+        launch_argmax(S, bf, zl, Vp, B, m.V, tokbuf, Ttot, 0, pos_dev);
+        return TT_OK;
+    };
+
+    tt_status st = step();
+    if (st != TT_OK || c->oom || L.dry || n_steps == 1) return c->oom ? TT_ERR_ARENA_OOM : st;
+    // capture the step once (its kernels go to a private stream while it is
+    // recorded) and replay it for the remaining positions
+    int done = 1;
+    cudaStream_t cap = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) == cudaSuccess) {
+        cudaStream_t own = c->stream;
+        const uint64_t n0 = c->launches;
+        c->stream = cap;
+        if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+            st = step();
+            if (cudaStreamEndCapture(cap, &graph) != cudaSuccess) graph = nullptr;
+        }
+        c->stream = own;
+        const uint64_t nodes = c->launches - n0;
+        c->launches = n0;
+        if (st != TT_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            cudaStreamDestroy(cap);
+            return st;
+        }
+        if (graph && cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess) {
+            for (; done < n_steps; done++) {
+                if (cudaGraphLaunch(exec, c->stream) != cudaSuccess) break;
+                c->launches += nodes;
+            }
+        }
+        cudaGetLastError();  // a failed capture leaves the eager steps below
+        if (exec) {
+            cudaStreamSynchronize(c->stream);
+            cudaGraphExecDestroy(exec);
+        }
+        if (graph) cudaGraphDestroy(graph);
+        cudaStreamDestroy(cap);
+    } else {
+        cudaGetLastError();
+    }
+    for (; done < n_steps; done++) {
+        st = step();
+        if (st != TT_OK) return st;
     }
     return TT_OK;
 }

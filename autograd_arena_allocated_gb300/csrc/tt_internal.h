@@ -135,18 +135,36 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
 bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
                              const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt);
 
-// decoding with a key/value cache (decode.cu); cache per layer [B, maxT, 2C]
+// decoding with a key/value cache (decode.cu); cache per layer [B, maxT, 2C].
+// The decode-step kernels read the newest position from device memory
+// (pos_dev); the step's last linear layer advances it (advance != nullptr).
 bool launch_kv_fill(const Launch& L, bool bf16, const void* qkv, void* cache, int B, int Tn, int C, int t0,
                     int maxT);
+void launch_set_int(const Launch& L, int* p, int v);  // *p = v
+void launch_add_int(const Launch& L, int* p, int v);  // *p += v
 void launch_embed_at(const Launch& L, bool bf16, const void* wte, const void* wpe, const int32_t* tok,
-                     int ld_tok, int pos, void* x, int B, int C, int V);
-bool launch_decode_attn(const Launch& L, bool bf16, const void* qkv, const void* cache, void* y, int B, int H,
-                        int C, int pos, int maxT);
+                     int ld_tok, const int* pos_dev, void* x, int B, int C, int V);
+// attention of the newest query against keys 0..pos (at most max_keys), which
+// also writes the newest key and value into the cache; part holds
+// decode_attn_scratch_floats() floats, counters B*H ints that start at zero
+// (and are left at zero)
+int decode_attn_splits(int max_keys);
+size_t decode_attn_scratch_floats(int B, int H, int max_keys);
+bool launch_decode_attn(const Launch& L, bool bf16, const void* qkv, void* cache, void* y, int B, int H, int C,
+                        const int* pos_dev, int max_keys, int maxT, float* part, int* counters);
+// greedy choice over stored logits into out[b][col_dev ? *col_dev : col]
 void launch_argmax(const Launch& L, bool bf16, const void* z, long long row_stride, int rows, int V, int32_t* out,
-                   int ld_out, int col);
+                   int ld_out, int col, const int* col_dev);
 // decode-step linear layers (M <= 16 rows); false = shape not taken
 bool launch_gemm_skinny(const Launch& L, bool bf16, const void* A, const void* W, const void* bias, const void* res,
-                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu);
+                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu, int* advance);
+// bf16 LM head with the greedy choice folded in: keys[m * skinny_pick_ctas(N) + cta]
+// holds each CTA's largest (logit, -index) key of row m; launch_pick reduces them
+int skinny_pick_ctas(int N);
+bool launch_gemm_skinny_pick(const Launch& L, const void* A, const void* W, int M, int N, int K,
+                             unsigned long long* keys, int* advance);
+void launch_pick(const Launch& L, const unsigned long long* keys, int nct, int rows, int32_t* tok, int ld_tok,
+                 const int* pos_dev);
 
 bool attention_mma_eligible(bool bf16, int C, int H);
 void launch_attention_fwd_mma(const Launch& L, const void* qkv, void* y, float* lse,

@@ -151,3 +151,21 @@ def test_generate_edges_and_errors(ctx):
         ctx.generate(params, bad, 2, 3, 4, np.zeros((2, 7), dtype=np.int32))
     ctx.reset()
     ctx.generate(params, prompt, 2, 3, 2, np.zeros((2, 5), dtype=np.int32))  # usable after the error
+
+
+@pytest.mark.parametrize("dtype,std,tol_rel,tol_abs", [("fp32", 0.2, 1e-5, 1e-6), ("bf16", 0.02, 3e-2, 1e-3)])
+def test_generate_long_context_matches_oracle(ctx, oracle, dtype, std, tol_rel, tol_abs):
+    """Prompts longer than one attention split (128 keys): every decode step
+    combines several splits' partial softmax sums."""
+    w = synth.WORKLOADS["char_bf16"]
+    sh = w.shape
+    p, cfg, params = _model(ctx, sh, dtype, std=std, jitter=0.05)
+    B, Tp, n_new = 2, 150, 8
+    assert Tp + n_new - 1 > 128
+    prompt, _ = synth.token_stream(B, Tp, sh.V, w.tokens, seed=21)
+    out = np.zeros((B, Tp + n_new), dtype=np.int32)
+    ctx.reset()
+    ctx.generate(params, prompt, B, Tp, n_new, out)
+    assert np.array_equal(out[:, :Tp], prompt)
+    po = p.astype(np.float64) if dtype == "fp32" else oracle.bf16_values(p)
+    _check_greedy(oracle, sh, po, out, Tp, tol_rel, tol_abs, f"char {dtype}, {Tp}-token prompts")
