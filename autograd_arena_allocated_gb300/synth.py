@@ -170,3 +170,33 @@ def init_params(sh: GPT2Shape, seed: int = PARAM_SEED, std: float = 0.02,
         at += n
     return out
 
+
+
+# ---------------------------------------------------------------- the small classifier
+# The tinytorch page's example (八.1 and 八.5): three features (colour, size,
+# weight) in [0, 1], a hidden layer of 32, three classes.  Sample r draws its
+# label y_r = floor(3 u_{4r}) and its features around the class centre,
+# x_r = centre[y_r] + 0.3 (u_{4r+1..4r+3} - 0.5).  Parameters are N(0, std)
+# in the flat order W1 [3, 32], b1 [32], W2 [32, 3], b2 [3] (RandomNorm).
+FRUIT_SEED = 2024
+FRUIT_SHAPE = (3, 32, 3)
+FRUIT_CENTRES = np.array([[0.8, 0.5, 0.4], [0.5, 0.3, 0.8], [0.3, 0.7, 0.3]])
+
+
+def fruit_batch(R: int, seed: int = FRUIT_SEED):
+    """x float32 [R, 3] and labels int32 [R]."""
+    u = uniforms(seed, 0, 4 * R).reshape(R, 4)
+    y = np.minimum((u[:, 0] * 3).astype(np.int32), 2)
+    x = FRUIT_CENTRES[y] + 0.3 * (u[:, 1:] - 0.5)
+    return x.astype(np.float32), y
+
+
+def mlp_init(nin: int, nh: int, nout: int, seed: int = PARAM_SEED, std: float = 1.0):
+    """(W1 [nin, nh], b1 [nh], W2 [nh, nout], b2 [nout]) as float32."""
+    sizes = [nin * nh, nh, nh * nout, nout]
+    flat = (std * normals(seed, 0, sum(sizes))).astype(np.float32)
+    out, o = [], 0
+    for n, shp in zip(sizes, [(nin, nh), (nh,), (nh, nout), (nout,)]):
+        out.append(flat[o:o + n].reshape(shp))
+        o += n
+    return tuple(out)

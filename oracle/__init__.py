@@ -49,6 +49,14 @@ def lib():
             "or_adamw": (None, [dp, dp, dp, dp, sz, d, d, d, d, d, i]),
             "or_gpt2_step": (d, [i, i, i, i, i, dp, ip, ip, i, i, dp, dp]),
             "or_gpt2_logits_last": (i, [i, i, i, i, i, dp, ip, i, i, dp]),
+            "or_matmul": (None, [dp, dp, i, i, i, dp]),
+            "or_matmul_bwd": (None, [dp, dp, dp, i, i, i, dp, dp]),
+            "or_add_row": (None, [dp, dp, i, i, dp]),
+            "or_add_row_bwd": (None, [dp, i, i, dp, dp]),
+            "or_softmax_rows": (None, [dp, i, i, dp]),
+            "or_softmax_rows_bwd": (None, [dp, dp, i, i, dp]),
+            "or_xent_probs": (d, [dp, ip, i, i, dp, d]),
+            "or_mlp_sgd": (None, [dp, ip, i, i, i, i, dp, dp, dp, dp, d, i, dp, dp]),
             "or_val_reset": (None, []),
             "or_val_leaf": (i, [d]),
             "or_val_add": (i, [i, i]),
@@ -249,6 +257,86 @@ def gpt2_logits_last(shape, params, tokens):
     if rc != 0:
         raise ValueError("bad arguments to or_gpt2_logits_last")
     return out
+
+
+# ---------------------------------------------------------------- generic ops
+def matmul(A, B):
+    """C = A B with B [K, N]."""
+    A, B = f64(A), f64(B)
+    M, K = A.shape
+    N = B.shape[1]
+    out = np.zeros((M, N))
+    lib().or_matmul(_d(A), _d(B), M, K, N, _d(out))
+    return out
+
+
+def matmul_bwd(A, B, dC):
+    A, B, dC = f64(A), f64(B), f64(dC)
+    M, K = A.shape
+    N = B.shape[1]
+    dA, dB = np.zeros_like(A), np.zeros_like(B)
+    lib().or_matmul_bwd(_d(A), _d(B), _d(dC), M, K, N, _d(dA), _d(dB))
+    return dA, dB
+
+
+def add_row(A, b):
+    A, b = f64(A), f64(b)
+    R, Cc = A.shape
+    out = np.zeros_like(A)
+    lib().or_add_row(_d(A), _d(b), R, Cc, _d(out))
+    return out
+
+
+def add_row_bwd(dC):
+    dC = f64(dC)
+    R, Cc = dC.shape
+    dA, db = np.zeros_like(dC), np.zeros(Cc)
+    lib().or_add_row_bwd(_d(dC), R, Cc, _d(dA), _d(db))
+    return dA, db
+
+
+def softmax_rows(Z):
+    Z = f64(Z)
+    R, Cc = Z.shape
+    P = np.zeros_like(Z)
+    lib().or_softmax_rows(_d(Z), R, Cc, _d(P))
+    return P
+
+
+def softmax_rows_bwd(P, dP):
+    P, dP = f64(P), f64(dP)
+    R, Cc = P.shape
+    dZ = np.zeros_like(P)
+    lib().or_softmax_rows_bwd(_d(P), _d(dP), R, Cc, _d(dZ))
+    return dZ
+
+
+def xent_probs(P, y, dloss=1.0):
+    """(loss, dP) of the cross entropy of probabilities P [R, C] at labels y."""
+    P = f64(P)
+    y = np.ascontiguousarray(y, dtype=np.int32)
+    R, Cc = P.shape
+    dP = np.zeros_like(P)
+    loss = lib().or_xent_probs(_d(P), _i(y), R, Cc, _d(dP), float(dloss))
+    return float(loss), dP
+
+
+def mlp_sgd(x, y, W1, b1, W2, b2, lr, steps):
+    """The small classifier trained by SGD on a fixed batch.  Returns
+    (losses [steps], updated (W1, b1, W2, b2), gradients of the last step)."""
+    x = f64(x)
+    y = np.ascontiguousarray(y, dtype=np.int32)
+    W1, b1, W2, b2 = (f64(a).copy() for a in (W1, b1, W2, b2))
+    R, nin = x.shape
+    nh, nout = W1.shape[1], W2.shape[1]
+    losses = np.zeros(max(steps, 1))
+    grads = np.zeros(W1.size + b1.size + W2.size + b2.size)
+    lib().or_mlp_sgd(_d(x), _i(y), R, nin, nh, nout, _d(W1), _d(b1), _d(W2), _d(b2), float(lr), int(steps),
+                     _d(losses), _d(grads))
+    n1, n2 = W1.size, W2.size
+    g = (grads[:n1].reshape(W1.shape), grads[n1:n1 + nh], grads[n1 + nh:n1 + nh + n2].reshape(W2.shape),
+         grads[n1 + nh + n2:])
+    return losses[:steps], (W1, b1, W2, b2), g
 
 
 # ---------------------------------------------------------------- scalar tape

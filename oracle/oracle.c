@@ -10,7 +10,8 @@
  * Pages followed (cited by title and section):
  *   [TT]    "不用PyTorch，一个头文件就能训练GPT-2：Arena内存池+自动微分的C++实现"
  *           (the tinytorch page): 三.1 Arena, 三.2 Tensor, 三.3 autograd and MatMul,
- *           三.4 GELU, 三.5 Softmax+CrossEntropy, 三.6 GPT-2 model, 三.7 training loop (Adam).
+ *           三.4 GELU, 三.5 Softmax+CrossEntropy, 三.6 GPT-2 model, 三.7 training loop (Adam),
+ *           八.1 and 八.5 the small classifier trained by SGD through the generic tensor API.
  *   [FORGE] "17岁少年用C++从零构建深度学习框架Forge，精确复现GPT-2": 核心组件清单
  *           (GELU tanh form, fused log-softmax CE, AdamW decoupled decay) and
  *           最硬的一关 (causal -inf mask, 1/sqrt(d_k), LayerNorm eps/variance).
@@ -29,7 +30,11 @@
  *   - the LM head is tied to the token embedding;
  *   - LayerNorm: biased variance, eps = 1e-5 inside the square root;
  *   - AdamW: eps = 1e-8, p -= lr*(mhat/(sqrt(vhat)+eps) + wd*p), every tensor
- *     decays, step t is 1-based ([TT] 三.7 uses step+1).
+ *     decays, step t is 1-based ([TT] 三.7 uses step+1);
+ *   - MatMul is C = A B with B [K, N] ([TT] 三.3); the classifier's weights are
+ *     therefore W1 [3, 32] and W2 [32, 3] ([TT] 八.5 declares them [32, 3] and
+ *     [3, 32], which does not compose with that MatMul);
+ *   - the classifier's SGD update is p[i] -= lr * g[i] for every element.
  *
  * Parity pins: every exported function is pinned by tests/test_oracle_*.py
  * against closed forms, worked examples printed on the pages, library
@@ -762,6 +767,153 @@ OR_EXPORT int or_gpt2_logits_last(int L, int C, int H, int V, int maxT, const do
         memcpy(logits_last + (size_t)b * V, z->v + ((size_t)b * T + (T - 1)) * V, sizeof(double) * (size_t)V);
     tp_free(&tp);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Generic tensor ops of the library API ([TT] 三.2-三.5) and the small      */
+/* classifier trained by SGD ([TT] 八.1 and 八.5: three features, a hidden   */
+/* GELU layer, three classes).  Gradients are accumulated (+=), as [TT] 三.3 */
+/* requires for a tensor with several consumers.                            */
+/* ------------------------------------------------------------------------ */
+
+/* C[M,N] = A[M,K] B[K,N]: B is [K,N] row-major ([TT] 三.3 MatMulForward). */
+OR_EXPORT void or_matmul(const double* A, const double* B, int M, int K, int N, double* C) {
+    for (int i = 0; i < M; i++)
+        for (int j = 0; j < N; j++) {
+            double s = 0.0;
+            for (int k = 0; k < K; k++) s += A[(size_t)i * K + k] * B[(size_t)k * N + j];
+            C[(size_t)i * N + j] = s;
+        }
+}
+
+/* dA += dC B^T and dB += A^T dC ([TT] 三.3 MatMulBackward); either may be NULL. */
+OR_EXPORT void or_matmul_bwd(const double* A, const double* B, const double* dC, int M, int K, int N,
+                             double* dA, double* dB) {
+    if (dA)
+        for (int i = 0; i < M; i++)
+            for (int k = 0; k < K; k++) {
+                double s = 0.0;
+                for (int j = 0; j < N; j++) s += dC[(size_t)i * N + j] * B[(size_t)k * N + j];
+                dA[(size_t)i * K + k] += s;
+            }
+    if (dB)
+        for (int k = 0; k < K; k++)
+            for (int j = 0; j < N; j++) {
+                double s = 0.0;
+                for (int i = 0; i < M; i++) s += A[(size_t)i * K + k] * dC[(size_t)i * N + j];
+                dB[(size_t)k * N + j] += s;
+            }
+}
+
+/* C[r, c] = A[r, c] + b[c] (a bias row added to every row); backward
+ * dA += dC, db[c] += sum_r dC[r, c]. */
+OR_EXPORT void or_add_row(const double* A, const double* b, int R, int Cc, double* C) {
+    for (int r = 0; r < R; r++)
+        for (int c = 0; c < Cc; c++) C[(size_t)r * Cc + c] = A[(size_t)r * Cc + c] + b[c];
+}
+OR_EXPORT void or_add_row_bwd(const double* dC, int R, int Cc, double* dA, double* db) {
+    for (int r = 0; r < R; r++)
+        for (int c = 0; c < Cc; c++) {
+            if (dA) dA[(size_t)r * Cc + c] += dC[(size_t)r * Cc + c];
+            if (db) db[c] += dC[(size_t)r * Cc + c];
+        }
+}
+
+/* Softmax of each row, the row maximum subtracted before exp ([TT] 四,
+ * Softmax 数值稳定性). */
+OR_EXPORT void or_softmax_rows(const double* Z, int R, int Cc, double* P) {
+    for (int r = 0; r < R; r++) {
+        const double* z = Z + (size_t)r * Cc;
+        double* p = P + (size_t)r * Cc;
+        double mx = -INFINITY, sum = 0.0;
+        for (int c = 0; c < Cc; c++) if (z[c] > mx) mx = z[c];
+        for (int c = 0; c < Cc; c++) { p[c] = exp(z[c] - mx); sum += p[c]; }
+        for (int c = 0; c < Cc; c++) p[c] /= sum;
+    }
+}
+
+/* Jacobian-vector product of the row softmax: dZ += P o (dP - <P, dP>). */
+OR_EXPORT void or_softmax_rows_bwd(const double* P, const double* dP, int R, int Cc, double* dZ) {
+    for (int r = 0; r < R; r++) {
+        const double* p = P + (size_t)r * Cc;
+        const double* dp = dP + (size_t)r * Cc;
+        double dot = 0.0;
+        for (int c = 0; c < Cc; c++) dot += p[c] * dp[c];
+        for (int c = 0; c < Cc; c++) dZ[(size_t)r * Cc + c] += p[c] * (dp[c] - dot);
+    }
+}
+
+/* CrossEntropy of probabilities ([TT] 三.2 probs.CrossEntropy(y)):
+ *   loss = -(1/R) sum_r log P[r, y_r];  dP[r, y_r] += -dloss / (R P[r, y_r]). */
+OR_EXPORT double or_xent_probs(const double* P, const int* y, int R, int Cc, double* dP, double dloss) {
+    double s = 0.0;
+    for (int r = 0; r < R; r++) {
+        double pr = P[(size_t)r * Cc + y[r]];
+        s -= log(pr);
+        if (dP) dP[(size_t)r * Cc + y[r]] += -dloss / (R * pr);
+    }
+    return R > 0 ? s / R : 0.0;
+}
+
+/* The classifier of [TT] 八.5, on a fixed batch of R rows:
+ *   h = gelu(x W1 + b1),  z = h W2 + b2,  p = softmax(z),  loss = CE(p, y),
+ * then the gradients of W1 [nin,nh], b1 [nh], W2 [nh,nout], b2 [nout] and
+ * SGD p -= lr g.  losses[s] is the loss of step s before its update.  With
+ * grads != NULL the gradients of the last step are copied there (W1, b1,
+ * W2, b2 in that order). */
+OR_EXPORT void or_mlp_sgd(const double* x, const int* y, int R, int nin, int nh, int nout, double* W1, double* b1,
+                          double* W2, double* b2, double lr, int steps, double* losses, double* grads) {
+    const size_t n1 = (size_t)nin * nh, n2 = (size_t)nh * nout;
+    double* a = (double*)calloc((size_t)R * nh, sizeof(double));   /* x W1 */
+    double* u = (double*)calloc((size_t)R * nh, sizeof(double));   /* + b1 */
+    double* h = (double*)calloc((size_t)R * nh, sizeof(double));   /* gelu */
+    double* m = (double*)calloc((size_t)R * nout, sizeof(double)); /* h W2 */
+    double* z = (double*)calloc((size_t)R * nout, sizeof(double)); /* + b2 */
+    double* p = (double*)calloc((size_t)R * nout, sizeof(double));
+    double* dp = (double*)calloc((size_t)R * nout, sizeof(double));
+    double* dz = (double*)calloc((size_t)R * nout, sizeof(double));
+    double* dh = (double*)calloc((size_t)R * nh, sizeof(double));
+    double* du = (double*)calloc((size_t)R * nh, sizeof(double));
+    double* gW1 = (double*)calloc(n1, sizeof(double));
+    double* gb1 = (double*)calloc((size_t)nh, sizeof(double));
+    double* gW2 = (double*)calloc(n2, sizeof(double));
+    double* gb2 = (double*)calloc((size_t)nout, sizeof(double));
+    for (int s = 0; s < steps; s++) {
+        or_matmul(x, W1, R, nin, nh, a);
+        or_add_row(a, b1, R, nh, u);
+        or_gelu_fwd(u, (size_t)R * nh, h);
+        or_matmul(h, W2, R, nh, nout, m);
+        or_add_row(m, b2, R, nout, z);
+        or_softmax_rows(z, R, nout, p);
+        memset(dp, 0, sizeof(double) * (size_t)R * nout);
+        memset(dz, 0, sizeof(double) * (size_t)R * nout);
+        memset(dh, 0, sizeof(double) * (size_t)R * nh);
+        memset(du, 0, sizeof(double) * (size_t)R * nh);
+        memset(gW1, 0, sizeof(double) * n1);
+        memset(gb1, 0, sizeof(double) * (size_t)nh);
+        memset(gW2, 0, sizeof(double) * n2);
+        memset(gb2, 0, sizeof(double) * (size_t)nout);
+        double loss = or_xent_probs(p, y, R, nout, dp, 1.0);
+        if (losses) losses[s] = loss;
+        or_softmax_rows_bwd(p, dp, R, nout, dz);
+        or_add_row_bwd(dz, R, nout, NULL, gb2);
+        or_matmul_bwd(h, W2, dz, R, nh, nout, dh, gW2);
+        or_gelu_bwd(u, dh, (size_t)R * nh, du);
+        or_add_row_bwd(du, R, nh, NULL, gb1);
+        or_matmul_bwd(x, W1, du, R, nin, nh, NULL, gW1);
+        for (size_t i = 0; i < n1; i++) W1[i] -= lr * gW1[i];
+        for (int i = 0; i < nh; i++) b1[i] -= lr * gb1[i];
+        for (size_t i = 0; i < n2; i++) W2[i] -= lr * gW2[i];
+        for (int i = 0; i < nout; i++) b2[i] -= lr * gb2[i];
+    }
+    if (grads && steps > 0) {
+        memcpy(grads, gW1, sizeof(double) * n1);
+        memcpy(grads + n1, gb1, sizeof(double) * (size_t)nh);
+        memcpy(grads + n1 + nh, gW2, sizeof(double) * n2);
+        memcpy(grads + n1 + nh + n2, gb2, sizeof(double) * (size_t)nout);
+    }
+    free(a); free(u); free(h); free(m); free(z); free(p); free(dp); free(dz); free(dh); free(du);
+    free(gW1); free(gb1); free(gW2); free(gb2);
 }
 
 /* ------------------------------------------------------------------------ */
