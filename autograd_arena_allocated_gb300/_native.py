@@ -1,4 +1,5 @@
-"""ctypes declarations of the C ABI in include/tt.h and include/tt_ops.h.
+"""ctypes declarations of the C ABI in include/tt.h, include/tt_ops.h and
+include/tt_graph.h.
 
 The shared library libtt.so is built in-tree by build.py.  There is no
 fallback: if the library is missing or fails to load, every call raises.
@@ -74,6 +75,21 @@ SIGNATURES = {
     "tt_op_embed_fwd": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i]),
     "tt_op_embed_bwd": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i]),
     "tt_linear_bwd_dw_noalloc": (_st, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i]),
+    # tt_graph.h (node handles are int32; negative = tt_status)
+    "tt_node_new": (_i, [_vp, _i, C.POINTER(_i), _i]),
+    "tt_node_matmul": (_i, [_vp, _i, _i]),
+    "tt_node_add": (_i, [_vp, _i, _i]),
+    "tt_node_mul": (_i, [_vp, _i, _i]),
+    "tt_node_gelu": (_i, [_vp, _i]),
+    "tt_node_softmax": (_i, [_vp, _i]),
+    "tt_node_cross_entropy": (_i, [_vp, _i, _i]),
+    "tt_node_forward": (_st, [_vp, _i]),
+    "tt_node_zero_grad": (_st, [_vp, _i]),
+    "tt_node_backward": (_st, [_vp, _i]),
+    "tt_node_fill": (_st, [_vp, _i, _vp, _sz]),
+    "tt_node_read": (_st, [_vp, _i, _i, _vp, _sz]),
+    "tt_node_info": (_st, [_vp, _i, C.POINTER(_i), C.POINTER(_i), C.POINTER(_vp), C.POINTER(_vp)]),
+    "tt_node_sgd": (_st, [_vp, C.POINTER(_i), _i, _f]),
 }
 
 _lib = None

@@ -223,3 +223,104 @@ class Context:
     def embed_bwd(self, dtype, dx, tokens, dwte, dwpe, B, T, C_, V, maxT):
         self._check(lib().tt_op_embed_bwd(self.h, DTYPES[dtype], _ptr(dx), _ptr(tokens), _ptr(dwte),
                                           _ptr(dwpe), B, T, C_, V, maxT))
+
+    # -------------------------------------------------------------- generic graph (tt_graph.h)
+    def _node(self, h: int) -> int:
+        if h < 0:
+            raise TTError(h, lib().tt_last_error(self.h).decode())
+        return h
+
+    def tensor(self, *shape, dtype: str = "f32") -> "Node":
+        """A new leaf of the given shape (values zero); dtype "f32" or "i32"."""
+        n = len(shape)
+        arr = (C.c_int * max(n, 1))(*[int(d) for d in shape])
+        return Node(self, self._node(lib().tt_node_new(self.h, n, arr, NODE_I32 if dtype == "i32" else NODE_F32)))
+
+    def sgd(self, params, lr: float):
+        """p -= lr * grad on the device for each node of params."""
+        hs = (C.c_int * max(len(params), 1))(*[p.h for p in params])
+        self._check(lib().tt_node_sgd(self.h, hs, len(params), float(lr)))
+
+
+# ---------------------------------------------------------------- generic tensor graph
+NODE_F32, NODE_I32 = 0, 1
+
+
+class Node:
+    """A tensor of a context's generic graph (tt_graph.h).  Operators build
+    new nodes; forward / zero_grad / backward / fill / numpy run on the
+    device through the C ABI."""
+
+    def __init__(self, ctx: "Context", h: int):
+        self.ctx = ctx
+        self.h = int(h)
+
+    def _made(self, h):
+        return Node(self.ctx, self.ctx._node(h))
+
+    def matmul(self, other: "Node") -> "Node":
+        return self._made(lib().tt_node_matmul(self.ctx.h, self.h, other.h))
+
+    __matmul__ = matmul
+
+    def __add__(self, other: "Node") -> "Node":
+        return self._made(lib().tt_node_add(self.ctx.h, self.h, other.h))
+
+    def __mul__(self, other: "Node") -> "Node":
+        return self._made(lib().tt_node_mul(self.ctx.h, self.h, other.h))
+
+    def gelu(self) -> "Node":
+        return self._made(lib().tt_node_gelu(self.ctx.h, self.h))
+
+    def softmax(self) -> "Node":
+        return self._made(lib().tt_node_softmax(self.ctx.h, self.h))
+
+    def cross_entropy(self, labels: "Node") -> "Node":
+        return self._made(lib().tt_node_cross_entropy(self.ctx.h, self.h, labels.h))
+
+    def forward(self):
+        self.ctx._check(lib().tt_node_forward(self.ctx.h, self.h))
+
+    def zero_grad(self):
+        self.ctx._check(lib().tt_node_zero_grad(self.ctx.h, self.h))
+
+    def backward(self):
+        self.ctx._check(lib().tt_node_backward(self.ctx.h, self.h))
+
+    def info(self):
+        nd, shp = C.c_int(), (C.c_int * 4)()
+        data, grad = C.c_void_p(), C.c_void_p()
+        self.ctx._check(lib().tt_node_info(self.ctx.h, self.h, C.byref(nd), shp, C.byref(data), C.byref(grad)))
+        return tuple(shp[:nd.value]), data.value, grad.value
+
+    @property
+    def shape(self):
+        return self.info()[0]
+
+    def fill(self, values):
+        """values: numpy array (host) or torch tensor (device) of the node's size."""
+        import numpy as np
+        if hasattr(values, "data_ptr"):
+            src, n = values, values.numel()
+        else:
+            src = np.ascontiguousarray(values)
+            n = src.size
+        self.ctx._check(lib().tt_node_fill(self.ctx.h, self.h, C.c_void_p(_ptr(src)), n))
+        return self
+
+    def numpy(self, grad: bool = False):
+        import math
+
+        import numpy as np
+        shp, _, g = self.info()
+        if grad and g is None:
+            raise ValueError("an int32 node has no gradient")
+        out = np.zeros(shp, dtype=np.float32 if (grad or g is not None) else np.int32)
+        self.ctx._check(lib().tt_node_read(self.ctx.h, self.h, 1 if grad else 0, C.c_void_p(out.ctypes.data),
+                                           math.prod(shp)))
+        return out
+
+    def grad(self):
+        return self.numpy(grad=True)
+
+

@@ -21,6 +21,7 @@
 #include "tt_internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -81,6 +82,21 @@ struct ProfEntry {
     cudaEvent_t e0, e1;
 };
 
+// A node of the generic tensor graph: its value and gradient in the arena,
+// the op that makes it and its inputs (tinytorch 三.2).
+enum GOp : int { G_LEAF = 0, G_MATMUL, G_ADD, G_ADD_ROW, G_MUL, G_GELU, G_SOFTMAX, G_XENT };
+struct GNode {
+    int op = G_LEAF;
+    int type = TT_NODE_F32;
+    int ndim = 0;
+    int shape[4] = {1, 1, 1, 1};
+    long long n = 0;
+    void* data = nullptr;
+    float* grad = nullptr;  // null for int32 nodes
+    int in0 = -1, in1 = -1;
+    int uses = 0;           // nodes that take this one as an input
+};
+
 struct tt_ctx {
     uint64_t magic = TT_MAGIC;
     int device = 0;
@@ -103,6 +119,9 @@ struct tt_ctx {
     bool profiling = false;
     std::vector<ProfEntry> prof;
     std::vector<cudaEvent_t> event_pool;
+    // the generic tensor graph (tt_graph.h): nodes made since the last reset
+    std::vector<struct GNode> gnodes;
+    uint32_t gepoch = 0;
 };
 
 // Brackets the launches of one op with events when profiling is on.
@@ -133,6 +152,15 @@ struct ProfScope {
 
 // ------------------------------------------------------------------ helpers
 static bool live(const tt_ctx* c) { return c && c->magic == TT_MAGIC; }
+
+// Graph handles carry an 11-bit epoch, new for every context and every reset,
+// so that a handle of an earlier epoch or of another context is refused.
+static uint32_t next_graph_epoch() {
+    static std::atomic<uint32_t> e{0};
+    uint32_t v;
+    do { v = (e.fetch_add(1) + 1) & 0x7FF; } while (v == 0);
+    return v;
+}
 
 static tt_status fail(tt_ctx* c, tt_status s, const char* fmt, ...) {
     if (c) {
@@ -737,6 +765,7 @@ tt_status tt_ctx_create(size_t arena_bytes, tt_ctx** out) {
     *out = nullptr;
     if (arena_bytes == 0) return TT_ERR_ARG;
     tt_ctx* c = new tt_ctx();
+    c->gepoch = next_graph_epoch();
     c->cap = arena_bytes + ARENA_HEADER;
     if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return TT_ERR_CUDA; }
     cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -803,6 +832,8 @@ tt_status tt_ctx_reset(tt_ctx* c) {
     c->off = ARENA_HEADER;
     begin_step(c);
     c->loss_dev = c->row_loss_dev = nullptr;
+    c->gnodes.clear();
+    c->gepoch = next_graph_epoch();
     if (cudaMemsetAsync(c->arena, 0, FLAG_COUNT * sizeof(int), c->stream) != cudaSuccess)
         return fail(c, TT_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(cudaGetLastError()));
     return TT_OK;
@@ -1297,6 +1328,329 @@ tt_status tt_op_embed_bwd(tt_ctx* c, tt_dtype dtype, const void* dx, const int32
     }
     c->off = mark;
     return op_epilogue(c, "embed_bwd");
+}
+
+// ------------------------------------------------------------------ generic tensor graph
+static constexpr int G_IDX_BITS = 20;
+
+static int g_index(const tt_ctx* c, tt_node h) {
+    if (h < 0) return -1;
+    const uint32_t ep = ((uint32_t)h >> G_IDX_BITS) & 0x7FF;
+    const int idx = h & ((1 << G_IDX_BITS) - 1);
+    if (ep != c->gepoch || idx >= (int)c->gnodes.size()) return -1;
+    return idx;
+}
+
+static tt_node g_handle(const tt_ctx* c, int idx) { return (tt_node)((c->gepoch << G_IDX_BITS) | (uint32_t)idx); }
+
+#define G_CTX()                                  \
+    if (!c) return TT_ERR_ARG;                   \
+    if (!live(c)) return TT_ERR_STALE
+
+static tt_node g_new(tt_ctx* c, int op, int type, int ndim, const int* shape, int in0, int in1) {
+    if ((int)c->gnodes.size() >= (1 << G_IDX_BITS)) return fail(c, TT_ERR_ARG, "graph: too many nodes");
+    GNode g;
+    g.op = op;
+    g.type = type;
+    g.ndim = ndim;
+    long long n = 1;
+    for (int i = 0; i < ndim; i++) {
+        if (shape[i] <= 0 || n > (1ll << 40) / shape[i]) return fail(c, TT_ERR_ARG, "graph: bad shape");
+        g.shape[i] = shape[i];
+        n *= shape[i];
+    }
+    g.n = n;
+    g.in0 = in0;
+    g.in1 = in1;
+    const size_t mark = c->off;
+    c->oom = false;
+    g.data = arena_alloc(c, (size_t)n * 4);
+    if (type == TT_NODE_F32) g.grad = (float*)arena_alloc(c, (size_t)n * 4);
+    if (c->oom) {
+        c->off = mark;
+        c->oom = false;
+        return fail(c, TT_ERR_ARENA_OOM, "graph: the arena cannot hold a node of %lld elements", n);
+    }
+    if (cudaMemsetAsync(g.data, 0, (size_t)n * 4, c->stream) != cudaSuccess ||
+        (g.grad && cudaMemsetAsync(g.grad, 0, (size_t)n * 4, c->stream) != cudaSuccess))
+        return fail(c, TT_ERR_CUDA, "graph: %s", cudaGetErrorString(cudaGetLastError()));
+    if (in0 >= 0) c->gnodes[in0].uses++;
+    if (in1 >= 0) c->gnodes[in1].uses++;
+    c->gnodes.push_back(g);
+    return g_handle(c, (int)c->gnodes.size() - 1);
+}
+
+static int g_rows(const GNode& g) { return (int)(g.n / g.shape[g.ndim - 1]); }
+static int g_cols(const GNode& g) { return g.shape[g.ndim - 1]; }
+static float* g_f(const GNode& g) { return (float*)g.data; }
+
+// run node i's forward
+static void g_forward_one(tt_ctx* c, int i) {
+    const Launch L = launch_of(c);
+    const GNode& g = c->gnodes[i];
+    const GNode* a = g.in0 >= 0 ? &c->gnodes[g.in0] : nullptr;
+    const GNode* b = g.in1 >= 0 ? &c->gnodes[g.in1] : nullptr;
+    switch (g.op) {
+    case G_MATMUL: {
+        const int M = a->shape[0], K = a->shape[1], N = b->shape[1];
+        launch_g_matmul(L, g_f(*a), K, 1, g_f(*b), N, 1, g_f(g), M, N, K, false);
+        break;
+    }
+    case G_ADD: launch_g_add(L, g_f(*a), g_f(*b), g_f(g), g.n, 0); break;
+    case G_ADD_ROW: launch_g_add(L, g_f(*a), g_f(*b), g_f(g), g.n, (int)b->n); break;
+    case G_MUL: launch_g_mul(L, g_f(*a), g_f(*b), g_f(g), g.n); break;
+    case G_GELU: launch_g_gelu(L, g_f(*a), g_f(g), g.n); break;
+    case G_SOFTMAX: launch_g_softmax(L, g_f(*a), g_f(g), g_rows(*a), g_cols(*a)); break;
+    case G_XENT: launch_g_xent(L, g_f(*a), (const int32_t*)b->data, g_rows(*a), g_cols(*a), g_f(g)); break;
+    default: break;
+    }
+}
+
+// nodes that n depends on (n included), as a mark per node
+static std::vector<char> g_ancestors(const tt_ctx* c, int n) {
+    std::vector<char> need(c->gnodes.size(), 0);
+    need[n] = 1;
+    for (int i = n; i >= 0; i--) {  // inputs have smaller indices than their consumers
+        if (!need[i]) continue;
+        const GNode& g = c->gnodes[i];
+        if (g.in0 >= 0) need[g.in0] = 1;
+        if (g.in1 >= 0) need[g.in1] = 1;
+    }
+    return need;
+}
+
+static tt_status g_done(tt_ctx* c, const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return TT_OK;
+}
+
+tt_node tt_node_new(tt_ctx* c, int ndim, const int* shape, tt_node_type type) {
+    G_CTX();
+    if (ndim < 1 || ndim > 4 || !shape || (type != TT_NODE_F32 && type != TT_NODE_I32))
+        return fail(c, TT_ERR_ARG, "node_new: ndim must be 1..4 with a shape and a known type");
+    return g_new(c, G_LEAF, type, ndim, shape, -1, -1);
+}
+
+static int g_input(tt_ctx* c, tt_node h, const char* what, bool f32) {
+    const int i = g_index(c, h);
+    if (i < 0) {
+        fail(c, TT_ERR_STALE, "%s: stale or foreign node handle %d", what, (int)h);
+        return -1;
+    }
+    if (f32 && c->gnodes[i].type != TT_NODE_F32) {
+        fail(c, TT_ERR_ARG, "%s: input %d is not float32", what, (int)h);
+        return -2;
+    }
+    return i;
+}
+
+#define G_IN(var, h, what, f32)                        \
+    const int var = g_input(c, h, what, f32);         \
+    if (var < 0) return var == -1 ? TT_ERR_STALE : TT_ERR_ARG
+
+tt_node tt_node_matmul(tt_ctx* c, tt_node ha, tt_node hb) {
+    G_CTX();
+    G_IN(a, ha, "matmul", true);
+    G_IN(b, hb, "matmul", true);
+    const GNode &A = c->gnodes[a], &B = c->gnodes[b];
+    if (A.ndim != 2 || B.ndim != 2 || A.shape[1] != B.shape[0])
+        return fail(c, TT_ERR_ARG, "matmul: needs A [M,K] and B [K,N]");
+    const int shp[2] = {A.shape[0], B.shape[1]};
+    return g_new(c, G_MATMUL, TT_NODE_F32, 2, shp, a, b);
+}
+
+tt_node tt_node_add(tt_ctx* c, tt_node ha, tt_node hb) {
+    G_CTX();
+    G_IN(a, ha, "add", true);
+    G_IN(b, hb, "add", true);
+    const GNode &A = c->gnodes[a], &B = c->gnodes[b];
+    bool same = A.ndim == B.ndim;
+    for (int i = 0; same && i < A.ndim; i++) same = A.shape[i] == B.shape[i];
+    const bool row = !same && B.ndim == 1 && B.shape[0] == g_cols(A);
+    if (!same && !row) return fail(c, TT_ERR_ARG, "add: b must have a's shape or be a row of a's last dimension");
+    int shp[4];
+    for (int i = 0; i < A.ndim; i++) shp[i] = A.shape[i];
+    return g_new(c, same ? G_ADD : G_ADD_ROW, TT_NODE_F32, A.ndim, shp, a, b);
+}
+
+tt_node tt_node_mul(tt_ctx* c, tt_node ha, tt_node hb) {
+    G_CTX();
+    G_IN(a, ha, "mul", true);
+    G_IN(b, hb, "mul", true);
+    const GNode &A = c->gnodes[a], &B = c->gnodes[b];
+    bool same = A.ndim == B.ndim;
+    for (int i = 0; same && i < A.ndim; i++) same = A.shape[i] == B.shape[i];
+    if (!same) return fail(c, TT_ERR_ARG, "mul: shapes differ");
+    int shp[4];
+    for (int i = 0; i < A.ndim; i++) shp[i] = A.shape[i];
+    return g_new(c, G_MUL, TT_NODE_F32, A.ndim, shp, a, b);
+}
+
+static tt_node g_unary(tt_ctx* c, tt_node ha, int op, const char* what) {
+    G_IN(a, ha, what, true);
+    const GNode& A = c->gnodes[a];
+    int shp[4];
+    for (int i = 0; i < A.ndim; i++) shp[i] = A.shape[i];
+    return g_new(c, op, TT_NODE_F32, A.ndim, shp, a, -1);
+}
+
+tt_node tt_node_gelu(tt_ctx* c, tt_node a) {
+    G_CTX();
+    return g_unary(c, a, G_GELU, "gelu");
+}
+
+tt_node tt_node_softmax(tt_ctx* c, tt_node a) {
+    G_CTX();
+    return g_unary(c, a, G_SOFTMAX, "softmax");
+}
+
+tt_node tt_node_cross_entropy(tt_ctx* c, tt_node hp, tt_node hy) {
+    G_CTX();
+    G_IN(p, hp, "cross_entropy", true);
+    G_IN(y, hy, "cross_entropy", false);
+    const GNode &P = c->gnodes[p], &Y = c->gnodes[y];
+    if (Y.type != TT_NODE_I32 || Y.n != g_rows(P))
+        return fail(c, TT_ERR_ARG, "cross_entropy: labels must be int32 with one per row of p");
+    const int one = 1;
+    return g_new(c, G_XENT, TT_NODE_F32, 1, &one, p, y);
+}
+
+tt_status tt_node_forward(tt_ctx* c, tt_node h) {
+    G_CTX();
+    G_IN(n, h, "forward", false);
+    const std::vector<char> need = g_ancestors(c, n);
+    for (int i = 0; i <= n; i++)
+        if (need[i] && c->gnodes[i].op != G_LEAF) g_forward_one(c, i);
+    return g_done(c, "forward");
+}
+
+tt_status tt_node_zero_grad(tt_ctx* c, tt_node h) {
+    G_CTX();
+    G_IN(n, h, "zero_grad", false);
+    const std::vector<char> need = g_ancestors(c, n);
+    for (int i = 0; i <= n; i++) {
+        const GNode& g = c->gnodes[i];
+        if (need[i] && g.grad && cudaMemsetAsync(g.grad, 0, (size_t)g.n * 4, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "zero_grad: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    return TT_OK;
+}
+
+tt_status tt_node_backward(tt_ctx* c, tt_node h) {
+    G_CTX();
+    G_IN(n, h, "backward", true);
+    const Launch L = launch_of(c);
+    const std::vector<char> need = g_ancestors(c, n);
+    for (int i = 0; i < n; i++) {
+        const GNode& g = c->gnodes[i];
+        if (need[i] && g.op != G_LEAF && cudaMemsetAsync(g.grad, 0, (size_t)g.n * 4, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "backward: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    launch_g_fill(L, c->gnodes[n].grad, c->gnodes[n].n, 1.0f);
+    std::vector<char> done(c->gnodes.size(), 0);  // a softmax whose gradient its cross entropy formed
+    for (int i = n; i >= 0; i--) {
+        if (!need[i] || done[i]) continue;
+        const GNode& g = c->gnodes[i];
+        if (g.op == G_LEAF) continue;
+        GNode* a = g.in0 >= 0 ? &c->gnodes[g.in0] : nullptr;
+        GNode* b = g.in1 >= 0 ? &c->gnodes[g.in1] : nullptr;
+        switch (g.op) {
+        case G_MATMUL: {
+            const int M = a->shape[0], K = a->shape[1], N = b->shape[1];
+            // dA += dC B^T: (m, k) <- sum_n dC[m, n] B[k, n]
+            launch_g_matmul(L, g.grad, N, 1, g_f(*b), 1, N, a->grad, M, K, N, true);
+            // dB += A^T dC: (k, n) <- sum_m A[m, k] dC[m, n]
+            launch_g_matmul(L, g_f(*a), 1, K, g.grad, N, 1, b->grad, K, N, M, true);
+            break;
+        }
+        case G_ADD:
+            launch_g_acc(L, a->grad, g.grad, g.n);
+            launch_g_acc(L, b->grad, g.grad, g.n);
+            break;
+        case G_ADD_ROW:
+            launch_g_acc(L, a->grad, g.grad, g.n);
+            launch_g_colsum_acc(L, g.grad, g_rows(g), g_cols(g), b->grad);
+            break;
+        case G_MUL:
+            launch_g_mul_bwd(L, g.grad, g_f(*a), g_f(*b), a->grad, b->grad, g.n);
+            break;
+        case G_GELU: launch_g_gelu_bwd(L, g.grad, g_f(*a), a->grad, g.n); break;
+        case G_SOFTMAX: launch_g_softmax_bwd(L, g_f(g), g.grad, a->grad, g_rows(g), g_cols(g)); break;
+        case G_XENT: {
+            const int rows = g_rows(*a), cols = g_cols(*a);
+            if (a->op == G_SOFTMAX && a->uses == 1) {
+                // the pair's gradient directly: (p - onehot) / R into the logits
+                GNode& z = c->gnodes[a->in0];
+                launch_g_softmax_xent_bwd(L, g_f(*a), (const int32_t*)b->data, g.grad, rows, cols, z.grad);
+                done[g.in0] = 1;
+            } else {
+                launch_g_xent_bwd(L, g_f(*a), (const int32_t*)b->data, g.grad, rows, cols, a->grad);
+            }
+            break;
+        }
+        default: break;
+        }
+    }
+    return g_done(c, "backward");
+}
+
+static bool is_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+tt_status tt_node_fill(tt_ctx* c, tt_node h, const void* src, size_t count) {
+    G_CTX();
+    G_IN(n, h, "fill", false);
+    const GNode& g = c->gnodes[n];
+    if (!src || count != (size_t)g.n) return fail(c, TT_ERR_ARG, "fill: %zu values for %lld elements", count, g.n);
+    const cudaMemcpyKind k = is_device_ptr(src) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    if (cudaMemcpyAsync(g.data, src, count * 4, k, c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "fill: %s", cudaGetErrorString(cudaGetLastError()));
+    if (k == cudaMemcpyHostToDevice && cudaStreamSynchronize(c->stream) != cudaSuccess)  // src may be reused
+        return fail(c, TT_ERR_CUDA, "fill: %s", cudaGetErrorString(cudaGetLastError()));
+    return TT_OK;
+}
+
+tt_status tt_node_read(tt_ctx* c, tt_node h, int grad, void* dst, size_t count) {
+    G_CTX();
+    G_IN(n, h, "read", false);
+    const GNode& g = c->gnodes[n];
+    if (!dst || count != (size_t)g.n) return fail(c, TT_ERR_ARG, "read: %zu values for %lld elements", count, g.n);
+    const void* s = grad ? (const void*)g.grad : g.data;
+    if (!s) return fail(c, TT_ERR_ARG, "read: an int32 node has no gradient");
+    if (cudaMemcpyAsync(dst, s, count * 4, cudaMemcpyDefault, c->stream) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "read: %s", cudaGetErrorString(cudaGetLastError()));
+    return tt_ctx_sync(c);
+}
+
+tt_status tt_node_info(tt_ctx* c, tt_node h, int* ndim, int* shape, void** data, float** grad) {
+    G_CTX();
+    G_IN(n, h, "info", false);
+    const GNode& g = c->gnodes[n];
+    if (ndim) *ndim = g.ndim;
+    if (shape)
+        for (int i = 0; i < 4; i++) shape[i] = g.shape[i];
+    if (data) *data = g.data;
+    if (grad) *grad = g.grad;
+    return TT_OK;
+}
+
+tt_status tt_node_sgd(tt_ctx* c, const tt_node* params, int n_params, float lr) {
+    G_CTX();
+    if (n_params < 0 || (n_params > 0 && !params)) return fail(c, TT_ERR_ARG, "sgd: bad parameter list");
+    const Launch L = launch_of(c);
+    for (int k = 0; k < n_params; k++) {
+        G_IN(i, params[k], "sgd", true);
+        const GNode& g = c->gnodes[i];
+        launch_g_sgd(L, g_f(g), g.grad, g.n, lr);
+    }
+    return g_done(c, "sgd");
 }
 
 }  // extern "C"

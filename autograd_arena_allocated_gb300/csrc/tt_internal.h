@@ -11,6 +11,7 @@
 
 #include "../../include/tt.h"
 #include "../../include/tt_ops.h"
+#include "../../include/tt_graph.h"
 
 namespace tt {
 
@@ -165,6 +166,27 @@ bool launch_gemm_skinny_pick(const Launch& L, const void* A, const void* W, int 
                              unsigned long long* keys, int* advance);
 void launch_pick(const Launch& L, const unsigned long long* keys, int nct, int rows, int32_t* tok, int ld_tok,
                  const int* pos_dev);
+
+// the generic tensor graph (graph.cu), fp32
+void launch_g_matmul(const Launch& L, const float* X, long long xi, long long xk, const float* Y, long long yk,
+                     long long yj, float* C, int M, int N, int K, bool accumulate);
+void launch_g_add(const Launch& L, const float* a, const float* b, float* c, long long n, int bcols);
+void launch_g_mul(const Launch& L, const float* a, const float* b, float* c, long long n);
+void launch_g_gelu(const Launch& L, const float* a, float* c, long long n);
+void launch_g_softmax(const Launch& L, const float* z, float* p, int rows, int cols);
+void launch_g_xent(const Launch& L, const float* p, const int32_t* y, int rows, int cols, float* loss);
+void launch_g_fill(const Launch& L, float* d, long long n, float v);
+void launch_g_acc(const Launch& L, float* d, const float* s, long long n);
+void launch_g_colsum_acc(const Launch& L, const float* dC, int rows, int cols, float* db);
+void launch_g_mul_bwd(const Launch& L, const float* dc, const float* a, const float* b, float* ga, float* gb,
+                      long long n);
+void launch_g_gelu_bwd(const Launch& L, const float* dc, const float* a, float* ga, long long n);
+void launch_g_softmax_bwd(const Launch& L, const float* p, const float* dp, float* dz, int rows, int cols);
+void launch_g_xent_bwd(const Launch& L, const float* p, const int32_t* y, const float* dloss, int rows, int cols,
+                       float* dp);
+void launch_g_softmax_xent_bwd(const Launch& L, const float* p, const int32_t* y, const float* dloss, int rows,
+                               int cols, float* dz);
+void launch_g_sgd(const Launch& L, float* w, const float* g, long long n, float lr);
 
 bool attention_mma_eligible(bool bf16, int C, int H);
 void launch_attention_fwd_mma(const Launch& L, const void* qkv, void* y, float* lse,

@@ -216,6 +216,8 @@ OP_SHAPES = {
     "eval": "forward-only evaluation loss (tt_gpt2_eval), 124M, B=32 T=1024, bf16",
     "generate": "greedy generation with the key/value cache (tt_gpt2_generate), 124M bf16, B=8, "
                 "64-token prompts, 448 new tokens",
+    "fruit": "the generic tensor graph: the tinytorch page's classifier (3 -> 32 GELU -> 3, softmax, "
+             "cross entropy) trained by SGD on 64 samples, one step = forward, zero_grad, backward, SGD",
 }
 
 
@@ -380,6 +382,56 @@ def run_inference(args):
     return 0
 
 
+def run_fruit(args):
+    """Steps/s of the generic graph's classifier loop on the device, and the
+    oracle's float64 loop on the host cores for the same steps."""
+    import numpy as np
+    import torch
+
+    from autograd_arena_allocated_gb300 import api, synth
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    x, y = synth.fruit_batch(64)
+    params = synth.mlp_init(*synth.FRUIT_SHAPE)
+    ctx = api.Context(64 << 20)
+    P = [ctx.tensor(*p.shape).fill(p) for p in params]
+    xn = ctx.tensor(*x.shape).fill(x)
+    yn = ctx.tensor(*y.shape, dtype="i32").fill(y)
+    loss = ((xn @ P[0] + P[1]).gelu() @ P[2] + P[3]).softmax().cross_entropy(yn)
+    steps = max(args.reps, 1) * 100
+
+    def run(n):
+        for _ in range(n):
+            loss.forward()
+            loss.zero_grad()
+            loss.backward()
+            ctx.sgd(P, 0.1)
+
+    run(max(args.warmup, 1) * 10)
+    torch.cuda.synchronize()
+    n0 = ctx.launches
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    run(steps)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    launches = (ctx.launches - n0) / steps
+    final = float(loss.numpy()[0])
+    ctx.close()
+    from oracle import mlp_sgd  # the oracle's float64 loop: the CPU baseline
+    t0 = time.perf_counter()
+    mlp_sgd(x, y, *params, 0.1, steps)
+    cpu_s = time.perf_counter() - t0
+    print(json.dumps({"op": "fruit", "what": OP_SHAPES["fruit"], "steps": steps, "us_per_step": 1e3 * ms / steps,
+                      "steps_per_s": steps / (ms * 1e-3), "kernel_launches_per_step": launches,
+                      "final_loss": final, "cpu_baseline": {"kind": "oracle", "cores": 1,
+                                                             "steps_per_s": steps / cpu_s}}), flush=True)
+    return 0
+
+
 def run_op(args):
     """Runs one kernel group `--reps` times through the C ABI (for profiling)."""
     import torch
@@ -505,6 +557,8 @@ def main():
         args.warmup = max(1, args.warmup)
         if args.op in ("eval", "generate"):
             return run_inference(args)
+        if args.op == "fruit":
+            return run_fruit(args)
         return run_gemm_shapes(args) if args.op == "gemm_shapes" else run_op(args)
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     world, rank, local = dist_setup()
