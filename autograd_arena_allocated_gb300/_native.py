@@ -90,6 +90,9 @@ SIGNATURES = {
     "tt_node_read": (_st, [_vp, _i, _i, _vp, _sz]),
     "tt_node_info": (_st, [_vp, _i, C.POINTER(_i), C.POINTER(_i), C.POINTER(_vp), C.POINTER(_vp)]),
     "tt_node_sgd": (_st, [_vp, C.POINTER(_i), _i, _f]),
+    "tt_capture_begin": (_st, [_vp]),
+    "tt_capture_end": (_st, [_vp]),
+    "tt_replay": (_st, [_vp, _i]),
 }
 
 _lib = None

@@ -241,6 +241,28 @@ class Context:
         hs = (C.c_int * max(len(params), 1))(*[p.h for p in params])
         self._check(lib().tt_node_sgd(self.h, hs, len(params), float(lr)))
 
+    def capture_begin(self):
+        self._check(lib().tt_capture_begin(self.h))
+
+    def capture_end(self):
+        self._check(lib().tt_capture_end(self.h))
+
+    def replay(self, times: int = 1):
+        self._check(lib().tt_replay(self.h, int(times)))
+
+    def record(self, fn):
+        """Record the graph calls fn() makes (run nothing); replay() runs them."""
+        self.capture_begin()
+        try:
+            fn()
+        except BaseException:
+            try:
+                self.capture_end()
+            except TTError:
+                pass
+            raise
+        self.capture_end()
+
 
 # ---------------------------------------------------------------- generic tensor graph
 NODE_F32, NODE_I32 = 0, 1

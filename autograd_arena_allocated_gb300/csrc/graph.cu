@@ -199,6 +199,15 @@ __global__ void k_g_softmax_xent_bwd(const float* __restrict__ p, const int32_t*
     }
 }
 
+// zero up to G_ZERO_MAX buffers in one launch: blockIdx.y picks the buffer
+__global__ void k_g_zero_many(GZeroList l) {
+    const int e = blockIdx.y;
+    float* d = l.p[e];
+    const long long n = l.n[e];
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        d[i] = 0.0f;
+}
+
 __global__ void k_g_sgd(float* __restrict__ w, const float* __restrict__ g, long long n, float lr) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
         w[i] -= lr * g[i];
@@ -245,6 +254,15 @@ void launch_g_softmax_xent_bwd(const Launch& L, const float* p, const int32_t* y
     G_EW(k_g_softmax_xent_bwd, p, y, dloss, rows, cols, dz);
 }
 #undef G_EW
+
+void launch_g_zero_many(const Launch& L, const GZeroList& l) {
+    if (L.dry || l.count <= 0) return;
+    L.count();
+    long long mx = 1;
+    for (int i = 0; i < l.count; i++) mx = std::max(mx, l.n[i]);
+    const dim3 grid((unsigned)std::min<long long>((mx + 255) / 256, 64), (unsigned)l.count);
+    k_g_zero_many<<<grid, 256, 0, L.stream>>>(l);
+}
 
 void launch_g_softmax(const Launch& L, const float* z, float* p, int rows, int cols) {
     if (L.dry || rows <= 0) return;

@@ -122,6 +122,11 @@ struct tt_ctx {
     // the generic tensor graph (tt_graph.h): nodes made since the last reset
     std::vector<struct GNode> gnodes;
     uint32_t gepoch = 0;
+    // a recording of graph calls (tt_capture_begin / tt_capture_end / tt_replay)
+    bool capturing = false;
+    cudaStream_t cap_stream = nullptr, saved_stream = nullptr;
+    cudaGraphExec_t recording = nullptr;
+    uint64_t rec_launches = 0, cap_launches0 = 0;
 };
 
 // Brackets the launches of one op with events when profiling is on.
@@ -788,7 +793,19 @@ tt_status tt_ctx_create(size_t arena_bytes, tt_ctx** out) {
 void tt_ctx_destroy(tt_ctx* c) {
     if (!live(c)) return;
     c->magic = TT_DEAD;
+    if (c->capturing) {
+        cudaGraph_t g = nullptr;
+        cudaStreamEndCapture(c->cap_stream, &g);
+        if (g) cudaGraphDestroy(g);
+        c->stream = c->saved_stream;
+        c->capturing = false;
+    }
     cudaStreamSynchronize(c->stream);
+    if (c->recording) cudaGraphExecDestroy(c->recording);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    c->recording = nullptr;
+    c->cap_stream = nullptr;
+    cudaGetLastError();
     cudaFree(c->arena);
     c->arena = nullptr;
     c->cap = 0;
@@ -829,6 +846,11 @@ tt_status tt_ctx_set_gemm_backend(tt_ctx* c, int backend) {
 tt_status tt_ctx_reset(tt_ctx* c) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
+    if (c->capturing) return fail(c, TT_ERR_STATE, "reset while recording");
+    if (c->recording) {  // freed once any replay in flight completes
+        cudaGraphExecDestroy(c->recording);
+        c->recording = nullptr;
+    }
     c->off = ARENA_HEADER;
     begin_step(c);
     c->loss_dev = c->row_loss_dev = nullptr;
@@ -842,6 +864,7 @@ tt_status tt_ctx_reset(tt_ctx* c) {
 tt_status tt_ctx_sync(tt_ctx* c) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
+    if (c->capturing) return fail(c, TT_ERR_STATE, "sync while recording");
     int flags[FLAG_COUNT];
     if (cudaMemcpyAsync(flags, c->arena, sizeof flags, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
         cudaStreamSynchronize(c->stream) != cudaSuccess)
@@ -954,6 +977,7 @@ tt_status tt_gpt2_step(tt_ctx* c, const void* params, float* grads, const int32_
                        const int32_t* targets, int B, int T, float* loss) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
+    if (c->capturing) return fail(c, TT_ERR_STATE, "GPT-2 calls cannot be recorded");
     if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
     if (!params || !grads || !tokens || !targets)
         return fail(c, TT_ERR_ARG, "NULL parameter, gradient or token pointer");
@@ -1015,6 +1039,7 @@ tt_status tt_gpt2_eval(tt_ctx* c, const void* params, const int32_t* tokens, con
                        float* loss) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
+    if (c->capturing) return fail(c, TT_ERR_STATE, "GPT-2 calls cannot be recorded");
     if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
     if (!params || !tokens || !targets) return fail(c, TT_ERR_ARG, "NULL parameter or token pointer");
     if (B <= 0 || T <= 0 || T > c->cfg.maxT)
@@ -1072,6 +1097,7 @@ tt_status tt_gpt2_generate(tt_ctx* c, const void* params, const int32_t* prompt,
                            int32_t* out) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
+    if (c->capturing) return fail(c, TT_ERR_STATE, "GPT-2 calls cannot be recorded");
     if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
     if (!params || !prompt || !out) return fail(c, TT_ERR_ARG, "NULL parameter, prompt or output pointer");
     if (B <= 0 || T_prompt <= 0 || n_new < 0 || T_prompt + n_new > c->cfg.maxT)
@@ -1348,6 +1374,7 @@ static tt_node g_handle(const tt_ctx* c, int idx) { return (tt_node)((c->gepoch 
     if (!live(c)) return TT_ERR_STALE
 
 static tt_node g_new(tt_ctx* c, int op, int type, int ndim, const int* shape, int in0, int in1) {
+    if (c->capturing) return fail(c, TT_ERR_STATE, "graph: nodes cannot be made while recording");
     if ((int)c->gnodes.size() >= (1 << G_IDX_BITS)) return fail(c, TT_ERR_ARG, "graph: too many nodes");
     GNode g;
     g.op = op;
@@ -1525,16 +1552,29 @@ tt_status tt_node_forward(tt_ctx* c, tt_node h) {
     return g_done(c, "forward");
 }
 
+// zero the gradients of the marked nodes (leaves only if with_leaves), a few
+// dozen buffers per launch
+static void g_zero_grads(tt_ctx* c, const std::vector<char>& need, int upto, bool with_leaves) {
+    const Launch L = launch_of(c);
+    GZeroList l{};
+    for (int i = 0; i <= upto; i++) {
+        const GNode& g = c->gnodes[i];
+        if (!need[i] || !g.grad || (!with_leaves && g.op == G_LEAF)) continue;
+        l.p[l.count] = g.grad;
+        l.n[l.count] = g.n;
+        if (++l.count == G_ZERO_MAX) {
+            launch_g_zero_many(L, l);
+            l.count = 0;
+        }
+    }
+    launch_g_zero_many(L, l);
+}
+
 tt_status tt_node_zero_grad(tt_ctx* c, tt_node h) {
     G_CTX();
     G_IN(n, h, "zero_grad", false);
-    const std::vector<char> need = g_ancestors(c, n);
-    for (int i = 0; i <= n; i++) {
-        const GNode& g = c->gnodes[i];
-        if (need[i] && g.grad && cudaMemsetAsync(g.grad, 0, (size_t)g.n * 4, c->stream) != cudaSuccess)
-            return fail(c, TT_ERR_CUDA, "zero_grad: %s", cudaGetErrorString(cudaGetLastError()));
-    }
-    return TT_OK;
+    g_zero_grads(c, g_ancestors(c, n), n, true);
+    return g_done(c, "zero_grad");
 }
 
 tt_status tt_node_backward(tt_ctx* c, tt_node h) {
@@ -1542,11 +1582,7 @@ tt_status tt_node_backward(tt_ctx* c, tt_node h) {
     G_IN(n, h, "backward", true);
     const Launch L = launch_of(c);
     const std::vector<char> need = g_ancestors(c, n);
-    for (int i = 0; i < n; i++) {
-        const GNode& g = c->gnodes[i];
-        if (need[i] && g.op != G_LEAF && cudaMemsetAsync(g.grad, 0, (size_t)g.n * 4, c->stream) != cudaSuccess)
-            return fail(c, TT_ERR_CUDA, "backward: %s", cudaGetErrorString(cudaGetLastError()));
-    }
+    g_zero_grads(c, need, n - 1, false);
     launch_g_fill(L, c->gnodes[n].grad, c->gnodes[n].n, 1.0f);
     std::vector<char> done(c->gnodes.size(), 0);  // a softmax whose gradient its cross entropy formed
     for (int i = n; i >= 0; i--) {
@@ -1610,6 +1646,8 @@ tt_status tt_node_fill(tt_ctx* c, tt_node h, const void* src, size_t count) {
     const GNode& g = c->gnodes[n];
     if (!src || count != (size_t)g.n) return fail(c, TT_ERR_ARG, "fill: %zu values for %lld elements", count, g.n);
     const cudaMemcpyKind k = is_device_ptr(src) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    if (c->capturing && k == cudaMemcpyHostToDevice)
+        return fail(c, TT_ERR_STATE, "fill from host memory while recording");
     if (cudaMemcpyAsync(g.data, src, count * 4, k, c->stream) != cudaSuccess)
         return fail(c, TT_ERR_CUDA, "fill: %s", cudaGetErrorString(cudaGetLastError()));
     if (k == cudaMemcpyHostToDevice && cudaStreamSynchronize(c->stream) != cudaSuccess)  // src may be reused
@@ -1624,6 +1662,7 @@ tt_status tt_node_read(tt_ctx* c, tt_node h, int grad, void* dst, size_t count) 
     if (!dst || count != (size_t)g.n) return fail(c, TT_ERR_ARG, "read: %zu values for %lld elements", count, g.n);
     const void* s = grad ? (const void*)g.grad : g.data;
     if (!s) return fail(c, TT_ERR_ARG, "read: an int32 node has no gradient");
+    if (c->capturing) return fail(c, TT_ERR_STATE, "read while recording");
     if (cudaMemcpyAsync(dst, s, count * 4, cudaMemcpyDefault, c->stream) != cudaSuccess)
         return fail(c, TT_ERR_CUDA, "read: %s", cudaGetErrorString(cudaGetLastError()));
     return tt_ctx_sync(c);
@@ -1651,6 +1690,62 @@ tt_status tt_node_sgd(tt_ctx* c, const tt_node* params, int n_params, float lr) 
         launch_g_sgd(L, g_f(g), g.grad, g.n, lr);
     }
     return g_done(c, "sgd");
+}
+
+tt_status tt_capture_begin(tt_ctx* c) {
+    G_CTX();
+    if (c->capturing) return fail(c, TT_ERR_STATE, "a recording is already open");
+    if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "capture: %s", cudaGetErrorString(cudaGetLastError()));
+    // the recording is replayed on the context's stream, after whatever is queued there then
+    if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+        return fail(c, TT_ERR_CUDA, "capture: %s", cudaGetErrorString(cudaGetLastError()));
+    c->saved_stream = c->stream;
+    c->stream = c->cap_stream;
+    c->capturing = true;
+    c->cap_launches0 = c->launches;
+    return TT_OK;
+}
+
+tt_status tt_capture_end(tt_ctx* c) {
+    G_CTX();
+    if (!c->capturing) return fail(c, TT_ERR_STATE, "no open recording");
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(c->cap_stream, &g);
+    c->stream = c->saved_stream;
+    c->capturing = false;
+    const uint64_t nodes = c->launches - c->cap_launches0;
+    c->launches = c->cap_launches0;  // recorded, not run
+    if (c->recording) {
+        cudaGraphExecDestroy(c->recording);
+        c->recording = nullptr;
+    }
+    if (e != cudaSuccess || !g) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return fail(c, TT_ERR_CUDA, "capture: %s", cudaGetErrorString(e));
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&c->recording, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) {
+        c->recording = nullptr;
+        cudaGetLastError();
+        return fail(c, TT_ERR_CUDA, "capture: %s", cudaGetErrorString(ei));
+    }
+    c->rec_launches = nodes;
+    return TT_OK;
+}
+
+tt_status tt_replay(tt_ctx* c, int times) {
+    G_CTX();
+    if (c->capturing || !c->recording) return fail(c, TT_ERR_STATE, "nothing recorded to replay");
+    if (times < 0) return fail(c, TT_ERR_ARG, "replay: times < 0");
+    for (int i = 0; i < times; i++) {
+        if (cudaGraphLaunch(c->recording, c->stream) != cudaSuccess)
+            return fail(c, TT_ERR_CUDA, "replay: %s", cudaGetErrorString(cudaGetLastError()));
+        c->launches += c->rec_launches;
+    }
+    return TT_OK;
 }
 
 }  // extern "C"

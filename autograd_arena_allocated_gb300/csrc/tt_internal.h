@@ -168,6 +168,13 @@ void launch_pick(const Launch& L, const unsigned long long* keys, int nct, int r
                  const int* pos_dev);
 
 // the generic tensor graph (graph.cu), fp32
+constexpr int G_ZERO_MAX = 32;
+struct GZeroList {  // buffers to zero in one launch (passed by value)
+    float* p[G_ZERO_MAX];
+    long long n[G_ZERO_MAX];
+    int count;
+};
+void launch_g_zero_many(const Launch& L, const GZeroList& l);
 void launch_g_matmul(const Launch& L, const float* X, long long xi, long long xk, const float* Y, long long yk,
                      long long yj, float* C, int M, int N, int K, bool accumulate);
 void launch_g_add(const Launch& L, const float* a, const float* b, float* c, long long n, int bcols);

@@ -409,16 +409,22 @@ def run_fruit(args):
             loss.backward()
             ctx.sgd(P, 0.1)
 
+    def timed(fn):
+        torch.cuda.synchronize()
+        n0 = ctx.launches
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), (ctx.launches - n0) / steps
+
     run(max(args.warmup, 1) * 10)
-    torch.cuda.synchronize()
-    n0 = ctx.launches
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    run(steps)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    launches = (ctx.launches - n0) / steps
+    ms, launches = timed(lambda: run(steps))
+    # the same step recorded once as a CUDA graph and replayed
+    ctx.record(lambda: run(1))
+    ctx.replay(max(args.warmup, 1) * 10)
+    ms_rec, _ = timed(lambda: ctx.replay(steps))
     final = float(loss.numpy()[0])
     ctx.close()
     from oracle import mlp_sgd  # the oracle's float64 loop: the CPU baseline
@@ -427,6 +433,7 @@ def run_fruit(args):
     cpu_s = time.perf_counter() - t0
     print(json.dumps({"op": "fruit", "what": OP_SHAPES["fruit"], "steps": steps, "us_per_step": 1e3 * ms / steps,
                       "steps_per_s": steps / (ms * 1e-3), "kernel_launches_per_step": launches,
+                      "recorded": {"us_per_step": 1e3 * ms_rec / steps, "steps_per_s": steps / (ms_rec * 1e-3)},
                       "final_loss": final, "cpu_baseline": {"kind": "oracle", "cores": 1,
                                                              "steps_per_s": steps / cpu_s}}), flush=True)
     return 0

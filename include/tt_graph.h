@@ -105,6 +105,30 @@ tt_status tt_node_info(tt_ctx* ctx, tt_node n, int* ndim, int* shape, void** dat
  * n_params f32 nodes (tinytorch 八.5). */
 tt_status tt_node_sgd(tt_ctx* ctx, const tt_node* params, int n_params, float lr);
 
+/* ---------------------------------------------------------------- recording
+ * A fixed sequence of graph calls (a training step: forward, zero_grad,
+ * backward, sgd) can be recorded once as a CUDA graph and replayed, so that
+ * each later step costs one graph launch instead of one launch per kernel.
+ * Between tt_capture_begin and tt_capture_end the calls of this header
+ * record their kernels and memsets instead of running them; calls that must
+ * wait for the device (tt_node_read, tt_node_fill from host memory,
+ * tt_ctx_sync, tt_ctx_reset, the GPT-2 calls of tt.h) and calls that make
+ * nodes return TT_ERR_STATE meanwhile.  A context keeps one recording: a new capture replaces it, and
+ * tt_ctx_reset drops it (its nodes are gone). */
+
+/* Start recording.  TT_ERR_STATE if a recording is already open. */
+tt_status tt_capture_begin(tt_ctx* ctx);
+
+/* Stop recording and keep what was recorded.  TT_ERR_STATE without an open
+ * recording; TT_ERR_CUDA if a recorded call could not be captured (the
+ * context is usable afterwards, with no recording). */
+tt_status tt_capture_end(tt_ctx* ctx);
+
+/* Run the recording `times` times on the context's stream, in order.
+ * TT_ERR_STATE if there is no recording (or one is open), TT_ERR_ARG for
+ * times < 0. */
+tt_status tt_replay(tt_ctx* ctx, int times);
+
 #ifdef __cplusplus
 }
 #endif

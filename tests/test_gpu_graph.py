@@ -235,3 +235,53 @@ def test_graph_errors(ctx):
         with pytest.raises(api.TTError, match="TT_ERR_ARENA_OOM"):
             small.tensor(1024, 1024)
         small.tensor(8)  # still usable
+
+
+def test_recorded_step_replays_the_loop(ctx, oracle):
+    """One step recorded as a CUDA graph and replayed gives the directly run
+    loop's weights bit for bit, and follows the oracle."""
+    x, y = synth.fruit_batch(64)
+    params = synth.mlp_init(*synth.FRUIT_SHAPE)
+    steps = 200
+    ctx.reset()
+    P, _, _, _, loss = _fruit_graph(ctx, x, y, params)
+
+    def step():
+        loss.forward()
+        loss.zero_grad()
+        loss.backward()
+        ctx.sgd(P, 0.1)
+
+    for _ in range(steps):
+        step()
+    direct = [p.numpy() for p in P]
+    ctx.reset()
+    P, _, _, _, loss = _fruit_graph(ctx, x, y, params)
+    step()
+    n0 = ctx.launches
+    ctx.record(step)  # recorded, not run
+    assert ctx.launches == n0
+    ctx.replay(steps - 1)
+    assert ctx.launches > n0
+    replayed = [p.numpy() for p in P]
+    for a, b in zip(direct, replayed):
+        assert np.array_equal(a, b)
+    _, new_params, _ = oracle.mlp_sgd(x, y, *params, 0.1, steps)
+    for got, want in zip(replayed, new_params):
+        assert _rel(got, want) <= 1e-4
+    # calls that wait for the device, or make nodes, are refused while recording
+    ctx.capture_begin()
+    for call in (lambda: loss.numpy(), ctx.sync, ctx.reset, lambda: ctx.tensor(3),
+                 lambda: P[0].fill(np.zeros(P[0].shape, dtype=np.float32))):
+        with pytest.raises(api.TTError, match="TT_ERR_STATE"):
+            call()
+    with pytest.raises(api.TTError, match="TT_ERR_STATE"):
+        ctx.capture_begin()
+    ctx.capture_end()
+    ctx.replay(0)
+    # a reset drops the recording
+    ctx.reset()
+    with pytest.raises(api.TTError, match="TT_ERR_STATE"):
+        ctx.replay(1)
+    with pytest.raises(api.TTError, match="TT_ERR_STATE"):
+        ctx.capture_end()
