@@ -57,6 +57,10 @@ def lib():
             "or_softmax_rows_bwd": (None, [dp, dp, i, i, dp]),
             "or_xent_probs": (d, [dp, ip, i, i, dp, d]),
             "or_mlp_sgd": (None, [dp, ip, i, i, i, i, dp, dp, dp, dp, d, i, dp, dp]),
+            "or_grad_norm": (d, [dp, sz, d, ip]),
+            "or_clip_coef": (d, [d, d]),
+            "or_adamw_ex": (i, [dp, dp, dp, dp, sz, d, d, d, d, d, i, d, d]),
+            "or_loss_scale_update": (None, [dp, ip, i, i, d, d]),
             "or_val_reset": (None, []),
             "or_val_leaf": (i, [d]),
             "or_val_add": (i, [i, i]),
@@ -337,6 +341,35 @@ def mlp_sgd(x, y, W1, b1, W2, b2, lr, steps):
     g = (grads[:n1].reshape(W1.shape), grads[n1:n1 + nh], grads[n1 + nh:n1 + nh + n2].reshape(W2.shape),
          grads[n1 + nh + n2:])
     return losses[:steps], (W1, b1, W2, b2), g
+
+
+# ---------------------------------------------------------------- update-side variants
+def grad_norm(g, scale=1.0):
+    """(||g / scale||_2, nonfinite flag)."""
+    g = f64(np.ravel(g))
+    bad = C.c_int()
+    n = lib().or_grad_norm(_d(g), g.size, float(scale), C.byref(bad))
+    return float(n), int(bad.value)
+
+
+def clip_coef(norm, max_norm):
+    return float(lib().or_clip_coef(float(norm), float(max_norm)))
+
+
+def adamw_ex(p, g, m, v, lr, beta1, beta2, eps, weight_decay, t, scale=1.0, max_norm=0.0):
+    """Updates copies of p, m, v; returns (p, m, v, skipped)."""
+    p, g, m, v = (f64(a).copy() for a in (p, g, m, v))
+    skipped = lib().or_adamw_ex(_d(p), _d(g), _d(m), _d(v), p.size, lr, beta1, beta2, eps, weight_decay, int(t),
+                                float(scale), float(max_norm))
+    return p, m, v, bool(skipped)
+
+
+def loss_scale_update(scale, clean, overflow, window=1000, growth=1.001, backoff=0.5):
+    """One update of the dynamic loss scale; returns (scale, clean)."""
+    s, c = C.c_double(scale), C.c_int(clean)
+    lib().or_loss_scale_update(C.byref(s), C.byref(c), int(bool(overflow)), int(window), float(growth),
+                               float(backoff))
+    return float(s.value), int(c.value)
 
 
 # ---------------------------------------------------------------- scalar tape

@@ -19,6 +19,9 @@
  *           3.2 gradient accumulation, 4.2 finite-difference check, 4.3 graph trace.
  *   [MCRAD] the "microcrad" page: Values 的工作原理, 操作, 反向传播 (topological
  *           backward returning 0 / -1).
+ *   [DLS]   "从零手写C++深度学习框架：Tensor设计、Autograd与CUDA优化实战" (the
+ *           dl-scratch page): 3.2 clip_grad_norm_ on the gradient storage, 3.4
+ *           dynamic loss scaling (halve on Inf/NaN, grow after a run of clean steps).
  *
  * Readings taken where the pages are silent or garbled (each is listed in
  * the design notes of the repository):
@@ -34,7 +37,13 @@
  *   - MatMul is C = A B with B [K, N] ([TT] 三.3); the classifier's weights are
  *     therefore W1 [3, 32] and W2 [32, 3] ([TT] 八.5 declares them [32, 3] and
  *     [3, 32], which does not compose with that MatMul);
- *   - the classifier's SGD update is p[i] -= lr * g[i] for every element.
+ *   - the classifier's SGD update is p[i] -= lr * g[i] for every element;
+ *   - gradient clipping is the global L2 norm clip with coefficient
+ *     min(1, max_norm / (norm + 1e-6)) ([DLS] 3.2 names clip_grad_norm_ only);
+ *   - loss scaling multiplies the loss by the scale, an overflow skips the
+ *     update and halves the scale, and every window-th clean step in a row
+ *     multiplies it by the growth factor ([DLS] 3.4: halve; x1.001 after
+ *     1000 clean steps).
  *
  * Parity pins: every exported function is pinned by tests/test_oracle_*.py
  * against closed forms, worked examples printed on the pages, library
@@ -501,6 +510,61 @@ OR_EXPORT void or_adamw(double* p, const double* g, double* m, double* v, size_t
         double mh = m[i] / c1;
         double vh = v[i] / c2;
         p[i] -= lr * (mh / (sqrt(vh) + eps) + wd * p[i]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Update-side variants ([DLS] 3.2: the global norm clip applied to the     */
+/* separate gradient storage; 3.4: dynamic loss scaling; accumulation of     */
+/* gradients over micro-batches is the += of [TT] 三.3).                     */
+/* ------------------------------------------------------------------------ */
+
+/* sqrt(sum_i (g_i / scale)^2); *nonfinite = 1 if the sum is Inf or NaN. */
+OR_EXPORT double or_grad_norm(const double* g, size_t n, double scale, int* nonfinite) {
+    double s = 0.0;
+    for (size_t i = 0; i < n; i++) {
+        double x = g[i] / scale;
+        s += x * x;
+    }
+    if (nonfinite) *nonfinite = isfinite(s) ? 0 : 1;
+    return sqrt(s);
+}
+
+/* The clip coefficient of a global norm clip: min(1, max_norm / (norm + 1e-6)). */
+OR_EXPORT double or_clip_coef(double norm, double max_norm) {
+    double c = max_norm / (norm + 1e-6);
+    return c < 1.0 ? c : 1.0;
+}
+
+/* AdamW step t on the gradient g / scale, clipped to max_norm (max_norm <= 0:
+ * no clip), skipped entirely (returns 1, nothing changed) when the unscaled
+ * gradient is not finite; returns 0 after an update. */
+OR_EXPORT int or_adamw_ex(double* p, const double* g, double* m, double* v, size_t n, double lr, double b1,
+                          double b2, double eps, double wd, int t, double scale, double max_norm) {
+    int bad = 0;
+    double norm = or_grad_norm(g, n, scale, &bad);
+    if (bad) return 1;
+    double k = 1.0 / scale;
+    if (max_norm > 0.0) k *= or_clip_coef(norm, max_norm);
+    double* ge = (double*)malloc(sizeof(double) * (n ? n : 1));
+    for (size_t i = 0; i < n; i++) ge[i] = g[i] * k;
+    or_adamw(p, ge, m, v, n, lr, b1, b2, eps, wd, t);
+    free(ge);
+    return 0;
+}
+
+/* Dynamic loss scale ([DLS] 3.4): an overflow multiplies the scale by backoff
+ * and restarts the count of clean steps; a clean step counts, and the
+ * window-th clean step in a row multiplies the scale by growth and restarts
+ * the count. */
+OR_EXPORT void or_loss_scale_update(double* scale, int* clean, int overflow, int window, double growth,
+                                    double backoff) {
+    if (overflow) {
+        *scale *= backoff;
+        *clean = 0;
+    } else if (++*clean >= window) {
+        *scale *= growth;
+        *clean = 0;
     }
 }
 
