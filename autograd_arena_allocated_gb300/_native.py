@@ -60,6 +60,10 @@ SIGNATURES = {
     "tt_adamw": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _i]),
     "tt_cast_f32_to_bf16": (_st, [_vp, _vp, _vp, _sz]),
     "tt_gpt2_eval": (_st, [_vp, _vp, _vp, _vp, _i, _i, C.POINTER(C.c_float)]),
+    "tt_gpt2_step_ex": (_st, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, C.POINTER(_f)]),
+    "tt_grad_stats": (_st, [_vp, _vp, _sz, _vp, _vp]),
+    "tt_adamw_ex": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _vp, _vp, _f, _vp]),
+    "tt_loss_scale_update": (_st, [_vp, _vp, _vp, _vp, _i, _f, _f]),
     "tt_gpt2_generate_arena_bytes": (_sz, [_vp, _i, _i, _i]),
     "tt_gpt2_generate": (_st, [_vp, _vp, _vp, _i, _i, _i, _vp]),
     # tt_ops.h

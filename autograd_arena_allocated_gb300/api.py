@@ -149,6 +149,33 @@ class Context:
                                        C.byref(loss) if sync else None))
         return float(loss.value) if sync else None
 
+    def step_ex(self, params, grads, tokens, targets, B: int, T: int, accumulate: bool = False,
+                loss_scale=None, sync: bool = True):
+        """tt_gpt2_step_ex: accumulate adds into grads; loss_scale is a device
+        float (torch tensor) that scales the backward."""
+        loss = C.c_float()
+        self._check(lib().tt_gpt2_step_ex(self.h, _ptr(params), _ptr(grads), _ptr(tokens), _ptr(targets),
+                                          int(B), int(T), 1 if accumulate else 0, _ptr(loss_scale),
+                                          C.byref(loss) if sync else None))
+        return float(loss.value) if sync else None
+
+    def grad_stats(self, grads, stats, loss_scale=None, n=None):
+        """stats (device float[2]) = (||grads / scale||, not finite)."""
+        n = grads.numel() if n is None else n
+        self._check(lib().tt_grad_stats(self.h, _ptr(grads), int(n), _ptr(loss_scale), _ptr(stats)))
+
+    def adamw_ex(self, master, lowp, grads, m, v, lr, beta1, beta2, eps, weight_decay, step, stats=None,
+                 max_norm=0.0, loss_scale=None, n=None):
+        """tt_adamw_ex; step is a device int32 tensor (updates taken so far)."""
+        n = master.numel() if n is None else n
+        self._check(lib().tt_adamw_ex(self.h, _ptr(master), _ptr(lowp), _ptr(grads), _ptr(m), _ptr(v), int(n),
+                                      float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                                      _ptr(step), _ptr(stats), float(max_norm), _ptr(loss_scale)))
+
+    def loss_scale_update(self, loss_scale, clean_steps, stats, window=1000, growth=1.001, backoff=0.5):
+        self._check(lib().tt_loss_scale_update(self.h, _ptr(loss_scale), _ptr(clean_steps), _ptr(stats),
+                                               int(window), float(growth), float(backoff)))
+
     def eval(self, params, tokens, targets, B: int, T: int) -> float:
         """tt_gpt2_eval: forward and mean loss only (synchronizes)."""
         loss = C.c_float()

@@ -213,14 +213,14 @@ __global__ void k_embed_segsum(const T* __restrict__ dx, const int32_t* __restri
 
 template <typename T>
 __global__ void k_embed_wpe(const T* __restrict__ dx, int B, int T_, int C, int maxT,
-                            float* __restrict__ dwpe) {
+                            float* __restrict__ dwpe, int acc) {
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long long)maxT * C) return;
     int t = (int)(i / C), c = (int)(i % C);
     float s = 0.0f;
     if (t < T_)
         for (int b = 0; b < B; b++) s += ld(dx, ((long long)b * T_ + t) * C + c);
-    dwpe[i] = s;
+    dwpe[i] = acc ? dwpe[i] + s : s;
 }
 
 // scratch: keys/values A and B [M] each, the digit counts [256 x tiles], then
@@ -234,7 +234,7 @@ size_t embed_bwd_scratch_bytes(int M, int C) {
 
 void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t* tok,
                       float* dwte, float* dwpe, int B, int T, int C, int V, int maxT,
-                      void* scratch) {
+                      void* scratch, bool acc_params) {
     if (L.dry) return;
     const int M = B * T;
     int32_t* s = (int32_t*)scratch;
@@ -275,10 +275,10 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
     L.count();
     if (bf16)
         k_embed_wpe<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, L.stream>>>(
-            (const __nv_bfloat16*)dx, B, T, C, maxT, dwpe);
+            (const __nv_bfloat16*)dx, B, T, C, maxT, dwpe, acc_params ? 1 : 0);
     else
         k_embed_wpe<float><<<blocks_for(n, 256), 256, 0, L.stream>>>((const float*)dx, B, T, C,
-                                                                     maxT, dwpe);
+                                                                     maxT, dwpe, acc_params ? 1 : 0);
 }
 
 // ================================================================== layernorm
@@ -398,13 +398,13 @@ __global__ void k_layernorm_bwd(const T* __restrict__ x, const T* __restrict__ w
 
 // out_a[c] = sum_b part[b][c], out_b[c] = sum_b part[b][C + c] (b in order)
 __global__ void k_sum_partials(const float* __restrict__ part, int nblk, int C,
-                               float* __restrict__ out_a, float* __restrict__ out_b) {
+                               float* __restrict__ out_a, float* __restrict__ out_b, int acc) {
     int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= 2 * C) return;
     float s = 0.0f;
     for (int b = 0; b < nblk; b++) s += part[(long long)b * 2 * C + c];
-    if (c < C) { if (out_a) out_a[c] = s; }
-    else if (out_b) out_b[c - C] = s;
+    if (c < C) { if (out_a) out_a[c] = acc ? out_a[c] + s : s; }
+    else if (out_b) out_b[c - C] = acc ? out_b[c - C] + s : s;
 }
 
 size_t layernorm_bwd_scratch_floats(int M, int C) {
@@ -415,9 +415,10 @@ size_t layernorm_bwd_scratch_floats(int M, int C) {
 
 void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const float* mean, const float* rstd, const void* dy, void* dx,
-                          float* dw, float* db, int M, int C, bool accumulate, float* scratch) {
+                          float* dw, float* db, int M, int C, bool accumulate, float* scratch,
+                          bool acc_params) {
     if (L.dry) return;
-    if (bf16 && launch_ln_bwd_bf16(L, x, w, mean, rstd, dy, dx, dw, db, M, C, accumulate, scratch))
+    if (bf16 && launch_ln_bwd_bf16(L, x, w, mean, rstd, dy, dx, dw, db, M, C, accumulate, scratch, acc_params))
         return;
     const int nblk = (M + LN_ROWS - 1) / LN_ROWS;
     const size_t smem = (size_t)LN_BWD_WARPS * 2 * C * sizeof(float);
@@ -439,7 +440,7 @@ void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void*
             (const float*)x, (const float*)w, mean, rstd, (const float*)dy, (float*)dx, scratch,
             M, C, accumulate ? 1 : 0);
     L.count();
-    k_sum_partials<<<blocks_for(2 * C, 256), 256, 0, L.stream>>>(scratch, nblk, C, dw, db);
+    k_sum_partials<<<blocks_for(2 * C, 256), 256, 0, L.stream>>>(scratch, nblk, C, dw, db, acc_params ? 1 : 0);
 }
 
 // ================================================================== cross entropy
@@ -457,8 +458,9 @@ __device__ __forceinline__ void online_merge(float& m, float& s, float m2, float
 template <typename T>
 __global__ void __launch_bounds__(XENT_THREADS)
 k_xent(T* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict__ row_loss,
-       int V, int ld_, float dscale, int* flags) {
+       int V, int ld_, float dscale, const float* __restrict__ scale_dev, int* flags) {
     __shared__ float s_m[XENT_THREADS / 32], s_s[XENT_THREADS / 32];
+    if (scale_dev) dscale *= *scale_dev;
     __shared__ float s_lse;
     const long long row = blockIdx.x;
     T* zr = z + row * (long long)ld_;
@@ -522,9 +524,10 @@ __global__ void k_mean_loss(const float* __restrict__ row_loss, int M, float* __
 }
 
 void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* targets,
-                 float* row_loss, float* mean_loss, int M, int V, int ld_, float dscale) {
+                 float* row_loss, float* mean_loss, int M, int V, int ld_, float dscale,
+                 const float* scale_dev) {
     if (L.dry) return;
-    if (bf16 && launch_xent_bf16(L, logits, targets, row_loss, M, V, ld_, dscale)) {
+    if (bf16 && launch_xent_bf16(L, logits, targets, row_loss, M, V, ld_, dscale, scale_dev)) {
         if (mean_loss) {
             L.count();
             k_mean_loss<<<1, 1024, 0, L.stream>>>(row_loss, M, mean_loss, L.flags);
@@ -534,10 +537,10 @@ void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* target
     L.count();
     if (bf16)
         k_xent<__nv_bfloat16><<<M, XENT_THREADS, 0, L.stream>>>(
-            (__nv_bfloat16*)logits, targets, row_loss, V, ld_, dscale, L.flags);
+            (__nv_bfloat16*)logits, targets, row_loss, V, ld_, dscale, scale_dev, L.flags);
     else
         k_xent<float><<<M, XENT_THREADS, 0, L.stream>>>((float*)logits, targets, row_loss, V, ld_,
-                                                        dscale, L.flags);
+                                                        dscale, scale_dev, L.flags);
     if (mean_loss) {
         L.count();
         k_mean_loss<<<1, 1024, 0, L.stream>>>(row_loss, M, mean_loss, L.flags);
@@ -559,12 +562,12 @@ __global__ void k_colsum_part(const T* __restrict__ x, int M, int N, float* __re
 }
 
 __global__ void k_colsum_final(const float* __restrict__ part, int nchunk, int N,
-                               float* __restrict__ out) {
+                               float* __restrict__ out, int acc) {
     int n = blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= N) return;
     float s = 0.0f;
     for (int c = 0; c < nchunk; c++) s += part[(long long)c * N + n];
-    out[n] = s;
+    out[n] = acc ? out[n] + s : s;
 }
 
 size_t colsum_scratch_floats(int M, int N) {
@@ -572,11 +575,11 @@ size_t colsum_scratch_floats(int M, int N) {
 }
 
 void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, float* out,
-                   float* scratch) {
+                   float* scratch, bool acc) {
     if (L.dry) return;
     int nchunk = (M + COLSUM_ROWS - 1) / COLSUM_ROWS;
     if (bf16 && launch_colsum_bf16(L, x, M, N, scratch)) {
-        launch_sum_rows(L, scratch, nchunk, N, N, out, nullptr);
+        launch_sum_rows(L, scratch, nchunk, N, N, out, nullptr, acc);
         return;
     }
     dim3 grid(blocks_for(N, 128), nchunk);
@@ -586,7 +589,7 @@ void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, floa
     else
         k_colsum_part<float><<<grid, 128, 0, L.stream>>>((const float*)x, M, N, scratch);
     L.count();
-    k_colsum_final<<<blocks_for(N, 256), 256, 0, L.stream>>>(scratch, nchunk, N, out);
+    k_colsum_final<<<blocks_for(N, 256), 256, 0, L.stream>>>(scratch, nchunk, N, out, acc ? 1 : 0);
 }
 
 // ================================================================== AdamW

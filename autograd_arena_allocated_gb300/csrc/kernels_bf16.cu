@@ -202,7 +202,7 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
 // out_a taking columns [0, C) and out_b columns [C, 2C), and for bias sums.)
 __global__ void __launch_bounds__(256)
 k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* __restrict__ out_a,
-           float* __restrict__ out_b) {
+           float* __restrict__ out_b, int acc) {
     __shared__ float sm[8][33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
@@ -225,16 +225,16 @@ k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* _
         float t = 0.0f;
 #pragma unroll
         for (int w = 0; w < 8; w++) t += sm[w][lane];
-        if (c < split) { if (out_a) out_a[c] = t; }
-        else if (out_b) out_b[c - split] = t;
+        if (c < split) { if (out_a) out_a[c] = acc ? out_a[c] + t : t; }
+        else if (out_b) out_b[c - split] = acc ? out_b[c - split] + t : t;
     }
 }
 
 void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int split, float* out_a,
-                     float* out_b) {
+                     float* out_b, bool acc) {
     if (L.dry) return;
     L.count();
-    k_sum_rows<<<(ncols + 31) / 32, 256, 0, L.stream>>>(part, G, ncols, split, out_a, out_b);
+    k_sum_rows<<<(ncols + 31) / 32, 256, 0, L.stream>>>(part, G, ncols, split, out_a, out_b, acc ? 1 : 0);
 }
 
 constexpr int LN_BWD_MAX_BLOCKS = 1024;
@@ -278,7 +278,7 @@ bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const voi
 
 bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
                         const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
-                        int C, bool accumulate, float* scratch) {
+                        int C, bool accumulate, float* scratch, bool acc_params) {
     if (C % 8 || C > 1024) return false;
     if (L.dry) return true;
     const int nv = (C / 8 + 31) / 32;
@@ -301,7 +301,7 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     if (nv == 1) { LNB(1); } else if (nv == 2) { LNB(2); } else if (nv == 3) { LNB(3); } else { LNB(4); }
 #undef LNB
     L.count();
-    k_sum_rows<<<(2 * C + 31) / 32, 256, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db);
+    k_sum_rows<<<(2 * C + 31) / 32, 256, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db, acc_params ? 1 : 0);
     return true;
 }
 
@@ -323,8 +323,9 @@ __device__ __forceinline__ float ex2f(float x) {
 
 __global__ void __launch_bounds__(XS_THREADS)
 k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict__ row_loss,
-            int V, int ld, float dscale, int* flags) {
+            int V, int ld, float dscale, const float* __restrict__ scale_dev, int* flags) {
     __shared__ float sm[XS_THREADS / 32];
+    if (scale_dev) dscale *= *scale_dev;
     const long long row = blockIdx.x;
     uint4* zr = reinterpret_cast<uint4*>(z + row * (long long)ld);
     const int nvec = ld >> 3;
@@ -409,12 +410,12 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
 }
 
 bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
-                      int V, int ld, float dscale) {
+                      int V, int ld, float dscale, const float* scale_dev) {
     if (ld % 8 || ((uintptr_t)logits & 15) || ld < 2048) return false;
     if (L.dry) return true;
     L.count();
     k_xent_bf16<<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
-                                                 L.flags);
+                                                 scale_dev, L.flags);
     return true;
 }
 

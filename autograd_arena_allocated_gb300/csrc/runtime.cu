@@ -122,6 +122,10 @@ struct tt_ctx {
     // the generic tensor graph (tt_graph.h): nodes made since the last reset
     std::vector<struct GNode> gnodes;
     uint32_t gepoch = 0;
+    // step variants (tt_gpt2_step_ex): parameter gradients added to the
+    // caller's buffers, and the device loss scale that seeds the backward
+    bool accum_params = false;
+    const float* loss_scale_dev = nullptr;
     // a recording of graph calls (tt_capture_begin / tt_capture_end / tt_replay)
     bool capturing = false;
     cudaStream_t cap_stream = nullptr, saved_stream = nullptr;
@@ -356,7 +360,7 @@ static void op_xent(tt_ctx* c, int z, const int32_t* targets, int V) {
     ProfScope ps(c, PK_XENT, 0.0, 2.0 * M * ld * esize(m.dtype) + 8.0 * M);
     if (!c->oom)
         launch_xent(launch_of(c), bf, c->tensors[z].data, targets, c->row_loss_dev, c->loss_dev, M, V,
-                    ld, 1.0f / (float)M);
+                    ld, 1.0f / (float)M, c->loss_scale_dev);
     Record r;
     r.kind = R_XENT;
     r.in = z; r.M = M; r.N = V; r.idx = targets;
@@ -420,9 +424,9 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
             }
             if (through_gelu) xt.grad_is_pre = true;
         }
-        // weight and bias gradients (fp32, first write overwrites)
+        // weight and bias gradients (fp32, first write overwrites unless the step accumulates)
         {
-            const bool accW = !first_write(c, r.dW);
+            const bool accW = !first_write(c, r.dW) || c->accum_params;
             GemmArgs g;
             g.A = dy; g.lda = r.N; g.a_kmajor = false;
             g.B = c->tensors[r.in].data; g.ldb = r.K; g.b_kmajor = false;
@@ -438,7 +442,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
                 size_t mark = c->off;
                 float* s = (float*)arena_alloc(c, colsum_scratch_floats(r.M, r.N) * 4);
                 ProfScope ps(c, PK_COLSUM, 0.0, (double)r.M * r.N * esize(m.dtype) + 4.0 * r.N);
-                if (!c->oom) launch_colsum(L, bf, dy, r.M, r.N, r.db, s);
+                if (!c->oom) launch_colsum(L, bf, dy, r.M, r.N, r.db, s, c->accum_params);
                 c->off = mark;
             }
         }
@@ -456,7 +460,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
         ProfScope ps(c, PK_LN_BWD, 0.0, (acc ? 4.0 : 3.0) * r.M * r.N * esize(m.dtype) + 8.0 * r.M);
         if (!c->oom)
             launch_layernorm_bwd(L, bf, c->tensors[r.in].data, r.W, r.mean, r.rstd, y.grad, dx, r.dW,
-                                 r.db, r.M, r.N, acc, s);
+                                 r.db, r.M, r.N, acc, s, c->accum_params);
         c->off = mark;
         return TT_OK;
     }
@@ -481,7 +485,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
     case R_EMBED: {
         TapeTensor& y = c->tensors[r.out];
         if (!y.grad) return TT_OK;
-        if (first_write(c, r.dW) && !c->dry) {
+        if (first_write(c, r.dW) && !c->accum_params && !c->dry) {
             if (cudaMemsetAsync(r.dW, 0, (size_t)r.V * r.N * 4, c->stream) != cudaSuccess)
                 return fail(c, TT_ERR_CUDA, "memset failed");
         }
@@ -491,7 +495,8 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
         ProfScope ps(c, PK_EMBED_BWD, 0.0,
                      (double)r.B * r.T * r.N * (esize(m.dtype) + 8.0) + 4.0 * r.maxT * r.N);
         if (!c->oom)
-            launch_embed_bwd(L, bf, y.grad, r.idx, r.dW, r.dwpe, r.B, r.T, r.N, r.V, r.maxT, s);
+            launch_embed_bwd(L, bf, y.grad, r.idx, r.dW, r.dwpe, r.B, r.T, r.N, r.V, r.maxT, s,
+                             c->accum_params);
         c->off = mark;
         return TT_OK;
     }
@@ -975,6 +980,11 @@ size_t tt_gpt2_arena_bytes(const tt_gpt2_config* m, int B, int T) {
 
 tt_status tt_gpt2_step(tt_ctx* c, const void* params, float* grads, const int32_t* tokens,
                        const int32_t* targets, int B, int T, float* loss) {
+    return tt_gpt2_step_ex(c, params, grads, tokens, targets, B, T, 0, nullptr, loss);
+}
+
+tt_status tt_gpt2_step_ex(tt_ctx* c, const void* params, float* grads, const int32_t* tokens,
+                          const int32_t* targets, int B, int T, int flags, const float* loss_scale, float* loss) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
     if (c->capturing) return fail(c, TT_ERR_STATE, "GPT-2 calls cannot be recorded");
@@ -1008,7 +1018,12 @@ tt_status tt_gpt2_step(tt_ctx* c, const void* params, float* grads, const int32_
             return fail(c, TT_ERR_CUDA, "target copy failed");
         tgt = st_tgt;
     }
+    if (flags & ~TT_STEP_ACCUMULATE) return fail(c, TT_ERR_ARG, "unknown step flags 0x%x", (unsigned)flags);
+    c->accum_params = (flags & TT_STEP_ACCUMULATE) != 0;
+    c->loss_scale_dev = loss_scale;
     tt_status s = gpt2_forward_backward(c, params, grads, tok, tgt, B, T);
+    c->accum_params = false;
+    c->loss_scale_dev = nullptr;
     if (s != TT_OK) {
         if (s == TT_ERR_ARENA_OOM) return fail(c, s, "arena exhausted during the step");
         return s;
@@ -1745,6 +1760,55 @@ tt_status tt_replay(tt_ctx* c, int times) {
             return fail(c, TT_ERR_CUDA, "replay: %s", cudaGetErrorString(cudaGetLastError()));
         c->launches += c->rec_launches;
     }
+    return TT_OK;
+}
+
+// ------------------------------------------------------------------ clipping and loss scaling
+tt_status tt_grad_stats(tt_ctx* c, const float* grads, size_t n, const float* loss_scale, float* stats) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!grads || !stats || n == 0) return fail(c, TT_ERR_ARG, "grad_stats: NULL pointer or n == 0");
+    const Launch L = launch_of(c);
+    const size_t mark = c->off;
+    c->oom = false;
+    double* s = (double*)arena_alloc(c, grad_stats_scratch_doubles(L) * sizeof(double));
+    if (c->oom) {
+        c->off = mark;
+        c->oom = false;
+        return fail(c, TT_ERR_ARENA_OOM, "grad_stats: no arena room for %zu partial sums", grad_stats_scratch_doubles(L));
+    }
+    launch_grad_stats(L, grads, n, loss_scale, stats, s);
+    c->off = mark;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "grad_stats: %s", cudaGetErrorString(e));
+    return TT_OK;
+}
+
+tt_status tt_adamw_ex(tt_ctx* c, float* master, void* params_lowp, const float* grads, float* m, float* v, size_t n,
+                      float lr, float beta1, float beta2, float eps, float weight_decay, int* step,
+                      const float* stats, float max_norm, const float* loss_scale) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!master || !grads || !m || !v || !step) return fail(c, TT_ERR_ARG, "adamw_ex: NULL pointer");
+    if (max_norm > 0.0f && !stats) return fail(c, TT_ERR_ARG, "adamw_ex: clipping needs the gradient statistics");
+    if (((uintptr_t)master | (uintptr_t)grads | (uintptr_t)m | (uintptr_t)v) & 15)
+        return fail(c, TT_ERR_ARG, "adamw_ex: buffers must be 16-byte aligned");
+    launch_adamw_ex(launch_of(c), master, (__nv_bfloat16*)params_lowp, grads, m, v, n, lr, beta1, beta2, eps,
+                    weight_decay, step, stats, max_norm, loss_scale);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "adamw_ex: %s", cudaGetErrorString(e));
+    return TT_OK;
+}
+
+tt_status tt_loss_scale_update(tt_ctx* c, float* loss_scale, int* clean_steps, const float* stats, int window,
+                               float growth, float backoff) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!loss_scale || !clean_steps || !stats || window < 1 || !(growth >= 1.0f) || !(backoff > 0.0f && backoff < 1.0f))
+        return fail(c, TT_ERR_ARG, "loss_scale_update: bad arguments");
+    launch_loss_scale_update(launch_of(c), loss_scale, clean_steps, stats, window, growth, backoff);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "loss_scale_update: %s", cudaGetErrorString(e));
     return TT_OK;
 }
 

@@ -85,26 +85,39 @@ void launch_embed_fwd(const Launch& L, bool bf16, const void* wte, const void* w
 size_t embed_bwd_scratch_bytes(int M, int C);
 void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t* tok,
                       float* dwte, float* dwpe, int B, int T, int C, int V, int maxT,
-                      void* scratch);
+                      void* scratch, bool acc_params = false);
 
 size_t layernorm_bwd_scratch_floats(int M, int C);
 void launch_layernorm_fwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const void* b, void* y, float* mean, float* rstd, int M, int C);
 void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const float* mean, const float* rstd, const void* dy, void* dx,
-                          float* dw, float* db, int M, int C, bool accumulate, float* scratch);
+                          float* dw, float* db, int M, int C, bool accumulate, float* scratch,
+                          bool acc_params = false);
 
+// dz = (softmax - onehot) * dscale (* *scale_dev when given: a device loss scale)
 void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* targets,
-                 float* row_loss, float* mean_loss, int M, int V, int ld, float dscale);
+                 float* row_loss, float* mean_loss, int M, int V, int ld, float dscale,
+                 const float* scale_dev = nullptr);
 
 size_t colsum_scratch_floats(int M, int N);
 void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, float* out,
-                   float* scratch);
+                   float* scratch, bool acc = false);
 
 void launch_adamw(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g,
                   float* m, float* v, size_t n, float lr, float b1, float b2, float eps,
                   float wd, int step);
 void launch_cast_bf16(const Launch& L, const float* src, __nv_bfloat16* dst, size_t n);
+// global gradient statistics: stats[0] = ||g / scale||_2, stats[1] = 1 if not finite
+size_t grad_stats_scratch_doubles(const Launch& L);
+void launch_grad_stats(const Launch& L, const float* g, size_t n, const float* scale_dev, float* stats,
+                       double* scratch);
+// AdamW whose gradient is g / scale * clip, skipped when stats[1] != 0; t = *step + 1
+void launch_adamw_ex(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g, float* m, float* v,
+                     size_t n, float lr, float b1, float b2, float eps, float wd, int* step, const float* stats,
+                     float max_norm, const float* scale_dev);
+void launch_loss_scale_update(const Launch& L, float* scale, int* clean, const float* stats, int window,
+                              float growth, float backoff);
 
 size_t attention_bwd_scratch_floats(int B, int T, int H);
 void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, float* lse,
@@ -117,14 +130,14 @@ bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const voi
                         float* mean, float* rstd, int M, int C);
 bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
                         const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
-                        int C, bool accumulate, float* scratch);
+                        int C, bool accumulate, float* scratch, bool acc_params = false);
 size_t ln_bwd_bf16_scratch_floats(int C);
 bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
-                      int V, int ld, float dscale);
+                      int V, int ld, float dscale, const float* scale_dev = nullptr);
 bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part);
 // out[c] = sum of the G rows of part[G][ncols] (fixed order); columns >= split go to out_b
 void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int split, float* out_a,
-                     float* out_b);
+                     float* out_b, bool acc = false);
 size_t embed_chunk_scratch_floats(int M, int C);
 bool launch_embed_chunks(const Launch& L, bool bf16, const void* dx, const int32_t* keys,
                          const int32_t* vals, int M, int C, int V, float* dwte, float* scratch);

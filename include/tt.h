@@ -177,6 +177,61 @@ tt_status tt_ctx_loss_device(const tt_ctx* ctx, const float** mean_loss,
  * may be host or device memory; synchronizes the context's stream. */
 tt_status tt_ctx_copy_row_losses(tt_ctx* ctx, float* dst, size_t n);
 
+/* ---------------------------------------------------------------- step variants
+ * Gradient accumulation, global gradient-norm clipping and dynamic loss
+ * scaling, with every decision taken on the device (no host round trip):
+ *  - accumulation: gradients add up (+=) over micro-batches as they do over a
+ *    tensor's consumers (tinytorch 三.3; NumPy framework page 3.2);
+ *  - clipping: the global norm clip of the dl-scratch page (3.2, clip_grad_norm_
+ *    applied to the separate gradient storage), with the usual coefficient
+ *    min(1, max_norm / (norm + 1e-6));
+ *  - loss scaling: the dl-scratch page's 3.4 (the loss is multiplied by a scale
+ *    before the backward; an Inf/NaN gradient halves the scale and the update
+ *    is skipped; after a run of clean steps the scale grows by a small factor).
+ * A typical loop: tt_ctx_reset, tt_gpt2_step_ex (first micro-batch without
+ * TT_STEP_ACCUMULATE, the rest with it), tt_grad_stats, tt_adamw_ex,
+ * tt_loss_scale_update. */
+
+/* tt_gpt2_step_ex flag: add this step's parameter gradients to grads instead
+ * of overwriting them. */
+#define TT_STEP_ACCUMULATE 1
+
+/* tt_gpt2_step with options.  flags: 0 or TT_STEP_ACCUMULATE (other bits:
+ * TT_ERR_ARG).  loss_scale: device float or NULL; when given, the gradients
+ * are those of (mean loss) * (*loss_scale), read on the device when the step
+ * runs (the reported loss is unscaled). */
+tt_status tt_gpt2_step_ex(tt_ctx* ctx, const void* params, float* grads, const int32_t* tokens,
+                          const int32_t* targets, int B, int T, int flags, const float* loss_scale,
+                          float* loss);
+
+/* Global gradient statistics, on the device: stats[0] = sqrt(sum_i (g_i /
+ * s)^2) and stats[1] = 1 if that sum is not finite (an Inf or NaN gradient, or
+ * one whose square overflows), else 0; s = *loss_scale when loss_scale is not
+ * NULL, else 1.  grads: device fp32 [n]; stats: device float[2].  The sum is
+ * taken in a fixed order (per-thread float sums, per-block partials added in
+ * double).  Uses a few KB of the arena for the partial sums. */
+tt_status tt_grad_stats(tt_ctx* ctx, const float* grads, size_t n, const float* loss_scale, float* stats);
+
+/* AdamW (as tt_adamw) on the gradient g * k, k = (1 / *loss_scale when
+ * loss_scale is not NULL) * (min(1, max_norm / (stats[0] + 1e-6)) when
+ * max_norm > 0).  step: device int, the number of updates taken so far; the
+ * update uses t = *step + 1 and then advances *step.  With stats given and
+ * stats[1] != 0 the whole update is skipped: master, params_lowp, m, v and
+ * *step keep their values.  max_norm > 0 needs stats (else TT_ERR_ARG). */
+tt_status tt_adamw_ex(tt_ctx* ctx, float* master, void* params_lowp, const float* grads, float* m,
+                      float* v, size_t n, float lr, float beta1, float beta2, float eps,
+                      float weight_decay, int* step, const float* stats, float max_norm,
+                      const float* loss_scale);
+
+/* Dynamic loss scale, on the device (loss_scale: device float; clean_steps:
+ * device int): after an overflow step (stats[1] != 0) *loss_scale *= backoff
+ * and *clean_steps = 0; after a clean step ++*clean_steps, and when it
+ * reaches window, *loss_scale *= growth and *clean_steps = 0.  The dl-scratch
+ * page's values are backoff 0.5, window 1000, growth 1.001.  TT_ERR_ARG for
+ * window < 1, growth < 1 or backoff outside (0, 1). */
+tt_status tt_loss_scale_update(tt_ctx* ctx, float* loss_scale, int* clean_steps, const float* stats, int window,
+                               float growth, float backoff);
+
 /* One AdamW step over n flat elements (tinytorch 三.7 Adam with bias
  * correction; Forge: weight decay decoupled from the gradient):
  *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
