@@ -12,22 +12,34 @@ namespace {
 constexpr int GS_THREADS = 256;
 
 // part[b] = sum of (g_i / s)^2 over the elements block b takes: float4 i of
-// the n/4 goes to block i mod gridDim in grid-stride order, the tail to block 0.
-// Per-thread float sums, combined within the block in a fixed order.
+// the n/4 goes to the thread i mod (gridDim * blockDim) in grid-stride order,
+// four strides per round with four loads in flight (one partial sum each,
+// added in order at the end), the tail to block 0.  Per-thread float sums,
+// combined within the block in a fixed order.
 __global__ void __launch_bounds__(GS_THREADS)
 k_grad_sq_part(const float* __restrict__ g, size_t n, const float* __restrict__ scale_dev, double* __restrict__ part) {
     __shared__ float s_w[GS_THREADS / 32];
     const float inv = scale_dev ? 1.0f / *scale_dev : 1.0f;
     const size_t n4 = n / 4, stride = (size_t)gridDim.x * blockDim.x;
-    float s = 0.0f;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-        const float4 v = reinterpret_cast<const float4*>(g)[i];
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    auto add = [&](float& s, const float4 v) {
         const float a = v.x * inv, b = v.y * inv, c = v.z * inv, d = v.w * inv;
         s = fmaf(a, a, s);
         s = fmaf(b, b, s);
         s = fmaf(c, c, s);
         s = fmaf(d, d, s);
+    };
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) v[u] = __ldcs(g4 + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; u++) add(acc[u], v[u]);
     }
+    for (int u = 0; i < n4; i += stride, u++) add(acc[u & 3], __ldcs(g4 + i));
+    float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     if (blockIdx.x == 0)
         for (size_t i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) {
             const float a = g[i] * inv;

@@ -216,6 +216,8 @@ OP_SHAPES = {
     "eval": "forward-only evaluation loss (tt_gpt2_eval), 124M, B=32 T=1024, bf16",
     "generate": "greedy generation with the key/value cache (tt_gpt2_generate), 124M bf16, B=8, "
                 "64-token prompts, 448 new tokens",
+    "update": "the update side over 124,439,808 parameters: plain AdamW, and the variant path "
+              "(global gradient statistics, AdamW with clipping, unscaling and overflow skip, loss-scale update)",
     "fruit": "the generic tensor graph: the tinytorch page's classifier (3 -> 32 GELU -> 3, softmax, "
              "cross entropy) trained by SGD on 64 samples, one step = forward, zero_grad, backward, SGD",
 }
@@ -378,6 +380,64 @@ def run_inference(args):
     ms = e0.elapsed_time(e1) / args.reps
     print(json.dumps({"op": args.op, "what": OP_SHAPES[args.op], "ms_per_call": ms,
                       "tokens_per_s": tokens_per_call / (ms * 1e-3)}), flush=True)
+    ctx.close()
+    return 0
+
+
+def run_update(args):
+    """Times tt_adamw against the device-decided variant path (tt_grad_stats +
+    tt_adamw_ex + tt_loss_scale_update) at the 124M parameter count; every
+    buffer is larger than L2.  Bytes are the algorithmic ones: AdamW reads
+    p, g, m, v and writes p, m, v and the bf16 copy (30 B per parameter); the
+    statistics read g once more (4 B)."""
+    import torch
+
+    from autograd_arena_allocated_gb300 import api, synth
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    dev = "cuda"
+    n = 124_439_808
+    ctx = api.Context(64 << 20)
+    p_ = torch.from_numpy(synth.normals(1, 0, n).astype("float32")).to(dev)
+    g_ = torch.from_numpy((synth.normals(2, 0, n) * 1e-2).astype("float32")).to(dev) * 1024.0
+    m_, v_ = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    low = torch.empty(n, device=dev, dtype=torch.bfloat16)
+    step = torch.zeros(1, device=dev, dtype=torch.int32)
+    scale = torch.tensor([1024.0], device=dev)
+    clean = torch.zeros(1, device=dev, dtype=torch.int32)
+    stats = torch.zeros(2, device=dev)
+
+    def plain():
+        ctx.adamw(p_, low, g_, m_, v_, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+
+    def variant():
+        ctx.grad_stats(g_, stats, loss_scale=scale)
+        ctx.adamw_ex(p_, low, g_, m_, v_, 1e-3, 0.9, 0.95, 1e-8, 0.1, step, stats=stats, max_norm=1.0,
+                     loss_scale=scale)
+        ctx.loss_scale_update(scale, clean, stats, window=10 ** 9)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.reps
+
+    peak = load_peaks()
+    out = {"op": "update", "what": OP_SHAPES["update"], "n": n, "peak_hbm_gbs": peak["hbm_gbs"],
+           "peak_source": peak["source"]}
+    for name, fn, bpp in [("adamw", plain, 30), ("stats+adamw_ex+scale", variant, 34)]:
+        ms = timed(fn)
+        gbs = bpp * n / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "gbps": gbs, "frac_of_peak": gbs / peak["hbm_gbs"]}
+    print(json.dumps(out), flush=True)
     ctx.close()
     return 0
 
@@ -566,6 +626,8 @@ def main():
             return run_inference(args)
         if args.op == "fruit":
             return run_fruit(args)
+        if args.op == "update":
+            return run_update(args)
         return run_gemm_shapes(args) if args.op == "gemm_shapes" else run_op(args)
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     world, rank, local = dist_setup()
