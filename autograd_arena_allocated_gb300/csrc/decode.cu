@@ -14,15 +14,42 @@
 //
 // The newest position lives in device memory (pos_dev) and the step's last
 // linear layer advances it, so one captured decode step replays for every
-// position.  The cache holds, per layer, [B, maxT, 2C]: the key row then the
+// position.  Within a step the kernels use programmatic dependent launch:
+// each lets the next one start at its own entry, and each waits for its
+// predecessor's results (griddepcontrol.wait) before it reads them; the
+// skinny GEMM issues its weight loads, which nothing in the step writes,
+// before that wait.  The cache holds, per layer, [B, maxT, 2C]: the key row then the
 // value row of each position, in the storage type of the step.  Every
 // reduction is in a fixed order, so decoding is deterministic.
 #include "tt_internal.h"
 
 #include <algorithm>
+#include <utility>
 
 namespace tt {
 namespace {
+
+// Programmatic dependent launch.  Both are no-ops in a kernel launched
+// without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+void launch_k(const Launch& L, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute at[1];
+    if (L.pdl) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+    }
+    cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 template <typename T> __device__ __forceinline__ float ld_f(const T* p);
 template <> __device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
@@ -79,6 +106,8 @@ template <typename T>
 __global__ void k_embed_at(const T* __restrict__ wte, const T* __restrict__ wpe, const int32_t* __restrict__ tok,
                            int ld_tok, const int* __restrict__ pos_dev, T* __restrict__ x, int B, int C, int V,
                            int* flags) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x, pos = *pos_dev;
     int id = tok[(long long)b * ld_tok + pos];
     if (id < 0 || id >= V) {
@@ -112,6 +141,8 @@ k_decode_attn(const T* __restrict__ qkv, T* __restrict__ cache, T* __restrict__ 
     __shared__ float s_acc[32][DA_DMAX];
     __shared__ float s_red[DA_THREADS / 32];
     __shared__ int s_last;
+    pdl_trigger();
+    pdl_wait();
     const int bh = blockIdx.x / S, s = blockIdx.x % S;
     const int b = bh / H, h = bh % H;
     const int D = C / H;
@@ -262,6 +293,8 @@ __global__ void __launch_bounds__(256)
 k_pick(const unsigned long long* __restrict__ keys, int nct, int32_t* __restrict__ tok, int ld_tok,
        const int* __restrict__ pos_dev) {
     __shared__ unsigned long long s_k[8];
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x;
     unsigned long long best = 0;
     for (int i = threadIdx.x; i < nct; i += 256) best = max(best, keys[(long long)b * nct + i]);
@@ -285,6 +318,8 @@ k_argmax(const T* __restrict__ z, long long row_stride, int V, int32_t* __restri
          const int* __restrict__ col_dev) {
     __shared__ float s_v[AM_THREADS / 32];
     __shared__ int s_i[AM_THREADS / 32];
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x;
     const T* zr = z + (long long)b * row_stride;
     float best = -INFINITY;
@@ -322,10 +357,36 @@ k_argmax(const T* __restrict__ z, long long row_stride, int V, int32_t* __restri
 // and 2s+1 where the instruction expects the pairs at k = 2q and 2q+8.  A CTA
 // owns 16 output columns; its 8 warps split K in chunks of 32 (chunk c to warp
 // c mod 8) and the partial sums meet in shared memory in warp order.
+//
+// With ln_w/ln_b the rows of A are first put through LayerNorm (the
+// arithmetic of the step's LayerNorm kernel, rounded to bf16) into shared
+// memory by the CTA itself, after its first weight loads are in flight: the
+// decode step then needs no separate LayerNorm launch.
 constexpr int SK_MMAX = 16;
 constexpr int SKM_WARPS = 8;
 constexpr int SKM_TN = 16;
 constexpr int SKM_UNR = 4;
+constexpr int SKM_LN_KMAX = 1024;  // LayerNorm rows live in registers: 4 x 8 values a lane
+
+__device__ __forceinline__ float sk_wsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint4 sk_pack8(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// shared-memory row stride of the normalised rows, in 16-byte units: K + 32
+// elements, so that rows r and r + 1 start 64 bytes apart modulo 128
+__host__ __device__ __forceinline__ int sk_ln_stride(int K) { return (K + 32) / 8; }
 
 __device__ __forceinline__ void mma_16816(float* d, const uint32_t a0, const uint32_t a1, const uint32_t a2,
                                           const uint32_t a3, const uint32_t b0, const uint32_t b1) {
@@ -341,8 +402,11 @@ __global__ void __launch_bounds__(SKM_WARPS * 32)
 k_gemm_skinny_mma(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ W,
                   const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
                   __nv_bfloat16* __restrict__ D, __nv_bfloat16* __restrict__ pre, int M, int N, int K, int ldd,
-                  int n_store, int gelu, unsigned long long* __restrict__ pick, int* __restrict__ advance) {
+                  int n_store, int gelu, unsigned long long* __restrict__ pick, int* __restrict__ advance,
+                  const __nv_bfloat16* __restrict__ ln_w, const __nv_bfloat16* __restrict__ ln_b) {
     __shared__ float s_part[SKM_WARPS][MT * 128];  // [warp][t*128 + row*16 + col]
+    extern __shared__ uint4 s_xn[];                // normalised rows [MT*8][sk_ln_stride(K)] (with ln_w)
+    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
     const int n0 = blockIdx.x * SKM_TN;
@@ -361,16 +425,89 @@ k_gemm_skinny_mma(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
 #pragma unroll
     for (int t = 0; t < MT; t++) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int c0 = warp; c0 < nch; c0 += SKM_WARPS * SKM_UNR) {
-        uint4 va[SKM_UNR], vb[SKM_UNR], vx[SKM_UNR][MT];
+    uint4 va[SKM_UNR], vb[SKM_UNR];
+    auto load_w = [&](int c0) {
 #pragma unroll
         for (int u = 0; u < SKM_UNR; u++) {
             const int c = c0 + u * SKM_WARPS;  // chunk: 32 k = 4 uint4 per row
             const bool in = c < nch;
             va[u] = (in && ra) ? __ldcs(wa + c * 4) : zero;
             vb[u] = (in && rb) ? __ldcs(wb + c * 4) : zero;
+        }
+    };
+    load_w(warp);
+    pdl_wait();  // A, the residual and the outputs belong to the kernels before
+    const int xs = sk_ln_stride(K);
+    if (ln_w) {
+        // warp w normalises rows w, w + 8 (rows >= M are zero)
+        const int nvec = K >> 3;
+        for (int r = warp; r < MT * 8; r += SKM_WARPS) {
+            uint4* dst = s_xn + r * xs;
+            if (r >= M) {
+                for (int vi = lane; vi < nvec; vi += 32) dst[vi] = zero;
+                continue;
+            }
+            const uint4* xr = reinterpret_cast<const uint4*>(A + (long long)r * K);
+            float v[4][8];
+            float s = 0.0f;
 #pragma unroll
-            for (int t = 0; t < MT; t++) vx[u][t] = (in && xv[t]) ? __ldg(xa[t] + c * 4) : zero;
+            for (int i = 0; i < 4; i++) {
+                const int vi = lane + 32 * i;
+                if (vi < nvec) {
+                    const uint4 u4 = xr[vi];
+                    const uint32_t wv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        v[i][2 * e] = __uint_as_float(wv[e] << 16);
+                        v[i][2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; e++) s += v[i][e];
+                }
+            }
+            const float mu = sk_wsum(s) / K;
+            float q2 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                if (lane + 32 * i < nvec)
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const float d = v[i][e] - mu;
+                        q2 += d * d;
+                    }
+            const float rs = rsqrtf(sk_wsum(q2) / K + 1e-5f);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int vi = lane + 32 * i;
+                if (vi < nvec) {
+                    const uint4 w4 = reinterpret_cast<const uint4*>(ln_w)[vi];
+                    const uint4 b4 = reinterpret_cast<const uint4*>(ln_b)[vi];
+                    const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        o[2 * e] = (v[i][2 * e] - mu) * rs * __uint_as_float(ww[e] << 16) +
+                                   __uint_as_float(bw[e] << 16);
+                        o[2 * e + 1] = (v[i][2 * e + 1] - mu) * rs * __uint_as_float(ww[e] & 0xFFFF0000u) +
+                                       __uint_as_float(bw[e] & 0xFFFF0000u);
+                    }
+                    dst[vi] = sk_pack8(o);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    for (int c0 = warp; c0 < nch; c0 += SKM_WARPS * SKM_UNR) {
+        uint4 vx[SKM_UNR][MT];
+#pragma unroll
+        for (int u = 0; u < SKM_UNR; u++) {
+            const int c = c0 + u * SKM_WARPS;
+            const bool in = c < nch;
+#pragma unroll
+            for (int t = 0; t < MT; t++) {
+                if (ln_w) vx[u][t] = in ? s_xn[(t * 8 + g) * xs + c * 4 + q] : zero;
+                else vx[u][t] = (in && xv[t]) ? __ldg(xa[t] + c * 4) : zero;
+            }
         }
 #pragma unroll
         for (int u = 0; u < SKM_UNR; u++) {
@@ -380,6 +517,7 @@ k_gemm_skinny_mma(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
                 mma_16816(acc[t], va[u].z, vb[u].z, va[u].w, vb[u].w, vx[u][t].z, vx[u][t].w);
             }
         }
+        if (c0 + SKM_WARPS * SKM_UNR < nch) load_w(c0 + SKM_WARPS * SKM_UNR);
     }
     // accumulator (i, j) of the 16 x 8 tile: column n0 + i, row t*8 + j, with
     // i = g (+8 for entries 2, 3) and j = 2q (+1 for entries 1, 3)
@@ -428,6 +566,8 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
 k_gemm_skinny(const T* __restrict__ A, const T* __restrict__ W, const T* __restrict__ bias,
               const T* __restrict__ res, T* __restrict__ D, T* __restrict__ pre, int M, int N, int K, int ldd,
               int n_store, int gelu, int* __restrict__ advance) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     if (advance && blockIdx.x == 0 && threadIdx.x == 0) *advance += 1;
     for (int n = blockIdx.x * SK_WARPS + (threadIdx.x >> 5); n < N; n += gridDim.x * SK_WARPS) {
@@ -512,12 +652,11 @@ void launch_embed_at(const Launch& L, bool bf16, const void* wte, const void* wp
     if (L.dry) return;
     L.count();
     if (bf16)
-        k_embed_at<__nv_bfloat16><<<B, 256, 0, L.stream>>>((const __nv_bfloat16*)wte, (const __nv_bfloat16*)wpe,
-                                                           tok, ld_tok, pos_dev, (__nv_bfloat16*)x, B, C, V,
-                                                           L.flags);
+        launch_k(L, k_embed_at<__nv_bfloat16>, B, 256, 0, (const __nv_bfloat16*)wte, (const __nv_bfloat16*)wpe, tok,
+                 ld_tok, pos_dev, (__nv_bfloat16*)x, B, C, V, L.flags);
     else
-        k_embed_at<float><<<B, 256, 0, L.stream>>>((const float*)wte, (const float*)wpe, tok, ld_tok, pos_dev,
-                                                   (float*)x, B, C, V, L.flags);
+        launch_k(L, k_embed_at<float>, B, 256, 0, (const float*)wte, (const float*)wpe, tok, ld_tok, pos_dev,
+                 (float*)x, B, C, V, L.flags);
 }
 
 int decode_attn_splits(int max_keys) { return (max_keys + DA_KEYS - 1) / DA_KEYS; }
@@ -537,52 +676,65 @@ bool launch_decode_attn(const Launch& L, bool bf16, const void* qkv, void* cache
     const float scale = 1.0f / sqrtf((float)(C / H));
     const unsigned grid = (unsigned)(B * H * S);
     if (bf16)
-        k_decode_attn<__nv_bfloat16><<<grid, DA_THREADS, 0, L.stream>>>(
-            (const __nv_bfloat16*)qkv, (__nv_bfloat16*)cache, (__nv_bfloat16*)y, H, C, pos_dev, maxT, S, scale, part,
-            counters);
+        launch_k(L, k_decode_attn<__nv_bfloat16>, grid, DA_THREADS, 0, (const __nv_bfloat16*)qkv,
+                 (__nv_bfloat16*)cache, (__nv_bfloat16*)y, H, C, pos_dev, maxT, S, scale, part, counters);
     else
-        k_decode_attn<float><<<grid, DA_THREADS, 0, L.stream>>>((const float*)qkv, (float*)cache, (float*)y, H, C,
-                                                                pos_dev, maxT, S, scale, part, counters);
+        launch_k(L, k_decode_attn<float>, grid, DA_THREADS, 0, (const float*)qkv, (float*)cache, (float*)y, H, C,
+                 pos_dev, maxT, S, scale, part, counters);
     return true;
 }
 
+static bool ln_ok(const void* ln_w, const void* ln_b, int K) {
+    if (!ln_w) return true;
+    return ln_b && K <= SKM_LN_KMAX && !((uintptr_t)ln_w & 15) && !((uintptr_t)ln_b & 15);
+}
+
+static size_t ln_smem(const void* ln_w, int M, int K) {
+    return ln_w ? (size_t)(M <= 8 ? 8 : 16) * sk_ln_stride(K) * 16 : 0;
+}
+
 bool launch_gemm_skinny(const Launch& L, bool bf16, const void* A, const void* W, const void* bias, const void* res,
-                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu, int* advance) {
+                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu, int* advance,
+                        const void* ln_w, const void* ln_b) {
     const size_t es = bf16 ? 2 : 4;
     if (M < 1 || M > SK_MMAX || K % 32 || ((uintptr_t)A & 15) || ((uintptr_t)W & 15) || ((K * es) & 15)) return false;
+    if (ln_w && (!bf16 || !ln_ok(ln_w, ln_b, K))) return false;
     if (L.dry) return true;
     L.count();
     if (bf16) {
         const long long grid = (N + SKM_TN - 1) / SKM_TN;
         if (grid > 0x7fffffff) return false;
-#define SKM(MT_)                                                                                          \
-    k_gemm_skinny_mma<MT_><<<(unsigned)grid, SKM_WARPS * 32, 0, L.stream>>>(                              \
-        (const __nv_bfloat16*)A, (const __nv_bfloat16*)W, (const __nv_bfloat16*)bias,                     \
-        (const __nv_bfloat16*)res, (__nv_bfloat16*)D, (__nv_bfloat16*)pre, M, N, K, ldd, n_store, gelu ? 1 : 0, \
-        nullptr, advance)
+        const size_t smem = ln_smem(ln_w, M, K);
+#define SKM(MT_)                                                                                               \
+    launch_k(L, k_gemm_skinny_mma<MT_>, (unsigned)grid, SKM_WARPS * 32, smem, (const __nv_bfloat16*)A,          \
+             (const __nv_bfloat16*)W, (const __nv_bfloat16*)bias, (const __nv_bfloat16*)res, (__nv_bfloat16*)D, \
+             (__nv_bfloat16*)pre, M, N, K, ldd, n_store, gelu ? 1 : 0, (unsigned long long*)nullptr, advance,  \
+             (const __nv_bfloat16*)ln_w, (const __nv_bfloat16*)ln_b)
         if (M <= 8) SKM(1); else SKM(2);
 #undef SKM
         return true;
     }
     const unsigned grid = (unsigned)std::min<long long>((N + SK_WARPS - 1) / SK_WARPS, 65535);
-    k_gemm_skinny<float><<<grid, SK_WARPS * 32, 0, L.stream>>>((const float*)A, (const float*)W, (const float*)bias,
-                                                               (const float*)res, (float*)D, (float*)pre, M, N, K,
-                                                               ldd, n_store, gelu ? 1 : 0, advance);
+    launch_k(L, k_gemm_skinny<float>, grid, SK_WARPS * 32, 0, (const float*)A, (const float*)W, (const float*)bias,
+             (const float*)res, (float*)D, (float*)pre, M, N, K, ldd, n_store, gelu ? 1 : 0, advance);
     return true;
 }
 
 int skinny_pick_ctas(int N) { return (N + SKM_TN - 1) / SKM_TN; }
 
 bool launch_gemm_skinny_pick(const Launch& L, const void* A, const void* W, int M, int N, int K,
-                             unsigned long long* keys, int* advance) {
+                             unsigned long long* keys, int* advance, const void* ln_w, const void* ln_b) {
     if (M < 1 || M > SK_MMAX || K % 32 || ((uintptr_t)A & 15) || ((uintptr_t)W & 15)) return false;
+    if (!ln_ok(ln_w, ln_b, K)) return false;
     if (L.dry) return true;
     L.count();
     const unsigned grid = (unsigned)skinny_pick_ctas(N);
+    const size_t smem = ln_smem(ln_w, M, K);
 #define SKP(MT_)                                                                                                \
-    k_gemm_skinny_mma<MT_><<<grid, SKM_WARPS * 32, 0, L.stream>>>((const __nv_bfloat16*)A,                     \
-                                                                  (const __nv_bfloat16*)W, nullptr, nullptr,   \
-                                                                  nullptr, nullptr, M, N, K, 0, N, 0, keys, advance)
+    launch_k(L, k_gemm_skinny_mma<MT_>, grid, SKM_WARPS * 32, smem, (const __nv_bfloat16*)A,                     \
+             (const __nv_bfloat16*)W, (const __nv_bfloat16*)nullptr, (const __nv_bfloat16*)nullptr,              \
+             (__nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr, M, N, K, 0, N, 0, keys, advance,                  \
+             (const __nv_bfloat16*)ln_w, (const __nv_bfloat16*)ln_b)
     if (M <= 8) SKP(1); else SKP(2);
 #undef SKP
     return true;
@@ -592,7 +744,7 @@ void launch_pick(const Launch& L, const unsigned long long* keys, int nct, int r
                  const int* pos_dev) {
     if (L.dry) return;
     L.count();
-    k_pick<<<rows, 256, 0, L.stream>>>(keys, nct, tok, ld_tok, pos_dev);
+    launch_k(L, k_pick, rows, 256, 0, keys, nct, tok, ld_tok, pos_dev);
 }
 
 void launch_argmax(const Launch& L, bool bf16, const void* z, long long row_stride, int rows, int V, int32_t* out,
@@ -600,11 +752,10 @@ void launch_argmax(const Launch& L, bool bf16, const void* z, long long row_stri
     if (L.dry) return;
     L.count();
     if (bf16)
-        k_argmax<__nv_bfloat16><<<rows, AM_THREADS, 0, L.stream>>>((const __nv_bfloat16*)z, row_stride, V, out,
-                                                                   ld_out, col, col_dev);
+        launch_k(L, k_argmax<__nv_bfloat16>, rows, AM_THREADS, 0, (const __nv_bfloat16*)z, row_stride, V, out, ld_out,
+                 col, col_dev);
     else
-        k_argmax<float><<<rows, AM_THREADS, 0, L.stream>>>((const float*)z, row_stride, V, out, ld_out, col,
-                                                           col_dev);
+        launch_k(L, k_argmax<float>, rows, AM_THREADS, 0, (const float*)z, row_stride, V, out, ld_out, col, col_dev);
 }
 
 }  // namespace tt

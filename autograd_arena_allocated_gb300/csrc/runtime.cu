@@ -647,7 +647,8 @@ static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* pro
     const size_t mark = c->off;
     auto step = [&]() -> tt_status {
         c->off = mark;
-        const Launch S = launch_of(c);
+        Launch S = launch_of(c);
+        S.pdl = true;
         auto linear = [&](const void* in, int K, const void* W, const void* bias, int N, void* out, const void* res,
                           void* pre) -> bool {
             // a few rows: the weight-streaming skinny GEMM
@@ -665,29 +666,37 @@ static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* pro
             ga.aux = pre;
             return run_gemm(c, ga, PK_GEMM_FWD);
         };
+        // LayerNorm then a linear layer: one launch when the skinny GEMM takes the LayerNorm
+        auto ln_linear = [&](const void* xin, const void* lw, const void* lb, const void* W, const void* bias, int N,
+                             void* out, void* pre) -> bool {
+            if (bf && launch_gemm_skinny(S, bf, xin, W, bias, nullptr, out, pre, B, N, C, N, N, pre != nullptr,
+                                         nullptr, lw, lb))
+                return true;
+            launch_layernorm_fwd(S, bf, xin, lw, lb, h, mean, rstd, B, C);
+            return linear(h, C, W, bias, N, out, nullptr, pre);
+        };
         void* x = xa;
         void* x2 = xb;
         launch_embed_at(S, bf, P(o.wte), P(o.wpe), tokbuf, Ttot, pos_dev, x, B, C, m.V);
         for (int l = 0; l < m.L; l++) {
             const size_t base = o.layers + (size_t)l * o.per_layer;
             auto PL = [&](int i) { return P(base + o.sub[i]); };
-            launch_layernorm_fwd(S, bf, x, PL(0), PL(1), h, mean, rstd, B, C);
-            if (!linear(h, C, PL(2), PL(3), 3 * C, qkv, nullptr, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            if (!ln_linear(x, PL(0), PL(1), PL(2), PL(3), 3 * C, qkv, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
             if (!launch_decode_attn(S, bf, qkv, cache + layer_cache * l, att, B, m.H, C, pos_dev, max_keys, m.maxT,
                                     part, counters))
                 return fail(c, TT_ERR_ARG, "generate: attention shape not supported");
             if (!linear(att, C, PL(4), PL(5), C, x1, x, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
-            launch_layernorm_fwd(S, bf, x1, PL(6), PL(7), h, mean, rstd, B, C);
-            if (!linear(h, C, PL(8), PL(9), 4 * C, g, nullptr, u)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
+            if (!ln_linear(x1, PL(6), PL(7), PL(8), PL(9), 4 * C, g, u)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
             if (!linear(g, 4 * C, PL(10), PL(11), C, x2, x1, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
             std::swap(x, x2);
         }
-        launch_layernorm_fwd(S, bf, x, P(o.lnfw), P(o.lnfb), h, mean, rstd, B, C);
-        // tied LM head over the V real rows of wte, which also advances the position
-        if (bf && launch_gemm_skinny_pick(S, h, P(o.wte), B, m.V, C, keys, pos_dev)) {
+        // final LayerNorm and the tied LM head over the V real rows of wte, which
+        // also advances the position
+        if (bf && launch_gemm_skinny_pick(S, x, P(o.wte), B, m.V, C, keys, pos_dev, P(o.lnfw), P(o.lnfb))) {
             launch_pick(S, keys, nct, B, tokbuf, Ttot, pos_dev);
             return TT_OK;
         }
+        launch_layernorm_fwd(S, bf, x, P(o.lnfw), P(o.lnfb), h, mean, rstd, B, C);
         if (!launch_gemm_skinny(S, bf, h, P(o.wte), nullptr, nullptr, zl, nullptr, B, m.V, C, Vp, m.V, false,
                                 pos_dev)) {
             GemmArgs ga;

@@ -35,6 +35,7 @@ struct Launch {
     bool dry = false;      // plan only: allocate, launch nothing
     int gemm_backend = 0;  // 0 auto, 1 SIMT only
     int num_sms = 148;
+    bool pdl = false;      // decode kernels: programmatic dependent launch
     void count() const { if (launches) ++*launches; }
 };
 
@@ -169,14 +170,17 @@ bool launch_decode_attn(const Launch& L, bool bf16, const void* qkv, void* cache
 // greedy choice over stored logits into out[b][col_dev ? *col_dev : col]
 void launch_argmax(const Launch& L, bool bf16, const void* z, long long row_stride, int rows, int V, int32_t* out,
                    int ld_out, int col, const int* col_dev);
-// decode-step linear layers (M <= 16 rows); false = shape not taken
+// decode-step linear layers (M <= 16 rows); false = shape not taken.  With
+// ln_w/ln_b (bf16 only, K <= 1024) the rows of A go through LayerNorm first.
 bool launch_gemm_skinny(const Launch& L, bool bf16, const void* A, const void* W, const void* bias, const void* res,
-                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu, int* advance);
+                        void* D, void* pre, int M, int N, int K, int ldd, int n_store, bool gelu, int* advance,
+                        const void* ln_w = nullptr, const void* ln_b = nullptr);
 // bf16 LM head with the greedy choice folded in: keys[m * skinny_pick_ctas(N) + cta]
 // holds each CTA's largest (logit, -index) key of row m; launch_pick reduces them
 int skinny_pick_ctas(int N);
 bool launch_gemm_skinny_pick(const Launch& L, const void* A, const void* W, int M, int N, int K,
-                             unsigned long long* keys, int* advance);
+                             unsigned long long* keys, int* advance, const void* ln_w = nullptr,
+                             const void* ln_b = nullptr);
 void launch_pick(const Launch& L, const unsigned long long* keys, int nct, int rows, int32_t* tok, int ld_tok,
                  const int* pos_dev);
 
