@@ -19,6 +19,17 @@
 //   DW  dW = dy^T x : A MN-major, B MN-major, split over tokens (K) with a
 //                     fixed-order reduction when the output has few tiles.
 //
+// Pair form (PAIR): the two CTAs of a cluster take the M tiles 2i and 2i + 1
+// of the same N tile as one 256 x BN tile of tcgen05.mma.cta_group::2, issued
+// by the even CTA (the leader).  Each CTA's shared memory holds its own A
+// tile and one half of the B tile, so per SM the operand bytes written by TMA
+// and read by the tensor cores fall by a third at BN = 256: a single-CTA
+// 128 x 256 tile needs more shared-memory bandwidth (A and B read by the MMA
+// plus the TMA writes) than an SM has.  Both CTAs' loads complete on the
+// leader's full barrier; the leader's commits arrive on both CTAs' empty and
+// accumulator-full barriers; both CTAs' epilogues release the leader's
+// accumulator.
+//
 // Every mbarrier wait is bounded (about two seconds of clock cycles); on
 // expiry the kernel raises FLAG_TIMEOUT, stops all roles, lets in-flight TMA
 // copies land, frees its tensor memory and returns.
@@ -27,6 +38,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -41,11 +53,11 @@ constexpr int EPI_WARPS = 8;
 constexpr int MN_BOX = 64;                  // MN extent of one MN-major TMA box
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB: 64 k-rows x 128 bytes
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct Cfg {
-    static constexpr int STAGES = (BN >= 192) ? 4 : 6;
+    static constexpr int STAGES = (PAIR || BN < 192) ? 6 : 4;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;  // this CTA's part of the B tile
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // two accumulators, power of two
     static constexpr int BAR_BYTES = 1024;                 // barriers, padded to keep staging aligned
@@ -68,6 +80,7 @@ struct Params {
     int* flags;
     int tma_store;  // bf16 outputs leave through shared memory and TMA stores
     int ext_tma;    // the extra epilogue operand (GELU' input or residual) arrives by TMA loads
+    int cl;         // pair form: CTA pairs take M tiles 2i, 2i + 1 (m_tiles even)
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -189,13 +202,74 @@ __device__ __forceinline__ void store32_f32(float* p, int valid, bool vec, const
 __device__ __forceinline__ int tile_m(const Params& p, int t) { return p.n_fast ? t / p.n_tiles : t % p.m_tiles; }
 __device__ __forceinline__ int tile_n(const Params& p, int t) { return p.n_fast ? t % p.n_tiles : t / p.m_tiles; }
 
+// The units (tile, split) this CTA takes: it = first, first + step, ... < count.
+// In the pair form a unit is a pair of M tiles and the CTA of rank r takes M
+// tile 2 * pair + r.
+struct UnitIter {
+    int first, step, count, rank;
+};
+__device__ __forceinline__ UnitIter unit_iter(const Params& p) {
+    if (p.cl) return {(int)blockIdx.x >> 1, (int)gridDim.x >> 1, p.units >> 1, (int)blockIdx.x & 1};
+    return {(int)blockIdx.x, (int)gridDim.x, p.units, 0};
+}
+// unit it -> tile number (the numbering tile_m / tile_n read) and split
+__device__ __forceinline__ int unit_tile(const Params& p, int it, int rank, int* split) {
+    const int t = it / p.splits;
+    *split = it - t * p.splits;
+    if (!p.cl) return t;
+    const int mpt = p.m_tiles >> 1;
+    const int mp = p.n_fast ? t / p.n_tiles : t % mpt;
+    const int n = p.n_fast ? t % p.n_tiles : t / mpt;
+    const int m = 2 * mp + rank;
+    return p.n_fast ? m * p.n_tiles + n : n * p.m_tiles + m;
+}
+
+// the shared::cluster address of the same variable in the leader CTA (rank 0)
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(0u));
+    return r;
+}
+// TMA load into this CTA's shared memory, completing on an mbarrier of
+// either CTA of the pair (bar: shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrives on the barrier at this offset in both CTAs of the pair once the
+// leader's MMAs issued so far have finished
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ the kernel
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
           const Params p) {
-    using CF = Cfg<BN>;
+    using CF = Cfg<BN, PAIR>;
     constexpr int S = CF::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzle atoms
@@ -220,7 +294,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], EPI_WARPS * 32);
+            // pair: both CTAs' epilogues release the leader's accumulator
+            mbar_init(&tempty[a], (PAIR ? 2 : 1) * EPI_WARPS * 32);
         }
         for (int e = 0; e < 2 * EPI_WARPS; e++) mbar_init(&ebar[e], 1);
         *abort_flag = 0;
@@ -233,15 +308,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_base_holder)),
-                     "r"((uint32_t)CF::TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        if (PAIR) {  // one warp of each CTA of the pair, collectively
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_base_holder)),
+                         "r"((uint32_t)CF::TMEM_COLS));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_base_holder)),
+                         "r"((uint32_t)CF::TMEM_COLS));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_holder;
+    if (PAIR) cluster_sync_all();  // the peer's barriers exist before any copy or commit reaches them
+    const UnitIter U = unit_iter(p);
+    const bool leader = U.rank == 0;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -250,18 +335,42 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-                const int tile = u / p.splits, split = u - tile * p.splits;
+            for (int it = U.first; it < U.count && ok; it += U.step) {
+                int split;
+                const int tile = unit_tile(p, it, U.rank, &split);
                 const int m0 = tile_m(p, tile) * BM;
                 const int n0 = tile_n(p, tile) * BN;
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 1)) { ok = false; break; }
-                    mbar_expect_tx(&full[stage], CF::STAGE_BYTES);
                     const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
                     const uint32_t sb = sa + CF::A_BYTES;
                     const int k0 = kb * BK;
+                    if (PAIR) {
+                        // own A tile and own half of B; both CTAs' bytes land on the leader's barrier
+                        if (leader) mbar_expect_tx(&full[stage], 2 * CF::STAGE_BYTES);
+                        const uint32_t fb = leader_addr(&full[stage]);
+                        if (!A_MN) {
+                            tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BM / MN_BOX; j++)
+                                tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmA, fb, m0 + j * MN_BOX, k0);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d_pair(sb, &tmB, fb, k0, n0 + U.rank * (BN / 2));
+                        } else {
+                            constexpr int HB = BN / MN_BOX / 2;
+#pragma unroll
+                            for (int j = 0; j < HB; j++)
+                                tma_load_2d_pair(sb + j * MN_BOX_BYTES, &tmB, fb, n0 + (U.rank * HB + j) * MN_BOX, k0);
+                        }
+                        ++issued;
+                        if (++stage == S) { stage = 0; phase ^= 1; }
+                        continue;
+                    }
+                    mbar_expect_tx(&full[stage], CF::STAGE_BYTES);
                     if (!A_MN) {
                         tma_load_2d(sa, &tmA, &full[stage], k0, m0);
                     } else {
@@ -280,8 +389,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
-                // let the copies already issued land before the CTA exits
+            if (ok && PAIR) {
+                // the leader's releases of the last stages have arrived before
+                // this CTA's barriers go away
+                for (int i = 0; i < S && ok; i++) {
+                    ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 7);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok && !PAIR) {
+                // let the copies already issued land before the CTA exits (in
+                // the pair form they complete on the leader's barriers, which
+                // this CTA cannot watch; the closing cluster barrier waits)
                 long long back = issued < S ? issued : S;
                 int st = stage;
                 uint32_t ph = phase;
@@ -294,16 +413,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+        if (lane == 0 && leader) {  // pair form: the leader issues for both CTAs
+            constexpr uint32_t IDESC = idesc_bf16(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-                const int tile = u / p.splits, split = u - tile * p.splits;
-                (void)tile;
+            for (int it = U.first; it < U.count && ok; it += U.step) {
+                int split;
+                (void)unit_tile(p, it, U.rank, &split);
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags, 0x400 + 2)) { ok = false; break; }
@@ -321,13 +440,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         else ad = sdesc(sa + k * (UMMA_K / 8) * 1024, MN_BOX_BYTES, 1024);
                         if (!B_MN) bd = sdesc(sb + k * (UMMA_K * 2), 16, 1024);
                         else bd = sdesc(sb + k * (UMMA_K / 8) * 1024, MN_BOX_BYTES, 1024);
-                        umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        else umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);  // slot free once these MMAs finish
+                    if (PAIR) umma_commit_pair(&empty[stage]);  // both CTAs' slots free once these MMAs finish
+                    else umma_commit(&empty[stage]);
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[acc]);  // accumulator complete
+                if (PAIR) umma_commit_pair(&tfull[acc]);  // accumulator complete, in both CTAs
+                else umma_commit(&tfull[acc]);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
         }
@@ -364,13 +486,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 pending |= 1u << b;
             };
             int k = 0;  // chunk counter of this warp; buffer k & 1
-            if (blockIdx.x < p.units) {
-                const int t0 = (int)blockIdx.x / p.splits;
+            if (U.first < U.count) {
+                int sp0;
+                const int t0 = unit_tile(p, U.first, U.rank, &sp0);
                 issue_ext(0, tile_n(p, t0) * BN + half * CHUNKS * 32, tile_m(p, t0) * BM + y_off);
             }
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-                const int tile = u / p.splits;
+            for (int it = U.first; it < U.count && ok; it += U.step) {
+                int split_;
+                const int tile = unit_tile(p, it, U.rank, &split_);
                 const int m0 = tile_m(p, tile) * BM;
                 const int n0 = tile_n(p, tile) * BN;
                 if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
@@ -389,8 +513,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (i + 1 < CHUNKS) {
                         nn = n + 32;
                         ny = m0 + y_off;
-                    } else if (u + (int)gridDim.x < p.units) {
-                        const int t2 = (u + (int)gridDim.x) / p.splits;
+                    } else if (it + U.step < U.count) {
+                        int sp2;
+                        const int t2 = unit_tile(p, it + U.step, U.rank, &sp2);
                         nn = tile_n(p, t2) * BN + half * CHUNKS * 32;
                         ny = tile_m(p, t2) * BM + y_off;
                     }
@@ -429,15 +554,17 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&tempty[acc]);
+                if (leader) mbar_arrive(&tempty[acc]);
+                else mbar_arrive_cluster(leader_addr(&tempty[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
             // a load still in flight must land before the CTA's shared memory goes away
             for (int b = 0; b < 2; b++)
                 if ((pending >> b) & 1u) mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 6);
         }
-        for (int u = blockIdx.x; u < p.units && !p.ext_tma; u += gridDim.x) {
-            const int tile = u / p.splits, split = u - tile * p.splits;
+        for (int it = U.first; it < U.count && !p.ext_tma; it += U.step) {
+            int split;
+            const int tile = unit_tile(p, it, U.rank, &split);
             const int m0 = tile_m(p, tile) * BM;
             const int n0 = tile_n(p, tile) * BN;
             if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
@@ -555,7 +682,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 store32_bf16(d, valid, out_vec, v);
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            if (leader) mbar_arrive(&tempty[acc]);
+            else mbar_arrive_cluster(leader_addr(&tempty[acc]));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
         if (p.tma_store && lane == 0) bulk_wait_all();  // staged stores done before exit
@@ -564,9 +692,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (PAIR) cluster_sync_all();  // neither CTA leaves while the other may still signal it
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"((uint32_t)CF::TMEM_COLS));
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"((uint32_t)CF::TMEM_COLS));
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"((uint32_t)CF::TMEM_COLS));
     }
 }
 
@@ -722,19 +855,82 @@ size_t gemm_tc_workspace_floats(const Launch& L, const GemmArgs& g) {
     return pl.p.splits > 1 ? (size_t)pl.p.splits * g.M * g.N : 0;
 }
 
+// Clusters of two that can be resident at once for the pair form of an
+// instantiation (0: not available).
 template <int BN, bool A_MN, bool B_MN>
+static int active_pairs(const Launch& L) {
+    static int pairs = -1;  // one value per instantiation
+    if (pairs < 0) {
+        auto kern = tc::k_gemm_tc<BN, A_MN, B_MN, true>;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (L.num_sms / 2));
+        cfg.blockDim = dim3(tc::THREADS);
+        cfg.dynamicSmemBytes = tc::Cfg<BN, true>::SMEM_BYTES;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<BN, true>::SMEM_BYTES) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess)
+            n = 0;
+        cudaGetLastError();
+        pairs = n;
+    }
+    return pairs;
+}
+
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma,
                       const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& mx) {
-    auto kern = tc::k_gemm_tc<BN, A_MN, B_MN>;
+    auto kern = tc::k_gemm_tc<BN, A_MN, B_MN, PAIR>;
+    constexpr int smem = tc::Cfg<BN, PAIR>::SMEM_BYTES;
     static bool attr_done = false;  // one flag per instantiation
     if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc::Cfg<BN>::SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return false;
         attr_done = true;
     }
     L.count();
-    kern<<<pl.grid, tc::THREADS, tc::Cfg<BN>::SMEM_BYTES, L.stream>>>(ma, mb, md, mx, pl.p);
+    if (!PAIR) {
+        kern<<<pl.grid, tc::THREADS, smem, L.stream>>>(ma, mb, md, mx, pl.p);
+        return true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid);
+    cfg.blockDim = dim3(tc::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, md, mx, pl.p) == cudaSuccess;
+}
+
+// Whether the pair form applies: an even number of M tiles, B splitting into
+// two equal halves, resident pairs available, and not switched off
+// (TT_GEMM_PAIR=0 in the environment).
+template <int BN, bool A_MN, bool B_MN>
+static bool use_pair(const Launch& L, tc::Plan& pl) {
+    static const bool off = [] {
+        const char* e = getenv("TT_GEMM_PAIR");
+        return e && e[0] == '0';
+    }();
+    if (off || (pl.p.m_tiles & 1) || pl.p.units < 2) return false;
+    if (B_MN && ((BN / tc::MN_BOX) & 1)) return false;
+    const int pairs = active_pairs<BN, A_MN, B_MN>(L);
+    if (pairs <= 0) return false;
+    const int want = pl.p.units / 2;
+    pl.p.cl = 1;
+    pl.grid = 2 * (want < pairs ? want : pairs);
     return true;
 }
 
@@ -750,12 +946,23 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
     const int a_rows = g.a_rows ? g.a_rows : g.M;
     const int b_rows = g.b_rows ? g.b_rows : g.N;
     const int kval = g.k_valid ? g.k_valid : g.K;
+    pl.p.cl = 0;
+    if (pl.BN == 256) {
+        if (!a_mn && !b_mn) use_pair<256, false, false>(L, pl);
+        else if (!a_mn) use_pair<256, false, true>(L, pl);
+        else use_pair<256, true, true>(L, pl);
+    } else if (pl.BN == 128) {
+        if (!a_mn && !b_mn) use_pair<128, false, false>(L, pl);
+        else if (!a_mn) use_pair<128, false, true>(L, pl);
+        else use_pair<128, true, true>(L, pl);
+    }
     CUtensorMap ma, mb;
     bool ok;
     if (!a_mn) ok = tc::make_map(&ma, g.A, kval, a_rows, g.lda, tc::BK, tc::BM);
     else ok = tc::make_map(&ma, g.A, a_rows, kval, g.lda, tc::MN_BOX, tc::BK);
     if (!ok) return false;
-    if (!b_mn) ok = tc::make_map(&mb, g.B, kval, b_rows, g.ldb, tc::BK, pl.BN);
+    // in the pair form each CTA loads half of a K-major B tile
+    if (!b_mn) ok = tc::make_map(&mb, g.B, kval, b_rows, g.ldb, tc::BK, pl.p.cl ? pl.BN / 2 : pl.BN);
     else ok = tc::make_map(&mb, g.B, b_rows, kval, g.ldb, tc::MN_BOX, tc::BK);
     if (!ok) return false;
     // bf16 outputs: TMA stores (box 32 x 32, 64-byte swizzle) when the rows allow
@@ -778,17 +985,21 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
             pl.p.ext_tma = 1;
     }
     bool launched;
+    const bool pr = pl.p.cl != 0;
+#define TC(BN_, AM_, BM_) \
+    (pr ? launch_tc<BN_, AM_, BM_, true>(L, pl, ma, mb, md, mx) : launch_tc<BN_, AM_, BM_, false>(L, pl, ma, mb, md, mx))
     if (pl.BN == 256) {
-        if (!a_mn && !b_mn) launched = launch_tc<256, false, false>(L, pl, ma, mb, md, mx);
-        else if (!a_mn) launched = launch_tc<256, false, true>(L, pl, ma, mb, md, mx);
-        else launched = launch_tc<256, true, true>(L, pl, ma, mb, md, mx);
-    } else if (pl.BN == 192) {  // weight-gradient form only
-        launched = (a_mn && b_mn) && launch_tc<192, true, true>(L, pl, ma, mb, md, mx);
+        if (!a_mn && !b_mn) launched = TC(256, false, false);
+        else if (!a_mn) launched = TC(256, false, true);
+        else launched = TC(256, true, true);
+    } else if (pl.BN == 192) {  // weight-gradient form only, never paired
+        launched = (a_mn && b_mn && !pr) && launch_tc<192, true, true, false>(L, pl, ma, mb, md, mx);
     } else {
-        if (!a_mn && !b_mn) launched = launch_tc<128, false, false>(L, pl, ma, mb, md, mx);
-        else if (!a_mn) launched = launch_tc<128, false, true>(L, pl, ma, mb, md, mx);
-        else launched = launch_tc<128, true, true>(L, pl, ma, mb, md, mx);
+        if (!a_mn && !b_mn) launched = TC(128, false, false);
+        else if (!a_mn) launched = TC(128, false, true);
+        else launched = TC(128, true, true);
     }
+#undef TC
     if (!launched) return false;
     if (pl.p.splits > 1) {
         long long total = (long long)g.M * pl.p.n_store;
