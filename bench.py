@@ -230,20 +230,20 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "f4b416334175f2a6",
+    "sources": "f279c6749b9fb895",
     "bytes_per_launch_group": {
-        "gemm_fwd": 346837065,
-        "gemm_dx": 297013467,
-        "gemm_dw": 294037765,
-        "attn_fwd": 179071061,
-        "attn_bwd": 560962261,
-        "xent": 6538611968,
-        "colsum": 114272165,
-        "ln_fwd": 54037279,
-        "ln_bwd": 170579395,
-        "adamw": 3671939072,
-        "embed_fwd": 12884224,
-        "embed_bwd": 124953344,
+        "gemm_fwd": 349008441,
+        "gemm_dx": 305927539,
+        "gemm_dw": 294065220,
+        "attn_fwd": 179029845,
+        "attn_bwd": 561052160,
+        "xent": 6538946560,
+        "colsum": 114288075,
+        "ln_fwd": 53969807,
+        "ln_bwd": 170552136,
+        "adamw": 3672358144,
+        "embed_fwd": 12703744,
+        "embed_bwd": 124936192,
     },
 }
 
