@@ -80,7 +80,8 @@ struct Params {
     int* flags;
     int tma_store;  // bf16 outputs leave through shared memory and TMA stores
     int ext_tma;    // the extra epilogue operand (GELU' input or residual) arrives by TMA loads
-    int cl;         // pair form: CTA pairs take M tiles 2i, 2i + 1 (m_tiles even)
+    int cl;         // pair form: CTA pairs take M tiles 2i, 2i + 1
+    int pair_units; // pair form: ceil(m_tiles / 2) * n_tiles * splits
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -204,24 +205,33 @@ __device__ __forceinline__ int tile_n(const Params& p, int t) { return p.n_fast 
 
 // The units (tile, split) this CTA takes: it = first, first + step, ... < count.
 // In the pair form a unit is a pair of M tiles and the CTA of rank r takes M
-// tile 2 * pair + r.
+// tile 2 * pair + r; with an odd number of M tiles the last pair's second
+// tile lies wholly past M (its loads read zeros, its rows are not written;
+// only the weight-gradient form, whose output is written row by row, pairs
+// an odd count).
 struct UnitIter {
     int first, step, count, rank;
 };
 __device__ __forceinline__ UnitIter unit_iter(const Params& p) {
-    if (p.cl) return {(int)blockIdx.x >> 1, (int)gridDim.x >> 1, p.units >> 1, (int)blockIdx.x & 1};
+    if (p.cl) return {(int)blockIdx.x >> 1, (int)gridDim.x >> 1, p.pair_units, (int)blockIdx.x & 1};
     return {(int)blockIdx.x, (int)gridDim.x, p.units, 0};
 }
-// unit it -> tile number (the numbering tile_m / tile_n read) and split
-__device__ __forceinline__ int unit_tile(const Params& p, int it, int rank, int* split) {
+// unit it -> first row m0, first column n0 and split
+__device__ __forceinline__ void unit_mn(const Params& p, int it, int rank, int bn, int* m0, int* n0, int* split) {
     const int t = it / p.splits;
     *split = it - t * p.splits;
-    if (!p.cl) return t;
-    const int mpt = p.m_tiles >> 1;
-    const int mp = p.n_fast ? t / p.n_tiles : t % mpt;
-    const int n = p.n_fast ? t % p.n_tiles : t / mpt;
-    const int m = 2 * mp + rank;
-    return p.n_fast ? m * p.n_tiles + n : n * p.m_tiles + m;
+    int m, n;
+    if (!p.cl) {
+        m = tile_m(p, t);
+        n = tile_n(p, t);
+    } else {
+        const int mpt = (p.m_tiles + 1) >> 1;
+        const int mp = p.n_fast ? t / p.n_tiles : t % mpt;
+        n = p.n_fast ? t % p.n_tiles : t / mpt;
+        m = 2 * mp + rank;
+    }
+    *m0 = m * BM;
+    *n0 = n * bn;
 }
 
 // the shared::cluster address of the same variable in the leader CTA (rank 0)
@@ -336,10 +346,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             long long issued = 0;
             bool ok = true;
             for (int it = U.first; it < U.count && ok; it += U.step) {
-                int split;
-                const int tile = unit_tile(p, it, U.rank, &split);
-                const int m0 = tile_m(p, tile) * BM;
-                const int n0 = tile_n(p, tile) * BN;
+                int split, m0, n0;
+                unit_mn(p, it, U.rank, BN, &m0, &n0, &split);
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 for (int kb = kb0; kb < kb1; kb++) {
@@ -421,8 +429,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int it = U.first; it < U.count && ok; it += U.step) {
-                int split;
-                (void)unit_tile(p, it, U.rank, &split);
+                int split, m0_, n0_;
+                unit_mn(p, it, U.rank, BN, &m0_, &n0_, &split);
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags, 0x400 + 2)) { ok = false; break; }
@@ -487,16 +495,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             };
             int k = 0;  // chunk counter of this warp; buffer k & 1
             if (U.first < U.count) {
-                int sp0;
-                const int t0 = unit_tile(p, U.first, U.rank, &sp0);
-                issue_ext(0, tile_n(p, t0) * BN + half * CHUNKS * 32, tile_m(p, t0) * BM + y_off);
+                int sp0, mf, nf;
+                unit_mn(p, U.first, U.rank, BN, &mf, &nf, &sp0);
+                issue_ext(0, nf + half * CHUNKS * 32, mf + y_off);
             }
             bool ok = true;
             for (int it = U.first; it < U.count && ok; it += U.step) {
-                int split_;
-                const int tile = unit_tile(p, it, U.rank, &split_);
-                const int m0 = tile_m(p, tile) * BM;
-                const int n0 = tile_n(p, tile) * BN;
+                int split_, m0, n0;
+                unit_mn(p, it, U.rank, BN, &m0, &n0, &split_);
                 if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -514,10 +520,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         nn = n + 32;
                         ny = m0 + y_off;
                     } else if (it + U.step < U.count) {
-                        int sp2;
-                        const int t2 = unit_tile(p, it + U.step, U.rank, &sp2);
-                        nn = tile_n(p, t2) * BN + half * CHUNKS * 32;
-                        ny = tile_m(p, t2) * BM + y_off;
+                        int sp2, m2, n2;
+                        unit_mn(p, it + U.step, U.rank, BN, &m2, &n2, &sp2);
+                        nn = n2 + half * CHUNKS * 32;
+                        ny = m2 + y_off;
                     }
                     if (nn >= 0) {
                         if (lane == 0) bulk_wait_read<0>();
@@ -563,10 +569,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if ((pending >> b) & 1u) mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 6);
         }
         for (int it = U.first; it < U.count && !p.ext_tma; it += U.step) {
-            int split;
-            const int tile = unit_tile(p, it, U.rank, &split);
-            const int m0 = tile_m(p, tile) * BM;
-            const int n0 = tile_n(p, tile) * BN;
+            int split, m0, n0;
+            unit_mn(p, it, U.rank, BN, &m0, &n0, &split);
             if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
             tc_fence_after();
             const int m = m0 + row;
@@ -810,16 +814,27 @@ static Plan finish_plan(const Launch& L, const GemmArgs& g, Plan pl) {
     return pl;
 }
 
-// Tile width: 128 for narrow outputs, else 256.  The weight-gradient form
-// (both operands MN-major, few output tiles, split K) may take 192 instead
-// when that needs clearly fewer tile-times (waves of the persistent grid x
-// width x k-blocks per unit): its tiles then fill more of the SMs (for the
-// [2304, 768] QKV weight, 144 units instead of 108).  N = 192 MMAs run at a
-// lower rate per FLOP than N = 256, which outweighs the better wave fill of
-// the other forms.
+// The pair form of the kernel (see its description) is on unless
+// TT_GEMM_PAIR=0 is in the environment.
+static bool pair_disabled() {
+    static const bool off = [] {
+        const char* e = getenv("TT_GEMM_PAIR");
+        return e && e[0] == '0';
+    }();
+    return off;
+}
+
+// Tile width: 128 for narrow outputs, else 256.  Without the pair form, the
+// weight-gradient form (both operands MN-major, few output tiles, split K)
+// may take 192 instead when that needs clearly fewer tile-times (waves of the
+// persistent grid x width x k-blocks per unit): its tiles then fill more of
+// the SMs (for the [2304, 768] QKV weight, 144 units instead of 108).  N = 192
+// MMAs run at a lower rate per FLOP than N = 256, which outweighs the better
+// wave fill of the other forms; and a 192-wide B tile does not split into the
+// pair form's halves, so with pairs the width stays 256.
 static Plan make_plan(const Launch& L, const GemmArgs& g) {
     if (g.N <= 128) return finish_plan(L, g, plan_for(L, g, 128));
-    if (g.a_kmajor || g.b_kmajor) return finish_plan(L, g, plan_for(L, g, 256));
+    if (g.a_kmajor || g.b_kmajor || !pair_disabled()) return finish_plan(L, g, plan_for(L, g, 256));
     const int sms = L.num_sms > 0 ? L.num_sms : 148;
     Plan best{};
     double best_cost = 0.0;
@@ -920,16 +935,15 @@ static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma
 // (TT_GEMM_PAIR=0 in the environment).
 template <int BN, bool A_MN, bool B_MN>
 static bool use_pair(const Launch& L, tc::Plan& pl) {
-    static const bool off = [] {
-        const char* e = getenv("TT_GEMM_PAIR");
-        return e && e[0] == '0';
-    }();
-    if (off || (pl.p.m_tiles & 1) || pl.p.units < 2) return false;
+    if (tc::pair_disabled() || pl.p.units < 2) return false;
+    // an odd M-tile count only where the output is written row by row
+    if ((pl.p.m_tiles & 1) && !(A_MN && B_MN)) return false;
     if (B_MN && ((BN / tc::MN_BOX) & 1)) return false;
     const int pairs = active_pairs<BN, A_MN, B_MN>(L);
     if (pairs <= 0) return false;
-    const int want = pl.p.units / 2;
+    const int want = ((pl.p.m_tiles + 1) / 2) * pl.p.n_tiles * pl.p.splits;
     pl.p.cl = 1;
+    pl.p.pair_units = want;
     pl.grid = 2 * (want < pairs ? want : pairs);
     return true;
 }
