@@ -3,7 +3,7 @@
 // registers between passes, grids sized from the SM count, and every
 // reduction in a fixed order (no floating-point atomics).
 //   LayerNorm forward / backward  (one warp per row)
-//   fused cross entropy           (one 512-thread CTA per row, three passes)
+//   fused cross entropy           (one 512-thread CTA per row, three passes, one exponential per logit)
 //   column sums (bias gradients)  (8 columns per thread)
 //   embedding-gradient scatter    (fixed 64-row chunks of the token-sorted
 //                                  positions, then chunk partials in order)
@@ -309,10 +309,13 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
 constexpr float XV_LOG2E = 1.4426950408889634f;
 
 // One CTA per row, three passes over the row (the first from HBM, the others
-// from L2): (1) the row max, on packed bf16 pairs; (2) the sum of
-// 2^((z - max) log2 e); (3) the gradient, written in place.  Few registers, so
-// several rows are in flight per SM; exponentials use the single hardware
-// instruction ex2.approx (relative error ~2^-22).
+// from L2): (1) the row max, on packed bf16 pairs; (2) e = 2^((z - max) log2 e),
+// summed, and written over z as bf16; (3) the gradient e * dscale / sum, written
+// in place.  Each logit costs one exponential (the special-function pipe, not
+// HBM, bounded the kernel when the gradient pass took a second one); the
+// extra rounding of e to bf16 keeps the gradient within 2^-8 of its exact
+// value.  Few registers, so several rows are in flight per SM; exponentials
+// use the single hardware instruction ex2.approx (relative error ~2^-22).
 constexpr int XS_THREADS = 512;
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -358,19 +361,30 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
 #pragma unroll
     for (int k = 1; k < XS_THREADS / 32; k++) mx = fmaxf(mx, sm[k]);
     const float ml = mx * XV_LOG2E;
-    // pass 2: sum of exponentials
-    float s = 0.0f;
+    const int tgt = targets[row];
+    const bool ok = tgt >= 0 && tgt < V;
+    const int tv = ok ? (tgt >> 3) : -1;
+    // pass 2: e = 2^((z - max) log2 e), summed, and kept in place of z (bf16)
+    // so that the gradient pass needs no second exponential
+    float s = 0.0f, ztgt = 0.0f;
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
-        float f[8];
+        float f[8], ex[8];
         unpack8(zr[vi], f);
+        if (vi == tv) ztgt = f[tgt & 7];
         if (vi < vfull) {
 #pragma unroll
-            for (int e = 0; e < 8; e++) s += ex2f(fmaf(f[e], XV_LOG2E, -ml));
+            for (int e = 0; e < 8; e++) {
+                ex[e] = ex2f(fmaf(f[e], XV_LOG2E, -ml));
+                s += ex[e];
+            }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; e++)
-                if (vi * 8 + e < V) s += ex2f(fmaf(f[e], XV_LOG2E, -ml));
+            for (int e = 0; e < 8; e++) {
+                ex[e] = (vi * 8 + e < V) ? ex2f(fmaf(f[e], XV_LOG2E, -ml)) : 0.0f;
+                s += ex[e];
+            }
         }
+        zr[vi] = pack8(ex);
     }
     s = wsum(s);
     __syncthreads();  // everyone has read sm[] above
@@ -380,30 +394,20 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
 #pragma unroll
     for (int k = 0; k < XS_THREADS / 32; k++) S_ += sm[k];  // same order in every thread
     const float lse = mx + logf(S_);
-    const float lsel = lse * XV_LOG2E;
-    const int tgt = targets[row];
-    const bool ok = tgt >= 0 && tgt < V;
     if (!ok && threadIdx.x == 0) {
         atomicOr(&flags[FLAG_BAD_TOKEN], 1);
         row_loss[row] = 0.0f;
     }
-    const int tv = ok ? (tgt >> 3) : -1;
-    // pass 3: gradient, in place
+    // pass 3: gradient, in place: softmax = e / S (pad columns hold e = 0)
+    const float k = dscale / S_;
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
-        float f[8], o[8];
-        unpack8(zr[vi], f);
-        if (vi < vfull) {
+        float ex[8], o[8];
+        unpack8(zr[vi], ex);
 #pragma unroll
-            for (int e = 0; e < 8; e++) o[e] = ex2f(fmaf(f[e], XV_LOG2E, -lsel)) * dscale;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; e++)
-                o[e] = (vi * 8 + e < V) ? ex2f(fmaf(f[e], XV_LOG2E, -lsel)) * dscale : 0.0f;
-        }
+        for (int e = 0; e < 8; e++) o[e] = ex[e] * k;
         if (vi == tv) {
-            const int e = tgt & 7;
-            row_loss[row] = lse - f[e];
-            o[e] -= dscale;
+            row_loss[row] = lse - ztgt;
+            o[tgt & 7] -= dscale;
         }
         zr[vi] = pack8(o);
     }

@@ -113,7 +113,8 @@ def test_linear_bwd_dx(ctx, oracle, dt, backend, M, K, N, variant):
 
 
 @pytest.mark.parametrize("dt,backend", [("fp32", 1), ("bf16", 1), ("bf16", 0)])
-@pytest.mark.parametrize("M,K,N", [(200, 64, 96), (4096, 256, 192), (1000, 768, 2304), (2048, 3072, 768)])
+@pytest.mark.parametrize("M,K,N", [(200, 64, 96), (4096, 256, 192), (1000, 768, 2304), (2048, 3072, 768),
+                                   (600, 512, 384)])  # 3 row tiles of dW: the pair form's odd count
 def test_linear_bwd_dw(ctx, oracle, dt, backend, M, K, N):
     ctx.set_gemm_backend(backend)
     dy, x = rnd(M, N), rnd(M, K)
@@ -326,10 +327,16 @@ def test_adamw_and_cast(ctx, oracle, n):
     torch.cuda.synchronize()
     rp, rm, rv = oracle.adamw(p0, g, m0, v0, args["lr"], args["beta1"], args["beta2"], args["eps"],
                               args["weight_decay"], 3)
-    # fp32 arithmetic on fp32 inputs: a few ulps of the operands' scale
+    # fp32 arithmetic on fp32 inputs: a few ulps of the operands' scale.  The
+    # moments are sums of two terms that can cancel, so their bound is taken
+    # from the terms (b1|m| + (1-b1)|g|, b2 v + (1-b2) g^2), not from the result.
     assert_close(host(P), rp, 1e-6, 1e-6, "master")
-    assert_close(host(Mm), rm, 1e-6, 1e-6, "m")
-    assert_close(host(Vv), rv, 1e-6, 1e-6, "v")
+    b1, b2 = args["beta1"], args["beta2"]
+    m_scale = b1 * np.abs(m0.astype(np.float64)) + (1 - b1) * np.abs(g.astype(np.float64))
+    v_scale = b2 * np.abs(v0.astype(np.float64)) + (1 - b2) * g.astype(np.float64) ** 2
+    for got, ref, sc, what in [(host(Mm), rm, m_scale, "m"), (host(Vv), rv, v_scale, "v")]:
+        err = np.abs(got - ref)
+        assert np.all(err <= 1e-6 * np.abs(ref) + 8 * 2.0 ** -24 * sc), (what, float(np.max(err / (sc + 1e-30))))
     # the bf16 copy is the nearest bf16 of the updated fp32 master
     assert np.array_equal(host(low), oracle.bf16_values(P.cpu().numpy()))
     cast = torch.empty(n, device=DEV, dtype=torch.bfloat16)
