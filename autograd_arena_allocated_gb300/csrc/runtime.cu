@@ -690,13 +690,14 @@ static tt_status gpt2_generate(tt_ctx* c, const void* params, const int32_t* pro
             if (!linear(g, 4 * C, PL(10), PL(11), C, x2, x1, nullptr)) return fail(c, TT_ERR_CUDA, "generate: GEMM");
             std::swap(x, x2);
         }
-        // final LayerNorm and the tied LM head over the V real rows of wte, which
-        // also advances the position
-        if (bf && launch_gemm_skinny_pick(S, x, P(o.wte), B, m.V, C, keys, pos_dev, P(o.lnfw), P(o.lnfb))) {
+        // final LayerNorm (its own launch: folded into the LM head it would be
+        // redone by each of that GEMM's thousands of CTAs), then the tied LM head
+        // over the V real rows of wte, which also advances the position
+        launch_layernorm_fwd(S, bf, x, P(o.lnfw), P(o.lnfb), h, mean, rstd, B, C);
+        if (bf && launch_gemm_skinny_pick(S, h, P(o.wte), B, m.V, C, keys, pos_dev)) {
             launch_pick(S, keys, nct, B, tokbuf, Ttot, pos_dev);
             return TT_OK;
         }
-        launch_layernorm_fwd(S, bf, x, P(o.lnfw), P(o.lnfb), h, mean, rstd, B, C);
         if (!launch_gemm_skinny(S, bf, h, P(o.wte), nullptr, nullptr, zl, nullptr, B, m.V, C, Vp, m.V, false,
                                 pos_dev)) {
             GemmArgs ga;
