@@ -230,20 +230,20 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "f279c6749b9fb895",
+    "sources": "0b0a063830509aa7",
     "bytes_per_launch_group": {
-        "gemm_fwd": 349008441,
-        "gemm_dx": 305927539,
-        "gemm_dw": 294065220,
-        "attn_fwd": 179029845,
-        "attn_bwd": 561052160,
-        "xent": 6538946560,
-        "colsum": 114288075,
-        "ln_fwd": 53969807,
-        "ln_bwd": 170552136,
-        "adamw": 3672358144,
-        "embed_fwd": 12703744,
-        "embed_bwd": 124936192,
+        "gemm_fwd": 350654652,
+        "gemm_dx": 299767996,
+        "gemm_dw": 294899017,
+        "attn_fwd": 179051904,
+        "attn_bwd": 560950485,
+        "xent": 6543710208,
+        "colsum": 114280677,
+        "ln_fwd": 53976934,
+        "ln_bwd": 170638991,
+        "adamw": 3672039168,
+        "embed_fwd": 12726528,
+        "embed_bwd": 124944640,
     },
 }
 
