@@ -209,6 +209,7 @@ OP_SHAPES = {
     "attn_bwd": "causal attention backward, B=32 T=1024 H=12 hd=64",
     "ln_fwd": "LayerNorm forward [32768,768]",
     "ln_bwd": "LayerNorm backward [32768,768], accumulating dx",
+    "colsum": "FC bias gradient: column sums of dy[32768,3072] (with the FC weight gradient)",
     "xent": "fused cross entropy over [32768,50304] logits",
     "embed_bwd": "embedding-gradient scatter, 32768 Zipf tokens, C=768",
     "adamw": "AdamW over 124,439,808 parameters",
@@ -532,6 +533,14 @@ def run_op(args):
         dy, x = rnd(M, 4 * C), rnd(M, C)
         dW = torch.empty(4 * C, C, device=dev)
         fn = lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", dy, x, dW, None, M, C, 4 * C))
+        flops = 2.0 * M * C * 4 * C
+    elif op == "colsum":
+        # the FC bias gradient with its weight gradient (the two launch groups
+        # are timed apart: gemm_dw and colsum)
+        dy, x = rnd(M, 4 * C), rnd(M, C)
+        dW = torch.empty(4 * C, C, device=dev)
+        db = torch.empty(4 * C, device=dev)
+        fn = lambda: (ctx.reset(), ctx.linear_bwd_dw("bf16", dy, x, dW, db, M, C, 4 * C))
         flops = 2.0 * M * C * 4 * C
     elif op == "gemm_lm":
         # the op takes W as [N, K] = [Vp, C]: the pad rows V..Vp-1 are zero
