@@ -17,7 +17,7 @@ STATUS_NAMES = {
     0: "TT_OK", -1: "TT_ERR", -2: "TT_ERR_ARG", -3: "TT_ERR_ARENA_OOM", -4: "TT_ERR_CUDA",
     -5: "TT_ERR_TIMEOUT", -6: "TT_ERR_NONFINITE", -7: "TT_ERR_STALE", -8: "TT_ERR_STATE",
 }
-TT_FP32, TT_BF16 = 0, 1
+TT_FP32, TT_BF16, TT_FP16 = 0, 1, 2
 
 
 class GPT2Config(C.Structure):
@@ -59,6 +59,7 @@ SIGNATURES = {
     "tt_ctx_copy_row_losses": (_st, [_vp, _vp, _sz]),
     "tt_adamw": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _i]),
     "tt_cast_f32_to_bf16": (_st, [_vp, _vp, _vp, _sz]),
+    "tt_cast_f32_to_f16": (_st, [_vp, _vp, _vp, _sz]),
     "tt_gpt2_eval": (_st, [_vp, _vp, _vp, _vp, _i, _i, C.POINTER(C.c_float)]),
     "tt_gpt2_step_ex": (_st, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, C.POINTER(_f)]),
     "tt_grad_stats": (_st, [_vp, _vp, _sz, _vp, _vp]),

@@ -9,9 +9,9 @@ from __future__ import annotations
 import ctypes as C
 from typing import Optional
 
-from ._native import GPT2Config, OpProfile, TT_BF16, TT_FP32, TTError, lib
+from ._native import GPT2Config, OpProfile, TT_BF16, TT_FP16, TT_FP32, TTError, lib
 
-DTYPES = {"fp32": TT_FP32, "bf16": TT_BF16}
+DTYPES = {"fp32": TT_FP32, "bf16": TT_BF16, "fp16": TT_FP16}
 
 
 def _ptr(x) -> Optional[int]:
@@ -208,6 +208,10 @@ class Context:
     def cast_bf16(self, src, dst, n=None):
         n = src.numel() if n is None else n
         self._check(lib().tt_cast_f32_to_bf16(self.h, _ptr(src), _ptr(dst), int(n)))
+
+    def cast_f16(self, src, dst, n=None):
+        n = src.numel() if n is None else n
+        self._check(lib().tt_cast_f32_to_f16(self.h, _ptr(src), _ptr(dst), int(n)))
 
     # -------------------------------------------------------------- ops
     def linear_fwd(self, dtype, x, W, b, residual, y, pre, M, K, N, gelu=False):

@@ -854,7 +854,7 @@ static Plan make_plan(const Launch& L, const GemmArgs& g) {
 }  // namespace tc
 
 bool gemm_tc_eligible(const GemmArgs& g) {
-    if (!g.in_bf16 || g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+    if (!g.in_bf16 || g.in_f16 || g.M <= 0 || g.N <= 0 || g.K <= 0) return false;  // bf16 operands only
     if (g.a_kmajor && g.b_kmajor && g.d_f32) return false;     // forward form writes bf16
     if (!g.a_kmajor && g.b_kmajor) return false;               // form not used by the step
     if (!g.a_kmajor && !(g.d_f32 && g.epi == EPI_STORE && !g.bias && !g.residual)) return false;

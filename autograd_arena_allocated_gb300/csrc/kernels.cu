@@ -12,8 +12,26 @@ namespace tt {
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ float ld(const float* p, long long i) { return p[i]; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float ld(const __half* p, long long i) { return __half2float(p[i]); }
 __device__ __forceinline__ void st(float* p, long long i, float v) { p[i] = v; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, long long i, float v) { p[i] = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void st(__half* p, long long i, float v) { p[i] = __float2half_rn(v); }
+
+// four floats rounded to nearest even into elements 4i..4i+3 of a 16-bit copy (one 8-byte store)
+__device__ __forceinline__ void st_low4(__nv_bfloat16* p, size_t i, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p)[i] = packed;
+}
+__device__ __forceinline__ void st_low4(__half* p, size_t i, float4 v) {
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p)[i] = packed;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -63,7 +81,11 @@ void launch_embed_fwd(const Launch& L, bool bf16, const void* wte, const void* w
     if (L.dry) return;
     long long total = (long long)B * T * C;
     L.count();
-    if (bf16)
+    if (bf16 && L.f16)
+        k_embed_fwd<__half><<<blocks_for(total, 256), 256, 0, L.stream>>>(
+            (const __half*)wte, (const __half*)wpe, tok, (__half*)x, T, C, V,
+            total, L.flags);
+    else if (bf16)
         k_embed_fwd<__nv_bfloat16><<<blocks_for(total, 256), 256, 0, L.stream>>>(
             (const __nv_bfloat16*)wte, (const __nv_bfloat16*)wpe, tok, (__nv_bfloat16*)x, T, C, V,
             total, L.flags);
@@ -265,7 +287,10 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
         int threads = (C + 7) / 8;
         threads = ((threads + 31) / 32) * 32;
         L.count();
-        if (bf16)
+        if (bf16 && L.f16)
+            k_embed_segsum<__half><<<M, threads, 0, L.stream>>>(
+                (const __half*)dx, s, s + M, M, C, V, dwte);
+        else if (bf16)
             k_embed_segsum<__nv_bfloat16><<<M, threads, 0, L.stream>>>(
                 (const __nv_bfloat16*)dx, s, s + M, M, C, V, dwte);
         else
@@ -273,7 +298,10 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
     }
     long long n = (long long)maxT * C;
     L.count();
-    if (bf16)
+    if (bf16 && L.f16)
+        k_embed_wpe<__half><<<blocks_for(n, 256), 256, 0, L.stream>>>(
+            (const __half*)dx, B, T, C, maxT, dwpe, acc_params ? 1 : 0);
+    else if (bf16)
         k_embed_wpe<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, L.stream>>>(
             (const __nv_bfloat16*)dx, B, T, C, maxT, dwpe, acc_params ? 1 : 0);
     else
@@ -322,7 +350,11 @@ void launch_layernorm_fwd(const Launch& L, bool bf16, const void* x, const void*
     if (bf16 && launch_ln_fwd_bf16(L, x, w, b, y, mean, rstd, M, C)) return;
     const int warps = 8;
     L.count();
-    if (bf16)
+    if (bf16 && L.f16)
+        k_layernorm_fwd<__half><<<blocks_for(M, warps), warps * 32, 0, L.stream>>>(
+            (const __half*)x, (const __half*)w, (const __half*)b,
+            (__half*)y, mean, rstd, M, C);
+    else if (bf16)
         k_layernorm_fwd<__nv_bfloat16><<<blocks_for(M, warps), warps * 32, 0, L.stream>>>(
             (const __nv_bfloat16*)x, (const __nv_bfloat16*)w, (const __nv_bfloat16*)b,
             (__nv_bfloat16*)y, mean, rstd, M, C);
@@ -428,10 +460,15 @@ void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void*
         cudaFuncSetAttribute(k_layernorm_bwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         cudaFuncSetAttribute(k_layernorm_bwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              max_smem);
+        cudaFuncSetAttribute(k_layernorm_bwd<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         attr = true;
     }
     L.count();
-    if (bf16)
+    if (bf16 && L.f16)
+        k_layernorm_bwd<__half><<<nblk, LN_BWD_WARPS * 32, smem, L.stream>>>(
+            (const __half*)x, (const __half*)w, mean, rstd,
+            (const __half*)dy, (__half*)dx, scratch, M, C, accumulate ? 1 : 0);
+    else if (bf16)
         k_layernorm_bwd<__nv_bfloat16><<<nblk, LN_BWD_WARPS * 32, smem, L.stream>>>(
             (const __nv_bfloat16*)x, (const __nv_bfloat16*)w, mean, rstd,
             (const __nv_bfloat16*)dy, (__nv_bfloat16*)dx, scratch, M, C, accumulate ? 1 : 0);
@@ -535,7 +572,10 @@ void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* target
         return;
     }
     L.count();
-    if (bf16)
+    if (bf16 && L.f16)
+        k_xent<__half><<<M, XENT_THREADS, 0, L.stream>>>(
+            (__half*)logits, targets, row_loss, V, ld_, dscale, scale_dev, L.flags);
+    else if (bf16)
         k_xent<__nv_bfloat16><<<M, XENT_THREADS, 0, L.stream>>>(
             (__nv_bfloat16*)logits, targets, row_loss, V, ld_, dscale, scale_dev, L.flags);
     else
@@ -584,7 +624,9 @@ void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, floa
     }
     dim3 grid(blocks_for(N, 128), nchunk);
     L.count();
-    if (bf16)
+    if (bf16 && L.f16)
+        k_colsum_part<__half><<<grid, 128, 0, L.stream>>>((const __half*)x, M, N, scratch);
+    else if (bf16)
         k_colsum_part<__nv_bfloat16><<<grid, 128, 0, L.stream>>>((const __nv_bfloat16*)x, M, N, scratch);
     else
         k_colsum_part<float><<<grid, 128, 0, L.stream>>>((const float*)x, M, N, scratch);
@@ -594,7 +636,8 @@ void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, floa
 
 // ================================================================== AdamW
 // Flat, grid-stride, four elements per thread per iteration (128-bit loads).
-__global__ void k_adamw(float* __restrict__ p, __nv_bfloat16* __restrict__ lowp,
+template <typename LT>
+__global__ void k_adamw(float* __restrict__ p, LT* __restrict__ lowp,
                         const float* __restrict__ g, float* __restrict__ m, float* __restrict__ v,
                         size_t n, float lr, float b1, float b2, float eps, float wd, float c1,
                         float c2) {
@@ -617,14 +660,7 @@ __global__ void k_adamw(float* __restrict__ p, __nv_bfloat16* __restrict__ lowp,
         reinterpret_cast<float4*>(p)[i] = pp;
         reinterpret_cast<float4*>(m)[i] = mm;
         reinterpret_cast<float4*>(v)[i] = vv;
-        if (lowp) {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(pp.z, pp.w);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<uint32_t*>(&hi);
-            reinterpret_cast<uint2*>(lowp)[i] = packed;
-        }
+        if (lowp) st_low4(lowp, i, pp);
     }
     // tail (n not a multiple of 4)
     for (size_t i = n4 * 4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -634,11 +670,11 @@ __global__ void k_adamw(float* __restrict__ p, __nv_bfloat16* __restrict__ lowp,
         v[i] = vv;
         float pp = p[i] - lr * ((mm / c1) / (sqrtf(vv / c2) + eps) + wd * p[i]);
         p[i] = pp;
-        if (lowp) lowp[i] = __float2bfloat16_rn(pp);
+        if (lowp) st(lowp, (long long)i, pp);
     }
 }
 
-void launch_adamw(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g, float* m,
+void launch_adamw(const Launch& L, float* master, void* lowp, const float* g, float* m,
                   float* v, size_t n, float lr, float b1, float b2, float eps, float wd, int step) {
     if (L.dry || n == 0) return;
     float c1 = (float)(1.0 - pow((double)b1, step));
@@ -646,21 +682,33 @@ void launch_adamw(const Launch& L, float* master, __nv_bfloat16* lowp, const flo
     long long want = (long long)((n / 4 + 255) / 256);
     int grid = (int)(want < (long long)L.num_sms * 8 ? (want < 1 ? 1 : want) : (long long)L.num_sms * 8);
     L.count();
-    k_adamw<<<grid, 256, 0, L.stream>>>(master, lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
+    if (L.f16)
+        k_adamw<<<grid, 256, 0, L.stream>>>(master, (__half*)lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
+    else
+        k_adamw<<<grid, 256, 0, L.stream>>>(master, (__nv_bfloat16*)lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
 }
 
-__global__ void k_cast_bf16(const float* __restrict__ s, __nv_bfloat16* __restrict__ d, size_t n) {
+template <typename T>
+__global__ void k_cast_low(const float* __restrict__ s, T* __restrict__ d, size_t n) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        d[i] = __float2bfloat16_rn(s[i]);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) st(d, (long long)i, s[i]);
+}
+
+static int cast_grid(const Launch& L, size_t n) {
+    long long want = (long long)((n + 255) / 256);
+    return (int)(want < (long long)L.num_sms * 8 ? want : (long long)L.num_sms * 8);
 }
 
 void launch_cast_bf16(const Launch& L, const float* src, __nv_bfloat16* dst, size_t n) {
     if (L.dry || n == 0) return;
-    long long want = (long long)((n + 255) / 256);
-    int grid = (int)(want < (long long)L.num_sms * 8 ? want : (long long)L.num_sms * 8);
     L.count();
-    k_cast_bf16<<<grid, 256, 0, L.stream>>>(src, dst, n);
+    k_cast_low<<<cast_grid(L, n), 256, 0, L.stream>>>(src, dst, n);
+}
+
+void launch_cast_f16(const Launch& L, const float* src, __half* dst, size_t n) {
+    if (L.dry || n == 0) return;
+    L.count();
+    k_cast_low<<<cast_grid(L, n), 256, 0, L.stream>>>(src, dst, n);
 }
 
 // ================================================================== SIMT GEMM
@@ -751,7 +799,10 @@ void gemm_simt_launch(const Launch& L, const GemmArgs& g) {
     if (L.dry) return;
     dim3 grid((g.N + SG_T - 1) / SG_T, (g.M + SG_T - 1) / SG_T);
     L.count();
-    if (g.in_bf16) {
+    if (g.in_bf16 && g.in_f16) {
+        if (g.d_f32) k_gemm_simt<__half, float><<<grid, 256, 0, L.stream>>>(g);
+        else k_gemm_simt<__half, __half><<<grid, 256, 0, L.stream>>>(g);
+    } else if (g.in_bf16) {
         if (g.d_f32) k_gemm_simt<__nv_bfloat16, float><<<grid, 256, 0, L.stream>>>(g);
         else k_gemm_simt<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, L.stream>>>(g);
     } else {
@@ -907,7 +958,11 @@ static void attn_bwd_simt(const Launch& L, const void* qkv, const void* y, const
 
 #define TT_HD_DISPATCH(hd, FN, ...)                                             \
     do {                                                                        \
-        if (bf16) {                                                             \
+        if (bf16 && L.f16) {                                                    \
+            if (hd == 16) FN<__half, 16>(__VA_ARGS__);                          \
+            else if (hd == 32) FN<__half, 32>(__VA_ARGS__);                     \
+            else FN<__half, 64>(__VA_ARGS__);                                   \
+        } else if (bf16) {                                                      \
             if (hd == 16) FN<__nv_bfloat16, 16>(__VA_ARGS__);                   \
             else if (hd == 32) FN<__nv_bfloat16, 32>(__VA_ARGS__);              \
             else FN<__nv_bfloat16, 64>(__VA_ARGS__);                            \
@@ -921,8 +976,9 @@ static void attn_bwd_simt(const Launch& L, const void* qkv, const void* y, const
 void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, float* lse,
                           int B, int T, int C, int H) {
     if (L.dry) return;
-    if (attention_tc_eligible(bf16, C, H) && launch_attention_fwd_tc(L, qkv, y, lse, B, T, C, H)) return;
-    if (attention_mma_eligible(bf16, C, H)) {
+    const bool bf_only = bf16 && !L.f16;  // the tensor-core attention kernels are bf16
+    if (attention_tc_eligible(bf_only, C, H) && launch_attention_fwd_tc(L, qkv, y, lse, B, T, C, H)) return;
+    if (attention_mma_eligible(bf_only, C, H)) {
         launch_attention_fwd_mma(L, qkv, y, lse, B, T, C, H);
         return;
     }
@@ -934,10 +990,11 @@ void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const voi
                           const float* lse, const void* dy, void* dqkv, int B, int T, int C,
                           int H, float* scratch) {
     if (L.dry) return;
-    if (attention_tc_eligible(bf16, C, H) &&
+    const bool bf_only = bf16 && !L.f16;
+    if (attention_tc_eligible(bf_only, C, H) &&
         launch_attention_bwd_tc(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch))
         return;
-    if (attention_mma_eligible(bf16, C, H)) {
+    if (attention_mma_eligible(bf_only, C, H)) {
         launch_attention_bwd_mma(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch);
         return;
     }

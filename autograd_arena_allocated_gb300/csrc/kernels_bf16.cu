@@ -264,7 +264,7 @@ size_t ln_bwd_bf16_scratch_floats(int C) { return (size_t)LN_BWD_MAX_BLOCKS * 2 
 
 bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const void* b, void* y,
                         float* mean, float* rstd, int M, int C) {
-    if (C % 8 || C > 1024) return false;
+    if (L.f16 || C % 8 || C > 1024) return false;
     if (L.dry) return true;
     const unsigned grid = (unsigned)((M + LNV_WARPS - 1) / LNV_WARPS);
     const int nv = (C / 8 + 31) / 32;
@@ -279,7 +279,7 @@ bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const voi
 bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
                         const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
                         int C, bool accumulate, float* scratch, bool acc_params) {
-    if (C % 8 || C > 1024) return false;
+    if (L.f16 || C % 8 || C > 1024) return false;
     if (L.dry) return true;
     const int nv = (C / 8 + 31) / 32;
     const size_t smem = (size_t)(LNV_WARPS * 2) * C * sizeof(float);
@@ -415,7 +415,7 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
 
 bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
                       int V, int ld, float dscale, const float* scale_dev) {
-    if (ld % 8 || ((uintptr_t)logits & 15) || ld < 2048) return false;
+    if (L.f16 || ld % 8 || ((uintptr_t)logits & 15) || ld < 2048) return false;
     if (L.dry) return true;
     L.count();
     k_xent_bf16<<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
@@ -472,7 +472,7 @@ k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part
 }
 
 bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part) {
-    if (N % 8 || ((uintptr_t)x & 15) || ((uintptr_t)part & 15)) return false;
+    if (L.f16 || N % 8 || ((uintptr_t)x & 15) || ((uintptr_t)part & 15)) return false;
     if (L.dry) return true;
     dim3 grid((N + 255) / 256, (M + CS_ROWS - 1) / CS_ROWS);
     L.count();
@@ -494,6 +494,17 @@ __device__ __forceinline__ void load8(const T* p, float* f);
 template <>
 __device__ __forceinline__ void load8<bf16>(const bf16* p, float* f) {
     unpack8(*reinterpret_cast<const uint4*>(p), f);
+}
+template <>
+__device__ __forceinline__ void load8<__half>(const __half* p, float* f) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
 }
 template <>
 __device__ __forceinline__ void load8<float>(const float* p, float* f) {
@@ -596,7 +607,10 @@ bool launch_embed_chunks(const Launch& L, bool is_bf16, const void* dx, const in
     float* last = scratch + (size_t)nchunk * C;
     const int threads = ((C / 8 + 31) / 32) * 32;
     L.count();
-    if (is_bf16)
+    if (is_bf16 && L.f16)
+        k_embed_chunks<__half><<<nchunk, threads, 0, L.stream>>>((const __half*)dx, keys, vals, M, C, V,
+                                                                 dwte, first, last);
+    else if (is_bf16)
         k_embed_chunks<bf16><<<nchunk, threads, 0, L.stream>>>((const bf16*)dx, keys, vals, M, C, V,
                                                                dwte, first, last);
     else

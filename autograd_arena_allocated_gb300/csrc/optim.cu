@@ -66,9 +66,28 @@ __global__ void k_grad_sq_final(const double* __restrict__ part, int nblk, float
     stats[1] = ok ? 0.0f : 1.0f;
 }
 
-// AdamW on g * k; the whole update is skipped when stats[1] != 0
+__device__ __forceinline__ void st_low4(__nv_bfloat16* p, size_t i, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p)[i] = packed;
+}
+__device__ __forceinline__ void st_low4(__half* p, size_t i, float4 v) {
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p)[i] = packed;
+}
+__device__ __forceinline__ void st_low(__nv_bfloat16* p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void st_low(__half* p, size_t i, float v) { p[i] = __float2half_rn(v); }
+
+// AdamW on g * k; the whole update is skipped when stats[1] != 0.  LT: the
+// 16-bit type of the parameter copy (bf16 or half)
+template <typename LT>
 __global__ void __launch_bounds__(256)
-k_adamw_ex(float* __restrict__ p, __nv_bfloat16* __restrict__ lowp, const float* __restrict__ g,
+k_adamw_ex(float* __restrict__ p, LT* __restrict__ lowp, const float* __restrict__ g,
            float* __restrict__ m, float* __restrict__ v, size_t n, float lr, float b1, float b2, float eps, float wd,
            const int* __restrict__ step, const float* __restrict__ stats, float max_norm,
            const float* __restrict__ scale_dev) {
@@ -98,14 +117,7 @@ k_adamw_ex(float* __restrict__ p, __nv_bfloat16* __restrict__ lowp, const float*
         reinterpret_cast<float4*>(p)[i] = pp;
         reinterpret_cast<float4*>(m)[i] = mm;
         reinterpret_cast<float4*>(v)[i] = vv;
-        if (lowp) {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(pp.z, pp.w);
-            uint2 packed;
-            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-            reinterpret_cast<uint2*>(lowp)[i] = packed;
-        }
+        if (lowp) st_low4(lowp, i, pp);
     }
     for (size_t i = n4 * 4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const float gi = g[i] * k;
@@ -115,7 +127,7 @@ k_adamw_ex(float* __restrict__ p, __nv_bfloat16* __restrict__ lowp, const float*
         v[i] = vi;
         const float pi = p[i] - lr * ((mi / c1) / (sqrtf(vi / c2) + eps) + wd * p[i]);
         p[i] = pi;
-        if (lowp) lowp[i] = __float2bfloat16_rn(pi);
+        if (lowp) st_low(lowp, i, pi);
     }
 }
 
@@ -151,7 +163,7 @@ void launch_grad_stats(const Launch& L, const float* g, size_t n, const float* s
     k_grad_sq_final<<<1, 32, 0, L.stream>>>(scratch, G, stats);
 }
 
-void launch_adamw_ex(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g, float* m, float* v,
+void launch_adamw_ex(const Launch& L, float* master, void* lowp, const float* g, float* m, float* v,
                      size_t n, float lr, float b1, float b2, float eps, float wd, int* step, const float* stats,
                      float max_norm, const float* scale_dev) {
     if (L.dry) return;
@@ -159,8 +171,12 @@ void launch_adamw_ex(const Launch& L, float* master, __nv_bfloat16* lowp, const 
         const long long want = (long long)((n / 4 + 255) / 256);
         const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)L.num_sms * 8));
         L.count();
-        k_adamw_ex<<<grid, 256, 0, L.stream>>>(master, lowp, g, m, v, n, lr, b1, b2, eps, wd, step, stats, max_norm,
-                                               scale_dev);
+        if (L.f16)
+            k_adamw_ex<<<grid, 256, 0, L.stream>>>(master, (__half*)lowp, g, m, v, n, lr, b1, b2, eps, wd, step,
+                                                   stats, max_norm, scale_dev);
+        else
+            k_adamw_ex<<<grid, 256, 0, L.stream>>>(master, (__nv_bfloat16*)lowp, g, m, v, n, lr, b1, b2, eps, wd,
+                                                   step, stats, max_norm, scale_dev);
     }
     L.count();
     k_step_advance<<<1, 1, 0, L.stream>>>(step, stats);

@@ -191,6 +191,14 @@ static Launch launch_of(tt_ctx* c) {
     L.dry = c->dry;
     L.gemm_backend = c->gemm_backend;
     L.num_sms = c->num_sms;
+    L.f16 = c->has_model && c->cfg.dtype == TT_FP16;
+    return L;
+}
+
+// the op-level calls name their own dtype (never TT_FP16), whatever the model
+static Launch op_launch(tt_ctx* c) {
+    Launch L = launch_of(c);
+    L.f16 = false;
     return L;
 }
 
@@ -209,7 +217,7 @@ static void* arena_alloc(tt_ctx* c, size_t bytes) {
     return c->dry ? (void*)(uintptr_t)(0x100000ull + at) : (void*)(c->arena + at);
 }
 
-static size_t esize(tt_dtype d) { return d == TT_BF16 ? 2 : 4; }
+static size_t esize(tt_dtype d) { return d == TT_FP32 ? 4 : 2; }
 
 static int new_tensor(tt_ctx* c, long long rows, long long cols, size_t elem) {
     TapeTensor t;
@@ -252,7 +260,7 @@ static bool run_gemm(tt_ctx* c, const GemmArgs& g, int kind) {
 static int op_embed(tt_ctx* c, const void* wte, const void* wpe, float* dwte, float* dwpe,
                     const int32_t* tok, int B, int T) {
     const tt_gpt2_config& m = c->cfg;
-    const bool bf = m.dtype == TT_BF16;
+    const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     int out = new_tensor(c, (long long)B * T, m.C, esize(m.dtype));
     ProfScope ps(c, PK_EMBED_FWD, 0.0, 3.0 * B * T * m.C * esize(m.dtype) + 4.0 * B * T);
     if (!c->oom) launch_embed_fwd(launch_of(c), bf, wte, wpe, tok, c->tensors[out].data, B, T, m.C, m.V);
@@ -272,7 +280,7 @@ static int op_embed(tt_ctx* c, const void* wte, const void* wpe, float* dwte, fl
 
 static int op_layernorm(tt_ctx* c, int x, const void* w, const void* b, float* dw, float* db) {
     const tt_gpt2_config& m = c->cfg;
-    const bool bf = m.dtype == TT_BF16;
+    const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     const int M = (int)c->tensors[x].rows, C = m.C;
     int out = new_tensor(c, M, C, esize(m.dtype));
     float* mean = (float*)arena_alloc(c, (size_t)M * 4);
@@ -295,7 +303,7 @@ static int op_layernorm(tt_ctx* c, int x, const void* w, const void* b, float* d
 static int op_linear(tt_ctx* c, int x, const void* W, const void* b, float* dW, float* db, int N,
                      int res, bool gelu, int b_rows = 0, int n_store = 0) {
     const tt_gpt2_config& m = c->cfg;
-    const bool bf = m.dtype == TT_BF16;
+    const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     const size_t es = esize(m.dtype);
     const int M = (int)c->tensors[x].rows, K = (int)c->tensors[x].cols;
     int out = new_tensor(c, M, N, es);
@@ -307,6 +315,7 @@ static int op_linear(tt_ctx* c, int x, const void* W, const void* b, float* dW, 
         g.M = M; g.N = N; g.K = K;
         g.b_rows = b_rows;
         g.in_bf16 = bf;
+        g.in_f16 = m.dtype == TT_FP16;
         g.D = c->tensors[out].data; g.ldd = N; g.d_f32 = !bf;
         g.n_store = n_store;
         g.epi = gelu ? EPI_GELU : EPI_STORE;
@@ -329,7 +338,7 @@ static int op_linear(tt_ctx* c, int x, const void* W, const void* b, float* dW, 
 
 static int op_attention(tt_ctx* c, int qkv, int B, int T) {
     const tt_gpt2_config& m = c->cfg;
-    const bool bf = m.dtype == TT_BF16;
+    const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     const int M = B * T;
     int out = new_tensor(c, M, m.C, esize(m.dtype));
     float* lse = (float*)arena_alloc(c, (size_t)B * m.H * T * 4);
@@ -353,7 +362,7 @@ static int op_attention(tt_ctx* c, int qkv, int B, int T) {
 // gradient in the same pass, so the logits tensor's gradient is its own buffer.
 static void op_xent(tt_ctx* c, int z, const int32_t* targets, int V) {
     const tt_gpt2_config& m = c->cfg;
-    const bool bf = m.dtype == TT_BF16;
+    const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     const int M = (int)c->tensors[z].rows, ld = (int)c->tensors[z].cols;
     c->row_loss_dev = (float*)arena_alloc(c, (size_t)M * 4);
     c->loss_dev = (float*)arena_alloc(c, 4);
@@ -386,7 +395,7 @@ static void* grad_for_write(tt_ctx* c, int t, bool* accumulate) {
 
 static tt_status backward_record(tt_ctx* c, const Record& r) {
     const tt_gpt2_config& m = c->cfg;
-    const bool bf = m.dtype == TT_BF16;
+    const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     Launch L = launch_of(c);
     switch (r.kind) {
     case R_XENT:
@@ -417,6 +426,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
                 g.M = r.M; g.N = r.K; g.K = r.N;
                 g.k_valid = r.b_rows ? r.b_rows : 0;  // tied head: rows of wte beyond V are zero
                 g.in_bf16 = bf;
+                g.in_f16 = m.dtype == TT_FP16;
                 g.D = dx; g.ldd = r.K; g.d_f32 = !bf;
                 g.accumulate = acc;
                 if (through_gelu) { g.epi = EPI_DGELU; g.aux = prod->pre; }
@@ -434,6 +444,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
             g.a_rows = g.M;
             g.N = r.K; g.K = r.M;
             g.in_bf16 = bf;
+            g.in_f16 = m.dtype == TT_FP16;
             g.D = r.dW; g.ldd = r.K; g.d_f32 = true;
             g.accumulate = accW;
             if (!c->oom && !run_gemm(c, g, PK_GEMM_DW)) return fail(c, TT_ERR_CUDA, "linear dW GEMM failed");
@@ -516,7 +527,7 @@ static tt_status tape_backward(tt_ctx* c) {
 static bool cfg_ok(const tt_gpt2_config* m) {
     if (!m || m->L < 0 || m->C <= 0 || m->H <= 0 || m->V <= 1 || m->maxT <= 0) return false;
     if (m->C % m->H || m->C % 64 || m->C > 1024 || m->V >= 65535 * 16) return false;
-    if (m->dtype != TT_FP32 && m->dtype != TT_BF16) return false;
+    if (m->dtype != TT_FP32 && m->dtype != TT_BF16 && m->dtype != TT_FP16) return false;
     const int hd = m->C / m->H;
     if (hd != 16 && hd != 32 && hd != 64) return false;
     if (m->dtype == TT_BF16 && hd != 64) return false;
@@ -1097,7 +1108,8 @@ tt_status tt_gpt2_eval(tt_ctx* c, const void* params, const int32_t* tokens, con
 }
 
 size_t tt_gpt2_generate_arena_bytes(const tt_gpt2_config* m, int B, int T_prompt, int n_new) {
-    if (!cfg_ok(m) || B <= 0 || T_prompt <= 0 || n_new < 0 || T_prompt + n_new > m->maxT) return 0;
+    if (!cfg_ok(m) || m->dtype == TT_FP16 || B <= 0 || T_prompt <= 0 || n_new < 0 || T_prompt + n_new > m->maxT)
+        return 0;
     tt_ctx c;
     c.cap = (size_t)-1 / 2;
     c.cfg = *m;
@@ -1124,6 +1136,7 @@ tt_status tt_gpt2_generate(tt_ctx* c, const void* params, const int32_t* prompt,
     if (!live(c)) return TT_ERR_STALE;
     if (c->capturing) return fail(c, TT_ERR_STATE, "GPT-2 calls cannot be recorded");
     if (!c->has_model) return fail(c, TT_ERR_STATE, "tt_ctx_set_model was not called");
+    if (c->cfg.dtype == TT_FP16) return fail(c, TT_ERR_ARG, "generation takes a TT_FP32 or TT_BF16 model");
     if (!params || !prompt || !out) return fail(c, TT_ERR_ARG, "NULL parameter, prompt or output pointer");
     if (B <= 0 || T_prompt <= 0 || n_new < 0 || T_prompt + n_new > c->cfg.maxT)
         return fail(c, TT_ERR_ARG, "bad generation shape B=%d prompt=%d new=%d (maxT=%d)", B, T_prompt, n_new,
@@ -1188,9 +1201,9 @@ tt_status tt_adamw(tt_ctx* c, float* master, void* params_lowp, const float* gra
     if (((uintptr_t)master | (uintptr_t)grads | (uintptr_t)m | (uintptr_t)v) & 15)
         return fail(c, TT_ERR_ARG, "adamw: pointers must be 16-byte aligned");
     if (params_lowp && ((uintptr_t)params_lowp & 7))
-        return fail(c, TT_ERR_ARG, "adamw: bf16 copy must be 8-byte aligned");
+        return fail(c, TT_ERR_ARG, "adamw: 16-bit copy must be 8-byte aligned");
     ProfScope ps(c, PK_ADAMW, 0.0, (double)n * (28.0 + (params_lowp ? 2.0 : 0.0)));
-    launch_adamw(launch_of(c), master, (__nv_bfloat16*)params_lowp, grads, m, v, n, lr, beta1, beta2,
+    launch_adamw(launch_of(c), master, params_lowp, grads, m, v, n, lr, beta1, beta2,
                  eps, weight_decay, step);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "adamw: %s", cudaGetErrorString(e));
@@ -1202,6 +1215,16 @@ tt_status tt_cast_f32_to_bf16(tt_ctx* c, const float* src, void* dst, size_t n) 
     if (!live(c)) return TT_ERR_STALE;
     if (!src || !dst) return fail(c, TT_ERR_ARG, "cast: NULL pointer");
     launch_cast_bf16(launch_of(c), src, (__nv_bfloat16*)dst, n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "cast: %s", cudaGetErrorString(e));
+    return TT_OK;
+}
+
+tt_status tt_cast_f32_to_f16(tt_ctx* c, const float* src, void* dst, size_t n) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    if (!src || !dst) return fail(c, TT_ERR_ARG, "cast: NULL pointer");
+    launch_cast_f16(launch_of(c), src, (__half*)dst, n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "cast: %s", cudaGetErrorString(e));
     return TT_OK;
@@ -1273,7 +1296,7 @@ tt_status tt_op_linear_bwd_dw(tt_ctx* c, tt_dtype dtype, const void* dy, const v
     if (db) {
         size_t mark = c->off;
         float* s = (float*)arena_alloc(c, colsum_scratch_floats(M, N) * 4);
-        if (!c->oom) launch_colsum(launch_of(c), bf, dy, M, N, db, s);
+        if (!c->oom) launch_colsum(op_launch(c), bf, dy, M, N, db, s);
         c->off = mark;
     }
     return op_epilogue(c, "linear_bwd_dw");
@@ -1288,7 +1311,7 @@ tt_status tt_op_attention_fwd(tt_ctx* c, tt_dtype dtype, const void* qkv, void* 
     {
         const double pairs = (double)B * H * T * (T + 1) / 2.0;
         ProfScope ps(c, PK_ATTN_FWD, 4.0 * pairs * hd, 4.0 * B * T * C * (dtype == TT_BF16 ? 2 : 4));
-        launch_attention_fwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, B, T, C, H);
+        launch_attention_fwd(op_launch(c), dtype == TT_BF16, qkv, y, lse, B, T, C, H);
     }
     return op_epilogue(c, "attention_fwd");
 }
@@ -1307,7 +1330,7 @@ tt_status tt_op_attention_bwd(tt_ctx* c, tt_dtype dtype, const void* qkv, const 
     if (!c->oom) {
         const double pairs = (double)B * H * T * (T + 1) / 2.0;
         ProfScope ps(c, PK_ATTN_BWD, 10.0 * pairs * hd, 8.0 * B * T * C * (dtype == TT_BF16 ? 2 : 4));
-        launch_attention_bwd(launch_of(c), dtype == TT_BF16, qkv, y, lse, dy, dqkv, B, T, C, H, s);
+        launch_attention_bwd(op_launch(c), dtype == TT_BF16, qkv, y, lse, dy, dqkv, B, T, C, H, s);
     }
     c->off = mark;
     return op_epilogue(c, "attention_bwd");
@@ -1320,7 +1343,7 @@ tt_status tt_op_layernorm_fwd(tt_ctx* c, tt_dtype dtype, const void* x, const vo
         return fail(c, TT_ERR_ARG, "layernorm_fwd: bad arguments");
     {
         ProfScope ps(c, PK_LN_FWD, 0.0, 2.0 * M * C * (dtype == TT_BF16 ? 2 : 4) + 8.0 * M);
-        launch_layernorm_fwd(launch_of(c), dtype == TT_BF16, x, w, b, y, mean, rstd, M, C);
+        launch_layernorm_fwd(op_launch(c), dtype == TT_BF16, x, w, b, y, mean, rstd, M, C);
     }
     return op_epilogue(c, "layernorm_fwd");
 }
@@ -1336,7 +1359,7 @@ tt_status tt_op_layernorm_bwd(tt_ctx* c, tt_dtype dtype, const void* x, const vo
     float* s = (float*)arena_alloc(c, layernorm_bwd_scratch_floats(M, C) * 4);
     if (!c->oom) {
         ProfScope ps(c, PK_LN_BWD, 0.0, (accumulate ? 4.0 : 3.0) * M * C * (dtype == TT_BF16 ? 2 : 4) + 8.0 * M);
-        launch_layernorm_bwd(launch_of(c), dtype == TT_BF16, x, w, mean, rstd, dy, dx, dw, db, M, C,
+        launch_layernorm_bwd(op_launch(c), dtype == TT_BF16, x, w, mean, rstd, dy, dx, dw, db, M, C,
                              accumulate != 0, s);
     }
     c->off = mark;
@@ -1350,7 +1373,7 @@ tt_status tt_op_xent(tt_ctx* c, tt_dtype dtype, void* logits, const int32_t* tar
         return fail(c, TT_ERR_ARG, "xent: bad arguments");
     {
         ProfScope ps(c, PK_XENT, 0.0, 2.0 * M * ld * (dtype == TT_BF16 ? 2 : 4) + 8.0 * M);
-        launch_xent(launch_of(c), dtype == TT_BF16, logits, targets, row_loss, mean_loss, M, V, ld, dscale);
+        launch_xent(op_launch(c), dtype == TT_BF16, logits, targets, row_loss, mean_loss, M, V, ld, dscale);
     }
     return op_epilogue(c, "xent");
 }
@@ -1360,7 +1383,7 @@ tt_status tt_op_embed_fwd(tt_ctx* c, tt_dtype dtype, const void* wte, const void
     TT_OP_PROLOGUE();
     if (!wte || !wpe || !tokens || !x || B <= 0 || T <= 0 || C <= 0 || V <= 0)
         return fail(c, TT_ERR_ARG, "embed_fwd: bad arguments");
-    launch_embed_fwd(launch_of(c), dtype == TT_BF16, wte, wpe, tokens, x, B, T, C, V);
+    launch_embed_fwd(op_launch(c), dtype == TT_BF16, wte, wpe, tokens, x, B, T, C, V);
     return op_epilogue(c, "embed_fwd");
 }
 
@@ -1375,7 +1398,7 @@ tt_status tt_op_embed_bwd(tt_ctx* c, tt_dtype dtype, const void* dx, const int32
     void* s = arena_alloc(c, embed_bwd_scratch_bytes(B * T, C));
     if (!c->oom) {
         ProfScope ps(c, PK_EMBED_BWD, 0.0, (double)B * T * C * ((dtype == TT_BF16 ? 2 : 4) + 8.0) + 4.0 * maxT * C);
-        launch_embed_bwd(launch_of(c), dtype == TT_BF16, dx, tokens, dwte, dwpe, B, T, C, V, maxT, s);
+        launch_embed_bwd(op_launch(c), dtype == TT_BF16, dx, tokens, dwte, dwpe, B, T, C, V, maxT, s);
     }
     c->off = mark;
     return op_epilogue(c, "embed_bwd");
@@ -1803,7 +1826,7 @@ tt_status tt_adamw_ex(tt_ctx* c, float* master, void* params_lowp, const float* 
     if (max_norm > 0.0f && !stats) return fail(c, TT_ERR_ARG, "adamw_ex: clipping needs the gradient statistics");
     if (((uintptr_t)master | (uintptr_t)grads | (uintptr_t)m | (uintptr_t)v) & 15)
         return fail(c, TT_ERR_ARG, "adamw_ex: buffers must be 16-byte aligned");
-    launch_adamw_ex(launch_of(c), master, (__nv_bfloat16*)params_lowp, grads, m, v, n, lr, beta1, beta2, eps,
+    launch_adamw_ex(launch_of(c), master, params_lowp, grads, m, v, n, lr, beta1, beta2, eps,
                     weight_decay, step, stats, max_norm, loss_scale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(c, TT_ERR_CUDA, "adamw_ex: %s", cudaGetErrorString(e));

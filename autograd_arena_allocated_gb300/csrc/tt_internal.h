@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 #include <stddef.h>
 
@@ -36,6 +37,7 @@ struct Launch {
     int gemm_backend = 0;  // 0 auto, 1 SIMT only
     int num_sms = 148;
     bool pdl = false;      // decode kernels: programmatic dependent launch
+    bool f16 = false;      // 16-bit storage is IEEE half, not bf16 (the model's TT_FP16 mode)
     void count() const { if (launches) ++*launches; }
 };
 
@@ -61,6 +63,7 @@ struct GemmArgs {
     int b_rows = 0;          // valid extent of B's MN dimension (rows beyond read as 0); 0 = N
     int k_valid = 0;         // valid extent of K (beyond reads as 0); 0 = K
     bool in_bf16 = true;     // operand storage: bf16 or fp32
+    bool in_f16 = false;     // with in_bf16: the 16-bit storage is IEEE half (SIMT kernel only)
     void* D = nullptr; long long ldd = 0; bool d_f32 = false;
     int n_store = 0;         // columns >= n_store are not stored; 0 = N
     int epi = EPI_STORE;
@@ -105,16 +108,17 @@ size_t colsum_scratch_floats(int M, int N);
 void launch_colsum(const Launch& L, bool bf16, const void* x, int M, int N, float* out,
                    float* scratch, bool acc = false);
 
-void launch_adamw(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g,
+void launch_adamw(const Launch& L, float* master, void* lowp, const float* g,
                   float* m, float* v, size_t n, float lr, float b1, float b2, float eps,
                   float wd, int step);
 void launch_cast_bf16(const Launch& L, const float* src, __nv_bfloat16* dst, size_t n);
+void launch_cast_f16(const Launch& L, const float* src, __half* dst, size_t n);
 // global gradient statistics: stats[0] = ||g / scale||_2, stats[1] = 1 if not finite
 size_t grad_stats_scratch_doubles(const Launch& L);
 void launch_grad_stats(const Launch& L, const float* g, size_t n, const float* scale_dev, float* stats,
                        double* scratch);
 // AdamW whose gradient is g / scale * clip, skipped when stats[1] != 0; t = *step + 1
-void launch_adamw_ex(const Launch& L, float* master, __nv_bfloat16* lowp, const float* g, float* m, float* v,
+void launch_adamw_ex(const Launch& L, float* master, void* lowp, const float* g, float* m, float* v,
                      size_t n, float lr, float b1, float b2, float eps, float wd, int* step, const float* stats,
                      float max_norm, const float* scale_dev);
 void launch_loss_scale_update(const Launch& L, float* scale, int* clean, const float* stats, int window,

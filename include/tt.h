@@ -51,14 +51,20 @@ typedef enum {
     TT_ERR_STATE = -8       /* call out of order (e.g. a step before tt_ctx_set_model) */
 } tt_status;
 
-typedef enum { TT_FP32 = 0, TT_BF16 = 1 } tt_dtype;
+typedef enum { TT_FP32 = 0, TT_BF16 = 1, TT_FP16 = 2 } tt_dtype;
 
 /* GPT-2 architecture.  V is the real vocabulary; the device pads the LM-head
  * width internally to a multiple of 128 (50257 -> 50304), the pad logits
  * being masked to -inf.  Requirements: C % H == 0, C % 64 == 0, C <= 1024,
  * maxT >= 1.  dtype TT_FP32: every tensor fp32; TT_BF16: bf16 weights,
  * activations and activation gradients with fp32 accumulation, fp32 LayerNorm
- * statistics, softmax, loss and parameter gradients (needs C / H == 64). */
+ * statistics, softmax, loss and parameter gradients (needs C / H == 64).
+ * TT_FP16: the same split with IEEE half storage (the mixed precision of the
+ * dl-scratch page, 3.4): a 10-bit mantissa but a 5-bit exponent, so small
+ * activation gradients underflow unless the loss is scaled
+ * (tt_gpt2_step_ex's loss_scale).  The half step runs on the SIMT kernels
+ * (the tensor-core kernels are bf16); the op-level calls, tt_gpt2_eval and
+ * tt_gpt2_generate take TT_FP32 and TT_BF16 only. */
 typedef struct {
     int L, C, H, V, maxT;
     tt_dtype dtype;
@@ -149,7 +155,7 @@ size_t tt_gpt2_arena_bytes(const tt_gpt2_config* cfg, int B, int T);
  * (tinytorch 三.6-三.7; the tape records every op of the forward and is
  * replayed in reverse record order, a reverse topological order).
  *   params  device, flat (tt_gpt2_num_params elements), fp32 in TT_FP32 mode,
- *           bf16 in TT_BF16 mode.  Read only.
+ *           bf16 in TT_BF16 mode, half in TT_FP16 mode.  Read only.
  *   grads   device fp32, flat, same layout.  OVERWRITTEN with
  *           d(mean loss)/d(params) (no separate zeroing is needed).
  *   tokens, targets  int32 [B*T] row-major (b, t); device OR host memory (host
@@ -237,8 +243,9 @@ tt_status tt_loss_scale_update(tt_ctx* ctx, float* loss_scale, int* clean_steps,
  *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
  *   master -= lr * ( m/(1-b1^step) / (sqrt(v/(1-b2^step)) + eps) + wd * master )
  * master, grads, m, v: device fp32 [n] (m, v start at zero).  params_lowp:
- * device bf16 [n] copy written from the updated master (round to nearest
- * even), or NULL (TT_FP32 mode trains the master directly).  step >= 1.
+ * device 16-bit [n] copy written from the updated master (round to nearest
+ * even): half when the context's model (tt_ctx_set_model) is TT_FP16, bf16
+ * otherwise; or NULL (TT_FP32 mode trains the master directly).  step >= 1.
  * Every element decays.  Pointers must be 16-byte aligned. */
 tt_status tt_adamw(tt_ctx* ctx, float* master, void* params_lowp, const float* grads,
                    float* m, float* v, size_t n, float lr, float beta1, float beta2,
@@ -247,6 +254,10 @@ tt_status tt_adamw(tt_ctx* ctx, float* master, void* params_lowp, const float* g
 /* dst[i] = bf16(src[i]) (round to nearest even); device pointers, n elements.
  * Used to make the bf16 parameter copy of a freshly initialized master. */
 tt_status tt_cast_f32_to_bf16(tt_ctx* ctx, const float* src, void* dst, size_t n);
+
+/* dst[i] = half(src[i]) (round to nearest even; beyond 65504 it is +-inf);
+ * device pointers, n elements.  The half copy of the master for TT_FP16. */
+tt_status tt_cast_f32_to_f16(tt_ctx* ctx, const float* src, void* dst, size_t n);
 
 /* ------------------------------------------------------------- inference */
 

@@ -128,6 +128,14 @@ def bf16_values(x) -> np.ndarray:
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def f16_values(x) -> np.ndarray:
+    """Nearest IEEE half value of each float32 (ties to even; beyond the
+    largest half, 65504, the value becomes +-inf; below the smallest
+    subnormal, 2^-24, it rounds to zero or 2^-24), as float64."""
+    with np.errstate(over="ignore"):
+        return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float64)
+
+
 # ---------------------------------------------------------------- ops
 def linear_fwd(x, W, b=None):
     x, W = f64(x), f64(W)

@@ -46,6 +46,10 @@ class Run:
             self.lowp = torch.empty(self.n, device=DEV, dtype=torch.bfloat16)
             ctx.cast_bf16(self.master, self.lowp)
             self.params = self.lowp
+        elif dtype == "fp16":
+            self.lowp = torch.empty(self.n, device=DEV, dtype=torch.float16)
+            ctx.cast_f16(self.master, self.lowp)
+            self.params = self.lowp
         else:
             self.lowp = None
             self.params = self.master
@@ -62,7 +66,11 @@ class Run:
 
 
 def oracle_params(oracle, p, dtype):
-    return oracle.bf16_values(p) if dtype == "bf16" else p.astype(np.float64)
+    if dtype == "bf16":
+        return oracle.bf16_values(p)
+    if dtype == "fp16":
+        return oracle.f16_values(p)
+    return p.astype(np.float64)
 
 
 def tensor_slices(cfg, L):
