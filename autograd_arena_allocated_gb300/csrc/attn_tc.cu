@@ -125,9 +125,11 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     uint32_t* tmem_holder = (uint32_t*)(bars + 13);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    const int nqt = gridDim.x;
-    const int qt = nqt - 1 - (int)blockIdx.x;  // longest rows first
-    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    // grid (B*H, tiles): every (batch, head) of the longest tiles is scheduled
+    // before any of the next length, so the last wave holds the shortest work
+    const int nqt = gridDim.y;
+    const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first
+    const int b = blockIdx.x / H, h = blockIdx.x % H;
     const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -391,9 +393,9 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint32_t* tmem_holder = (uint32_t*)(bars + 19);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    const int nqt = gridDim.x;
-    const int qt = nqt - 1 - (int)blockIdx.x;
-    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    const int nqt = gridDim.y;
+    const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first
+    const int b = blockIdx.x / H, h = blockIdx.x % H;
     const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -634,8 +636,8 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint32_t* tmem_holder = (uint32_t*)(bars + 10);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    const int kt = (int)blockIdx.x;  // key tile; low tiles see the most query blocks
-    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    const int kt = (int)blockIdx.y;  // key tile; low tiles see the most query blocks
+    const int b = blockIdx.x / H, h = blockIdx.x % H;
     const int row0 = b * T;
     const int nqb = (T + BN - 1) / BN;
     const int j0 = 2 * kt;
@@ -864,7 +866,7 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
     if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
     if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
     if (!attn_set_smem()) return false;
-    dim3 grid((T + fa5::BQ - 1) / fa5::BQ, B * H);
+    dim3 grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C,
                                                                      H, L.flags);
@@ -882,7 +884,7 @@ bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, co
     if (!tc::make_tmap_bf16(&to64, dy, (long long)C, (long long)B * T, (long long)C, fa5::D, fa5::BN))
         return false;
     if (!attn_set_smem()) return false;
-    dim3 grid((T + fa5::BQ - 1) / fa5::BQ, B * H);
+    dim3 grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_bwd_dq_tc<<<grid, fa5::THREADS, fa5::Q_SMEM, L.stream>>>(
         tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);

@@ -720,6 +720,36 @@ __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M,
     *d = accumulate ? *d + s : s;
 }
 
+// The same, four consecutive outputs per thread (16-byte loads and stores;
+// needs N, n_store and ldd multiples of 4 and 16-byte aligned ws and D), the
+// loads of up to eight splits in flight before their adds, in split order.
+__global__ void k_splitk_reduce4(const float* __restrict__ ws, int splits, int M, int N, int n_store,
+                                 float* __restrict__ D, long long ldd, int accumulate) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int nq = n_store >> 2;
+    if (i >= (long long)M * nq) return;
+    const int m = (int)(i / nq), n = 4 * (int)(i % nq);
+    const long long plane = (long long)M * N;
+    const float4* src = reinterpret_cast<const float4*>(ws + (long long)m * N + n);
+    const long long step = plane >> 2;  // one split, in float4 units
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int k0 = 0; k0 < splits; k0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+            if (k0 + u < splits) v[u] = src[(k0 + u) * step];
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+            if (k0 + u < splits) { s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w; }
+    }
+    float4* d = reinterpret_cast<float4*>(D + (long long)m * ldd + n);
+    if (accumulate) {
+        const float4 o = *d;
+        s.x = o.x + s.x; s.y = o.y + s.y; s.z = o.z + s.z; s.w = o.w + s.w;
+    }
+    *d = s;
+}
+
 // ------------------------------------------------------------------ host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1016,11 +1046,18 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
 #undef TC
     if (!launched) return false;
     if (pl.p.splits > 1) {
-        long long total = (long long)g.M * pl.p.n_store;
+        const bool vec = (g.N % 4) == 0 && (pl.p.n_store % 4) == 0 && (g.ldd % 4) == 0 &&
+                         ((uintptr_t)workspace & 15) == 0 && ((uintptr_t)g.D & 15) == 0;
         L.count();
-        tc::k_splitk_reduce<<<(unsigned)((total + 255) / 256), 256, 0, L.stream>>>(
-            workspace, pl.p.splits, g.M, g.N, pl.p.n_store, (float*)g.D, g.ldd,
-            g.accumulate ? 1 : 0);
+        if (vec) {
+            const long long total = (long long)g.M * (pl.p.n_store / 4);
+            tc::k_splitk_reduce4<<<(unsigned)((total + 255) / 256), 256, 0, L.stream>>>(
+                workspace, pl.p.splits, g.M, g.N, pl.p.n_store, (float*)g.D, g.ldd, g.accumulate ? 1 : 0);
+        } else {
+            const long long total = (long long)g.M * pl.p.n_store;
+            tc::k_splitk_reduce<<<(unsigned)((total + 255) / 256), 256, 0, L.stream>>>(
+                workspace, pl.p.splits, g.M, g.N, pl.p.n_store, (float*)g.D, g.ldd, g.accumulate ? 1 : 0);
+        }
     }
     return true;
 }

@@ -197,34 +197,38 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
 }
 
 // out[c] = sum_g part[g][c] over the G partial rows, in a fixed order: block
-// = 32 columns x 8 warps; warp w adds rows w, w+8, ...; the 8 warp sums are
-// then added in warp order.  (Used for the LayerNorm dw/db partials, with
-// out_a taking columns [0, C) and out_b columns [C, 2C), and for bias sums.)
-__global__ void __launch_bounds__(256)
+// = 32 columns x SR_WARPS warps; warp w adds rows w, w+SR_WARPS, ... (eight
+// loads in flight); the warp sums are then added in warp order.  The G rows
+// are few (a few hundred at most), so the kernel is latency bound: many warps
+// keep the number of dependent load rounds per warp at one or two.  (Used for
+// the LayerNorm dw/db partials, with out_a taking columns [0, C) and out_b
+// columns [C, 2C), and for bias sums.)
+constexpr int SR_WARPS = 32;
+
+__global__ void __launch_bounds__(SR_WARPS * 32)
 k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* __restrict__ out_a,
            float* __restrict__ out_b, int acc) {
-    __shared__ float sm[8][33];
+    __shared__ float sm[SR_WARPS][33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
     float s = 0.0f;
     if (c < ncols) {
-        // rows warp, warp + 8, ... added in that order; eight loads in flight
         int g = warp;
-        for (; g + 56 < G; g += 64) {
+        for (; g + 7 * SR_WARPS < G; g += 8 * SR_WARPS) {
             float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; u++) v[u] = part[(long long)(g + 8 * u) * ncols + c];
+            for (int u = 0; u < 8; u++) v[u] = part[(long long)(g + SR_WARPS * u) * ncols + c];
 #pragma unroll
             for (int u = 0; u < 8; u++) s += v[u];
         }
-        for (; g < G; g += 8) s += part[(long long)g * ncols + c];
+        for (; g < G; g += SR_WARPS) s += part[(long long)g * ncols + c];
     }
     sm[warp][lane] = s;
     __syncthreads();
     if (warp == 0 && c < ncols) {
         float t = 0.0f;
 #pragma unroll
-        for (int w = 0; w < 8; w++) t += sm[w][lane];
+        for (int w = 0; w < SR_WARPS; w++) t += sm[w][lane];
         if (c < split) { if (out_a) out_a[c] = acc ? out_a[c] + t : t; }
         else if (out_b) out_b[c - split] = acc ? out_b[c - split] + t : t;
     }
@@ -234,7 +238,7 @@ void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int s
                      float* out_b, bool acc) {
     if (L.dry) return;
     L.count();
-    k_sum_rows<<<(ncols + 31) / 32, 256, 0, L.stream>>>(part, G, ncols, split, out_a, out_b, acc ? 1 : 0);
+    k_sum_rows<<<(ncols + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(part, G, ncols, split, out_a, out_b, acc ? 1 : 0);
 }
 
 constexpr int LN_BWD_MAX_BLOCKS = 1024;
@@ -301,7 +305,8 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     if (nv == 1) { LNB(1); } else if (nv == 2) { LNB(2); } else if (nv == 3) { LNB(3); } else { LNB(4); }
 #undef LNB
     L.count();
-    k_sum_rows<<<(2 * C + 31) / 32, 256, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db, acc_params ? 1 : 0);
+    k_sum_rows<<<(2 * C + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db,
+                                                                  acc_params ? 1 : 0);
     return true;
 }
 
