@@ -51,6 +51,17 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float SL2 = 0.125f * LOG2E;  // 1/sqrt(64), base-2 units
 
+// Forward grid: one dimension of B*H*ntiles CTAs, taken in bands of
+// FWD_BAND (batch, head) pairs.  Within a band the CTAs go out longest tile
+// first (every pair's last query tile, then every pair's next), so the short
+// tiles fill the gaps at the band's end while the next band starts, and the
+// keys and values of a band's pairs (256 KB a pair, read by all its tiles)
+// stay in L2 while it runs: DRAM reads stay at one pass over q, k and v.
+// (The backward kernels keep a two-dimensional grid, (B*H, tiles), heaviest
+// tiles of every pair first: for them the balance matters more than the
+// re-reads.)
+constexpr int FWD_BAND = 64;
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
@@ -125,11 +136,13 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     uint32_t* tmem_holder = (uint32_t*)(bars + 13);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    // grid (B*H, tiles): every (batch, head) of the longest tiles is scheduled
-    // before any of the next length, so the last wave holds the shortest work
-    const int nqt = gridDim.y;
-    const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first
-    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const int nqt = (T + BQ - 1) / BQ;
+    const int bh_total = (int)(gridDim.x / (unsigned)nqt);
+    const int hb0 = ((int)blockIdx.x / (FWD_BAND * nqt)) * FWD_BAND;
+    const int nb = min(FWD_BAND, bh_total - hb0);
+    const int j = (int)blockIdx.x - hb0 * nqt;
+    const int qt = nqt - 1 - j / nb;  // longest rows first within the band
+    const int b = (hb0 + j % nb) / H, h = (hb0 + j % nb) % H;
     const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,6 +406,8 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint32_t* tmem_holder = (uint32_t*)(bars + 19);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
+    // grid (B*H, tiles): every (batch, head) of the longest tiles is scheduled
+    // before any of the next length, so the last wave holds the shortest work
     const int nqt = gridDim.y;
     const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first
     const int b = blockIdx.x / H, h = blockIdx.x % H;
@@ -866,7 +881,7 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
     if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
     if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
     if (!attn_set_smem()) return false;
-    dim3 grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
+    const dim3 grid((unsigned)(B * H * ((T + fa5::BQ - 1) / fa5::BQ)));
     L.count();
     fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C,
                                                                      H, L.flags);

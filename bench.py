@@ -231,20 +231,20 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "0b0a063830509aa7",
+    "sources": "8d6bf29a4b768973",
     "bytes_per_launch_group": {
-        "gemm_fwd": 350654652,
-        "gemm_dx": 299767996,
-        "gemm_dw": 294899017,
-        "attn_fwd": 179051904,
-        "attn_bwd": 560950485,
-        "xent": 6543710208,
-        "colsum": 114280677,
-        "ln_fwd": 53976934,
-        "ln_bwd": 170638991,
-        "adamw": 3672039168,
-        "embed_fwd": 12726528,
-        "embed_bwd": 124944640,
+        "gemm_fwd": 347053834,
+        "gemm_dx": 323521567,
+        "gemm_dw": 312085708,
+        "attn_fwd": 178261803,
+        "attn_bwd": 852428757,
+        "xent": 6542916608,
+        "colsum": 114261515,
+        "ln_fwd": 53969746,
+        "ln_bwd": 170587310,
+        "adamw": 3672179456,
+        "embed_fwd": 12834816,
+        "embed_bwd": 124957440,
     },
 }
 
