@@ -788,7 +788,8 @@ def main():
 
     if rank == 0:
         stage("cpu baseline")
-        cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w)
+        # about ten seconds of oracle work on the host cores (512 tokens of the 124M model)
+        cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w, min(512, w.shape.maxT))
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
