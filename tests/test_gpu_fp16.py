@@ -83,6 +83,28 @@ def test_scaled_fp16_step_matches_oracle(ctx, oracle, reference):
     assert ctx.eval(run.params, _dev(tok), _dev(tgt), B, T) == loss
 
 
+def test_fp16_small_heads_and_accumulation(ctx, oracle):
+    """The tiny model (head dim 16) in half: two accumulated micro-batches
+    against the oracle's summed gradients, scaled by 2^10."""
+    w = synth.WORKLOADS["tiny_fp32"]
+    sh = w.shape
+    p, tok, tgt = make_inputs(sh, 4, w.T, w.tokens, jitter=0.05)
+    run = Run(ctx, sh, "fp16", p)
+    B, T = tok.shape
+    h = B // 2
+    scale = torch.tensor([1024.0], device=DEV)
+    ctx.reset()
+    la = ctx.step_ex(run.params, run.grads, _dev(tok[:h]), _dev(tgt[:h]), h, T, loss_scale=scale)
+    ctx.reset()
+    lb = ctx.step_ex(run.params, run.grads, _dev(tok[h:]), _dev(tgt[h:]), h, T, accumulate=True, loss_scale=scale)
+    po = oracle_params(oracle, p, "fp16")
+    ra, ga, _ = oracle.gpt2_step(sh, po, tok[:h], tgt[:h])
+    rb, gb, _ = oracle.gpt2_step(sh, po, tok[h:], tgt[h:])
+    assert abs(la - ra) <= LOSS_TOL * ra and abs(lb - rb) <= LOSS_TOL * rb
+    g = run.grads.cpu().numpy().astype(np.float64) / 1024.0
+    compare_grads(run.cfg, sh.L, g, ga + gb, GRAD_TOL, MIN_COS, label="fp16 tiny accumulated")
+
+
 def test_unscaled_fp16_gradients_underflow(ctx, oracle):
     """A larger batch (B T = 2048) makes the logit gradients p / (B T) about
     7e-6, subnormal in half, and the activation gradients below them a few
