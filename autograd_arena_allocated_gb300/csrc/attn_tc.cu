@@ -51,16 +51,14 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float SL2 = 0.125f * LOG2E;  // 1/sqrt(64), base-2 units
 
-// Forward grid: one dimension of B*H*ntiles CTAs, taken in bands of
-// FWD_BAND (batch, head) pairs.  Within a band the CTAs go out longest tile
-// first (every pair's last query tile, then every pair's next), so the short
-// tiles fill the gaps at the band's end while the next band starts, and the
-// keys and values of a band's pairs (256 KB a pair, read by all its tiles)
-// stay in L2 while it runs: DRAM reads stay at one pass over q, k and v.
-// (The backward kernels keep a two-dimensional grid, (B*H, tiles), heaviest
-// tiles of every pair first: for them the balance matters more than the
-// re-reads.)
-constexpr int FWD_BAND = 64;
+// Grid (band, tiles, bands): blockIdx.x is a (batch, head) pair within a band
+// of BAND pairs, y the tile (heaviest first), z the band.  The hardware hands
+// CTAs out x fastest, so a band's pairs go out together, every pair's heaviest
+// tile first: the short tiles fill the gaps at the band's end while the next
+// band starts, and the operands of a band's pairs (256 KB a pair, read by all
+// its tiles) stay in L2 while it runs, so each kernel reads them from DRAM
+// about once.  Slots past the last pair return at once.
+constexpr int BAND = 64;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
@@ -120,7 +118,7 @@ constexpr uint32_t F_TMEM = 128;    // S: cols 0..63, O: 64..127
 
 __global__ void __launch_bounds__(THREADS, 3)
 k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int* flags) {
+              bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int nbh, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + F_BAR);
@@ -136,13 +134,11 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     uint32_t* tmem_holder = (uint32_t*)(bars + 13);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    const int nqt = (T + BQ - 1) / BQ;
-    const int bh_total = (int)(gridDim.x / (unsigned)nqt);
-    const int hb0 = ((int)blockIdx.x / (FWD_BAND * nqt)) * FWD_BAND;
-    const int nb = min(FWD_BAND, bh_total - hb0);
-    const int j = (int)blockIdx.x - hb0 * nqt;
-    const int qt = nqt - 1 - j / nb;  // longest rows first within the band
-    const int b = (hb0 + j % nb) / H, h = (hb0 + j % nb) % H;
+    const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (bh >= nbh) return;  // the last band's unused slots (uniform over the CTA, before any setup)
+    const int nqt = gridDim.y;
+    const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first within the band
+    const int b = bh / H, h = bh % H;
     const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,11 +380,11 @@ constexpr int Q_SMEM = Q_BAR + 256 + 1024;
 constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191, Q 192..223, dO 224..255
 constexpr uint32_t Q_TQ = 192, Q_TO = 224;
 
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 2)
 k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
                  const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
-                 int T, int C, int H, int* flags) {
+                 int T, int C, int H, int nbh, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
@@ -406,11 +402,11 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint32_t* tmem_holder = (uint32_t*)(bars + 19);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
-    // grid (B*H, tiles): every (batch, head) of the longest tiles is scheduled
-    // before any of the next length, so the last wave holds the shortest work
+    const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (bh >= nbh) return;
     const int nqt = gridDim.y;
-    const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first
-    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const int qt = nqt - 1 - (int)blockIdx.y;  // longest rows first within the band
+    const int b = bh / H, h = bh % H;
     const int nkv = min(2 * qt + 2, (T + BN - 1) / BN);
     const int row0 = b * T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -635,7 +631,7 @@ constexpr uint32_t K_TMEM = 256;    // S^T 0..63, dP^T 64..127, dV 128..191, dK 
 __global__ void __launch_bounds__(THREADS)
 k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
-                   const float* __restrict__ Dlt, bf16* __restrict__ dqkv, int T, int C, int H,
+                   const float* __restrict__ Dlt, bf16* __restrict__ dqkv, int T, int C, int H, int nbh,
                    int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
@@ -651,8 +647,10 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint32_t* tmem_holder = (uint32_t*)(bars + 10);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
+    const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (bh >= nbh) return;
     const int kt = (int)blockIdx.y;  // key tile; low tiles see the most query blocks
-    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const int b = bh / H, h = bh % H;
     const int row0 = b * T;
     const int nqb = (T + BN - 1) / BN;
     const int j0 = 2 * kt;
@@ -874,6 +872,11 @@ static bool attn_set_smem() {
     return done == 1;
 }
 
+static dim3 attn_grid(int bh, int tiles) {
+    const int band = bh < fa5::BAND ? bh : fa5::BAND;
+    return dim3((unsigned)band, (unsigned)tiles, (unsigned)((bh + band - 1) / band));
+}
+
 bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T,
                              int C, int H) {
     if (L.dry) return true;
@@ -881,10 +884,10 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
     if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
     if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
     if (!attn_set_smem()) return false;
-    const dim3 grid((unsigned)(B * H * ((T + fa5::BQ - 1) / fa5::BQ)));
+    const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C,
-                                                                     H, L.flags);
+                                                                     H, B * H, L.flags);
     return true;
 }
 
@@ -899,13 +902,13 @@ bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, co
     if (!tc::make_tmap_bf16(&to64, dy, (long long)C, (long long)B * T, (long long)C, fa5::D, fa5::BN))
         return false;
     if (!attn_set_smem()) return false;
-    dim3 grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
+    const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_bwd_dq_tc<<<grid, fa5::THREADS, fa5::Q_SMEM, L.stream>>>(
-        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);
+        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, B * H, L.flags);
     L.count();
     fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::THREADS, fa5::K_SMEM, L.stream>>>(
-        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, L.flags);
+        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, B * H, L.flags);
     return true;
 }
 

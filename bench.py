@@ -231,20 +231,20 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "8d6bf29a4b768973",
+    "sources": "ee92a3052a7592a7",
     "bytes_per_launch_group": {
-        "gemm_fwd": 347053834,
-        "gemm_dx": 323521567,
-        "gemm_dw": 312085708,
-        "attn_fwd": 178261803,
-        "attn_bwd": 852428757,
-        "xent": 6542916608,
-        "colsum": 114261515,
-        "ln_fwd": 53969746,
-        "ln_bwd": 170587310,
-        "adamw": 3672179456,
-        "embed_fwd": 12834816,
-        "embed_bwd": 124957440,
+        "gemm_fwd": 349031581,
+        "gemm_dx": 339794667,
+        "gemm_dw": 331005853,
+        "attn_fwd": 178190912,
+        "attn_bwd": 559331797,
+        "xent": 6543062272,
+        "colsum": 114252992,
+        "ln_fwd": 54011341,
+        "ln_bwd": 170545644,
+        "adamw": 3672140544,
+        "embed_fwd": 12711936,
+        "embed_bwd": 124966144,
     },
 }
 
