@@ -118,3 +118,19 @@ def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libtt.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _native.lib()
+
+
+def test_fp16_configs(lib):
+    """IEEE half storage: any head dim the SIMT kernels take, the same
+    parameter layout, 16-bit activations (a smaller arena than fp32), and no
+    generation plan."""
+    tiny16 = api.make_config(2, 64, 4, 256, 32, "fp16")  # head dim 16
+    tiny32 = api.make_config(2, 64, 4, 256, 32, "fp32")
+    assert api.num_params(tiny16) == api.num_params(tiny32) > 0
+    assert 0 < api.arena_bytes(tiny16, 4, 32) < api.arena_bytes(tiny32, 4, 32)
+    m16 = api.make_config(12, 768, 12, 50257, 1024, "fp16")
+    mbf = api.make_config(12, 768, 12, 50257, 1024, "bf16")
+    for layer, which in [(0, 0), (0, 1), (5, 8), (11, 13), (0, 15)]:
+        assert api.param_offset(m16, layer, which) == api.param_offset(mbf, layer, which)
+    assert api.generate_arena_bytes(m16, 8, 64, 16) == 0
+    assert api.generate_arena_bytes(mbf, 8, 64, 16) > 0
