@@ -231,7 +231,7 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "ee92a3052a7592a7",
+    "sources": "8b0edd2a44713283",
     "bytes_per_launch_group": {
         "gemm_fwd": 349031581,
         "gemm_dx": 339794667,
@@ -249,8 +249,36 @@ MEASURED_TRAFFIC = {
 }
 
 
+def _code_tokens(text):
+    """C/C++/CUDA source with comments removed and whitespace collapsed, so that
+    the digest below changes with the code but not with its comments."""
+    import re
+
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_sources_digest():
-    """Digest of the native sources (kernels, their headers and the C ABI)."""
+    """Digest of the native sources (kernels, their headers and the C ABI),
+    comments excluded."""
     import hashlib
 
     root = os.path.dirname(os.path.abspath(__file__))
@@ -261,8 +289,8 @@ def kernel_sources_digest():
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -63,8 +63,8 @@ typedef enum { TT_FP32 = 0, TT_BF16 = 1, TT_FP16 = 2 } tt_dtype;
  * dl-scratch page, 3.4): a 10-bit mantissa but a 5-bit exponent, so small
  * activation gradients underflow unless the loss is scaled
  * (tt_gpt2_step_ex's loss_scale).  The half step runs on the SIMT kernels
- * (the tensor-core kernels are bf16); the op-level calls, tt_gpt2_eval and
- * tt_gpt2_generate take TT_FP32 and TT_BF16 only. */
+ * (the tensor-core kernels are bf16).  tt_gpt2_eval takes it too; the
+ * op-level calls and tt_gpt2_generate take TT_FP32 and TT_BF16 only. */
 typedef struct {
     int L, C, H, V, maxT;
     tt_dtype dtype;
