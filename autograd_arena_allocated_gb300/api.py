@@ -168,6 +168,7 @@ class Context:
                  max_norm=0.0, loss_scale=None, n=None):
         """tt_adamw_ex; step is a device int32 tensor (updates taken so far)."""
         n = master.numel() if n is None else n
+        self._check_lowp(lowp)
         self._check(lib().tt_adamw_ex(self.h, _ptr(master), _ptr(lowp), _ptr(grads), _ptr(m), _ptr(v), int(n),
                                       float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
                                       _ptr(step), _ptr(stats), float(max_norm), _ptr(loss_scale)))
@@ -200,8 +201,21 @@ class Context:
         self._check(lib().tt_ctx_copy_row_losses(self.h, _ptr(out), int(out.numel() if hasattr(out, "numel") else out.size)))
         return out
 
+    def _check_lowp(self, lowp):
+        """The 16-bit parameter copy's element type follows the model's dtype:
+        half for a TT_FP16 model, bf16 otherwise (torch tensors are checked)."""
+        import torch
+
+        dt = getattr(lowp, "dtype", None)
+        if not isinstance(dt, torch.dtype):
+            return
+        want = torch.float16 if (self.cfg is not None and self.cfg.dtype == TT_FP16) else torch.bfloat16
+        if dt != want:
+            raise ValueError(f"the 16-bit parameter copy is {dt}; this context's model writes {want}")
+
     def adamw(self, master, lowp, grads, m, v, lr, beta1, beta2, eps, weight_decay, step, n=None):
         n = master.numel() if n is None else n
+        self._check_lowp(lowp)
         self._check(lib().tt_adamw(self.h, _ptr(master), _ptr(lowp), _ptr(grads), _ptr(m), _ptr(v),
                                    int(n), lr, beta1, beta2, eps, weight_decay, int(step)))
 

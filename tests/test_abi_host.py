@@ -134,3 +134,20 @@ def test_fp16_configs(lib):
         assert api.param_offset(m16, layer, which) == api.param_offset(mbf, layer, which)
     assert api.generate_arena_bytes(m16, 8, 64, 16) == 0
     assert api.generate_arena_bytes(mbf, 8, 64, 16) > 0
+
+
+def test_binding_checks_the_16bit_copy_type():
+    """tt_adamw writes half for a TT_FP16 model and bf16 otherwise; the
+    binding refuses a torch tensor of the other type before any call."""
+    import torch
+
+    c = object.__new__(api.Context)  # no device context needed for the check
+    c.cfg = None
+    c._check_lowp(None)
+    c._check_lowp(torch.empty(2, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        c._check_lowp(torch.empty(2, dtype=torch.float16))
+    c.cfg = api.make_config(2, 64, 4, 256, 32, "fp16")
+    c._check_lowp(torch.empty(2, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        c._check_lowp(torch.empty(2, dtype=torch.bfloat16))
