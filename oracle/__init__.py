@@ -121,7 +121,10 @@ def param_offset(L, C_, H, V, maxT, layer, which):
 
 # ---------------------------------------------------------------- bf16 values
 def bf16_values(x) -> np.ndarray:
-    """Nearest bfloat16 value of each float32 (ties to even), as float64."""
+    """Nearest bfloat16 value of each float32 (ties to even), as float64: the
+    16-bit parameter copy of the mixed-precision step (dl-scratch page, 3.4,
+    which stores fp16; bf16 is the storage type this library reads it with on
+    the tensor cores)."""
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
     lsb = (b >> np.uint64(16)) & np.uint64(1)
     r = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
@@ -131,7 +134,8 @@ def bf16_values(x) -> np.ndarray:
 def f16_values(x) -> np.ndarray:
     """Nearest IEEE half value of each float32 (ties to even; beyond the
     largest half, 65504, the value becomes +-inf; below the smallest
-    subnormal, 2^-24, it rounds to zero or 2^-24), as float64."""
+    subnormal, 2^-24, it rounds to zero or 2^-24), as float64: the fp16
+    parameter copy of the dl-scratch page's mixed precision (3.4)."""
     with np.errstate(over="ignore"):
         return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float64)
 
