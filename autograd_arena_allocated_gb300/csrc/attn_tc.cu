@@ -858,18 +858,15 @@ bool attention_tc_eligible(bool bf16, int C, int H) {
 }
 
 static bool attn_set_smem() {
-    static int done = 0;  // 1 ok, -1 failed
-    if (!done) {
-        done = (cudaFuncSetAttribute(fa5::k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     fa5::F_SMEM) == cudaSuccess &&
-                cudaFuncSetAttribute(fa5::k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     fa5::Q_SMEM) == cudaSuccess &&
-                cudaFuncSetAttribute(fa5::k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     fa5::K_SMEM) == cudaSuccess)
-                   ? 1
-                   : -1;
-    }
-    return done == 1;
+    static PerDevice done;
+    return done.once([] {
+        return cudaFuncSetAttribute(fa5::k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    fa5::F_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(fa5::k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    fa5::Q_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(fa5::k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    fa5::K_SMEM) == cudaSuccess;
+    });
 }
 
 static dim3 attn_grid(int bh, int tiles) {

@@ -904,8 +904,8 @@ size_t gemm_tc_workspace_floats(const Launch& L, const GemmArgs& g) {
 // instantiation (0: not available).
 template <int BN, bool A_MN, bool B_MN>
 static int active_pairs(const Launch& L) {
-    static int pairs = -1;  // one value per instantiation
-    if (pairs < 0) {
+    static PerDevice pairs;  // one value per instantiation and device
+    return pairs.value([&]() -> int {
         auto kern = tc::k_gemm_tc<BN, A_MN, B_MN, true>;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (L.num_sms / 2));
@@ -924,9 +924,8 @@ static int active_pairs(const Launch& L) {
             cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess)
             n = 0;
         cudaGetLastError();
-        pairs = n;
-    }
-    return pairs;
+        return n;
+    });
 }
 
 template <int BN, bool A_MN, bool B_MN, bool PAIR>
@@ -934,11 +933,12 @@ static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma
                       const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& mx) {
     auto kern = tc::k_gemm_tc<BN, A_MN, B_MN, PAIR>;
     constexpr int smem = tc::Cfg<BN, PAIR>::SMEM_BYTES;
-    static bool attr_done = false;  // one flag per instantiation
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return false;
-        attr_done = true;
+    static PerDevice attr;  // one flag per instantiation and device
+    if (!attr.once([&] {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+        })) {
+        cudaGetLastError();
+        return false;
     }
     L.count();
     if (!PAIR) {

@@ -454,15 +454,15 @@ void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void*
         return;
     const int nblk = (M + LN_ROWS - 1) / LN_ROWS;
     const size_t smem = (size_t)LN_BWD_WARPS * 2 * C * sizeof(float);
-    static bool attr = false;
-    if (!attr) {
+    static PerDevice attr;
+    attr.once([] {
         const int max_smem = LN_BWD_WARPS * 2 * 1024 * (int)sizeof(float);
         cudaFuncSetAttribute(k_layernorm_bwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         cudaFuncSetAttribute(k_layernorm_bwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              max_smem);
         cudaFuncSetAttribute(k_layernorm_bwd<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        attr = true;
-    }
+        return true;
+    });
     L.count();
     if (bf16 && L.f16)
         k_layernorm_bwd<__half><<<nblk, LN_BWD_WARPS * 32, smem, L.stream>>>(

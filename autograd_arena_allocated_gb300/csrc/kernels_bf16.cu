@@ -287,15 +287,15 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     if (L.dry) return true;
     const int nv = (C / 8 + 31) / 32;
     const size_t smem = (size_t)(LNV_WARPS * 2) * C * sizeof(float);
-    static bool attr = false;
-    if (!attr) {
+    static PerDevice attr;
+    attr.once([] {
         const int mx = (LNV_WARPS * 2) * 1024 * (int)sizeof(float);
         cudaFuncSetAttribute(k_ln_bwd_bf16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         cudaFuncSetAttribute(k_ln_bwd_bf16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        attr = true;
-    }
+        return true;
+    });
     L.count();
     int G = 0;
 #define LNB(NV) G = ln_bwd_blocks<NV>(L, M); \

@@ -25,16 +25,15 @@ static_assert(kFlagBytes + 4 * (kSplitFloats + kBiasFloats) == TT_NOALLOC_SCRATC
 // returns for the current device.
 static __device__ __align__(256) unsigned char g_scratch[TT_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
-int g_sms[kMaxDevices] = {};
+void* g_addr[tt::kMaxDevices] = {};
+int g_sms[tt::kMaxDevices] = {};
 
 // Set-up, once per device, with that device current: look up (and cache) the
 // device address of g_scratch and the device's SM count.
 tt_status scratch_for_current_device(void** addr, int* sms) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= tt::kMaxDevices) {
         cudaGetLastError();
         return TT_ERR_CUDA;
     }

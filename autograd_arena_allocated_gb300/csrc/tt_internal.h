@@ -41,6 +41,44 @@ struct Launch {
     void count() const { if (launches) ++*launches; }
 };
 
+// ------------------------------------------------------------ per-device set-up
+// Kernel attributes (the dynamic shared-memory limit) and occupancy results
+// belong to one device: a process that drives several GPUs must set them once
+// on each, with that device current.  PerDevice keeps one state per device
+// ordinal: 0 not yet done, 1 done, -1 failed (or a cached value >= 0 for
+// `value`).  Two host threads racing on the same device may both run the
+// set-up; it is idempotent.
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return d;
+}
+
+struct PerDevice {
+    volatile int state[kMaxDevices] = {};
+    // runs f() (returning bool) once for the current device; its result is kept
+    template <class F>
+    bool once(F&& f) {
+        const int d = current_device();
+        if (d < 0 || d >= kMaxDevices) return f();
+        if (state[d] == 0) state[d] = f() ? 1 : -1;
+        return state[d] == 1;
+    }
+    // runs f() (returning int >= 0) once for the current device; its value is kept
+    template <class F>
+    int value(F&& f) {
+        const int d = current_device();
+        if (d < 0 || d >= kMaxDevices) return f();
+        if (state[d] == 0) state[d] = f() + 1;
+        return state[d] - 1;
+    }
+};
+
 // ------------------------------------------------------------ GEMM
 // Logical contraction D[m,n] = sum_k A(m,k) B(n,k) with
 //   A(m,k) = a_kmajor ? A[m*lda + k] : A[k*lda + m]

@@ -539,13 +539,18 @@ def run_op(args):
     torch.cuda.set_device(0)
     dev = "cuda"
     bf = torch.bfloat16
-    M, C, V, Vp, B, T, H = 32768, 768, 50257, 50304, 32, 1024, 12
+    # --batch sequences of 1024 tokens (default: the 124M workload's 32); a
+    # profiler capture uses a smaller case of the same kernel
+    B, T, C, V, Vp, H = args.batch, 1024, 768, 50257, 50304, 12
+    M = B * T
 
     def rnd(*shape, dtype=bf, scale=1.0):
         g = torch.Generator(device=dev).manual_seed(0)
         return (torch.randn(*shape, device=dev, generator=g) * scale).to(dtype)
 
-    ctx = api.Context(8 << 30)
+    # the ops' own scratch (split-K partials, column-sum and attention
+    # partials, sort keys) is all this context holds
+    ctx = api.Context(512 << 20)
     op = args.op
     if op == "gemm_fwd":
         x, W, b = rnd(M, C), rnd(4 * C, C, scale=0.02), rnd(4 * C)
@@ -656,6 +661,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", default=None, help="run one kernel group: " + ", ".join(OP_SHAPES))
     ap.add_argument("--reps", type=int, default=5)
+    ap.add_argument("--batch", type=int, default=32, help="--op: sequences of 1024 tokens")
     args = ap.parse_args()
     if args.op:
         args.warmup = max(1, args.warmup)

@@ -41,7 +41,7 @@ def lib():
             "or_layernorm_bwd": (None, [dp, dp, dp, dp, dp, i, i, dp, dp, dp]),
             "or_gelu_fwd": (None, [dp, sz, dp]),
             "or_gelu_bwd": (None, [dp, dp, sz, dp]),
-            "or_attention_fwd": (None, [dp, i, i, i, i, dp, dp]),
+            "or_attention_fwd": (None, [dp, i, i, i, i, dp, dp, dp]),
             "or_attention_bwd": (None, [dp, dp, dp, i, i, i, i, dp]),
             "or_xent": (d, [dp, ip, i, i, dp, dp, d]),
             "or_embed_fwd": (None, [dp, dp, ip, i, i, i, dp]),
@@ -191,12 +191,15 @@ def gelu_bwd(u, dg):
     return du
 
 
-def attention_fwd(qkv, B, T, C_, H):
+def attention_fwd(qkv, B, T, C_, H, want_lse=False):
+    """(y, P), or (y, P, lse) with lse [B, H, T] the log of each row's softmax
+    denominator over the scaled scores."""
     qkv = f64(qkv)
     y = np.zeros((B * T, C_))
     P = np.zeros((B, H, T, T))
-    lib().or_attention_fwd(_d(qkv), B, T, C_, H, _d(y), _d(P))
-    return y, P
+    lse = np.zeros((B, H, T)) if want_lse else None
+    lib().or_attention_fwd(_d(qkv), B, T, C_, H, _d(y), _d(P), _d(lse) if want_lse else None)
+    return (y, P, lse) if want_lse else (y, P)
 
 
 def attention_bwd(qkv, P, dy, B, T, C_, H):

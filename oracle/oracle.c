@@ -356,9 +356,12 @@ OR_EXPORT void or_gelu_bwd(const double* u, const double* dg, size_t n, double* 
 /* Causal multi-head self-attention ([FORGE] 最硬的一关: scores divided by
  * sqrt(d_k), future positions masked with -inf; softmax with max
  * subtraction, [TT] 四).  qkv is [B*T, 3C] with columns [q | k | v], each
- * split [H, hd] head-major.  P is saved as [B, H, T, T] (masked entries 0). */
+ * split [H, hd] head-major.  P is saved as [B, H, T, T] (masked entries 0).
+ * lse (may be NULL) receives, per [B, H, T] row, the natural log of the
+ * softmax denominator taken over the scaled scores: m + ln(sum exp(s - m)),
+ * the normaliser the backward needs to rebuild P from the scores. */
 OR_EXPORT void or_attention_fwd(const double* qkv, int B, int T, int C, int H,
-                                double* y, double* P) {
+                                double* y, double* P, double* lse) {
     int hd = C / H;
     double scale = 1.0 / sqrt((double)hd);
     size_t ld = (size_t)3 * C;
@@ -384,6 +387,7 @@ OR_EXPORT void or_attention_fwd(const double* qkv, int B, int T, int C, int H,
                     sum += prow[s];
                 }
                 for (int s = 0; s < T; s++) prow[s] /= sum;
+                if (lse) lse[((size_t)b * H + h) * T + t] = mx + log(sum);
                 double* yr = y + ((size_t)b * T + t) * C + (size_t)h * hd;
                 for (int i = 0; i < hd; i++) {
                     double acc = 0.0;
@@ -677,7 +681,7 @@ static otensor* tp_add(otape* tp, otensor* a, otensor* b) {
 static otensor* tp_attention(otape* tp, otensor* qkv, int B, int T, int C, int H) {
     otensor* out = ot_new(tp, (size_t)B * T * C);
     double* P = ar_new(&tp->arena, (size_t)B * H * T * T);
-    or_attention_fwd(qkv->v, B, T, C, H, out->v, P);
+    or_attention_fwd(qkv->v, B, T, C, H, out->v, P, NULL);
     orecord* r = tp_push(tp, OP_ATTENTION);
     r->a = qkv; r->out = out; r->s0 = P; r->B = B; r->T = T; r->N = C; r->H = H;
     return out;

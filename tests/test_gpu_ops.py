@@ -136,9 +136,32 @@ def test_linear_bwd_dw(ctx, oracle, dt, backend, M, K, N):
 
 
 # ----------------------------------------------------------------- attention
+def _check_attention(dt, got_y, got_lse, got_dqkv, ry, rlse, rd):
+    """y, the saved log-sum-exp and dqkv against the oracle, element by element.
+    bf16 mode feeds P (rounded to bf16, 2^-9 relative) into the tensor-core
+    P.V and dS into dS.K / dS^T.Q: with unit-variance inputs and short rows
+    (few keys, large p) that is up to ~1-2% of the output's rms per element.
+    The log-sum-exp is accumulated in fp32 from the exact products of the
+    (same) 16-bit q and k, so it is held to fp32-level error."""
+    rtol, atol = TOL[dt] if dt == "fp32" else (8e-3, 3e-2)
+    assert_close(got_y, ry, rtol, atol, "attention y")
+    err = np.abs(got_lse - rlse)
+    assert np.all(err <= 2e-5 * np.abs(rlse) + 1e-4), f"lse: worst abs err {np.max(err):.3e}"
+    assert_close(got_dqkv, rd, 4 * rtol, 2 * atol, "attention dqkv")
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    if dt == "bf16":
+        assert rel(got_y, ry) < 5e-3
+        assert rel(got_dqkv, rd) < 1e-2
+    return rel(got_y, ry), float(np.max(err)), rel(got_dqkv, rd)
+
+
+# (6, 256, 768, 12): 72 (batch, head) pairs, i.e. two bands of 64 pairs with
+# the second band's 56 unused slots; (1, 1024, 128, 2): the benchmark's
+# sequence length, every key tile of a 1024-long row.
 @pytest.mark.parametrize("dt,B,T,C_,H", [("fp32", 2, 37, 64, 4), ("fp32", 1, 70, 64, 2),
                                          ("bf16", 2, 100, 128, 2), ("bf16", 1, 257, 384, 6),
-                                         ("bf16", 3, 1, 128, 2)])
+                                         ("bf16", 3, 1, 128, 2), ("bf16", 6, 256, 768, 12),
+                                         ("bf16", 1, 1024, 128, 2), ("fp32", 5, 70, 960, 15)])
 def test_attention(ctx, oracle, dt, B, T, C_, H):
     qkv, dy = rnd(B * T, 3 * C_), rnd(B * T, C_)
     qd, dyd = to_dev(qkv, dt), to_dev(dy, dt)
@@ -149,18 +172,46 @@ def test_attention(ctx, oracle, dt, B, T, C_, H):
     ctx.attention_bwd(dt, qd, y, lse, dyd, dqkv, B, T, C_, H)
     torch.cuda.synchronize()
     q64 = ovals(qkv, dt, oracle)
-    ry, P = oracle.attention_fwd(q64, B, T, C_, H)
-    # bf16 mode feeds P (rounded to bf16, 2^-9 relative) into the tensor-core
-    # P.V and dS into dS.K / dS^T.Q: with unit-variance inputs and short rows
-    # (few keys, large p) that is up to ~1-2% of the output's rms per element
-    rtol, atol = TOL[dt] if dt == "fp32" else (8e-3, 3e-2)
-    assert_close(host(y), ry, rtol, atol, "attention y")
+    ry, P, rlse = oracle.attention_fwd(q64, B, T, C_, H, want_lse=True)
     rd = oracle.attention_bwd(q64, P, ovals(dy, dt, oracle), B, T, C_, H)
-    assert_close(host(dqkv), rd, 4 * rtol, 2 * atol, "attention dqkv")
-    if dt == "bf16":
-        rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
-        assert rel(host(y), ry) < 5e-3
-        assert rel(host(dqkv), rd) < 1e-2
+    e = _check_attention(dt, host(y), host(lse), host(dqkv), ry, rlse, rd)
+    print(f"[attention {dt} B={B} T={T} H={H}] y rel-L2 {e[0]:.2e}, lse max abs err {e[1]:.2e}, "
+          f"dqkv rel-L2 {e[2]:.2e}")
+
+
+def test_attention_benchmark_shape_sampled(ctx, oracle):
+    """The step's own attention call at the benchmark's size (B=32, T=1024,
+    C=768, H=12: 384 (batch, head) pairs in six bands), in the launch
+    configuration the step uses.  (batch, head) pairs are independent, so
+    sampled pairs -- the first and last of a band, either side of a band edge,
+    and the last pair -- are each checked against the oracle run on that
+    pair's head alone."""
+    B, T, C_, H = 32, 1024, 768, 12
+    D = C_ // H
+    qkv, dy = rnd(B * T, 3 * C_), rnd(B * T, C_)
+    qd, dyd = to_dev(qkv, "bf16"), to_dev(dy, "bf16")
+    with api.Context(4 << 30) as big:
+        y = torch.empty(B * T, C_, device=DEV, dtype=qd.dtype)
+        lse = torch.empty(B, H, T, device=DEV)
+        big.attention_fwd("bf16", qd, y, lse, B, T, C_, H)
+        dqkv = torch.empty_like(qd)
+        big.attention_bwd("bf16", qd, y, lse, dyd, dqkv, B, T, C_, H)
+        torch.cuda.synchronize()
+    q16 = ovals(qkv, "bf16", oracle)
+    dy16 = ovals(dy, "bf16", oracle)
+    y_h, lse_h, dqkv_h = host(y), host(lse), host(dqkv)
+    for pair in (0, 63, 64, 200, 383):
+        b, h = divmod(pair, H)
+        rows = slice(b * T, (b + 1) * T)
+        cols = [slice(j * C_ + h * D, j * C_ + (h + 1) * D) for j in range(3)]
+        one = np.ascontiguousarray(np.concatenate([q16[rows, c] for c in cols], axis=1))
+        ry, P, rlse = oracle.attention_fwd(one, 1, T, D, 1, want_lse=True)
+        rd = oracle.attention_bwd(one, P, np.ascontiguousarray(dy16[rows, h * D:(h + 1) * D]), 1, T, D, 1)
+        got_d = np.concatenate([dqkv_h[rows, c] for c in cols], axis=1)
+        e = _check_attention("bf16", y_h[rows, h * D:(h + 1) * D], lse_h[b, h][None, None, :], got_d,
+                             ry, rlse, rd)
+        print(f"[attention B=32 T=1024 pair {pair}] y rel-L2 {e[0]:.2e}, lse max abs err {e[1]:.2e}, "
+              f"dqkv rel-L2 {e[2]:.2e}")
 
 
 @pytest.mark.parametrize("T", [384, 1000])
@@ -186,12 +237,9 @@ def test_attention_growing_max(ctx, oracle, T):
     ctx.attention_bwd("bf16", qd, y, lse, dyd, dqkv, B, T, C_, H)
     torch.cuda.synchronize()
     q64 = ovals(qkv, "bf16", oracle)
-    ry, P = oracle.attention_fwd(q64, B, T, C_, H)
-    assert_close(host(y), ry, 8e-3, 3e-2, "attention y")
+    ry, P, rlse = oracle.attention_fwd(q64, B, T, C_, H, want_lse=True)
     rd = oracle.attention_bwd(q64, P, ovals(dy, "bf16", oracle), B, T, C_, H)
-    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
-    assert rel(host(y), ry) < 5e-3
-    assert rel(host(dqkv), rd) < 1e-2
+    _check_attention("bf16", host(y), host(lse), host(dqkv), ry, rlse, rd)
 
 
 # ----------------------------------------------------------------- layernorm

@@ -163,8 +163,11 @@ def _bf16_parity(ctx, oracle, sh, B, T, kind, jitter, label):
 
 
 def test_char_bf16_step_matches_oracle(ctx, oracle):
+    """The char workload at its full batch (B=64, T=256): loss, every gradient
+    tensor, and the AdamW-updated parameters."""
     w = synth.WORKLOADS["char_bf16"]
-    run, p, rg = _bf16_parity(ctx, oracle, w.shape, 4, 128, "zipf", jitter=0.05, label="char bf16")
+    assert (w.B, w.T) == (64, 256)
+    run, p, rg = _bf16_parity(ctx, oracle, w.shape, w.B, w.T, "zipf", jitter=0.05, label="char bf16")
     lr, b1, b2, eps, wd = w.lr, w.beta1, w.beta2, w.eps, w.weight_decay
     rp, _, _ = oracle.adamw(p.astype(np.float64), rg, np.zeros(p.size), np.zeros(p.size), lr, b1, b2,
                             eps, wd, 1)
@@ -186,17 +189,29 @@ def test_char_bf16_step_matches_oracle(ctx, oracle):
     assert np.array_equal(low.float().cpu().numpy().astype(np.float64),
                           oracle.bf16_values(master.cpu().numpy()))
     # (2) end to end: the update of the GPU's own bf16-mode gradient.  At step 1
-    #     Adam moves every element by ~lr*sign(g), so the few components whose
-    #     sign the bf16 gradient gets wrong (|g| near zero) move by 2*lr.
+    #     the bias-corrected moments are m = g and v = g^2, so AdamW moves each
+    #     component by lr * (g / (|g| + eps) + wd * p): a step function of g.
+    #     A gradient within the bf16 tolerance can still have the other sign
+    #     where |g| is near zero, and there the update jumps by up to 2 * lr
+    #     whatever the gradient's accuracy.  So the 1e-3 bound on updated
+    #     parameters is applied to the components whose two gradients agree in
+    #     sign (where the update is continuous in g); each other component must
+    #     be within the 2 * lr jump; the whole vector's rel-L2 is printed.
     ctx.adamw(run.master, run.lowp, run.grads, run.m, run.v, lr, b1, b2, eps, wd, 1)
     torch.cuda.synchronize()
     got = run.master.cpu().numpy().astype(np.float64)
-    e2e = rel(got, rp)
-    g = run.grads.cpu().numpy()
-    flips = float(np.mean(np.sign(g) != np.sign(rg)))
-    print(f"[char bf16] AdamW after the bf16 step: params rel-L2 {e2e:.2e}, "
-          f"gradient sign disagreements {100 * flips:.3f}%")
-    assert e2e <= 2 * lr * math.sqrt(flips) * math.sqrt(p.size) / np.linalg.norm(rp) + 1e-3
+    g = run.grads.cpu().numpy().astype(np.float64)
+    agree = np.sign(g) == np.sign(rg)
+    flips = float(np.mean(~agree))
+    e_agree = rel(got[agree], rp[agree])
+    e_all = rel(got, rp)
+    jump = float(np.max(np.abs(got[~agree] - rp[~agree]))) if flips > 0 else 0.0
+    print(f"[char bf16] AdamW after the bf16 step: params rel-L2 {e_all:.2e} over all "
+          f"{p.size} components, {e_agree:.2e} over the {int(agree.sum())} whose gradient signs agree; "
+          f"sign disagreements {100 * flips:.3f}%, largest jump there {jump:.2e} (2*lr = {2 * lr:.1e})")
+    assert e_agree <= 1e-3
+    assert jump <= 2 * lr * (1 + 1e-6) + 1e-7
+    assert flips <= 0.05
     assert np.array_equal(run.lowp.float().cpu().numpy().astype(np.float64),
                           oracle.bf16_values(run.master.cpu().numpy()))
 
@@ -319,3 +334,24 @@ def test_boundary_errors(ctx):
     with api.Context(1 << 20) as c3:
         with pytest.raises(api.TTError, match="TT_ERR_STATE"):
             c3.step(run.params, run.grads, tok, tgt, 2, 8)
+
+
+def test_nonfinite_parameter_is_reported_and_context_recovers(ctx):
+    """A NaN planted on the host in one parameter (the final LayerNorm's first
+    bias) reaches every logit, so the step's loss is NaN: the step must return
+    TT_ERR_NONFINITE (read from the device flag at its sync), and the context
+    must run a clean step normally after a reset."""
+    w = synth.WORKLOADS["char_bf16"]
+    sh = w.shape
+    p, tok, tgt = make_inputs(sh, 2, 64, "zipf", jitter=0.05)
+    cfg = api.make_config(sh.L, sh.C, sh.H, sh.V, sh.maxT, "bf16")
+    off, _ = api.param_offset(cfg, 0, 15)  # lnf_b
+    bad = p.copy()
+    bad[off] = np.nan
+    run = Run(ctx, sh, "bf16", bad)
+    with pytest.raises(api.TTError, match="TT_ERR_NONFINITE"):
+        run.step(tok, tgt)
+    clean = Run(ctx, sh, "bf16", p)
+    loss = clean.step(tok, tgt)
+    assert math.isfinite(loss)
+    assert torch.isfinite(clean.grads).all()

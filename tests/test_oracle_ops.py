@@ -145,6 +145,36 @@ def test_attention_special_cases(oracle):
     np.testing.assert_allclose(y.reshape(B, T, C), cm, rtol=1e-13, atol=1e-14)
 
 
+def test_attention_lse(oracle):
+    """The saved log-sum-exp: torch's float64 logsumexp of the masked, scaled
+    scores; with T = 1 the single score q.k/sqrt(hd); with zero queries every
+    visible score is 0, so row t gives ln(t + 1)."""
+    B, T, C, H = 2, 7, 12, 3
+    hd = C // H
+    qkv = rng.normal(size=(B * T, 3 * C))
+    _, P, lse = oracle.attention_fwd(qkv, B, T, C, H, want_lse=True)
+    q, k, _ = (_t(a) for a in _split(qkv, B, T, C, H))
+    s = (q @ k.transpose(-1, -2)) / np.sqrt(hd)
+    s = s.masked_fill(torch.triu(torch.ones(T, T, dtype=torch.bool), 1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=1e-13, atol=1e-13)
+    # P is rebuilt from the scores and lse alone: exp(s - lse)
+    np.testing.assert_allclose(P, torch.exp(s - _t(lse)[..., None]).numpy(), rtol=1e-12, atol=1e-15)
+    # T = 1
+    B, T = 3, 1
+    qkv = rng.normal(size=(B * T, 3 * C))
+    _, _, lse = oracle.attention_fwd(qkv, B, T, C, H, want_lse=True)
+    qh = qkv[:, :C].reshape(B, H, hd)
+    kh = qkv[:, C:2 * C].reshape(B, H, hd)
+    np.testing.assert_allclose(lse[:, :, 0], np.sum(qh * kh, axis=-1) / np.sqrt(hd), rtol=1e-14, atol=1e-14)
+    # zero queries
+    B, T = 2, 9
+    qkv = rng.normal(size=(B * T, 3 * C))
+    qkv[:, :C] = 0.0
+    _, _, lse = oracle.attention_fwd(qkv, B, T, C, H, want_lse=True)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, T + 1)), (B, H, T)), rtol=0,
+                               atol=1e-15)
+
+
 def test_attention_backward_fd(oracle):
     B, T, C, H = 2, 4, 6, 2
     qkv = rng.normal(size=(B * T, 3 * C))
