@@ -167,9 +167,11 @@ def run_reference(args, world, rank):
 
 
 def config_of(w, world, args):
+    mode = getattr(args, "dp", "replicas") if world > 1 else "replicas"
+    par = f"replicas x{world}" if mode == "replicas" else f"dp{world} ({mode} gradient exchange)"
     return {"workload": f"{w.name}: GPT-2 L={w.shape.L} C={w.shape.C} H={w.shape.H} "
                         f"V={w.shape.V} (tied head), B={w.B} T={w.T} per GPU, {w.dtype}",
-            "global_batch": w.B * world, "seq_len": w.T, "parallelism": f"replicas x{world}",
+            "global_batch": w.B * world, "seq_len": w.T, "parallelism": par,
             "l2": "working set (~20 GB arena) far above the 129 MB L2; no flush needed",
             "tokens": w.tokens}
 
@@ -662,6 +664,9 @@ def main():
     ap.add_argument("--op", default=None, help="run one kernel group: " + ", ".join(OP_SHAPES))
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--batch", type=int, default=32, help="--op: sequences of 1024 tokens")
+    ap.add_argument("--dp", default="replicas", choices=["replicas", "allreduce", "sharded"],
+                    help="N > 1: independent replicas, or data parallelism with a gradient "
+                         "all-reduce / reduce-scatter + sharded AdamW + all-gather")
     args = ap.parse_args()
     if args.op:
         args.warmup = max(1, args.warmup)
@@ -706,16 +711,27 @@ def main():
     peaks = load_peaks()
 
     p = synth.init_params(sh)
-    # each replica trains on its own token stream (rank 0: the single-GPU stream)
+    # each rank trains on its own token stream (rank 0: the single-GPU stream)
     tok, tgt = synth.token_stream(B, T, sh.V, w.tokens, seed=token_seed(synth.TOKEN_SEED, rank))
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
-    master = torch.from_numpy(p).to(dev)
-    grads = torch.empty(n, device=dev)
-    m = torch.zeros(n, device=dev)
-    v = torch.zeros(n, device=dev)
     bf16 = w.dtype == "bf16"
-    lowp = torch.empty(n, device=dev, dtype=torch.bfloat16) if bf16 else None
+    dp_mode = args.dp if world > 1 else "replicas"
+    if dp_mode == "sharded" and not bf16:
+        raise SystemExit("--dp sharded gathers the 16-bit compute copy: a bf16 workload is needed")
+    ex = None
+    n_buf = n
+    if dp_mode != "replicas":
+        from autograd_arena_allocated_gb300 import dp as dpx
+
+        ex = dpx.DataParallel(dist, n, boundaries=dpx.tensor_starts(cfg))
+        n_buf = ex.n_pad  # flat vectors padded to equal, aligned slices
+    master = torch.zeros(n_buf, device=dev)
+    master[:n] = torch.from_numpy(p).to(dev)
+    grads = torch.zeros(n_buf, device=dev)
+    m = torch.zeros(n_buf, device=dev)
+    v = torch.zeros(n_buf, device=dev)
+    lowp = torch.zeros(n_buf, device=dev, dtype=torch.bfloat16) if bf16 else None
     tok_d = torch.from_numpy(tok).to(dev)
     tgt_d = torch.from_numpy(tgt).to(dev)
     ctx = api.Context(api.arena_bytes(cfg, B, T) + (64 << 20), stream=stream.cuda_stream)
@@ -726,11 +742,25 @@ def main():
     hp = (w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     step_no = [0]
 
+    if dp_mode == "sharded":
+        # this rank keeps the master weights and moments of its slice only
+        master = master[ex.lo:ex.hi].clone()
+        m, v = m[ex.lo:ex.hi].clone(), v[ex.lo:ex.hi].clone()
+        grad_shard = torch.empty(ex.hi - ex.lo, device=dev)
+    if ex is not None:
+        update = dpx.native_update(ctx)
+        hyper = dpx.Hyper(*hp)
+
     def train_step(tokens, targets, sync):
         ctx.reset()
         loss = ctx.step(params, grads, tokens, targets, B, T, sync=sync)
         step_no[0] += 1
-        ctx.adamw(master, lowp, grads, m, v, *hp, step_no[0])
+        if dp_mode == "allreduce":
+            ex.step_allreduce(update, master, lowp, grads, m, v, hyper, step_no[0])
+        elif dp_mode == "sharded":
+            ex.step_sharded(update, master, lowp, grads, grad_shard, m, v, hyper, step_no[0])
+        else:
+            ctx.adamw(master, lowp, grads, m, v, *hp, step_no[0])
         return loss
 
     group = Group(dist, device=dev, sync=torch.cuda.synchronize)
