@@ -368,19 +368,80 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     if (warp == 1) tmem_dealloc(tmem, F_TMEM);
 }
 
-// ================================================================== backward: dQ
-constexpr int Q_Q = 0;
-constexpr int Q_O = Q_Q + T128;     // dO tile
-constexpr int Q_KST = 3;             // K stages: K_j is held until dQ_j
-constexpr int Q_K = Q_O + T128;
-constexpr int Q_V = Q_K + Q_KST * T64;  // 2 stages: V_j is free once dP_j is done
-constexpr int Q_S = Q_V + 2 * T64;      // dS: 2 x [128 x 64] bf16
-constexpr int Q_BAR = Q_S + 2 * T128;
-constexpr int Q_SMEM = Q_BAR + 256 + 1024;
-constexpr uint32_t Q_TMEM = 256;    // S 0..63, dP 64..127, dQ 128..191, Q 192..223, dO 224..255
-constexpr uint32_t Q_TQ = 192, Q_TO = 224;
+// ================================================================== backward
+// Both backward kernels run 320 threads: warp 0 loads by TMA, warp 1 owns the
+// tensor memory and issues the MMAs, and warps 2..9 are the row warps.  Two
+// row warps share each 32-lane quarter of tensor memory (quarter = warp & 3)
+// and split the streamed block's 64 columns: half (warp - 2) >> 2 takes
+// columns [32 half, 32 half + 32).  Each thread therefore owns one row and
+// 32 columns of the score block.
+//
+// The bf16 operand that the row threads produce (dS in the dQ kernel, P^T and
+// dS^T in the dK/dV kernel) is written into tensor memory over the scores it
+// was computed from -- half h writes the 16 columns [32 h, 32 h + 16) of its
+// own 32 -- and the next MMAs read it from there as their A operand, so the
+// N = 64 products read only their B operand from shared memory.  The next
+// block's score MMAs overwrite those columns; they are issued after the MMAs
+// that read them, and one thread's tcgen05.mma operations run in issue order.
+constexpr int BW_THREADS = 320;
+constexpr int BW_ROWS = 256;  // row threads
 
-__global__ void __launch_bounds__(THREADS, 2)
+// tensor-memory column of the A operand for K step k (16 elements) of a
+// 64-wide bf16 operand written as two 16-column halves 32 columns apart
+__device__ __forceinline__ uint32_t split_a_col(int k) { return (uint32_t)(8 * k + (k >= 2 ? 16 : 0)); }
+
+__device__ __forceinline__ void store_out32(bf16* dst, const uint32_t (&w)[32], float scale) {
+    uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        o[i] = make_uint4(pack_bf2(__uint_as_float(w[8 * i]) * scale, __uint_as_float(w[8 * i + 1]) * scale),
+                          pack_bf2(__uint_as_float(w[8 * i + 2]) * scale, __uint_as_float(w[8 * i + 3]) * scale),
+                          pack_bf2(__uint_as_float(w[8 * i + 4]) * scale, __uint_as_float(w[8 * i + 5]) * scale),
+                          pack_bf2(__uint_as_float(w[8 * i + 6]) * scale, __uint_as_float(w[8 * i + 7]) * scale));
+}
+
+// One arrival per warp: every lane has passed its own fences (the caller's
+// tcgen05.fence / fence.proxy.async) before lane 0 arrives for the warp.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+// Named barrier for the 256 row threads only.
+__device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Spins until the phase completes or the long landing bound passes, with no
+// abort check: used only to let copies already issued land before a CTA
+// that gave up exits.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity) && clock64() - t0 < WAIT_CYCLES) {}
+}
+
+// ------------------------------------------------------------------ dQ
+// One CTA per 128 queries (2 CTAs per SM).  S = Q K_j^T and dP = dO V_j^T
+// (Q and dO are A operands read from shared memory); the row threads form
+// dS = P o (dP - D), P from the saved log-sum-exp, into one of two bf16
+// buffers in tensor memory; dQ += dS K_j accumulates in tensor memory.
+// D = rowsum(dO o O) is computed here and saved for the dK/dV kernel.
+//
+// A tcgen05.mma costs its issuing thread tens of cycles, about twice the
+// tensor time of an N = 64 product, so the MMA thread is the critical
+// resource: the dQ MMAs of block j - 1 are issued after S_j and dP_j, while
+// the row threads work on block j, and dS is double-buffered so that block
+// j's dS never overwrites the operand of block j - 1's dQ MMAs.
+constexpr int Q_Q = 0;
+constexpr int Q_O = Q_Q + T128;          // dO tile
+constexpr int Q_KST = 3;                 // K stages: K_j is read by S_j and by dQ_j
+constexpr int Q_K = Q_O + T128;
+constexpr int Q_V = Q_K + Q_KST * T64;   // 2 stages: V_j is free once dP_j is done
+constexpr int Q_DP = Q_V + 2 * T64;      // D partials [2 halves][128 rows]
+constexpr int Q_BAR = Q_DP + 2 * 128 * 4;
+constexpr int Q_SMEM = Q_BAR + 256 + 1024;
+constexpr uint32_t Q_TMEM = 256;         // S 0..63, dP 64..127, dS[2] 128..191, dQ 192..255
+constexpr uint32_t Q_TS = 0, Q_TP = 64, Q_TDS = 128, Q_TACC = 192;
+
+__global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
                  const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
@@ -393,13 +454,11 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint64_t* k_empty = bars + 4;   // [3]
     uint64_t* v_full = bars + 7;    // [2]
     uint64_t* v_empty = bars + 9;   // [2]
-    uint64_t* s_full = bars + 11;
-    uint64_t* s_free = bars + 12;
-    uint64_t* ds_full = bars + 13;  // [2]: dS buffer written
-    uint64_t* ds_free = bars + 15;  // [2]: dS buffer consumed by its dQ MMA
-    uint64_t* acc_full = bars + 17;
-    uint64_t* qo_tm = bars + 18;    // Q and dO copied into TMEM
-    uint32_t* tmem_holder = (uint32_t*)(bars + 19);
+    uint64_t* s_full = bars + 11;   // S_j, dP_j (and every earlier MMA) done
+    uint64_t* ds_full = bars + 12;  // block j's S, dP read and its dS written
+    uint64_t* acc_full = bars + 13;
+    uint64_t* drain = bars + 14;    // MMAs issued before an abort are done
+    uint32_t* tmem_holder = (uint32_t*)(bars + 15);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
@@ -422,13 +481,9 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_init(&v_empty[i], 1);
         }
         mbar_init(s_full, 1);
-        mbar_init(s_free, 128);
-        mbar_init(&ds_full[0], 128);
-        mbar_init(&ds_full[1], 128);
-        mbar_init(&ds_free[0], 1);
-        mbar_init(&ds_free[1], 1);
+        mbar_init(ds_full, BW_ROWS / 32);
         mbar_init(acc_full, 1);
-        mbar_init(qo_tm, 128);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         init_done();
     }
@@ -459,155 +514,125 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 ++issued_v;
             }
             if (!ok) {  // let issued copies land before the CTA exits
-                const long long t0 = clock64();
-                while (!mbar_try_wait(qo_full, 0) && clock64() - t0 < WAIT_CYCLES) {}
+                mbar_drain(qo_full, 0);
                 for (int j = (issued_k > Q_KST ? issued_k - Q_KST : 0); j < issued_k; j++)
-                    while (!mbar_try_wait(&k_full[j % Q_KST], (j / Q_KST) & 1) && clock64() - t0 < 2 * WAIT_CYCLES) {}
+                    mbar_drain(&k_full[j % Q_KST], (j / Q_KST) & 1);
                 for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; j++)
-                    while (!mbar_try_wait(&v_full[j & 1], (j >> 1) & 1) && clock64() - t0 < 3 * WAIT_CYCLES) {}
+                    mbar_drain(&v_full[j & 1], (j >> 1) & 1);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_Q = idesc_bf16(BQ, D, false, true);
-            // Q and dO, fixed for the CTA, are A operands read from TMEM
-            bool ok = mbar_wait(qo_tm, 0, abort_flag, flags, 0x200 + 2);
-            tc_fence_after();
-            // S_{j+1} and dP_{j+1} are issued as soon as the row threads hold
-            // S_j and dP_j in registers, overlapping their elementwise work
-            auto issue_sdp = [&](int j) -> bool {
-                const int ks = j % Q_KST, vs = j & 1;
-                if (!mbar_wait(&k_full[ks], (j / Q_KST) & 1, abort_flag, flags, 0x200 + 3)) return false;
-                if (!mbar_wait(&v_full[vs], (j >> 1) & 1, abort_flag, flags, 0x200 + 11)) return false;
-                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x200 + 4)) return false;
-                tc_fence_after();
-                const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sv = smem_u32(sm + Q_V + vs * T64);
-                // the S and dP chains are independent: interleaved, so the tensor
-                // pipe overlaps them
-#pragma unroll
-                for (int k = 0; k < D / 16; k++) {
-                    umma_bf16_ts(tmem, tmem + Q_TQ + 8 * k, sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
-                    umma_bf16_ts(tmem + BN, tmem + Q_TO + 8 * k, sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
-                }
-                umma_commit(s_full);
-                umma_commit(&v_empty[vs]);  // V_j is no longer needed
-                return true;
-            };
-            if (ok) ok = issue_sdp(0);
-            for (int j = 0; j < nkv && ok; j++) {
-                if (j + 1 < nkv && !issue_sdp(j + 1)) { ok = false; break; }
-                const int db = j & 1, ks = j % Q_KST;
-                if (!mbar_wait(&ds_full[db], (j >> 1) & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sds = smem_u32(sm + Q_S + db * T128);
+            const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O);
+            bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2);
+            bool issued = false;
+            // dQ += dS_j K_j: dS from tensor-memory buffer j & 1, K_j read MN-major
+            auto issue_dq = [&](int j) {
+                const uint32_t sk = smem_u32(sm + Q_K + (j % Q_KST) * T64);
+                const uint32_t ta = tmem + Q_TDS + 32 * (j & 1);
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++)
-                    umma_bf16(tmem + 2 * BN, sdesc(sds + 32 * k, 16, 1024), sdesc(sk + k * 2048, T64, 1024),
-                              ID_Q, (j > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&k_empty[ks]);
-                umma_commit(&ds_free[db]);
+                    umma_bf16_ts(tmem + Q_TACC, ta + 8 * k, sdesc(sk + k * 2048, T64, 1024), ID_Q,
+                                 (j > 0 || k > 0) ? 1u : 0u);
+                umma_commit(&k_empty[j % Q_KST]);
+            };
+            for (int j = 0; j < nkv && ok; j++) {
+                const int ks = j % Q_KST, vs = j & 1;
+                if (!mbar_wait(&k_full[ks], (j / Q_KST) & 1, abort_flag, flags, 0x200 + 3)) { ok = false; break; }
+                if (!mbar_wait(&v_full[vs], (j >> 1) & 1, abort_flag, flags, 0x200 + 11)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sv = smem_u32(sm + Q_V + vs * T64);
+                // S_j and dP_j: two independent chains, interleaved
+#pragma unroll
+                for (int k = 0; k < D / 16; k++) {
+                    umma_bf16(tmem + Q_TS, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
+                    umma_bf16(tmem + Q_TP, sdesc(so + 32 * k, 16, 1024), sdesc(sv + 32 * k, 16, 1024), ID, k > 0);
+                }
+                issued = true;
+                umma_commit(s_full);
+                umma_commit(&v_empty[vs]);  // V_j is no longer needed
+                if (j > 0) issue_dq(j - 1);  // overlaps the row threads' work on block j
+                if (!mbar_wait(ds_full, j & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
+                tc_fence_after();
             }
-            if (ok) umma_commit(acc_full);
+            if (ok) {
+                issue_dq(nkv - 1);
+                umma_commit(acc_full);
+            } else if (issued) {  // the MMAs already issued finish before tensor memory is freed
+                umma_commit(drain);
+                mbar_drain(drain, 0);
+            }
         }
     } else {
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int q = qt * BQ + r;
         const bool qv = q < T;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const long long bh = (long long)b * H + h;
+        const long long bhl = (long long)b * H + h;
+        float* dpart = reinterpret_cast<float*>(sm + Q_DP);
         bool ok = mbar_wait_warp(qo_full, 0, abort_flag, flags, 0x200 + 6);
-        // Copy this row of Q and of dO from the swizzled tiles into TMEM (the A
-        // operands of S and dP), and form D = rowsum(dO o O) from the dO row.
+        // This thread's half of D = rowsum(dO o O) (16-byte chunks 4 half ..
+        // 4 half + 3 of the swizzled dO row); the two halves meet in shared memory.
         float Dq = 0.0f;
         if (ok) {
-            const uint8_t* qrow = sm + Q_Q + r * 128;
             const uint8_t* orow = sm + Q_O + r * 128;
-            uint32_t w[32];
-#pragma unroll
-            for (int c = 0; c < 8; c++) {
-                const uint4 a = *reinterpret_cast<const uint4*>(qrow + ((c ^ (r & 7)) << 4));
-                w[4 * c] = a.x; w[4 * c + 1] = a.y; w[4 * c + 2] = a.z; w[4 * c + 3] = a.w;
-            }
-            tmem_st32(tl + Q_TQ, w);
-#pragma unroll
-            for (int c = 0; c < 8; c++) {
-                const uint4 a = *reinterpret_cast<const uint4*>(orow + ((c ^ (r & 7)) << 4));
-                w[4 * c] = a.x; w[4 * c + 1] = a.y; w[4 * c + 2] = a.z; w[4 * c + 3] = a.w;
-            }
-            tmem_st32(tl + Q_TO, w);
-            tmem_st_wait();
+            float part = 0.0f;
             if (qv) {
-                const uint4* yr = reinterpret_cast<const uint4*>(y + (long long)(row0 + q) * C + h * D);
+                const uint4* yr = reinterpret_cast<const uint4*>(y + (long long)(row0 + q) * C + h * D + 32 * half);
 #pragma unroll
-                for (int c = 0; c < 8; c++) {
+                for (int c = 0; c < 4; c++) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(orow + (((4 * half + c) ^ (r & 7)) << 4));
                     const uint4 bb = yr[c];
+                    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
                     const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
-                        const uint32_t aw = w[4 * c + i];
-                        Dq = fmaf(__uint_as_float(aw << 16), __uint_as_float(bw[i] << 16), Dq);
-                        Dq = fmaf(__uint_as_float(aw & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), Dq);
+                        part = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), part);
+                        part = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), part);
                     }
                 }
-                Dlt[bh * T + q] = Dq;
             }
+            dpart[half * 128 + r] = part;
         }
-        tc_fence_before();
-        mbar_arrive(qo_tm);
-        const float Lq = qv ? lse[bh * T + q] * LOG2E : 0.0f;
+        rows_sync();
+        if (ok) {
+            Dq = dpart[r] + dpart[128 + r];  // the two halves in a fixed order
+            if (qv && half == 0) Dlt[bhl * T + q] = Dq;
+        }
+        const float Lq = qv ? lse[bhl * T + q] * LOG2E : 0.0f;
         for (int j = 0; j < nkv && ok; j++) {
             if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x200 + 7)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (j >= 2 * qt);
-            const int kq = q - j * BN;
-            // dS = P o (dP - D), packed bf16 in registers
-            uint32_t pk[32];
+            const int kq = q - j * BN - 32 * half;  // on the diagonal, this half's columns > kq are masked
+            uint32_t sw[32], pw[32];
+            tmem_ld32x2(tl + Q_TS + 32 * half, sw, tl + Q_TP + 32 * half, pw);
+            // dS = P o (dP - D), packed bf16
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 2; c++) {
-                uint32_t sw[32], pw[32];
-                tmem_ld32x2(tl + c * 32, sw, tl + BN + c * 32, pw);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float d0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -Lq)) * (__uint_as_float(pw[e]) - Dq);
-                    float d1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -Lq)) * (__uint_as_float(pw[e + 1]) - Dq);
-                    if (diag) {
-                        if (c * 32 + e > kq) d0 = 0.0f;
-                        if (c * 32 + e + 1 > kq) d1 = 0.0f;
-                    }
-                    pk[c * 16 + (e >> 1)] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
+            for (int e = 0; e < 32; e += 2) {
+                float d0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -Lq)) * (__uint_as_float(pw[e]) - Dq);
+                float d1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -Lq)) * (__uint_as_float(pw[e + 1]) - Dq);
+                if (diag) {
+                    if (e > kq) d0 = 0.0f;
+                    if (e + 1 > kq) d1 = 0.0f;
                 }
+                pk[e >> 1] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
             }
+            tmem_st16(tl + Q_TDS + 32 * (j & 1) + 16 * half, pk);
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(s_free);  // S and dP are consumed: the next pair may be computed
-            const int db = j & 1;
-            // buffer db was last read by the dQ MMA of block j - 2
-            if (j >= 2 && !mbar_wait_warp(&ds_free[db], ((j - 2) >> 1) & 1, abort_flag, flags, 0x200 + 8)) {
-                ok = false;
-                break;
-            }
-            uint32_t half[16];
-#pragma unroll
-            for (int i = 0; i < 16; i++) half[i] = pk[i];
-            store_row32(sm + Q_S + db * T128, r, 0, half);
-#pragma unroll
-            for (int i = 0; i < 16; i++) half[i] = pk[16 + i];
-            store_row32(sm + Q_S + db * T128, r, 32, half);
-            fence_proxy_async_smem();
-            mbar_arrive(&ds_full[db]);
+            warp_arrive(ds_full, lane);
         }
         if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x200 + 9)) {
             tc_fence_after();
-            float acc[64];
             uint32_t w[32];
-            tmem_ld32(tl + 2 * BN, w);
-#pragma unroll
-            for (int d = 0; d < 32; d++) acc[d] = __uint_as_float(w[d]);
-            tmem_ld32(tl + 2 * BN + 32, w);
-#pragma unroll
-            for (int d = 0; d < 32; d++) acc[32 + d] = __uint_as_float(w[d]);
-            if (qv) store_out64(dqkv + (long long)(row0 + q) * 3 * C + h * D, acc, 0.125f);
+            tmem_ld32(tl + Q_TACC + 32 * half, w);
+            if (qv) store_out32(dqkv + (long long)(row0 + q) * 3 * C + h * D + 32 * half, w, 0.125f);
         }
     }
     tc_fence_before();
@@ -616,19 +641,24 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     if (warp == 1) tmem_dealloc(tmem, Q_TMEM);
 }
 
-// ================================================================== backward: dK, dV
+// ------------------------------------------------------------------ dK, dV
+// One CTA per 128 keys (2 CTAs per SM), streaming the query blocks at and
+// after the diagonal: S^T = K Q_j^T and dP^T = V dO_j^T (K and V as A operands
+// from shared memory), then P^T and dS^T into tensor memory, and
+// dV += P^T dO_j, dK += dS^T Q_j (Q_j and dO_j read again as MN-major
+// operands) accumulate in tensor memory.
 constexpr int K_K = 0;
 constexpr int K_V = K_K + T128;
-constexpr int K_Q = K_V + T128;     // 2 stages
-constexpr int K_O = K_Q + 2 * T64;  // 2 stages
-constexpr int K_P = K_O + 2 * T64;  // P^T: [128 keys x 64 queries]
-constexpr int K_S = K_P + T128;     // dS^T
-constexpr int K_LD = K_S + T128;    // per row warp: log-sum-exp and D of the block's 64 queries
-constexpr int K_BAR = K_LD + 4 * 128 * 4;
+constexpr int K_ST = 3;                  // Q / dO block stages
+constexpr int K_Q = K_V + T128;
+constexpr int K_O = K_Q + K_ST * T64;
+constexpr int K_LD = K_O + K_ST * T64;   // per row warp: log-sum-exp and D of its 32 queries
+constexpr int K_BAR = K_LD + 8 * 64 * 4;
 constexpr int K_SMEM = K_BAR + 256 + 1024;
-constexpr uint32_t K_TMEM = 256;    // S^T 0..63, dP^T 64..127, dV 128..191, dK 192..255
+constexpr uint32_t K_TMEM = 256;         // S^T 0..63, dP^T 64..127, dV 128..191, dK 192..255
+constexpr uint32_t K_TS = 0, K_TP = 64, K_TV = 128, K_TK = 192;
 
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
                    const float* __restrict__ Dlt, bf16* __restrict__ dqkv, int T, int C, int H, int nbh,
@@ -637,14 +667,13 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + K_BAR);
     uint64_t* kv_full = bars + 0;
-    uint64_t* qo_full = bars + 1;   // [2]
-    uint64_t* qo_empty = bars + 3;  // [2]
-    uint64_t* st_full = bars + 5;
-    uint64_t* st_free = bars + 6;
-    uint64_t* ps_full = bars + 7;
-    uint64_t* ps_free = bars + 8;
+    uint64_t* qo_full = bars + 1;   // [3]
+    uint64_t* qo_empty = bars + 4;  // [3]
+    uint64_t* st_full = bars + 7;   // S^T_i, dP^T_i (and every earlier MMA) done
+    uint64_t* ps_full = bars + 8;   // P^T_i, dS^T_i written to tensor memory
     uint64_t* acc_full = bars + 9;
-    uint32_t* tmem_holder = (uint32_t*)(bars + 10);
+    uint64_t* drain = bars + 10;
+    uint32_t* tmem_holder = (uint32_t*)(bars + 11);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
@@ -659,15 +688,14 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        mbar_init(&qo_full[0], 1);
-        mbar_init(&qo_full[1], 1);
-        mbar_init(&qo_empty[0], 1);
-        mbar_init(&qo_empty[1], 1);
+        for (int i = 0; i < K_ST; i++) {
+            mbar_init(&qo_full[i], 1);
+            mbar_init(&qo_empty[i], 1);
+        }
         mbar_init(st_full, 1);
-        mbar_init(st_free, 128);
-        mbar_init(ps_full, 128);
-        mbar_init(ps_free, 1);
+        mbar_init(ps_full, BW_ROWS / 32);
         mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         init_done();
     }
@@ -686,18 +714,17 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < nq; i++) {
-                const int st = i & 1, j = j0 + i;
-                if (!mbar_wait(&qo_empty[st], ((i >> 1) & 1) ^ 1, abort_flag, flags, 0x300 + 1)) { ok = false; break; }
+                const int st = i % K_ST, j = j0 + i;
+                if (!mbar_wait(&qo_empty[st], ((i / K_ST) & 1) ^ 1, abort_flag, flags, 0x300 + 1)) { ok = false; break; }
                 mbar_expect_tx(&qo_full[st], 2 * T64);
                 tma_load_2d(smem_u32(sm + K_Q + st * T64), &tk, &qo_full[st], xq, row0 + j * BN);
                 tma_load_2d(smem_u32(sm + K_O + st * T64), &to, &qo_full[st], h * D, row0 + j * BN);
                 ++issued;
             }
             if (!ok) {
-                const long long t0 = clock64();
-                while (!mbar_try_wait(kv_full, 0) && clock64() - t0 < WAIT_CYCLES) {}
-                for (int i = (issued > 2 ? issued - 2 : 0); i < issued; i++)
-                    while (!mbar_try_wait(&qo_full[i & 1], (i >> 1) & 1) && clock64() - t0 < 2 * WAIT_CYCLES) {}
+                mbar_drain(kv_full, 0);
+                for (int i = (issued > K_ST ? issued - K_ST : 0); i < issued; i++)
+                    mbar_drain(&qo_full[i % K_ST], (i / K_ST) & 1);
             }
         }
     } else if (warp == 1) {
@@ -705,144 +732,108 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_A = idesc_bf16(BQ, D, false, true);
             const uint32_t sk = smem_u32(sm + K_K), sv = smem_u32(sm + K_V);
-            const uint32_t sp = smem_u32(sm + K_P), sds = smem_u32(sm + K_S);
             bool ok = mbar_wait(kv_full, 0, abort_flag, flags, 0x300 + 2);
-            // S^T_{i+1} and dP^T_{i+1} are issued as soon as the row threads
-            // hold S^T_i and dP^T_i in registers
-            auto issue_st = [&](int i) -> bool {
-                const int st = i & 1;
-                if (!mbar_wait(&qo_full[st], (i >> 1) & 1, abort_flag, flags, 0x300 + 3)) return false;
-                if (!mbar_wait(st_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 4)) return false;
+            bool issued = false;
+            for (int i = 0; i < nq && ok; i++) {
+                const int st = i % K_ST;
+                if (!mbar_wait(&qo_full[st], (i / K_ST) & 1, abort_flag, flags, 0x300 + 3)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
+                // S^T_i and dP^T_i (two independent chains, interleaved); they
+                // overwrite P^T_{i-1} and dS^T_{i-1}, read by MMAs issued before
 #pragma unroll
-                for (int k = 0; k < D / 16; k++) {  // two independent chains, interleaved
-                    umma_bf16(tmem, sdesc(sk + 32 * k, 16, 1024), sdesc(sq + 32 * k, 16, 1024), ID, k > 0);
-                    umma_bf16(tmem + BN, sdesc(sv + 32 * k, 16, 1024), sdesc(so + 32 * k, 16, 1024), ID, k > 0);
+                for (int k = 0; k < D / 16; k++) {
+                    umma_bf16(tmem + K_TS, sdesc(sk + 32 * k, 16, 1024), sdesc(sq + 32 * k, 16, 1024), ID, k > 0);
+                    umma_bf16(tmem + K_TP, sdesc(sv + 32 * k, 16, 1024), sdesc(so + 32 * k, 16, 1024), ID, k > 0);
                 }
+                issued = true;
                 umma_commit(st_full);
-                return true;
-            };
-            if (ok) ok = issue_st(0);
-            for (int i = 0; i < nq && ok; i++) {
-                if (i + 1 < nq && !issue_st(i + 1)) { ok = false; break; }
-                const int st = i & 1;
                 if (!mbar_wait(ps_full, i & 1, abort_flag, flags, 0x300 + 5)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++) {
                     const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
-                    umma_bf16(tmem + 2 * BN, sdesc(sp + 32 * k, 16, 1024), sdesc(so + k * 2048, T64, 1024),
-                              ID_A, acc);
-                    umma_bf16(tmem + 3 * BN, sdesc(sds + 32 * k, 16, 1024), sdesc(sq + k * 2048, T64, 1024),
-                              ID_A, acc);
+                    umma_bf16_ts(tmem + K_TV, tmem + K_TS + split_a_col(k), sdesc(so + k * 2048, T64, 1024), ID_A, acc);
+                    umma_bf16_ts(tmem + K_TK, tmem + K_TP + split_a_col(k), sdesc(sq + k * 2048, T64, 1024), ID_A, acc);
                 }
                 umma_commit(&qo_empty[st]);
-                umma_commit(ps_free);
             }
             if (ok) umma_commit(acc_full);
+            else if (issued) {
+                umma_commit(drain);
+                mbar_drain(drain, 0);
+            }
         }
     } else {
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int key = kt * BQ + r;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const long long bh = (long long)b * H + h;
-        const float* lrow = lse + bh * T;
-        const float* drow = Dlt + bh * T;
+        const long long bhl = (long long)b * H + h;
+        const float* lrow = lse + bhl * T;
+        const float* drow = Dlt + bhl * T;
         bool ok = true;
-        // The log-sum-exp (base 2) and D of query block i are fetched one block
-        // ahead into registers (lane l: queries 64i + l and 64i + 32 + l), then
-        // placed in this warp's slice of shared memory, from which every lane
-        // reads them as broadcasts.
-        float* sl = reinterpret_cast<float*>(sm + K_LD) + quarter * 128;  // [64 L | 64 D]
-        float Ln[2], Dn[2];
+        // The log-sum-exp (base 2) and D of this warp's 32 queries of block i
+        // are fetched one block ahead (lane l: query 64 (j0 + i) + 32 half + l),
+        // then placed in this warp's slice of shared memory, from which every
+        // lane reads them as broadcasts.
+        float* sl = reinterpret_cast<float*>(sm + K_LD) + (warp - 2) * 64;  // [32 L | 32 D]
+        float Ln, Dn;
         auto fetch = [&](int i) {
-#pragma unroll
-            for (int c = 0; c < 2; c++) {
-                const int qq = (j0 + i) * BN + c * 32 + lane;
-                Ln[c] = qq < T ? __ldg(lrow + qq) * LOG2E : INFINITY;
-                Dn[c] = qq < T ? __ldg(drow + qq) : 0.0f;
-            }
+            const int qq = (j0 + i) * BN + 32 * half + lane;
+            Ln = qq < T ? __ldg(lrow + qq) * LOG2E : INFINITY;
+            Dn = qq < T ? __ldg(drow + qq) : 0.0f;
         };
         fetch(0);
         for (int i = 0; i < nq; i++) {
             const int j = j0 + i;
             __syncwarp();  // the previous block's reads of the slice are done
-            sl[lane] = Ln[0];
-            sl[32 + lane] = Ln[1];
-            sl[64 + lane] = Dn[0];
-            sl[96 + lane] = Dn[1];
+            sl[lane] = Ln;
+            sl[32 + lane] = Dn;
             __syncwarp();
             if (i + 1 < nq) fetch(i + 1);
             if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (i < 2);  // query blocks that overlap this key tile
-            uint32_t pk[32], dk[32];
+            const int q0 = j * BN + 32 * half;
+            uint32_t sw[32], dw[32];
+            tmem_ld32x2(tl + K_TS + 32 * half, sw, tl + K_TP + 32 * half, dw);
+            uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int c = 0; c < 2; c++) {
-                const int q0 = j * BN + c * 32;
-                uint32_t sw[32], dw[32];
-                tmem_ld32x2(tl + c * 32, sw, tl + BN + c * 32, dw);
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 L4 = *reinterpret_cast<const float4*>(sl + c * 32 + e);
-                    const float4 D4 = *reinterpret_cast<const float4*>(sl + 64 + c * 32 + e);
-                    float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L4.x));
-                    float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L4.y));
-                    float p2 = ex2(fmaf(__uint_as_float(sw[e + 2]), SL2, -L4.z));
-                    float p3 = ex2(fmaf(__uint_as_float(sw[e + 3]), SL2, -L4.w));
-                    if (diag) {
-                        if (q0 + e < key) p0 = 0.0f;
-                        if (q0 + e + 1 < key) p1 = 0.0f;
-                        if (q0 + e + 2 < key) p2 = 0.0f;
-                        if (q0 + e + 3 < key) p3 = 0.0f;
-                    }
-                    pk[c * 16 + (e >> 1)] = pack_bf2(p0, p1);
-                    pk[c * 16 + (e >> 1) + 1] = pack_bf2(p2, p3);
-                    dk[c * 16 + (e >> 1)] =
-                        pack_bf2(p0 * (__uint_as_float(dw[e]) - D4.x), p1 * (__uint_as_float(dw[e + 1]) - D4.y));
-                    dk[c * 16 + (e >> 1) + 1] =
-                        pack_bf2(p2 * (__uint_as_float(dw[e + 2]) - D4.z), p3 * (__uint_as_float(dw[e + 3]) - D4.w));
+            for (int e = 0; e < 32; e += 4) {
+                const float4 L4 = *reinterpret_cast<const float4*>(sl + e);
+                const float4 D4 = *reinterpret_cast<const float4*>(sl + 32 + e);
+                float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L4.x));
+                float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L4.y));
+                float p2 = ex2(fmaf(__uint_as_float(sw[e + 2]), SL2, -L4.z));
+                float p3 = ex2(fmaf(__uint_as_float(sw[e + 3]), SL2, -L4.w));
+                if (diag) {
+                    if (q0 + e < key) p0 = 0.0f;
+                    if (q0 + e + 1 < key) p1 = 0.0f;
+                    if (q0 + e + 2 < key) p2 = 0.0f;
+                    if (q0 + e + 3 < key) p3 = 0.0f;
                 }
+                pk[e >> 1] = pack_bf2(p0, p1);
+                pk[(e >> 1) + 1] = pack_bf2(p2, p3);
+                dk[e >> 1] = pack_bf2(p0 * (__uint_as_float(dw[e]) - D4.x), p1 * (__uint_as_float(dw[e + 1]) - D4.y));
+                dk[(e >> 1) + 1] =
+                    pack_bf2(p2 * (__uint_as_float(dw[e + 2]) - D4.z), p3 * (__uint_as_float(dw[e + 3]) - D4.w));
             }
+            tmem_st16(tl + K_TS + 32 * half, pk);
+            tmem_st16(tl + K_TP + 32 * half, dk);
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(st_free);  // S^T and dP^T are consumed
-            // P^T and dS^T buffers: read by the dV / dK MMAs of block i - 1
-            if (!mbar_wait_warp(ps_free, (i & 1) ^ 1, abort_flag, flags, 0x300 + 7)) { ok = false; break; }
-            uint32_t half[16];
-#pragma unroll
-            for (int c = 0; c < 2; c++) {
-#pragma unroll
-                for (int t = 0; t < 16; t++) half[t] = pk[c * 16 + t];
-                store_row32(sm + K_P, r, c * 32, half);
-#pragma unroll
-                for (int t = 0; t < 16; t++) half[t] = dk[c * 16 + t];
-                store_row32(sm + K_S, r, c * 32, half);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(ps_full);
+            warp_arrive(ps_full, lane);
         }
         if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x300 + 8)) {
             tc_fence_after();
-            float acc[64];
             uint32_t w[32];
-            bf16* base = dqkv + (long long)(row0 + key) * 3 * C + h * D;
-            tmem_ld32(tl + 2 * BN, w);
-#pragma unroll
-            for (int d = 0; d < 32; d++) acc[d] = __uint_as_float(w[d]);
-            tmem_ld32(tl + 2 * BN + 32, w);
-#pragma unroll
-            for (int d = 0; d < 32; d++) acc[32 + d] = __uint_as_float(w[d]);
-            if (key < T) store_out64(base + 2 * C, acc, 1.0f);  // dV
-            tmem_ld32(tl + 3 * BN, w);
-#pragma unroll
-            for (int d = 0; d < 32; d++) acc[d] = __uint_as_float(w[d]);
-            tmem_ld32(tl + 3 * BN + 32, w);
-#pragma unroll
-            for (int d = 0; d < 32; d++) acc[32 + d] = __uint_as_float(w[d]);
-            if (key < T) store_out64(base + C, acc, 0.125f);  // dK, times 1/sqrt(64)
+            bf16* base = dqkv + (long long)(row0 + key) * 3 * C + h * D + 32 * half;
+            tmem_ld32(tl + K_TV + 32 * half, w);
+            if (key < T) store_out32(base + 2 * C, w, 1.0f);  // dV
+            tmem_ld32(tl + K_TK + 32 * half, w);
+            if (key < T) store_out32(base + C, w, 0.125f);   // dK, times 1/sqrt(64)
         }
     }
     tc_fence_before();
@@ -901,10 +892,10 @@ bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, co
     if (!attn_set_smem()) return false;
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
-    fa5::k_attn_bwd_dq_tc<<<grid, fa5::THREADS, fa5::Q_SMEM, L.stream>>>(
+    fa5::k_attn_bwd_dq_tc<<<grid, fa5::BW_THREADS, fa5::Q_SMEM, L.stream>>>(
         tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, B * H, L.flags);
     L.count();
-    fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::THREADS, fa5::K_SMEM, L.stream>>>(
+    fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::BW_THREADS, fa5::K_SMEM, L.stream>>>(
         tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, B * H, L.flags);
     return true;
 }
