@@ -410,6 +410,37 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 // Named barrier for the 256 row threads only.
 __device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// Column sums of a 32 x 32 block held one row per lane (v: the lane's 32
+// columns): after a butterfly that halves the columns each lane keeps at each
+// step, lane l holds the sum over the 32 rows of column l.  The order of the
+// additions is fixed, so the result is deterministic.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; i++) {
+            const float send = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+// The tile's column sums of one 32-column output half: each warp's 32 rows by
+// warp_colsum32, then the four quarter warps of the half in quarter order
+// (cs: [2 halves][4 quarters][32] floats of shared memory).  Reached by all
+// 256 row threads; `v` holds zeros for rows that are not valid.
+__device__ __forceinline__ void tile_colsum(float (&v)[32], float* cs, float* dst, int half, int quarter, int lane) {
+    cs[(half * 4 + quarter) * 32 + lane] = warp_colsum32(v, lane);
+    rows_sync();
+    if (quarter == 0 && dst)
+        dst[lane] = cs[(half * 4) * 32 + lane] + cs[(half * 4 + 1) * 32 + lane] + cs[(half * 4 + 2) * 32 + lane] +
+                    cs[(half * 4 + 3) * 32 + lane];
+    rows_sync();
+}
+
 // Spins until the phase completes or the long landing bound passes, with no
 // abort check: used only to let copies already issued land before a CTA
 // that gave up exits.
@@ -436,7 +467,8 @@ constexpr int Q_KST = 3;                 // K stages: K_j is read by S_j and by 
 constexpr int Q_K = Q_O + T128;
 constexpr int Q_V = Q_K + Q_KST * T64;   // 2 stages: V_j is free once dP_j is done
 constexpr int Q_DP = Q_V + 2 * T64;      // D partials [2 halves][128 rows]
-constexpr int Q_BAR = Q_DP + 2 * 128 * 4;
+constexpr int Q_CS = Q_DP + 2 * 128 * 4; // column sums [2 halves][4 quarters][32]
+constexpr int Q_BAR = Q_CS + 2 * 4 * 32 * 4;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
 constexpr uint32_t Q_TMEM = 256;         // S 0..63, dP 64..127, dS[2] 128..191, dQ 192..255
 constexpr uint32_t Q_TS = 0, Q_TP = 64, Q_TDS = 128, Q_TACC = 192;
@@ -445,7 +477,7 @@ __global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
                  const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
-                 int T, int C, int H, int nbh, int* flags) {
+                 float* __restrict__ bpart, int T, int C, int H, int nbh, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
@@ -628,12 +660,22 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tc_fence_before();
             warp_arrive(ds_full, lane);
         }
+        float cv[32];
+#pragma unroll
+        for (int d = 0; d < 32; d++) cv[d] = 0.0f;
         if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x200 + 9)) {
             tc_fence_after();
             uint32_t w[32];
             tmem_ld32(tl + Q_TACC + 32 * half, w);
-            if (qv) store_out32(dqkv + (long long)(row0 + q) * 3 * C + h * D + 32 * half, w, 0.125f);
+            if (qv) {
+                store_out32(dqkv + (long long)(row0 + q) * 3 * C + h * D + 32 * half, w, 0.125f);
+#pragma unroll
+                for (int d = 0; d < 32; d++) cv[d] = __uint_as_float(w[d]) * 0.125f;
+            }
         }
+        if (bpart)  // the qkv bias gradient's partial: this tile's column sums of dQ
+            tile_colsum(cv, reinterpret_cast<float*>(sm + Q_CS),
+                        bpart + ((long long)b * nqt + qt) * 3 * C + h * D + 32 * half, half, quarter, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -653,7 +695,8 @@ constexpr int K_ST = 3;                  // Q / dO block stages
 constexpr int K_Q = K_V + T128;
 constexpr int K_O = K_Q + K_ST * T64;
 constexpr int K_LD = K_O + K_ST * T64;   // per row warp: log-sum-exp and D of its 32 queries
-constexpr int K_BAR = K_LD + 8 * 64 * 4;
+constexpr int K_CS = K_LD + 8 * 64 * 4;  // column sums [2 halves][4 quarters][32]
+constexpr int K_BAR = K_CS + 2 * 4 * 32 * 4;
 constexpr int K_SMEM = K_BAR + 256 + 1024;
 constexpr uint32_t K_TMEM = 256;         // S^T 0..63, dP^T 64..127, dV 128..191, dK 192..255
 constexpr uint32_t K_TS = 0, K_TP = 64, K_TV = 128, K_TK = 192;
@@ -661,8 +704,8 @@ constexpr uint32_t K_TS = 0, K_TP = 64, K_TV = 128, K_TK = 192;
 __global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
-                   const float* __restrict__ Dlt, bf16* __restrict__ dqkv, int T, int C, int H, int nbh,
-                   int* flags) {
+                   const float* __restrict__ Dlt, bf16* __restrict__ dqkv, float* __restrict__ bpart, int T,
+                   int C, int H, int nbh, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + K_BAR);
@@ -826,14 +869,27 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tc_fence_before();
             warp_arrive(ps_full, lane);
         }
-        if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x300 + 8)) {
-            tc_fence_after();
-            uint32_t w[32];
-            bf16* base = dqkv + (long long)(row0 + key) * 3 * C + h * D + 32 * half;
-            tmem_ld32(tl + K_TV + 32 * half, w);
-            if (key < T) store_out32(base + 2 * C, w, 1.0f);  // dV
-            tmem_ld32(tl + K_TK + 32 * half, w);
-            if (key < T) store_out32(base + C, w, 0.125f);   // dK, times 1/sqrt(64)
+        const bool got = ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x300 + 8);
+        if (got) tc_fence_after();
+        bf16* base = dqkv + (long long)(row0 + key) * 3 * C + h * D + 32 * half;
+        // the qkv bias gradient's partials: this tile's column sums of dV, then dK
+        float* brow = bpart ? bpart + ((long long)b * gridDim.y + kt) * 3 * C + h * D + 32 * half : nullptr;
+#pragma unroll 1
+        for (int which = 0; which < 2; which++) {  // 0: dV, 1: dK (times 1/sqrt(64))
+            const float scale = which ? 0.125f : 1.0f;
+            float v[32];
+#pragma unroll
+            for (int d = 0; d < 32; d++) v[d] = 0.0f;
+            if (got) {
+                uint32_t w[32];
+                tmem_ld32(tl + (which ? K_TK : K_TV) + 32 * half, w);
+                if (key < T) {
+                    store_out32(base + (which ? C : 2 * C), w, scale);
+#pragma unroll
+                    for (int d = 0; d < 32; d++) v[d] = __uint_as_float(w[d]) * scale;
+                }
+            }
+            if (brow) tile_colsum(v, reinterpret_cast<float*>(sm + K_CS), brow + (which ? C : 2 * C), half, quarter, lane);
         }
     }
     tc_fence_before();
@@ -880,7 +936,8 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
 }
 
 bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
-                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt) {
+                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt,
+                             float* bpart) {
     if (L.dry) return true;
     CUtensorMap tq, tk, to128, to64;
     if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
@@ -893,10 +950,10 @@ bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, co
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_bwd_dq_tc<<<grid, fa5::BW_THREADS, fa5::Q_SMEM, L.stream>>>(
-        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, B * H, L.flags);
+        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags);
     L.count();
     fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::BW_THREADS, fa5::K_SMEM, L.stream>>>(
-        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, T, C, H, B * H, L.flags);
+        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags);
     return true;
 }
 

@@ -442,16 +442,18 @@ __global__ void k_sum_partials(const float* __restrict__ part, int nblk, int C,
 size_t layernorm_bwd_scratch_floats(int M, int C) {
     size_t a = (size_t)((M + LN_ROWS - 1) / LN_ROWS) * 2 * C + 64;
     size_t b = ln_bwd_bf16_scratch_floats(C);
-    return a > b ? a : b;
+    size_t c = colsum_scratch_floats(M, C);
+    return a > b ? (a > c ? a : c) : (b > c ? b : c);
 }
 
 void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const float* mean, const float* rstd, const void* dy, void* dx,
                           float* dw, float* db, int M, int C, bool accumulate, float* scratch,
-                          bool acc_params) {
-    if (L.dry) return;
-    if (bf16 && launch_ln_bwd_bf16(L, x, w, mean, rstd, dy, dx, dw, db, M, C, accumulate, scratch, acc_params))
+                          bool acc_params, float* dres) {
+    if (bf16 && launch_ln_bwd_bf16(L, x, w, mean, rstd, dy, dx, dw, db, M, C, accumulate, scratch, acc_params,
+                                   dres))
         return;
+    if (L.dry) return;
     const int nblk = (M + LN_ROWS - 1) / LN_ROWS;
     const size_t smem = (size_t)LN_BWD_WARPS * 2 * C * sizeof(float);
     static PerDevice attr;
@@ -478,6 +480,9 @@ void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void*
             M, C, accumulate ? 1 : 0);
     L.count();
     k_sum_partials<<<blocks_for(2 * C, 256), 256, 0, L.stream>>>(scratch, nblk, C, dw, db, acc_params ? 1 : 0);
+    // the column sums of the finished dx, in a second pass (the scratch is free
+    // again once the partials above are summed: stream order)
+    if (dres) launch_colsum(L, bf16, dx, M, C, dres, scratch, acc_params);
 }
 
 // ================================================================== cross entropy
@@ -930,7 +935,15 @@ __global__ void k_attn_bwd_dkv_simt(const T* __restrict__ qkv, const float* __re
     }
 }
 
-size_t attention_bwd_scratch_floats(int B, int T, int H) { return (size_t)B * H * T + 64; }
+// D = rowsum(dO o O) [B, H, T], then the qkv bias-gradient partials: one row
+// of 3C per (sequence, 128-row tile) for the tensor-core kernels, or the
+// column-sum partials of the generic pass, whichever is larger
+static size_t attn_d_floats(int B, int T, int H) { return ((size_t)B * H * T + 63) / 64 * 64; }
+size_t attention_bwd_scratch_floats(int B, int T, int C, int H) {
+    const size_t tiles = (size_t)B * ((T + 127) / 128) * 3 * C;
+    const size_t cs = colsum_scratch_floats(B * T, 3 * C);
+    return attn_d_floats(B, T, H) + (tiles > cs ? tiles : cs) + 64;
+}
 
 template <typename T, int HD>
 static void attn_fwd_simt(const Launch& L, const void* qkv, void* y, float* lse, int B, int T_,
@@ -988,18 +1001,23 @@ void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, 
 
 void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const void* y,
                           const float* lse, const void* dy, void* dqkv, int B, int T, int C,
-                          int H, float* scratch) {
+                          int H, float* scratch, float* dbias, bool acc_bias) {
     if (L.dry) return;
     const bool bf_only = bf16 && !L.f16;
+    float* bpart = scratch + attn_d_floats(B, T, H);
     if (attention_tc_eligible(bf_only, C, H) &&
-        launch_attention_bwd_tc(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch))
-        return;
-    if (attention_mma_eligible(bf_only, C, H)) {
-        launch_attention_bwd_mma(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch);
+        launch_attention_bwd_tc(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch, dbias ? bpart : nullptr)) {
+        if (dbias) launch_sum_rows(L, bpart, B * ((T + 127) / 128), 3 * C, 3 * C, dbias, nullptr, acc_bias);
         return;
     }
-    const int hd = C / H;
-    TT_HD_DISPATCH(hd, attn_bwd_simt, L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch);
+    if (attention_mma_eligible(bf_only, C, H)) {
+        launch_attention_bwd_mma(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch);
+    } else {
+        const int hd = C / H;
+        TT_HD_DISPATCH(hd, attn_bwd_simt, L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch);
+    }
+    // the bias gradient of the qkv layer: column sums of dqkv, a second pass
+    if (dbias) launch_colsum(L, bf16, dqkv, B * T, 3 * C, dbias, bpart, acc_bias);
 }
 
 }  // namespace tt

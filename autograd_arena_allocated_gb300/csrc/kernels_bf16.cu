@@ -94,22 +94,29 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
 // rows; at the end the block adds its warps' partials in warp order through
 // shared memory and writes one partial row, and k_sum_rows adds the G block
 // rows in block order (no atomics anywhere).
-template <int NV>
+//
+// With RES, the column sums of the finished dx (after the accumulation into
+// the residual stream's gradient) are kept as a third partial: this
+// LayerNorm's input is a residual-stream tensor whose gradient is complete
+// once this kernel has added its share, and that tensor is the output of a
+// linear layer, whose bias gradient is exactly these column sums.
+template <int NV, bool RES>
 __global__ void __launch_bounds__(LNV_WARPS * 32, 2)
 k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
               const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
               float* __restrict__ part, int M, int C, int accumulate) {
-    extern __shared__ float s_part[];  // [LNV_WARPS][2C]: each warp's dw | db partials
+    constexpr int NP = RES ? 3 : 2;
+    extern __shared__ float s_part[];  // [LNV_WARPS][NP C]: each warp's dw | db (| dres) partials
     __shared__ uint4 s_gamma[128];        // gamma, 8 bf16 per entry (C <= 1024)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvec = C >> 3;
     const float inv_c = 1.0f / (float)C;
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) s_gamma[v] = reinterpret_cast<const uint4*>(w)[v];
-    float aw[NV][8], ab[NV][8];
+    float aw[NV][8], ab[NV][8], ar[RES ? NV : 1][8];
 #pragma unroll
     for (int i = 0; i < NV; i++)
 #pragma unroll
-        for (int e = 0; e < 8; e++) { aw[i][e] = 0.0f; ab[i][e] = 0.0f; }
+        for (int e = 0; e < 8; e++) { aw[i][e] = 0.0f; ab[i][e] = 0.0f; if (RES) ar[RES ? i : 0][e] = 0.0f; }
     __syncthreads();
     for (long long row = (long long)blockIdx.x * LNV_WARPS + warp; row < M;
          row += (long long)gridDim.x * LNV_WARPS) {
@@ -169,12 +176,16 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
 #pragma unroll
                     for (int e = 0; e < 8; e++) o[e] += old[e];
                 }
+                if (RES) {
+#pragma unroll
+                    for (int e = 0; e < 8; e++) ar[RES ? i : 0][e] += o[e];
+                }
                 xo[vi] = pack8(o);
             }
         }
     }
     // the block's partials: warps in warp order
-    float* pw = s_part + warp * 2 * C;
+    float* pw = s_part + warp * NP * C;
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int vi = lane + 32 * i;
@@ -185,14 +196,20 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
             dwp[1] = make_float4(aw[i][4], aw[i][5], aw[i][6], aw[i][7]);
             dbp[0] = make_float4(ab[i][0], ab[i][1], ab[i][2], ab[i][3]);
             dbp[1] = make_float4(ab[i][4], ab[i][5], ab[i][6], ab[i][7]);
+            if (RES) {
+                const int ri = RES ? i : 0;
+                float4* drp = reinterpret_cast<float4*>(pw + 2 * C + vi * 8);
+                drp[0] = make_float4(ar[ri][0], ar[ri][1], ar[ri][2], ar[ri][3]);
+                drp[1] = make_float4(ar[ri][4], ar[ri][5], ar[ri][6], ar[ri][7]);
+            }
         }
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+    for (int c = threadIdx.x; c < NP * C; c += blockDim.x) {
         float s = 0.0f;
 #pragma unroll
-        for (int k = 0; k < LNV_WARPS; k++) s += s_part[k * 2 * C + c];
-        part[(long long)blockIdx.x * 2 * C + c] = s;
+        for (int k = 0; k < LNV_WARPS; k++) s += s_part[k * NP * C + c];
+        part[(long long)blockIdx.x * NP * C + c] = s;
     }
 }
 
@@ -201,13 +218,13 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
 // loads in flight); the warp sums are then added in warp order.  The G rows
 // are few (a few hundred at most), so the kernel is latency bound: many warps
 // keep the number of dependent load rounds per warp at one or two.  (Used for
-// the LayerNorm dw/db partials, with out_a taking columns [0, C) and out_b
-// columns [C, 2C), and for bias sums.)
+// the LayerNorm dw/db (and dres) partials, with out_a taking columns [0, C),
+// out_b columns [C, 2C) and out_c columns [2C, 3C), and for bias sums.)
 constexpr int SR_WARPS = 32;
 
 __global__ void __launch_bounds__(SR_WARPS * 32)
 k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* __restrict__ out_a,
-           float* __restrict__ out_b, int acc) {
+           float* __restrict__ out_b, float* __restrict__ out_c, int acc) {
     __shared__ float sm[SR_WARPS][33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
@@ -230,41 +247,43 @@ k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* _
 #pragma unroll
         for (int w = 0; w < SR_WARPS; w++) t += sm[w][lane];
         if (c < split) { if (out_a) out_a[c] = acc ? out_a[c] + t : t; }
-        else if (out_b) out_b[c - split] = acc ? out_b[c - split] + t : t;
+        else if (c < 2 * split) { if (out_b) out_b[c - split] = acc ? out_b[c - split] + t : t; }
+        else if (out_c) out_c[c - 2 * split] = acc ? out_c[c - 2 * split] + t : t;
     }
 }
 
 void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int split, float* out_a,
-                     float* out_b, bool acc) {
+                     float* out_b, bool acc, float* out_c) {
     if (L.dry) return;
     L.count();
-    k_sum_rows<<<(ncols + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(part, G, ncols, split, out_a, out_b, acc ? 1 : 0);
+    k_sum_rows<<<(ncols + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(part, G, ncols, split, out_a, out_b, out_c,
+                                                                  acc ? 1 : 0);
 }
 
 constexpr int LN_BWD_MAX_BLOCKS = 1024;
 
 // G = the blocks that are resident at once (SMs x blocks per SM), so that
 // every block runs its rows in one wave; fewer when M is small.
-template <int NV>
+template <int NV, bool RES>
 static int ln_bwd_blocks(const Launch& L, int M) {
-    static int per_sm[5] = {0, 0, 0, 0, 0};
-    if (!per_sm[NV]) {
-        int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_ln_bwd_bf16<NV>, LNV_WARPS * 32,
-                                                          (LNV_WARPS * 2) * 1024 * sizeof(float)) !=
-                cudaSuccess || b < 1) {
+    static PerDevice per_sm;
+    const int b = per_sm.value([] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_ln_bwd_bf16<NV, RES>, LNV_WARPS * 32,
+                                                          (LNV_WARPS * (RES ? 3 : 2)) * 1024 * sizeof(float)) !=
+                cudaSuccess || n < 1) {
             cudaGetLastError();
-            b = 1;
+            n = 1;
         }
-        per_sm[NV] = b;
-    }
-    int g = per_sm[NV] * (L.num_sms > 0 ? L.num_sms : 148);
+        return n;
+    });
+    int g = b * (L.num_sms > 0 ? L.num_sms : 148);
     if (g > LN_BWD_MAX_BLOCKS) g = LN_BWD_MAX_BLOCKS;
     const int need = (M + LNV_WARPS - 1) / LNV_WARPS;
     return need < g ? need : g;
 }
 
-size_t ln_bwd_bf16_scratch_floats(int C) { return (size_t)LN_BWD_MAX_BLOCKS * 2 * C + 64; }
+size_t ln_bwd_bf16_scratch_floats(int C) { return (size_t)LN_BWD_MAX_BLOCKS * 3 * C + 64; }
 
 bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const void* b, void* y,
                         float* mean, float* rstd, int M, int C) {
@@ -282,31 +301,38 @@ bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const voi
 
 bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
                         const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
-                        int C, bool accumulate, float* scratch, bool acc_params) {
+                        int C, bool accumulate, float* scratch, bool acc_params, float* dres) {
     if (L.f16 || C % 8 || C > 1024) return false;
     if (L.dry) return true;
     const int nv = (C / 8 + 31) / 32;
-    const size_t smem = (size_t)(LNV_WARPS * 2) * C * sizeof(float);
+    const int np = dres ? 3 : 2;
+    const size_t smem = (size_t)(LNV_WARPS * np) * C * sizeof(float);
     static PerDevice attr;
     attr.once([] {
-        const int mx = (LNV_WARPS * 2) * 1024 * (int)sizeof(float);
-        cudaFuncSetAttribute(k_ln_bwd_bf16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        cudaFuncSetAttribute(k_ln_bwd_bf16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        cudaFuncSetAttribute(k_ln_bwd_bf16<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        cudaFuncSetAttribute(k_ln_bwd_bf16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        const int mx2 = (LNV_WARPS * 2) * 1024 * (int)sizeof(float);
+        const int mx3 = (LNV_WARPS * 3) * 1024 * (int)sizeof(float);
+#define LNA(NV)                                                                                        \
+        cudaFuncSetAttribute(k_ln_bwd_bf16<NV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx2); \
+        cudaFuncSetAttribute(k_ln_bwd_bf16<NV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx3)
+        LNA(1); LNA(2); LNA(3); LNA(4);
+#undef LNA
         return true;
     });
     L.count();
     int G = 0;
-#define LNB(NV) G = ln_bwd_blocks<NV>(L, M); \
-    k_ln_bwd_bf16<NV><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
+#define LNB(NV, RES) G = ln_bwd_blocks<NV, RES>(L, M); \
+    k_ln_bwd_bf16<NV, RES><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
         (const bf16*)x, (const bf16*)w, mean, rstd, (const bf16*)dy, (bf16*)dx, scratch, M, C, \
         accumulate ? 1 : 0)
-    if (nv == 1) { LNB(1); } else if (nv == 2) { LNB(2); } else if (nv == 3) { LNB(3); } else { LNB(4); }
+    if (dres) {
+        if (nv == 1) { LNB(1, true); } else if (nv == 2) { LNB(2, true); } else if (nv == 3) { LNB(3, true); } else { LNB(4, true); }
+    } else {
+        if (nv == 1) { LNB(1, false); } else if (nv == 2) { LNB(2, false); } else if (nv == 3) { LNB(3, false); } else { LNB(4, false); }
+    }
 #undef LNB
     L.count();
-    k_sum_rows<<<(2 * C + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(scratch, G, 2 * C, C, dw, db,
-                                                                  acc_params ? 1 : 0);
+    k_sum_rows<<<(np * C + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(scratch, G, np * C, C, dw, db, dres,
+                                                                   acc_params ? 1 : 0);
     return true;
 }
 

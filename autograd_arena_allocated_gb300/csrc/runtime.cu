@@ -40,6 +40,7 @@ struct TapeTensor {
     long long rows = 0, cols = 0;
     int producer = -1;       // record index
     int consumers = 0;
+    int first_consumer = -1;  // record index of the first record that read it
     bool grad_is_pre = false;  // grad holds d/d(pre-activation) of a GELU producer
 };
 
@@ -65,6 +66,9 @@ struct Record {
     int b_rows = 0, n_store = 0;
     long long ldy = 0;
     bool gelu = false;
+    // LINEAR: the bias gradient was produced by the backward of a consumer of
+    // this layer's output (it is the column sum of that output's gradient)
+    bool db_fused = false;
 };
 
 // ------------------------------------------------------------------ profiling
@@ -219,6 +223,13 @@ static void* arena_alloc(tt_ctx* c, size_t bytes) {
 
 static size_t esize(tt_dtype d) { return d == TT_FP32 ? 4 : 2; }
 
+// record `rec` reads tensor t
+static void add_consumer(tt_ctx* c, int t, int rec) {
+    TapeTensor& x = c->tensors[t];
+    if (x.first_consumer < 0) x.first_consumer = rec;
+    x.consumers++;
+}
+
 static int new_tensor(tt_ctx* c, long long rows, long long cols, size_t elem) {
     TapeTensor t;
     t.rows = rows;
@@ -294,7 +305,7 @@ static int op_layernorm(tt_ctx* c, int x, const void* w, const void* b, float* d
     r.in = x; r.out = out; r.W = w; r.b = b; r.dW = dw; r.db = db;
     r.mean = mean; r.rstd = rstd; r.M = M; r.N = C;
     c->tape.push_back(r);
-    c->tensors[x].consumers++;
+    add_consumer(c, x, (int)c->tape.size() - 1);
     c->tensors[out].producer = (int)c->tape.size() - 1;
     return out;
 }
@@ -330,8 +341,8 @@ static int op_linear(tt_ctx* c, int x, const void* W, const void* b, float* dW, 
     r.W = W; r.b = b; r.dW = dW; r.db = db;
     r.M = M; r.K = K; r.N = N; r.b_rows = b_rows; r.n_store = n_store; r.gelu = gelu;
     c->tape.push_back(r);
-    c->tensors[x].consumers++;
-    if (res >= 0) c->tensors[res].consumers++;
+    add_consumer(c, x, (int)c->tape.size() - 1);
+    if (res >= 0) add_consumer(c, res, (int)c->tape.size() - 1);
     c->tensors[out].producer = (int)c->tape.size() - 1;
     return out;
 }
@@ -353,7 +364,7 @@ static int op_attention(tt_ctx* c, int qkv, int B, int T) {
     r.kind = R_ATTN;
     r.in = qkv; r.out = out; r.lse = lse; r.B = B; r.T = T; r.H = m.H; r.N = m.C; r.M = M;
     c->tape.push_back(r);
-    c->tensors[qkv].consumers++;
+    add_consumer(c, qkv, (int)c->tape.size() - 1);
     c->tensors[out].producer = (int)c->tape.size() - 1;
     return out;
 }
@@ -374,7 +385,7 @@ static void op_xent(tt_ctx* c, int z, const int32_t* targets, int V) {
     r.kind = R_XENT;
     r.in = z; r.M = M; r.N = V; r.idx = targets;
     c->tape.push_back(r);
-    c->tensors[z].consumers++;
+    add_consumer(c, z, (int)c->tape.size() - 1);
     c->tensors[z].grad = c->tensors[z].data;
 }
 
@@ -393,7 +404,8 @@ static void* grad_for_write(tt_ctx* c, int t, bool* accumulate) {
     return x.grad;
 }
 
-static tt_status backward_record(tt_ctx* c, const Record& r) {
+static tt_status backward_record(tt_ctx* c, int idx) {
+    const Record& r = c->tape[idx];
     const tt_gpt2_config& m = c->cfg;
     const bool bf = m.dtype != TT_FP32;  // 16-bit storage (bf16 or half)
     Launch L = launch_of(c);
@@ -448,7 +460,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
             g.D = r.dW; g.ldd = r.K; g.d_f32 = true;
             g.accumulate = accW;
             if (!c->oom && !run_gemm(c, g, PK_GEMM_DW)) return fail(c, TT_ERR_CUDA, "linear dW GEMM failed");
-            if (r.db) {
+            if (r.db && !r.db_fused) {
                 if (!first_write(c, r.db)) return fail(c, TT_ERR, "tape: bias used twice");
                 size_t mark = c->off;
                 float* s = (float*)arena_alloc(c, colsum_scratch_floats(r.M, r.N) * 4);
@@ -466,12 +478,29 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
         void* dx = grad_for_write(c, r.in, &acc);
         if (!first_write(c, r.dW) || !first_write(c, r.db))
             return fail(c, TT_ERR, "tape: LayerNorm parameters used twice");
+        // The input is complete once this LayerNorm has added its share when
+        // this LayerNorm is its first consumer (reverse order: its last).  If
+        // the input is the output of a linear layer with a bias, that bias's
+        // gradient is the column sum of the finished gradient: the kernel
+        // forms it on the way (no second pass over the gradient).
+        Record* prod = nullptr;
+        {
+            const TapeTensor& xt = c->tensors[r.in];
+            if (xt.first_consumer == idx && xt.producer >= 0) {
+                Record& p = c->tape[xt.producer];
+                if (p.kind == R_LINEAR && p.db && !p.gelu && p.out == r.in) prod = &p;
+            }
+        }
         size_t mark = c->off;
         float* s = (float*)arena_alloc(c, layernorm_bwd_scratch_floats(r.M, r.N) * 4);
         ProfScope ps(c, PK_LN_BWD, 0.0, (acc ? 4.0 : 3.0) * r.M * r.N * esize(m.dtype) + 8.0 * r.M);
+        if (prod) {
+            if (!first_write(c, prod->db)) return fail(c, TT_ERR, "tape: bias used twice");
+            prod->db_fused = true;
+        }
         if (!c->oom)
-            launch_layernorm_bwd(L, bf, c->tensors[r.in].data, r.W, r.mean, r.rstd, y.grad, dx, r.dW,
-                                 r.db, r.M, r.N, acc, s, c->accum_params);
+            launch_layernorm_bwd(L, bf, c->tensors[r.in].data, r.W, r.mean, r.rstd, y.grad, dx, r.dW, r.db, r.M,
+                                 r.N, acc, s, c->accum_params, prod ? prod->db : nullptr);
         c->off = mark;
         return TT_OK;
     }
@@ -481,15 +510,30 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
         bool acc = false;
         void* dqkv = grad_for_write(c, r.in, &acc);
         if (acc) return fail(c, TT_ERR, "tape: attention input gradient already allocated");
+        // qkv is the output of the qkv linear layer and attention its only
+        // consumer: that layer's bias gradient, the column sums of dqkv, is
+        // formed by the attention backward itself
+        Record* prod = nullptr;
+        {
+            const TapeTensor& xt = c->tensors[r.in];
+            if (xt.consumers == 1 && xt.producer >= 0) {
+                Record& p = c->tape[xt.producer];
+                if (p.kind == R_LINEAR && p.db && !p.gelu && p.out == r.in) prod = &p;
+            }
+        }
+        if (prod) {
+            if (!first_write(c, prod->db)) return fail(c, TT_ERR, "tape: bias used twice");
+            prod->db_fused = true;
+        }
         size_t mark = c->off;
-        float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(r.B, r.T, r.H) * 4);
+        float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(r.B, r.T, r.N, r.H) * 4);
         // recompute QK^T, then dV, dP, dQ, dK: five products over the causal pairs
         const double pairs = (double)r.B * r.H * r.T * (r.T + 1) / 2.0;
         ProfScope ps(c, PK_ATTN_BWD, 10.0 * pairs * (r.N / r.H),
                      (3.0 + 2.0 + 3.0) * r.M * r.N * esize(m.dtype) + 4.0 * r.B * r.H * r.T);
         if (!c->oom)
             launch_attention_bwd(L, bf, c->tensors[r.in].data, y.data, r.lse, y.grad, dqkv, r.B, r.T,
-                                 r.N, r.H, s);
+                                 r.N, r.H, s, prod ? prod->db : nullptr, c->accum_params);
         c->off = mark;
         return TT_OK;
     }
@@ -517,7 +561,7 @@ static tt_status backward_record(tt_ctx* c, const Record& r) {
 
 static tt_status tape_backward(tt_ctx* c) {
     for (int i = (int)c->tape.size() - 1; i >= 0; i--) {
-        tt_status s = backward_record(c, c->tape[i]);
+        tt_status s = backward_record(c, i);
         if (s != TT_OK) return s;
     }
     return TT_OK;
@@ -1326,7 +1370,7 @@ tt_status tt_op_attention_bwd(tt_ctx* c, tt_dtype dtype, const void* qkv, const 
     if (hd != 16 && hd != 32 && hd != 64) return fail(c, TT_ERR_ARG, "attention: head dim must be 16, 32 or 64");
     c->oom = false;
     size_t mark = c->off;
-    float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(B, T, H) * 4);
+    float* s = (float*)arena_alloc(c, attention_bwd_scratch_floats(B, T, C, H) * 4);
     if (!c->oom) {
         const double pairs = (double)B * H * T * (T + 1) / 2.0;
         ProfScope ps(c, PK_ATTN_BWD, 10.0 * pairs * hd, 8.0 * B * T * C * (dtype == TT_BF16 ? 2 : 4));

@@ -132,10 +132,13 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
 size_t layernorm_bwd_scratch_floats(int M, int C);
 void launch_layernorm_fwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const void* b, void* y, float* mean, float* rstd, int M, int C);
+// dres (may be NULL): also the column sums of the finished dx -- the bias
+// gradient of the linear layer that produced x (the bf16 vector kernel forms
+// them on the way; the others in a second pass)
 void launch_layernorm_bwd(const Launch& L, bool bf16, const void* x, const void* w,
                           const float* mean, const float* rstd, const void* dy, void* dx,
                           float* dw, float* db, int M, int C, bool accumulate, float* scratch,
-                          bool acc_params = false);
+                          bool acc_params = false, float* dres = nullptr);
 
 // dz = (softmax - onehot) * dscale (* *scale_dev when given: a device loss scale)
 void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* targets,
@@ -162,25 +165,29 @@ void launch_adamw_ex(const Launch& L, float* master, void* lowp, const float* g,
 void launch_loss_scale_update(const Launch& L, float* scale, int* clean, const float* stats, int window,
                               float growth, float backoff);
 
-size_t attention_bwd_scratch_floats(int B, int T, int H);
+size_t attention_bwd_scratch_floats(int B, int T, int C, int H);
 void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, float* lse,
                           int B, int T, int C, int H);
+// dbias (may be NULL): also the column sums of dqkv -- the qkv layer's bias
+// gradient (accumulated into when acc_bias)
 void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const void* y,
                           const float* lse, const void* dy, void* dqkv, int B, int T, int C,
-                          int H, float* scratch);
+                          int H, float* scratch, float* dbias = nullptr, bool acc_bias = false);
 // bandwidth-oriented bf16 kernels (kernels_bf16.cu); false = shape not taken
 bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const void* b, void* y,
                         float* mean, float* rstd, int M, int C);
 bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
                         const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
-                        int C, bool accumulate, float* scratch, bool acc_params = false);
+                        int C, bool accumulate, float* scratch, bool acc_params = false,
+                        float* dres = nullptr);
 size_t ln_bwd_bf16_scratch_floats(int C);
 bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
                       int V, int ld, float dscale, const float* scale_dev = nullptr);
 bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part);
-// out[c] = sum of the G rows of part[G][ncols] (fixed order); columns >= split go to out_b
+// out[c] = sum of the G rows of part[G][ncols] (fixed order); columns [0, split)
+// go to out_a, [split, 2 split) to out_b, [2 split, 3 split) to out_c
 void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int split, float* out_a,
-                     float* out_b, bool acc = false);
+                     float* out_b, bool acc = false, float* out_c = nullptr);
 size_t embed_chunk_scratch_floats(int M, int C);
 bool launch_embed_chunks(const Launch& L, bool bf16, const void* dx, const int32_t* keys,
                          const int32_t* vals, int M, int C, int V, float* dwte, float* scratch);
@@ -189,8 +196,11 @@ bool launch_embed_chunks(const Launch& L, bool bf16, const void* dx, const int32
 bool attention_tc_eligible(bool bf16, int C, int H);
 bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T,
                              int C, int H);
+// bpart (may be NULL): per (sequence, 128-row tile) row of 3C column sums of
+// dqkv over the tile's rows (the qkv bias gradient's partials)
 bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
-                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt);
+                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt,
+                             float* bpart = nullptr);
 
 // decoding with a key/value cache (decode.cu); cache per layer [B, maxT, 2C].
 // The decode-step kernels read the newest position from device memory
