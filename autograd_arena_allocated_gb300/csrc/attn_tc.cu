@@ -410,24 +410,6 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 // Named barrier for the 256 row threads only.
 __device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Column sums of a 32 x 32 block held one row per lane (v: the lane's 32
-// columns): after a butterfly that halves the columns each lane keeps at each
-// step, lane l holds the sum over the 32 rows of column l.  The order of the
-// additions is fixed, so the result is deterministic.
-__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool up = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; i++) {
-            const float send = up ? v[i] : v[i + s];
-            const float keep = up ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-    return v[0];
-}
-
 // The tile's column sums of one 32-column output half: each warp's 32 rows by
 // warp_colsum32, then the four quarter warps of the half in quarter order
 // (cs: [2 halves][4 quarters][32] floats of shared memory).  Reached by all

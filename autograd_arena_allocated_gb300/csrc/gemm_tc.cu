@@ -82,6 +82,7 @@ struct Params {
     int ext_tma;    // the extra epilogue operand (GELU' input or residual) arrives by TMA loads
     int cl;         // pair form: CTA pairs take M tiles 2i, 2i + 1
     int pair_units; // pair form: ceil(m_tiles / 2) * n_tiles * splits
+    float* colsum;  // ext_tma path: column sums of each 32-row slice of the result, [M/32][N]
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -552,6 +553,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         for (int j = 0; j < 32; j++) v[j] += e[j];
                     }
                     stage_row32(stg + b * 2048, lane, v);
+                    if (p.colsum) {
+                        // this chunk's 32 rows summed per column (rows past M
+                        // hold zeros: their A rows were read as zero)
+                        const float cs = warp_colsum32(v, lane);
+                        p.colsum[(long long)((m0 + y_off) >> 5) * p.N + n + lane] = cs;
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -978,6 +985,9 @@ static bool use_pair(const Launch& L, tc::Plan& pl) {
     return true;
 }
 
+// every column of the result is stored (the column sums then cover all N)
+static bool ns_all(const GemmArgs& g) { return g.n_store == 0 || g.n_store == g.N; }
+
 bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t workspace_floats) {
     if (!gemm_tc_eligible(g)) return false;
     tc::Plan pl = tc::make_plan(L, g);
@@ -1028,6 +1038,8 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
             tc::make_map(&mx, ext, ns, g.M, g.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
             pl.p.ext_tma = 1;
     }
+    pl.p.colsum = nullptr;
+    if (g.colsum_part && pl.p.ext_tma && ns_all(g)) pl.p.colsum = g.colsum_part;
     bool launched;
     const bool pr = pl.p.cl != 0;
 #define TC(BN_, AM_, BM_) \
@@ -1045,6 +1057,7 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
     }
 #undef TC
     if (!launched) return false;
+    if (pl.p.colsum && g.colsum_done) *g.colsum_done = true;
     if (pl.p.splits > 1) {
         const bool vec = (g.N % 4) == 0 && (pl.p.n_store % 4) == 0 && (g.ldd % 4) == 0 &&
                          ((uintptr_t)workspace & 15) == 0 && ((uintptr_t)g.D & 15) == 0;

@@ -428,9 +428,22 @@ static tt_status backward_record(tt_ctx* c, int idx) {
         {
             TapeTensor& xt = c->tensors[r.in];
             bool acc = false;
-            const Record* prod = xt.producer >= 0 ? &c->tape[xt.producer] : nullptr;
+            Record* prod = xt.producer >= 0 ? &c->tape[xt.producer] : nullptr;
             const bool through_gelu = prod && prod->kind == R_LINEAR && prod->gelu && xt.consumers == 1;
             void* dx = grad_for_write(c, r.in, &acc);
+            // Through the GELU, dx is the gradient of the GELU layer's
+            // pre-activation, whose column sums are that layer's bias gradient:
+            // the GEMM's epilogue forms them per 32-row slice (or, on paths
+            // without that epilogue, one column-sum pass follows)
+            float* cpart = nullptr;
+            bool cdone = false;
+            const size_t cmark = c->off;
+            if (through_gelu && prod->db) {
+                if (!first_write(c, prod->db)) return fail(c, TT_ERR, "tape: bias used twice");
+                prod->db_fused = true;
+                const size_t a = (size_t)gemm_colsum_rows(r.M) * r.K, b = colsum_scratch_floats(r.M, r.K);
+                cpart = (float*)arena_alloc(c, (a > b ? a : b) * 4);
+            }
             if (!c->oom) {
                 GemmArgs g;
                 g.A = dy; g.lda = r.N; g.a_kmajor = true;
@@ -442,7 +455,19 @@ static tt_status backward_record(tt_ctx* c, int idx) {
                 g.D = dx; g.ldd = r.K; g.d_f32 = !bf;
                 g.accumulate = acc;
                 if (through_gelu) { g.epi = EPI_DGELU; g.aux = prod->pre; }
+                g.colsum_part = cpart;
+                g.colsum_done = &cdone;
                 if (!run_gemm(c, g, PK_GEMM_DX)) return fail(c, TT_ERR_CUDA, "linear dx GEMM failed");
+            }
+            if (cpart) {
+                ProfScope ps(c, PK_COLSUM, 0.0, cdone ? 4.0 * gemm_colsum_rows(r.M) * r.K
+                                                      : (double)r.M * r.K * esize(m.dtype) + 4.0 * r.K);
+                if (!c->oom) {
+                    if (cdone) launch_sum_rows(L, cpart, gemm_colsum_rows(r.M), r.K, r.K, prod->db, nullptr,
+                                               c->accum_params);
+                    else launch_colsum(L, bf, dx, r.M, r.K, prod->db, cpart, c->accum_params);
+                }
+                c->off = cmark;
             }
             if (through_gelu) xt.grad_is_pre = true;
         }

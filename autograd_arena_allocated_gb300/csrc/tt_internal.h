@@ -109,7 +109,13 @@ struct GemmArgs {
     const void* residual = nullptr;  // [M, ldd] same type as D
     void* aux = nullptr;             // EPI_GELU: out pre-activation; EPI_DGELU: in
     bool accumulate = false;         // D += result
+    // optional: column sums of the result over each 32-row slice,
+    // colsum_part[m / 32][n] (gemm_colsum_rows(M) rows); *colsum_done is set
+    // when the kernel wrote them (the tensor-core GELU' epilogue does)
+    float* colsum_part = nullptr;
+    bool* colsum_done = nullptr;
 };
+inline int gemm_colsum_rows(int M) { return ((M + 127) / 128) * 4; }
 
 // Runs the GEMM; `workspace` (fp32, may be needed for split-K of the DW form)
 // is sized by gemm_workspace_floats.  Returns false on unsupported arguments.
