@@ -69,6 +69,7 @@ SIGNATURES = {
     "tt_gpt2_generate": (_st, [_vp, _vp, _vp, _i, _i, _i, _vp]),
     # tt_ops.h
     "tt_ctx_set_gemm_backend": (_st, [_vp, _i]),
+    "tt_ctx_set_wait_limit": (_st, [_vp, C.c_longlong]),
     "tt_op_linear_fwd": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i]),
     "tt_op_linear_bwd_dx": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i]),
     "tt_op_linear_bwd_dw": (_st, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i]),

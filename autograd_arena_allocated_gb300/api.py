@@ -99,7 +99,12 @@ class Context:
         self.cfg = cfg
 
     def set_gemm_backend(self, backend: int):
+        """0 automatic, 1 SIMT only, 2 tensor cores without the two-CTA pair form."""
         self._check(lib().tt_ctx_set_gemm_backend(self.h, int(backend)))
+
+    def set_wait_limit(self, cycles: int):
+        """Limit of the device-side bounded waits in clock64 cycles (<= 0: the default)."""
+        self._check(lib().tt_ctx_set_wait_limit(self.h, int(cycles)))
 
     def reset(self):
         self._check(lib().tt_ctx_reset(self.h))

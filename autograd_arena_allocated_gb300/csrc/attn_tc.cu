@@ -118,7 +118,8 @@ constexpr uint32_t F_TMEM = 128;    // S: cols 0..63, O: 64..127
 
 __global__ void __launch_bounds__(THREADS, 3)
 k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int nbh, int* flags) {
+              bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int nbh, int* flags,
+              long long wl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + F_BAR);
@@ -131,7 +132,8 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     uint64_t* s_free = bars + 8;
     uint64_t* p_full = bars + 9;   // [2]: P buffer written
     uint64_t* o_full = bars + 11;  // [2]: P.V of a block in buffer s done (buffer s consumed)
-    uint32_t* tmem_holder = (uint32_t*)(bars + 13);
+    uint64_t* drain = bars + 13;   // MMAs issued before an abort are done
+    uint32_t* tmem_holder = (uint32_t*)(bars + 14);
     volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
     const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
@@ -157,6 +159,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(&p_full[1], 128);
         mbar_init(&o_full[0], 1);
         mbar_init(&o_full[1], 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         init_done();
     }
@@ -177,7 +180,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             bool ok = true;
             auto load_k = [&](int j) -> bool {
                 const int st = j & 1;
-                if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x100 + 1)) return false;
+                if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x100 + 1, wl)) return false;
                 mbar_expect_tx(&k_full[st], T64);
                 tma_load_2d(smem_u32(sm + F_K + st * T64), &tk, &k_full[st], xk, row0 + j * BN);
                 ++issued_k;
@@ -185,19 +188,17 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             };
             ok = load_k(0) && (nkv < 2 || load_k(1));
             for (int j = 0; j < nkv && ok; j++) {
-                if (!mbar_wait(v_empty, (j & 1) ^ 1, abort_flag, flags, 0x100 + 2)) { ok = false; break; }
+                if (!mbar_wait(v_empty, (j & 1) ^ 1, abort_flag, flags, 0x100 + 2, wl)) { ok = false; break; }
                 mbar_expect_tx(v_full, T64);
                 tma_load_2d(smem_u32(sm + F_V), &tk, v_full, xv, row0 + j * BN);
                 ++issued_v;
                 if (j + 2 < nkv && !load_k(j + 2)) { ok = false; break; }
             }
             if (!ok) {  // let issued copies land before the CTA exits
-                const long long t0 = clock64();
-                while (!mbar_try_wait(q_full, 0) && clock64() - t0 < WAIT_CYCLES) {}
+                mbar_drain(q_full, 0);
                 for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; j++)
-                    while (!mbar_try_wait(&k_full[j & 1], (j >> 1) & 1) && clock64() - t0 < 2 * WAIT_CYCLES) {}
-                if (issued_v > 0)
-                    while (!mbar_try_wait(v_full, (issued_v - 1) & 1) && clock64() - t0 < 3 * WAIT_CYCLES) {}
+                    mbar_drain(&k_full[j & 1], (j >> 1) & 1);
+                if (issued_v > 0) mbar_drain(v_full, (issued_v - 1) & 1);
             }
         }
     } else if (warp == 1) {
@@ -205,28 +206,30 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_O = idesc_bf16(BQ, D, false, true);
             const uint32_t sq = smem_u32(sm + F_Q), sv = smem_u32(sm + F_V);
-            bool ok = mbar_wait(q_full, 0, abort_flag, flags, 0x100 + 3);
+            bool ok = mbar_wait(q_full, 0, abort_flag, flags, 0x100 + 3, wl);
+            bool issued = false;
             // S_{j+1} is issued as soon as the row threads hold S_j in registers,
             // so that it overlaps the softmax of block j
             auto issue_s = [&](int j) -> bool {
                 const int st = j & 1;
-                if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, flags, 0x100 + 4)) return false;
-                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x100 + 5)) return false;
+                if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, flags, 0x100 + 4, wl)) return false;
+                if (!mbar_wait(s_free, (j & 1) ^ 1, abort_flag, flags, 0x100 + 5, wl)) return false;
                 tc_fence_after();
                 const uint32_t sk = smem_u32(sm + F_K + st * T64);
 #pragma unroll
                 for (int k = 0; k < D / 16; k++)
                     umma_bf16(tmem, sdesc(sq + 32 * k, 16, 1024), sdesc(sk + 32 * k, 16, 1024), ID, k > 0);
+                issued = true;
                 umma_commit(s_full);
                 umma_commit(&k_empty[st]);
                 return true;
             };
             if (ok) ok = issue_s(0);
             for (int j = 0; j < nkv && ok; j++) {
-                if (j + 1 < nkv && !issue_s(j + 1)) break;
+                if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
                 const int pb = j & 1;
-                if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, flags, 0x100 + 6)) break;
-                if (!mbar_wait(v_full, j & 1, abort_flag, flags, 0x100 + 7)) break;
+                if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, flags, 0x100 + 6, wl)) { ok = false; break; }
+                if (!mbar_wait(v_full, j & 1, abort_flag, flags, 0x100 + 7, wl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sp = smem_u32(sm + F_P + pb * T128);
 #pragma unroll
@@ -235,6 +238,10 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                               (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(&o_full[pb]);
                 umma_commit(v_empty);
+            }
+            if (!ok && issued) {  // the MMAs already issued finish before tensor memory is freed
+                umma_commit(drain);
+                mbar_drain(drain, 0);
             }
         }
     } else {
@@ -249,7 +256,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; j++) {
-            if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x100 + 8)) { ok = false; break; }
+            if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x100 + 8, wl)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (j >= 2 * qt);
             const int kq = q - j * BN;  // on the diagonal, key columns > kq are masked
@@ -283,7 +290,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if (j == 0 || rescale) m = mn;
             const int pb = j & 1;
             // buffer pb was last read by P_{j-2} V_{j-2} (long done, as a rule)
-            if (j >= 2 && !mbar_wait_warp(&o_full[pb], ((j - 2) >> 1) & 1, abort_flag, flags, 0x100 + 9)) {
+            if (j >= 2 && !mbar_wait_warp(&o_full[pb], ((j - 2) >> 1) & 1, abort_flag, flags, 0x100 + 9, wl)) {
                 ok = false;
                 break;
             }
@@ -322,7 +329,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const float rs = rs0 + rs1;
             if (rescale) {
                 // O must hold P_{j-1} V_{j-1} before it is scaled
-                if (!mbar_wait_warp(&o_full[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag, flags, 0x100 + 10)) {
+                if (!mbar_wait_warp(&o_full[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag, flags, 0x100 + 10, wl)) {
                     ok = false;
                     break;
                 }
@@ -346,7 +353,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_arrive(&p_full[pb]);
         }
         const int jl = nkv - 1;
-        if (ok && mbar_wait_warp(&o_full[jl & 1], (jl >> 1) & 1, abort_flag, flags, 0x100 + 11)) {
+        if (ok && mbar_wait_warp(&o_full[jl & 1], (jl >> 1) & 1, abort_flag, flags, 0x100 + 11, wl)) {
             tc_fence_after();
             float o[D];
             uint32_t v[32];
@@ -423,14 +430,6 @@ __device__ __forceinline__ void tile_colsum(float (&v)[32], float* cs, float* ds
     rows_sync();
 }
 
-// Spins until the phase completes or the long landing bound passes, with no
-// abort check: used only to let copies already issued land before a CTA
-// that gave up exits.
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity) && clock64() - t0 < WAIT_CYCLES) {}
-}
-
 // ------------------------------------------------------------------ dQ
 // One CTA per 128 queries (2 CTAs per SM).  S = Q K_j^T and dP = dO V_j^T
 // (Q and dO are A operands read from shared memory); the row threads form
@@ -459,7 +458,7 @@ __global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
                  const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
-                 float* __restrict__ bpart, int T, int C, int H, int nbh, int* flags) {
+                 float* __restrict__ bpart, int T, int C, int H, int nbh, int* flags, long long wl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
@@ -517,12 +516,12 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             bool ok = true;
             for (int j = 0; j < nkv; j++) {
                 const int ks = j % Q_KST, kr = j / Q_KST;
-                if (!mbar_wait(&k_empty[ks], (kr & 1) ^ 1, abort_flag, flags, 0x200 + 1)) { ok = false; break; }
+                if (!mbar_wait(&k_empty[ks], (kr & 1) ^ 1, abort_flag, flags, 0x200 + 1, wl)) { ok = false; break; }
                 mbar_expect_tx(&k_full[ks], T64);
                 tma_load_2d(smem_u32(sm + Q_K + ks * T64), &tk, &k_full[ks], xk, row0 + j * BN);
                 ++issued_k;
                 const int vs = j & 1;
-                if (!mbar_wait(&v_empty[vs], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x200 + 10)) { ok = false; break; }
+                if (!mbar_wait(&v_empty[vs], ((j >> 1) & 1) ^ 1, abort_flag, flags, 0x200 + 10, wl)) { ok = false; break; }
                 mbar_expect_tx(&v_full[vs], T64);
                 tma_load_2d(smem_u32(sm + Q_V + vs * T64), &tk, &v_full[vs], xv, row0 + j * BN);
                 ++issued_v;
@@ -540,7 +539,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_Q = idesc_bf16(BQ, D, false, true);
             const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O);
-            bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2);
+            bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2, wl);
             bool issued = false;
             // dQ += dS_j K_j: dS from tensor-memory buffer j & 1, K_j read MN-major
             auto issue_dq = [&](int j) {
@@ -554,8 +553,8 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             };
             for (int j = 0; j < nkv && ok; j++) {
                 const int ks = j % Q_KST, vs = j & 1;
-                if (!mbar_wait(&k_full[ks], (j / Q_KST) & 1, abort_flag, flags, 0x200 + 3)) { ok = false; break; }
-                if (!mbar_wait(&v_full[vs], (j >> 1) & 1, abort_flag, flags, 0x200 + 11)) { ok = false; break; }
+                if (!mbar_wait(&k_full[ks], (j / Q_KST) & 1, abort_flag, flags, 0x200 + 3, wl)) { ok = false; break; }
+                if (!mbar_wait(&v_full[vs], (j >> 1) & 1, abort_flag, flags, 0x200 + 11, wl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sk = smem_u32(sm + Q_K + ks * T64), sv = smem_u32(sm + Q_V + vs * T64);
                 // S_j and dP_j: two independent chains, interleaved
@@ -568,7 +567,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 umma_commit(s_full);
                 umma_commit(&v_empty[vs]);  // V_j is no longer needed
                 if (j > 0) issue_dq(j - 1);  // overlaps the row threads' work on block j
-                if (!mbar_wait(ds_full, j & 1, abort_flag, flags, 0x200 + 5)) { ok = false; break; }
+                if (!mbar_wait(ds_full, j & 1, abort_flag, flags, 0x200 + 5, wl)) { ok = false; break; }
                 tc_fence_after();
             }
             if (ok) {
@@ -588,7 +587,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
         const long long bhl = (long long)b * H + h;
         float* dpart = reinterpret_cast<float*>(sm + Q_DP);
-        bool ok = mbar_wait_warp(qo_full, 0, abort_flag, flags, 0x200 + 6);
+        bool ok = mbar_wait_warp(qo_full, 0, abort_flag, flags, 0x200 + 6, wl);
         // This thread's half of D = rowsum(dO o O) (16-byte chunks 4 half ..
         // 4 half + 3 of the swizzled dO row); the two halves meet in shared memory.
         float Dq = 0.0f;
@@ -619,7 +618,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         const float Lq = qv ? lse[bhl * T + q] * LOG2E : 0.0f;
         for (int j = 0; j < nkv && ok; j++) {
-            if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x200 + 7)) { ok = false; break; }
+            if (!mbar_wait_warp(s_full, j & 1, abort_flag, flags, 0x200 + 7, wl)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (j >= 2 * qt);
             const int kq = q - j * BN - 32 * half;  // on the diagonal, this half's columns > kq are masked
@@ -645,7 +644,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         float cv[32];
 #pragma unroll
         for (int d = 0; d < 32; d++) cv[d] = 0.0f;
-        if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x200 + 9)) {
+        if (ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x200 + 9, wl)) {
             tc_fence_after();
             uint32_t w[32];
             tmem_ld32(tl + Q_TACC + 32 * half, w);
@@ -687,7 +686,7 @@ __global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
                    const float* __restrict__ Dlt, bf16* __restrict__ dqkv, float* __restrict__ bpart, int T,
-                   int C, int H, int nbh, int* flags) {
+                   int C, int H, int nbh, int* flags, long long wl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + K_BAR);
@@ -740,7 +739,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             bool ok = true;
             for (int i = 0; i < nq; i++) {
                 const int st = i % K_ST, j = j0 + i;
-                if (!mbar_wait(&qo_empty[st], ((i / K_ST) & 1) ^ 1, abort_flag, flags, 0x300 + 1)) { ok = false; break; }
+                if (!mbar_wait(&qo_empty[st], ((i / K_ST) & 1) ^ 1, abort_flag, flags, 0x300 + 1, wl)) { ok = false; break; }
                 mbar_expect_tx(&qo_full[st], 2 * T64);
                 tma_load_2d(smem_u32(sm + K_Q + st * T64), &tk, &qo_full[st], xq, row0 + j * BN);
                 tma_load_2d(smem_u32(sm + K_O + st * T64), &to, &qo_full[st], h * D, row0 + j * BN);
@@ -757,11 +756,11 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
             constexpr uint32_t ID_A = idesc_bf16(BQ, D, false, true);
             const uint32_t sk = smem_u32(sm + K_K), sv = smem_u32(sm + K_V);
-            bool ok = mbar_wait(kv_full, 0, abort_flag, flags, 0x300 + 2);
+            bool ok = mbar_wait(kv_full, 0, abort_flag, flags, 0x300 + 2, wl);
             bool issued = false;
             for (int i = 0; i < nq && ok; i++) {
                 const int st = i % K_ST;
-                if (!mbar_wait(&qo_full[st], (i / K_ST) & 1, abort_flag, flags, 0x300 + 3)) { ok = false; break; }
+                if (!mbar_wait(&qo_full[st], (i / K_ST) & 1, abort_flag, flags, 0x300 + 3, wl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sq = smem_u32(sm + K_Q + st * T64), so = smem_u32(sm + K_O + st * T64);
                 // S^T_i and dP^T_i (two independent chains, interleaved); they
@@ -773,7 +772,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
                 issued = true;
                 umma_commit(st_full);
-                if (!mbar_wait(ps_full, i & 1, abort_flag, flags, 0x300 + 5)) { ok = false; break; }
+                if (!mbar_wait(ps_full, i & 1, abort_flag, flags, 0x300 + 5, wl)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / 16; k++) {
@@ -818,7 +817,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             sl[32 + lane] = Dn;
             __syncwarp();
             if (i + 1 < nq) fetch(i + 1);
-            if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6)) { ok = false; break; }
+            if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6, wl)) { ok = false; break; }
             tc_fence_after();
             const bool diag = (i < 2);  // query blocks that overlap this key tile
             const int q0 = j * BN + 32 * half;
@@ -851,7 +850,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tc_fence_before();
             warp_arrive(ps_full, lane);
         }
-        const bool got = ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x300 + 8);
+        const bool got = ok && mbar_wait_warp(acc_full, 0, abort_flag, flags, 0x300 + 8, wl);
         if (got) tc_fence_after();
         bf16* base = dqkv + (long long)(row0 + key) * 3 * C + h * D + 32 * half;
         // the qkv bias gradient's partials: this tile's column sums of dV, then dK
@@ -913,7 +912,7 @@ bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* l
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C,
-                                                                     H, B * H, L.flags);
+                                                                     H, B * H, L.flags, L.wait_cycles);
     return true;
 }
 
@@ -932,10 +931,11 @@ bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, co
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
     fa5::k_attn_bwd_dq_tc<<<grid, fa5::BW_THREADS, fa5::Q_SMEM, L.stream>>>(
-        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags);
+        tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags,
+        L.wait_cycles);
     L.count();
     fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::BW_THREADS, fa5::K_SMEM, L.stream>>>(
-        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags);
+        tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags, L.wait_cycles);
     return true;
 }
 

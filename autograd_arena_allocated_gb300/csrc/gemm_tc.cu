@@ -83,6 +83,7 @@ struct Params {
     int cl;         // pair form: CTA pairs take M tiles 2i, 2i + 1
     int pair_units; // pair form: ceil(m_tiles / 2) * n_tiles * splits
     float* colsum;  // ext_tma path: column sums of each 32-row slice of the result, [M/32][N]
+    long long wait_limit;  // bounded-wait limit (clock64 cycles)
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -294,6 +295,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     volatile int* abort_flag = (volatile int*)(tmem_base_holder + 1);
     // two per epilogue warp: the extra operand's tile has landed in staging buffer 0 / 1
     uint64_t* ebar = (uint64_t*)(smem + S * CF::STAGE_BYTES + 512);
+    uint64_t* drain = ebar + 2 * EPI_WARPS;  // MMAs issued before an abort are done
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -309,6 +311,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_init(&tempty[a], (PAIR ? 2 : 1) * EPI_WARPS * 32);
         }
         for (int e = 0; e < 2 * EPI_WARPS; e++) mbar_init(&ebar[e], 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
@@ -352,7 +355,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 1)) { ok = false; break; }
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 1, p.wait_limit)) { ok = false; break; }
                     const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
                     const uint32_t sb = sa + CF::A_BYTES;
                     const int k0 = kb * BK;
@@ -402,7 +405,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // the leader's releases of the last stages have arrived before
                 // this CTA's barriers go away
                 for (int i = 0; i < S && ok; i++) {
-                    ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 7);
+                    ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.flags, 0x400 + 7, p.wait_limit);
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
@@ -434,11 +437,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 unit_mn(p, it, U.rank, BN, &m0_, &n0_, &split);
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags, 0x400 + 2)) { ok = false; break; }
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.flags, 0x400 + 2, p.wait_limit)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.flags, 0x400 + 3)) { ok = false; break; }
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.flags, 0x400 + 3, p.wait_limit)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(tiles + stage * CF::STAGE_BYTES);
                     const uint32_t sb = sa + CF::A_BYTES;
@@ -460,6 +463,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if (PAIR) umma_commit_pair(&tfull[acc]);  // accumulator complete, in both CTAs
                 else umma_commit(&tfull[acc]);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            if (!ok) {  // the MMAs already issued finish before tensor memory is freed
+                if (PAIR) umma_commit_pair(drain);
+                else umma_commit(drain);
+                mbar_drain(drain, 0);
             }
         }
     } else {
@@ -504,7 +512,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             for (int it = U.first; it < U.count && ok; it += U.step) {
                 int split_, m0, n0;
                 unit_mn(p, it, U.rank, BN, &m0, &n0, &split_);
-                if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
+                if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4, p.wait_limit)) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int i = 0; i < CHUNKS; i++, k++) {
@@ -540,7 +548,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                         for (int j = 0; j < 32; j++) v[j] += bb[j];
                     }
-                    if (!mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 5)) { ok = false; break; }
+                    if (!mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 5, p.wait_limit)) { ok = false; break; }
                     eph ^= 1u << b;
                     pending &= ~(1u << b);
                     float e[32];
@@ -571,14 +579,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 else mbar_arrive_cluster(leader_addr(&tempty[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
-            // a load still in flight must land before the CTA's shared memory goes away
+            // a load still in flight must land before the CTA's shared memory
+            // goes away (also after an abort: no abort check here)
             for (int b = 0; b < 2; b++)
-                if ((pending >> b) & 1u) mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 6);
+                if ((pending >> b) & 1u) mbar_drain(&eb[b], (eph >> b) & 1u);
         }
         for (int it = U.first; it < U.count && !p.ext_tma; it += U.step) {
             int split, m0, n0;
             unit_mn(p, it, U.rank, BN, &m0, &n0, &split);
-            if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4)) break;
+            if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.flags, 0x400 + 4, p.wait_limit)) break;
             tc_fence_after();
             const int m = m0 + row;
             const bool row_ok = m < p.M;
@@ -972,7 +981,7 @@ static bool launch_tc(const Launch& L, const tc::Plan& pl, const CUtensorMap& ma
 // (TT_GEMM_PAIR=0 in the environment).
 template <int BN, bool A_MN, bool B_MN>
 static bool use_pair(const Launch& L, tc::Plan& pl) {
-    if (tc::pair_disabled() || pl.p.units < 2) return false;
+    if (tc::pair_disabled() || L.no_pair || pl.p.units < 2) return false;
     // an odd M-tile count only where the output is written row by row
     if ((pl.p.m_tiles & 1) && !(A_MN && B_MN)) return false;
     if (B_MN && ((BN / tc::MN_BOX) & 1)) return false;
@@ -1039,6 +1048,7 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
             pl.p.ext_tma = 1;
     }
     pl.p.colsum = nullptr;
+    pl.p.wait_limit = L.wait_cycles;
     if (g.colsum_part && pl.p.ext_tma && ns_all(g)) pl.p.colsum = g.colsum_part;
     bool launched;
     const bool pr = pl.p.cl != 0;

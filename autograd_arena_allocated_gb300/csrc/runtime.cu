@@ -110,6 +110,7 @@ struct tt_ctx {
     uint64_t launches = 0;
     int num_sms = 148;
     int gemm_backend = 0;
+    long long wait_cycles = 4000000000LL;  // bounded-wait limit of the tensor-core kernels
     bool has_model = false;
     tt_gpt2_config cfg{};
     bool dry = false;
@@ -193,7 +194,9 @@ static Launch launch_of(tt_ctx* c) {
     L.flags = (int*)c->arena;
     L.launches = &c->launches;
     L.dry = c->dry;
-    L.gemm_backend = c->gemm_backend;
+    L.gemm_backend = c->gemm_backend == 1 ? 1 : 0;
+    L.no_pair = c->gemm_backend == 2;
+    L.wait_cycles = c->wait_cycles;
     L.num_sms = c->num_sms;
     L.f16 = c->has_model && c->cfg.dtype == TT_FP16;
     return L;
@@ -933,8 +936,15 @@ tt_status tt_ctx_set_model(tt_ctx* c, const tt_gpt2_config* m) {
 tt_status tt_ctx_set_gemm_backend(tt_ctx* c, int backend) {
     if (!c) return TT_ERR_ARG;
     if (!live(c)) return TT_ERR_STALE;
-    if (backend != 0 && backend != 1) return fail(c, TT_ERR_ARG, "backend must be 0 or 1");
+    if (backend < 0 || backend > 2) return fail(c, TT_ERR_ARG, "backend must be 0, 1 or 2");
     c->gemm_backend = backend;
+    return TT_OK;
+}
+
+tt_status tt_ctx_set_wait_limit(tt_ctx* c, long long cycles) {
+    if (!c) return TT_ERR_ARG;
+    if (!live(c)) return TT_ERR_STALE;
+    c->wait_cycles = cycles > 0 ? cycles : 4000000000LL;
     return TT_OK;
 }
 

@@ -42,11 +42,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: true when the phase with the given parity has completed;
-// false if another role aborted or the deadline passed (then FLAG_TIMEOUT).
+// false if another role aborted or the limit passed (then FLAG_TIMEOUT and
+// FLAG_SITE).  The limit (clock64 cycles) is a kernel argument taken from the
+// context; WAIT_CYCLES is the default.  A limit below SHORT_WAIT polls with
+// the non-suspending test_wait and looks at the clock on every poll, so that
+// a wait that is not complete when it starts runs out within the limit --
+// the form a test uses to make a wait run out.
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+constexpr long long SHORT_WAIT = 1000000LL;
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_give_up(volatile int* abort_flag, int* flags, int site) {
+    atomicCAS(&flags[FLAG_SITE], 0, site);
+    atomicOr(&flags[FLAG_TIMEOUT], 1);
+    *abort_flag = 1;
+    return false;
+}
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* flags, int site = 0) {
+                                          int* flags, int site = 0, long long limit = WAIT_CYCLES) {
+    if (limit < SHORT_WAIT) {
+        const long long t0 = clock64();
+        for (;;) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (((volatile int*)flags)[FLAG_TIMEOUT]) {
+                *abort_flag = 1;
+                return false;
+            }
+            if (clock64() - t0 > limit) return mbar_give_up(abort_flag, flags, site);
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
@@ -58,12 +95,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                 *abort_flag = 1;
                 return false;
             }
-            if (clock64() - t0 > WAIT_CYCLES) {
-                atomicOr(&flags[FLAG_TIMEOUT], 1);
-                atomicCAS(&flags[FLAG_SITE], 0, site);
-                *abort_flag = 1;
-                return false;
-            }
+            if (clock64() - t0 > limit) return mbar_give_up(abort_flag, flags, site);
         }
     }
 }
@@ -72,9 +104,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // the warp-collective tcgen05.ld/st that follow it must run converged, so no
 // lane may leave the loop that issues them alone.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                               int* flags, int site = 0) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, flags, site);
+                                               int* flags, int site = 0, long long limit = WAIT_CYCLES) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, flags, site, limit);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Spins until the phase completes or the fixed landing bound (WAIT_CYCLES,
+// whatever the context's limit) passes, with no abort check: used only to let
+// copies and MMAs already issued finish before a CTA that gave up frees the
+// shared or tensor memory they write.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity) && clock64() - t0 < WAIT_CYCLES) {}
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,

@@ -38,6 +38,8 @@ struct Launch {
     int num_sms = 148;
     bool pdl = false;      // decode kernels: programmatic dependent launch
     bool f16 = false;      // 16-bit storage is IEEE half, not bf16 (the model's TT_FP16 mode)
+    bool no_pair = false;  // tensor-core GEMMs without the two-CTA pair form
+    long long wait_cycles = 4000000000LL;  // limit of every bounded device-side wait (clock64 cycles)
     void count() const { if (launches) ++*launches; }
 };
 

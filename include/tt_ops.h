@@ -21,8 +21,26 @@ extern "C" {
 #endif
 
 /* GEMM engine selection: 0 = automatic (tcgen05 tensor cores whenever the
- * operands allow: bf16, 16-byte aligned rows; else SIMT), 1 = SIMT only. */
+ * operands allow: bf16, 16-byte aligned rows; else SIMT, and the two-CTA
+ * pair form wherever the M-tile count allows), 1 = SIMT only, 2 = tensor
+ * cores with one CTA per 128-row tile (no pair form).  Returns TT_ERR_ARG
+ * for any other value. */
 tt_status tt_ctx_set_gemm_backend(tt_ctx* ctx, int backend);
+
+/* Limit of every bounded device-side wait of the tensor-core kernels
+ * launched through this context, in SM clock cycles (clock64).  cycles <= 0
+ * restores the default, 4e9 cycles (about 2 s).  A wait that runs out sets
+ * the context's timeout flag and a code naming the wait; the kernel lets its
+ * copies and MMAs already issued finish, frees its tensor memory and returns;
+ * every kernel that sees the flag gives up at its next wait; and the next
+ * call that synchronises (tt_ctx_sync, a step with a loss pointer) returns
+ * TT_ERR_TIMEOUT with the code in tt_last_error.  tt_ctx_reset clears the
+ * flag; the context is usable again.  Below 1e6 cycles the waits poll
+ * without suspending, so a wait that is not complete when it starts runs
+ * out within the limit (the form used to exercise the timeout path).  The
+ * pages' boundary reports failure by status codes (microcrad page,
+ * 反向传播); this is how a device-side wait reports one. */
+tt_status tt_ctx_set_wait_limit(tt_ctx* ctx, long long cycles);
 
 /* Linear layer forward (tinytorch 三.3 MatMul with the [out, in] weight
  * layout of 八.5):  u = x W^T + b;  y = gelu(u) if gelu (tanh form, tinytorch
