@@ -44,58 +44,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait: true when the phase with the given parity has completed;
 // false if another role aborted or the limit passed (then FLAG_TIMEOUT and
 // FLAG_SITE).  The limit (clock64 cycles) is a kernel argument taken from the
-// context; WAIT_CYCLES is the default.  A limit below SHORT_WAIT polls with
-// the non-suspending test_wait and looks at the clock on every poll, so that
-// a wait that is not complete when it starts runs out within the limit --
-// the form a test uses to make a wait run out.
+// context; WAIT_CYCLES is the default.  A failing try_wait returns after a
+// couple of hundred cycles, and the abort flags and the clock are looked at
+// every 64 polls -- every poll when the limit is below SHORT_WAIT, so that a
+// wait that is not complete within a few hundred cycles of its start runs
+// out (the form a test uses to make a wait run out).
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 constexpr long long SHORT_WAIT = 1000000LL;
 
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_give_up(volatile int* abort_flag, int* flags, int site) {
-    atomicCAS(&flags[FLAG_SITE], 0, site);
-    atomicOr(&flags[FLAG_TIMEOUT], 1);
-    *abort_flag = 1;
-    return false;
-}
-
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* flags, int site = 0, long long limit = WAIT_CYCLES) {
-    if (limit < SHORT_WAIT) {
-        const long long t0 = clock64();
-        for (;;) {
-            if (mbar_test_wait(bar, parity)) return true;
-            if (*abort_flag) return false;
-            if (((volatile int*)flags)[FLAG_TIMEOUT]) {
-                *abort_flag = 1;
-                return false;
-            }
-            if (clock64() - t0 > limit) return mbar_give_up(abort_flag, flags, site);
-        }
-    }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    const uint32_t mask = limit < SHORT_WAIT ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
+        if ((it & mask) == 0) {
             if (*abort_flag) return false;
             // another CTA (or an earlier kernel) gave up: stop at once
             if (((volatile int*)flags)[FLAG_TIMEOUT]) {
                 *abort_flag = 1;
                 return false;
             }
-            if (clock64() - t0 > limit) return mbar_give_up(abort_flag, flags, site);
+            if (clock64() - t0 > limit) {
+                atomicCAS(&flags[FLAG_SITE], 0, site);
+                atomicOr(&flags[FLAG_TIMEOUT], 1);
+                *abort_flag = 1;
+                return false;
+            }
         }
     }
 }

@@ -35,11 +35,11 @@ tt_status tt_ctx_set_gemm_backend(tt_ctx* ctx, int backend);
  * every kernel that sees the flag gives up at its next wait; and the next
  * call that synchronises (tt_ctx_sync, a step with a loss pointer) returns
  * TT_ERR_TIMEOUT with the code in tt_last_error.  tt_ctx_reset clears the
- * flag; the context is usable again.  Below 1e6 cycles the waits poll
- * without suspending, so a wait that is not complete when it starts runs
- * out within the limit (the form used to exercise the timeout path).  The
- * pages' boundary reports failure by status codes (microcrad page,
- * 反向传播); this is how a device-side wait reports one. */
+ * flag; the context is usable again.  Below 1e6 cycles the waits look at
+ * the clock on every poll, so a wait that is not complete within a few
+ * hundred cycles of its start runs out (the form used to exercise the
+ * timeout path).  The pages' boundary reports failure by status codes
+ * (microcrad page, 反向传播); this is how a device-side wait reports one. */
 tt_status tt_ctx_set_wait_limit(tt_ctx* ctx, long long cycles);
 
 /* Linear layer forward (tinytorch 三.3 MatMul with the [out, in] weight
