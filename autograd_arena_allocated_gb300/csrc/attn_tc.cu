@@ -71,11 +71,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
 // 32 bf16 values (columns k0..k0+31, k0 in {0, 32}) of row r of a K-major,
 // 128-byte-swizzled [128 rows x 64 columns] operand (16-byte chunk c of row r
 // at c ^ (r mod 8)).  Rows of 32 consecutive lanes: conflict-free.
@@ -88,14 +83,15 @@ __device__ __forceinline__ void store_row32(uint8_t* base, int r, int k0, const 
             make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
+template <bool F16>
 __device__ __forceinline__ void store_out64(bf16* dst, const float* v, float scale) {
     uint4* o = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int i = 0; i < 8; i++)
-        o[i] = make_uint4(pack_bf2(v[8 * i] * scale, v[8 * i + 1] * scale),
-                          pack_bf2(v[8 * i + 2] * scale, v[8 * i + 3] * scale),
-                          pack_bf2(v[8 * i + 4] * scale, v[8 * i + 5] * scale),
-                          pack_bf2(v[8 * i + 6] * scale, v[8 * i + 7] * scale));
+        o[i] = make_uint4(pack2<F16>(v[8 * i] * scale, v[8 * i + 1] * scale),
+                          pack2<F16>(v[8 * i + 2] * scale, v[8 * i + 3] * scale),
+                          pack2<F16>(v[8 * i + 4] * scale, v[8 * i + 5] * scale),
+                          pack2<F16>(v[8 * i + 6] * scale, v[8 * i + 7] * scale));
 }
 
 __device__ __forceinline__ void init_done() {
@@ -116,6 +112,7 @@ constexpr int F_BAR = F_P + 2 * T128;
 constexpr int F_SMEM = F_BAR + 256 + 1024;
 constexpr uint32_t F_TMEM = 128;    // S: cols 0..63, O: 64..127
 
+template <bool F16>
 __global__ void __launch_bounds__(THREADS, 3)
 k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int nbh, int* flags,
@@ -203,8 +200,8 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
-            constexpr uint32_t ID_O = idesc_bf16(BQ, D, false, true);
+            constexpr uint32_t ID = idesc16<F16>(BQ, BN, false, false);
+            constexpr uint32_t ID_O = idesc16<F16>(BQ, D, false, true);
             const uint32_t sq = smem_u32(sm + F_Q), sv = smem_u32(sm + F_V);
             bool ok = mbar_wait(q_full, 0, abort_flag, flags, 0x100 + 3, wl);
             bool issued = false;
@@ -309,7 +306,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     }
                     rs0 += p0;
                     rs1 += p1;
-                    pk[e >> 1] = pack_bf2(p0, p1);
+                    pk[e >> 1] = pack2<F16>(p0, p1);
                 }
                 store_row32(pbuf, r, 0, pk);
 #pragma unroll
@@ -322,7 +319,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     }
                     rs0 += p0;
                     rs1 += p1;
-                    pk[e >> 1] = pack_bf2(p0, p1);
+                    pk[e >> 1] = pack2<F16>(p0, p1);
                 }
                 store_row32(pbuf, r, 32, pk);
             }
@@ -364,7 +361,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #pragma unroll
             for (int d = 0; d < 32; d++) o[32 + d] = __uint_as_float(v[d]);
             if (q < T) {
-                store_out64(y + (long long)(row0 + q) * C + h * D, o, 1.0f / l);
+                store_out64<F16>(y + (long long)(row0 + q) * C + h * D, o, 1.0f / l);
                 lse[((long long)b * H + h) * T + q] = (m + log2f(l)) * LN2;
             }
         }
@@ -397,14 +394,15 @@ constexpr int BW_ROWS = 256;  // row threads
 // 64-wide bf16 operand written as two 16-column halves 32 columns apart
 __device__ __forceinline__ uint32_t split_a_col(int k) { return (uint32_t)(8 * k + (k >= 2 ? 16 : 0)); }
 
+template <bool F16>
 __device__ __forceinline__ void store_out32(bf16* dst, const uint32_t (&w)[32], float scale) {
     uint4* o = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        o[i] = make_uint4(pack_bf2(__uint_as_float(w[8 * i]) * scale, __uint_as_float(w[8 * i + 1]) * scale),
-                          pack_bf2(__uint_as_float(w[8 * i + 2]) * scale, __uint_as_float(w[8 * i + 3]) * scale),
-                          pack_bf2(__uint_as_float(w[8 * i + 4]) * scale, __uint_as_float(w[8 * i + 5]) * scale),
-                          pack_bf2(__uint_as_float(w[8 * i + 6]) * scale, __uint_as_float(w[8 * i + 7]) * scale));
+        o[i] = make_uint4(pack2<F16>(__uint_as_float(w[8 * i]) * scale, __uint_as_float(w[8 * i + 1]) * scale),
+                          pack2<F16>(__uint_as_float(w[8 * i + 2]) * scale, __uint_as_float(w[8 * i + 3]) * scale),
+                          pack2<F16>(__uint_as_float(w[8 * i + 4]) * scale, __uint_as_float(w[8 * i + 5]) * scale),
+                          pack2<F16>(__uint_as_float(w[8 * i + 6]) * scale, __uint_as_float(w[8 * i + 7]) * scale));
 }
 
 // One arrival per warp: every lane has passed its own fences (the caller's
@@ -454,6 +452,7 @@ constexpr int Q_SMEM = Q_BAR + 256 + 1024;
 constexpr uint32_t Q_TMEM = 256;         // S 0..63, dP 64..127, dS[2] 128..191, dQ 192..255
 constexpr uint32_t Q_TS = 0, Q_TP = 64, Q_TDS = 128, Q_TACC = 192;
 
+template <bool F16>
 __global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
@@ -536,8 +535,8 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
-            constexpr uint32_t ID_Q = idesc_bf16(BQ, D, false, true);
+            constexpr uint32_t ID = idesc16<F16>(BQ, BN, false, false);
+            constexpr uint32_t ID_Q = idesc16<F16>(BQ, D, false, true);
             const uint32_t sq = smem_u32(sm + Q_Q), so = smem_u32(sm + Q_O);
             bool ok = mbar_wait(qo_full, 0, abort_flag, flags, 0x200 + 2, wl);
             bool issued = false;
@@ -604,8 +603,8 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
-                        part = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), part);
-                        part = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), part);
+                        part = fmaf(lo16<F16>(aw[i]), lo16<F16>(bw[i]), part);
+                        part = fmaf(hi16<F16>(aw[i]), hi16<F16>(bw[i]), part);
                     }
                 }
             }
@@ -634,7 +633,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     if (e > kq) d0 = 0.0f;
                     if (e + 1 > kq) d1 = 0.0f;
                 }
-                pk[e >> 1] = pack_bf2(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
+                pk[e >> 1] = pack2<F16>(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
             }
             tmem_st16(tl + Q_TDS + 32 * (j & 1) + 16 * half, pk);
             tmem_st_wait();
@@ -649,7 +648,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             uint32_t w[32];
             tmem_ld32(tl + Q_TACC + 32 * half, w);
             if (qv) {
-                store_out32(dqkv + (long long)(row0 + q) * 3 * C + h * D + 32 * half, w, 0.125f);
+                store_out32<F16>(dqkv + (long long)(row0 + q) * 3 * C + h * D + 32 * half, w, 0.125f);
 #pragma unroll
                 for (int d = 0; d < 32; d++) cv[d] = __uint_as_float(w[d]) * 0.125f;
             }
@@ -682,6 +681,7 @@ constexpr int K_SMEM = K_BAR + 256 + 1024;
 constexpr uint32_t K_TMEM = 256;         // S^T 0..63, dP^T 64..127, dV 128..191, dK 192..255
 constexpr uint32_t K_TS = 0, K_TP = 64, K_TV = 128, K_TK = 192;
 
+template <bool F16>
 __global__ void __launch_bounds__(BW_THREADS, 2)
 k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
@@ -753,8 +753,8 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID = idesc_bf16(BQ, BN, false, false);
-            constexpr uint32_t ID_A = idesc_bf16(BQ, D, false, true);
+            constexpr uint32_t ID = idesc16<F16>(BQ, BN, false, false);
+            constexpr uint32_t ID_A = idesc16<F16>(BQ, D, false, true);
             const uint32_t sk = smem_u32(sm + K_K), sv = smem_u32(sm + K_V);
             bool ok = mbar_wait(kv_full, 0, abort_flag, flags, 0x300 + 2, wl);
             bool issued = false;
@@ -838,11 +838,11 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (q0 + e + 2 < key) p2 = 0.0f;
                     if (q0 + e + 3 < key) p3 = 0.0f;
                 }
-                pk[e >> 1] = pack_bf2(p0, p1);
-                pk[(e >> 1) + 1] = pack_bf2(p2, p3);
-                dk[e >> 1] = pack_bf2(p0 * (__uint_as_float(dw[e]) - D4.x), p1 * (__uint_as_float(dw[e + 1]) - D4.y));
+                pk[e >> 1] = pack2<F16>(p0, p1);
+                pk[(e >> 1) + 1] = pack2<F16>(p2, p3);
+                dk[e >> 1] = pack2<F16>(p0 * (__uint_as_float(dw[e]) - D4.x), p1 * (__uint_as_float(dw[e + 1]) - D4.y));
                 dk[(e >> 1) + 1] =
-                    pack_bf2(p2 * (__uint_as_float(dw[e + 2]) - D4.z), p3 * (__uint_as_float(dw[e + 3]) - D4.w));
+                    pack2<F16>(p2 * (__uint_as_float(dw[e + 2]) - D4.z), p3 * (__uint_as_float(dw[e + 3]) - D4.w));
             }
             tmem_st16(tl + K_TS + 32 * half, pk);
             tmem_st16(tl + K_TP + 32 * half, dk);
@@ -865,7 +865,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 uint32_t w[32];
                 tmem_ld32(tl + (which ? K_TK : K_TV) + 32 * half, w);
                 if (key < T) {
-                    store_out32(base + (which ? C : 2 * C), w, scale);
+                    store_out32<F16>(base + (which ? C : 2 * C), w, scale);
 #pragma unroll
                     for (int d = 0; d < 32; d++) v[d] = __uint_as_float(w[d]) * scale;
                 }
@@ -881,18 +881,20 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
 }  // namespace fa5
 
+// bf16 or IEEE-half storage (the caller says which through Launch::f16)
 bool attention_tc_eligible(bool bf16, int C, int H) {
     return bf16 && H > 0 && C % H == 0 && C / H == fa5::D && C % 8 == 0;
 }
 
+template <bool F16>
 static bool attn_set_smem() {
     static PerDevice done;
     return done.once([] {
-        return cudaFuncSetAttribute(fa5::k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(fa5::k_attn_fwd_tc<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     fa5::F_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(fa5::k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+               cudaFuncSetAttribute(fa5::k_attn_bwd_dq_tc<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     fa5::Q_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(fa5::k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+               cudaFuncSetAttribute(fa5::k_attn_bwd_dkdv_tc<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     fa5::K_SMEM) == cudaSuccess;
     });
 }
@@ -902,24 +904,23 @@ static dim3 attn_grid(int bh, int tiles) {
     return dim3((unsigned)band, (unsigned)tiles, (unsigned)((bh + band - 1) / band));
 }
 
-bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T,
-                             int C, int H) {
-    if (L.dry) return true;
+template <bool F16>
+static bool attn_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T, int C, int H) {
     CUtensorMap tq, tk;
     if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
     if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
-    if (!attn_set_smem()) return false;
+    if (!attn_set_smem<F16>()) return false;
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
-    fa5::k_attn_fwd_tc<<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C,
-                                                                     H, B * H, L.flags, L.wait_cycles);
+    fa5::k_attn_fwd_tc<F16><<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C, H,
+                                                                          B * H, L.flags, L.wait_cycles);
     return true;
 }
 
-bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
-                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt,
-                             float* bpart) {
-    if (L.dry) return true;
+template <bool F16>
+static bool attn_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse, const void* dy,
+                        void* dqkv, int B, int T, int C, int H, float* Dlt, float* bpart) {
+    // the maps only move 16-bit elements (no conversion), for bf16 and half alike
     CUtensorMap tq, tk, to128, to64;
     if (!tc::make_tmap_bf16(&tq, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BQ)) return false;
     if (!tc::make_tmap_bf16(&tk, qkv, 3LL * C, (long long)B * T, 3LL * C, fa5::D, fa5::BN)) return false;
@@ -927,16 +928,30 @@ bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, co
         return false;
     if (!tc::make_tmap_bf16(&to64, dy, (long long)C, (long long)B * T, (long long)C, fa5::D, fa5::BN))
         return false;
-    if (!attn_set_smem()) return false;
+    if (!attn_set_smem<F16>()) return false;
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
-    fa5::k_attn_bwd_dq_tc<<<grid, fa5::BW_THREADS, fa5::Q_SMEM, L.stream>>>(
+    fa5::k_attn_bwd_dq_tc<F16><<<grid, fa5::BW_THREADS, fa5::Q_SMEM, L.stream>>>(
         tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags,
         L.wait_cycles);
     L.count();
-    fa5::k_attn_bwd_dkdv_tc<<<grid, fa5::BW_THREADS, fa5::K_SMEM, L.stream>>>(
+    fa5::k_attn_bwd_dkdv_tc<F16><<<grid, fa5::BW_THREADS, fa5::K_SMEM, L.stream>>>(
         tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags, L.wait_cycles);
     return true;
+}
+
+bool launch_attention_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, int B, int T,
+                             int C, int H) {
+    if (L.dry) return true;
+    return L.f16 ? attn_fwd_tc<true>(L, qkv, y, lse, B, T, C, H) : attn_fwd_tc<false>(L, qkv, y, lse, B, T, C, H);
+}
+
+bool launch_attention_bwd_tc(const Launch& L, const void* qkv, const void* y, const float* lse,
+                             const void* dy, void* dqkv, int B, int T, int C, int H, float* Dlt,
+                             float* bpart) {
+    if (L.dry) return true;
+    return L.f16 ? attn_bwd_tc<true>(L, qkv, y, lse, dy, dqkv, B, T, C, H, Dlt, bpart)
+                 : attn_bwd_tc<false>(L, qkv, y, lse, dy, dqkv, B, T, C, H, Dlt, bpart);
 }
 
 }  // namespace tt

@@ -989,8 +989,9 @@ static void attn_bwd_simt(const Launch& L, const void* qkv, const void* y, const
 void launch_attention_fwd(const Launch& L, bool bf16, const void* qkv, void* y, float* lse,
                           int B, int T, int C, int H) {
     if (L.dry) return;
-    const bool bf_only = bf16 && !L.f16;  // the tensor-core attention kernels are bf16
-    if (attention_tc_eligible(bf_only, C, H) && launch_attention_fwd_tc(L, qkv, y, lse, B, T, C, H)) return;
+    const bool bf_only = bf16 && !L.f16;  // the mma.sync attention kernels are bf16 only
+    // the tensor-core kernels take bf16 or half (L.f16)
+    if (attention_tc_eligible(bf16, C, H) && launch_attention_fwd_tc(L, qkv, y, lse, B, T, C, H)) return;
     if (attention_mma_eligible(bf_only, C, H)) {
         launch_attention_fwd_mma(L, qkv, y, lse, B, T, C, H);
         return;
@@ -1005,7 +1006,7 @@ void launch_attention_bwd(const Launch& L, bool bf16, const void* qkv, const voi
     if (L.dry) return;
     const bool bf_only = bf16 && !L.f16;
     float* bpart = scratch + attn_d_floats(B, T, H);
-    if (attention_tc_eligible(bf_only, C, H) &&
+    if (attention_tc_eligible(bf16, C, H) &&
         launch_attention_bwd_tc(L, qkv, y, lse, dy, dqkv, B, T, C, H, scratch, dbias ? bpart : nullptr)) {
         if (dbias) launch_sum_rows(L, bpart, B * ((T + 127) / 128), 3 * C, 3 * C, dbias, nullptr, acc_bias);
         return;

@@ -10,27 +10,43 @@
 #include "tt_internal.h"
 
 #include <math.h>
+#include <type_traits>
 
 namespace tt {
 
 typedef __nv_bfloat16 bf16;
 
+// Eight 16-bit values of a 16-byte vector as floats, and back (round to
+// nearest even): bf16, or IEEE half when F16 (the fp16 mixed-precision step).
+template <bool F16 = false>
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        if constexpr (F16) {
+            f[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFFu)));
+            f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+        } else {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
     }
 }
 
+template <bool F16 = false>
 __device__ __forceinline__ uint32_t pk2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
+    if constexpr (F16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
 }
 
+template <bool F16 = false>
 __device__ __forceinline__ uint4 pack8(const float* f) {
-    return make_uint4(pk2(f[0], f[1]), pk2(f[2], f[3]), pk2(f[4], f[5]), pk2(f[6], f[7]));
+    return make_uint4(pk2<F16>(f[0], f[1]), pk2<F16>(f[2], f[3]), pk2<F16>(f[4], f[5]), pk2<F16>(f[6], f[7]));
 }
 
 __device__ __forceinline__ float wsum(float v) {
@@ -42,7 +58,7 @@ __device__ __forceinline__ float wsum(float v) {
 // ================================================================== LayerNorm
 constexpr int LNV_WARPS = 8;
 
-template <int NV>
+template <int NV, bool F16>
 __global__ void __launch_bounds__(LNV_WARPS * 32)
 k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16* __restrict__ b,
               bf16* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, int M, int C) {
@@ -57,7 +73,7 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
     for (int i = 0; i < NV; i++) {
         const int vi = lane + 32 * i;
         if (vi < nvec) {
-            unpack8(xr[vi], v[i]);
+            unpack8<F16>(xr[vi], v[i]);
 #pragma unroll
             for (int e = 0; e < 8; e++) s += v[i][e];
         }
@@ -78,11 +94,11 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
         const int vi = lane + 32 * i;
         if (vi < nvec) {
             float wf[8], bfv[8], o[8];
-            unpack8(wr[vi], wf);
-            unpack8(br[vi], bfv);
+            unpack8<F16>(wr[vi], wf);
+            unpack8<F16>(br[vi], bfv);
 #pragma unroll
             for (int e = 0; e < 8; e++) o[e] = (v[i][e] - mu) * rs * wf[e] + bfv[e];
-            yr[vi] = pack8(o);
+            yr[vi] = pack8<F16>(o);
         }
     }
     if (lane == 0) { mean[row] = mu; rstd[row] = rs; }
@@ -100,7 +116,7 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
 // LayerNorm's input is a residual-stream tensor whose gradient is complete
 // once this kernel has added its share, and that tensor is the output of a
 // linear layer, whose bias gradient is exactly these column sums.
-template <int NV, bool RES>
+template <int NV, bool RES, bool F16>
 __global__ void __launch_bounds__(LNV_WARPS * 32, 2)
 k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
               const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
@@ -141,9 +157,9 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
         for (int i = 0; i < NV; i++) {
             if (lane + 32 * i < nvec) {
                 float xf[8], df[8], wf[8];
-                unpack8(xv[i], xf);
-                unpack8(dv[i], df);
-                unpack8(s_gamma[lane + 32 * i], wf);
+                unpack8<F16>(xv[i], xf);
+                unpack8<F16>(dv[i], df);
+                unpack8<F16>(s_gamma[lane + 32 * i], wf);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const float xh = (xf[e] - mu) * rs;
@@ -162,9 +178,9 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
             const int vi = lane + 32 * i;
             if (vi < nvec) {
                 float xf[8], df[8], wf[8], o[8];
-                unpack8(xv[i], xf);
-                unpack8(dv[i], df);
-                unpack8(s_gamma[vi], wf);
+                unpack8<F16>(xv[i], xf);
+                unpack8<F16>(dv[i], df);
+                unpack8<F16>(s_gamma[vi], wf);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const float xh = (xf[e] - mu) * rs;
@@ -172,7 +188,7 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
                 }
                 if (accumulate) {
                     float old[8];
-                    unpack8(ov[i], old);
+                    unpack8<F16>(ov[i], old);
 #pragma unroll
                     for (int e = 0; e < 8; e++) o[e] += old[e];
                 }
@@ -180,7 +196,7 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
 #pragma unroll
                     for (int e = 0; e < 8; e++) ar[RES ? i : 0][e] += o[e];
                 }
-                xo[vi] = pack8(o);
+                xo[vi] = pack8<F16>(o);
             }
         }
     }
@@ -269,7 +285,7 @@ static int ln_bwd_blocks(const Launch& L, int M) {
     static PerDevice per_sm;
     const int b = per_sm.value([] {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_ln_bwd_bf16<NV, RES>, LNV_WARPS * 32,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_ln_bwd_bf16<NV, RES, false>, LNV_WARPS * 32,
                                                           (LNV_WARPS * (RES ? 3 : 2)) * 1024 * sizeof(float)) !=
                 cudaSuccess || n < 1) {
             cudaGetLastError();
@@ -287,14 +303,18 @@ size_t ln_bwd_bf16_scratch_floats(int C) { return (size_t)LN_BWD_MAX_BLOCKS * 3 
 
 bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const void* b, void* y,
                         float* mean, float* rstd, int M, int C) {
-    if (L.f16 || C % 8 || C > 1024) return false;
+    if (C % 8 || C > 1024) return false;
     if (L.dry) return true;
     const unsigned grid = (unsigned)((M + LNV_WARPS - 1) / LNV_WARPS);
     const int nv = (C / 8 + 31) / 32;
     L.count();
-#define LNF(NV) k_ln_fwd_bf16<NV><<<grid, LNV_WARPS * 32, 0, L.stream>>>( \
+#define LNF(NV, F) k_ln_fwd_bf16<NV, F><<<grid, LNV_WARPS * 32, 0, L.stream>>>( \
         (const bf16*)x, (const bf16*)w, (const bf16*)b, (bf16*)y, mean, rstd, M, C)
-    if (nv == 1) LNF(1); else if (nv == 2) LNF(2); else if (nv == 3) LNF(3); else LNF(4);
+    if (L.f16) {
+        if (nv == 1) LNF(1, true); else if (nv == 2) LNF(2, true); else if (nv == 3) LNF(3, true); else LNF(4, true);
+    } else {
+        if (nv == 1) LNF(1, false); else if (nv == 2) LNF(2, false); else if (nv == 3) LNF(3, false); else LNF(4, false);
+    }
 #undef LNF
     return true;
 }
@@ -302,7 +322,7 @@ bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const voi
 bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const float* mean,
                         const float* rstd, const void* dy, void* dx, float* dw, float* db, int M,
                         int C, bool accumulate, float* scratch, bool acc_params, float* dres) {
-    if (L.f16 || C % 8 || C > 1024) return false;
+    if (C % 8 || C > 1024) return false;
     if (L.dry) return true;
     const int nv = (C / 8 + 31) / 32;
     const int np = dres ? 3 : 2;
@@ -311,24 +331,28 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     attr.once([] {
         const int mx2 = (LNV_WARPS * 2) * 1024 * (int)sizeof(float);
         const int mx3 = (LNV_WARPS * 3) * 1024 * (int)sizeof(float);
-#define LNA(NV)                                                                                        \
-        cudaFuncSetAttribute(k_ln_bwd_bf16<NV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx2); \
-        cudaFuncSetAttribute(k_ln_bwd_bf16<NV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx3)
-        LNA(1); LNA(2); LNA(3); LNA(4);
+#define LNA(NV, F)                                                                                        \
+        cudaFuncSetAttribute(k_ln_bwd_bf16<NV, false, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx2); \
+        cudaFuncSetAttribute(k_ln_bwd_bf16<NV, true, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx3)
+        LNA(1, false); LNA(2, false); LNA(3, false); LNA(4, false);
+        LNA(1, true); LNA(2, true); LNA(3, true); LNA(4, true);
 #undef LNA
         return true;
     });
     L.count();
     int G = 0;
-#define LNB(NV, RES) G = ln_bwd_blocks<NV, RES>(L, M); \
-    k_ln_bwd_bf16<NV, RES><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
+#define LNB(NV, RES, F) G = ln_bwd_blocks<NV, RES>(L, M); \
+    k_ln_bwd_bf16<NV, RES, F><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
         (const bf16*)x, (const bf16*)w, mean, rstd, (const bf16*)dy, (bf16*)dx, scratch, M, C, \
         accumulate ? 1 : 0)
-    if (dres) {
-        if (nv == 1) { LNB(1, true); } else if (nv == 2) { LNB(2, true); } else if (nv == 3) { LNB(3, true); } else { LNB(4, true); }
+#define LNB_NV(RES, F) \
+    if (nv == 1) { LNB(1, RES, F); } else if (nv == 2) { LNB(2, RES, F); } else if (nv == 3) { LNB(3, RES, F); } else { LNB(4, RES, F); }
+    if (L.f16) {
+        if (dres) { LNB_NV(true, true) } else { LNB_NV(false, true) }
     } else {
-        if (nv == 1) { LNB(1, false); } else if (nv == 2) { LNB(2, false); } else if (nv == 3) { LNB(3, false); } else { LNB(4, false); }
+        if (dres) { LNB_NV(true, false) } else { LNB_NV(false, false) }
     }
+#undef LNB_NV
 #undef LNB
     L.count();
     k_sum_rows<<<(np * C + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(scratch, G, np * C, C, dw, db, dres,
@@ -355,6 +379,7 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(XS_THREADS)
 k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict__ row_loss,
             int V, int ld, float dscale, const float* __restrict__ scale_dev, int* flags) {
@@ -366,18 +391,22 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
     const int vfull = V >> 3;  // vectors whose 8 columns are all < V
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // pass 1: max
-    __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+    // the max on packed pairs of the storage type (exact in any order)
+    using P2 = typename std::conditional<F16, __half2, __nv_bfloat162>::type;
+    P2 m2;
+    if constexpr (F16) m2 = __floats2half2_rn(-INFINITY, -INFINITY);
+    else m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
     float mx = -INFINITY;
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
         const uint4 u = zr[vi];
         if (vi < vfull) {
-            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.x));
-            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.y));
-            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.z));
-            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&u.w));
+            m2 = __hmax2(m2, *reinterpret_cast<const P2*>(&u.x));
+            m2 = __hmax2(m2, *reinterpret_cast<const P2*>(&u.y));
+            m2 = __hmax2(m2, *reinterpret_cast<const P2*>(&u.z));
+            m2 = __hmax2(m2, *reinterpret_cast<const P2*>(&u.w));
         } else {
             float f[8];
-            unpack8(u, f);
+            unpack8<F16>(u, f);
 #pragma unroll
             for (int e = 0; e < 8; e++)
                 if (vi * 8 + e < V) mx = fmaxf(mx, f[e]);
@@ -400,7 +429,7 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
     float s = 0.0f, ztgt = 0.0f;
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
         float f[8], ex[8];
-        unpack8(zr[vi], f);
+        unpack8<F16>(zr[vi], f);
         if (vi == tv) ztgt = f[tgt & 7];
         if (vi < vfull) {
 #pragma unroll
@@ -415,7 +444,7 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
                 s += ex[e];
             }
         }
-        zr[vi] = pack8(ex);
+        zr[vi] = pack8<F16>(ex);
     }
     s = wsum(s);
     __syncthreads();  // everyone has read sm[] above
@@ -433,24 +462,28 @@ k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __
     const float k = dscale / S_;
     for (int vi = threadIdx.x; vi < nvec; vi += XS_THREADS) {
         float ex[8], o[8];
-        unpack8(zr[vi], ex);
+        unpack8<F16>(zr[vi], ex);
 #pragma unroll
         for (int e = 0; e < 8; e++) o[e] = ex[e] * k;
         if (vi == tv) {
             row_loss[row] = lse - ztgt;
             o[tgt & 7] -= dscale;
         }
-        zr[vi] = pack8(o);
+        zr[vi] = pack8<F16>(o);
     }
 }
 
 bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, float* row_loss, int M,
                       int V, int ld, float dscale, const float* scale_dev) {
-    if (L.f16 || ld % 8 || ((uintptr_t)logits & 15) || ld < 2048) return false;
+    if (ld % 8 || ((uintptr_t)logits & 15) || ld < 2048) return false;
     if (L.dry) return true;
     L.count();
-    k_xent_bf16<<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
-                                                 scale_dev, L.flags);
+    if (L.f16)
+        k_xent_bf16<true><<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
+                                                           scale_dev, L.flags);
+    else
+        k_xent_bf16<false><<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
+                                                            scale_dev, L.flags);
     return true;
 }
 
@@ -459,6 +492,7 @@ constexpr int CS_ROWS = 256;  // rows per partial (the same chunking as the gene
 
 // block: 32 lanes x 8 columns = 256 columns, 8 warps split the 256 rows of
 // one partial (warp w takes rows w, w+8, ...); warps combine in warp order
+template <bool F16>
 __global__ void __launch_bounds__(256)
 k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part) {
     __shared__ float sm[8][256];
@@ -478,14 +512,14 @@ k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part
 #pragma unroll
             for (int u = 0; u < U; u++) {
                 float f[8];
-                unpack8(v[u], f);
+                unpack8<F16>(v[u], f);
 #pragma unroll
                 for (int e = 0; e < 8; e++) acc[e] += f[e];
             }
         }
         for (; r < r1; r += 8) {
             float f[8];
-            unpack8(*reinterpret_cast<const uint4*>(x + r * N + n8), f);
+            unpack8<F16>(*reinterpret_cast<const uint4*>(x + r * N + n8), f);
 #pragma unroll
             for (int e = 0; e < 8; e++) acc[e] += f[e];
         }
@@ -503,11 +537,12 @@ k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part
 }
 
 bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* part) {
-    if (L.f16 || N % 8 || ((uintptr_t)x & 15) || ((uintptr_t)part & 15)) return false;
+    if (N % 8 || ((uintptr_t)x & 15) || ((uintptr_t)part & 15)) return false;
     if (L.dry) return true;
     dim3 grid((N + 255) / 256, (M + CS_ROWS - 1) / CS_ROWS);
     L.count();
-    k_colsum_bf16<<<grid, 256, 0, L.stream>>>((const bf16*)x, M, N, part);
+    if (L.f16) k_colsum_bf16<true><<<grid, 256, 0, L.stream>>>((const bf16*)x, M, N, part);
+    else k_colsum_bf16<false><<<grid, 256, 0, L.stream>>>((const bf16*)x, M, N, part);
     return true;
 }
 

@@ -5,6 +5,8 @@
 
 #include <cuda.h>
 #include <stdint.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "tt_internal.h"
 
@@ -186,6 +188,45 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+
+// 16-bit storage: bf16, or IEEE half when F16 (the fp16 mixed-precision
+// step); every sum stays fp32.  lo16 / hi16 unpack the element in the low /
+// high half of a 32-bit word, pack2 rounds two floats to nearest even.
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t u) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu)));
+    else return __uint_as_float(u << 16);
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t u) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(u >> 16)));
+    else return __uint_as_float(u & 0xFFFF0000u);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (F16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+template <bool F16>
+__device__ __forceinline__ float ld16(const void* p, int j) {
+    if constexpr (F16) return __half2float(reinterpret_cast<const __half*>(p)[j]);
+    else return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[j]);
+}
+template <bool F16>
+__device__ __forceinline__ void st16(void* p, int j, float v) {
+    if constexpr (F16) reinterpret_cast<__half*>(p)[j] = __float2half_rn(v);
+    else reinterpret_cast<__nv_bfloat16*>(p)[j] = __float2bfloat16_rn(v);
+}
+// the MMA instruction descriptor for 16-bit operands of either format
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc16(int M, int N, bool a_mn, bool b_mn) {
+    return F16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10))) : idesc_bf16(M, N, a_mn, b_mn);
+}
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(

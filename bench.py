@@ -223,6 +223,8 @@ OP_SHAPES = {
               "(global gradient statistics, AdamW with clipping, unscaling and overflow skip, loss-scale update)",
     "fruit": "the generic tensor graph: the tinytorch page's classifier (3 -> 32 GELU -> 3, softmax, "
              "cross entropy) trained by SGD on 64 samples, one step = forward, zero_grad, backward, SGD",
+    "step_dtypes": "forward + backward (tt_gpt2_step_ex with a device loss scale of 2^10) in bf16 and in "
+                   "IEEE half, char B=64 T=256 and 124M B=8 T=1024",
 }
 
 
@@ -537,6 +539,53 @@ def run_fruit(args):
     return 0
 
 
+def run_step_dtypes(args):
+    """Times the forward + backward of the char and 124M B=8 workloads with bf16
+    and with IEEE-half storage (fp32 master, loss scale 2^10), CUDA events
+    around `--reps` steps after `--warmup`."""
+    import torch
+
+    from autograd_arena_allocated_gb300 import api, synth
+    from autograd_arena_allocated_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    out = {"op": "step_dtypes", "what": OP_SHAPES["step_dtypes"]}
+    for name, B, T in (("char_bf16", 64, 256), ("gpt2_124m_b8", 8, 1024)):
+        w = synth.WORKLOADS[name]
+        sh = w.shape
+        p = torch.from_numpy(synth.init_params(sh)).cuda()
+        tok, tgt = synth.token_stream(B, T, sh.V, w.tokens)
+        td, gd = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+        for dt in ("bf16", "fp16"):
+            cfg = api.make_config(sh.L, sh.C, sh.H, sh.V, sh.maxT, dt)
+            ctx = api.Context(api.arena_bytes(cfg, B, T) + (64 << 20))
+            ctx.set_model(cfg)
+            low = torch.empty(p.numel(), device="cuda", dtype=torch.bfloat16 if dt == "bf16" else torch.float16)
+            (ctx.cast_bf16 if dt == "bf16" else ctx.cast_f16)(p, low)
+            grads = torch.empty(p.numel(), device="cuda")
+            scale = torch.tensor([1024.0], device="cuda")
+
+            def step():
+                ctx.reset()
+                ctx.step_ex(low, grads, td, gd, B, T, loss_scale=scale, sync=False)
+
+            for _ in range(max(args.warmup, 1)):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.reps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.reps
+            out[f"{name}/{dt}"] = {"B": B, "T": T, "ms_per_fwd_bwd": ms, "tokens_per_s": B * T / ms * 1e3}
+            ctx.close()
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_op(args):
     """Runs one kernel group `--reps` times through the C ABI (for profiling)."""
     import torch
@@ -684,6 +733,8 @@ def main():
             return run_fruit(args)
         if args.op == "update":
             return run_update(args)
+        if args.op == "step_dtypes":
+            return run_step_dtypes(args)
         return run_gemm_shapes(args) if args.op == "gemm_shapes" else run_op(args)
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     world, rank, local = dist_setup()
