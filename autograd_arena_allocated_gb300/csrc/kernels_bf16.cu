@@ -11,6 +11,7 @@
 
 #include <math.h>
 #include <type_traits>
+#include <algorithm>
 
 namespace tt {
 
@@ -116,17 +117,42 @@ k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16
 // LayerNorm's input is a residual-stream tensor whose gradient is complete
 // once this kernel has added its share, and that tensor is the output of a
 // linear layer, whose bias gradient is exactly these column sums.
+// Rows reach shared memory by cp.async (16 bytes per lane, each lane copying
+// exactly the vectors it later reads), LN_DEPTH(NV) rows ahead of the row the
+// warp works on, so that a warp keeps several rows of loads in flight while it
+// reduces one; both passes read the row from shared memory.
+__host__ __device__ constexpr int ln_depth(int nv) { return nv <= 3 ? 3 : 2; }
+// per warp: the row slots, reused at the end for the warp's partials
+__host__ __device__ constexpr size_t ln_bwd_warp_bytes(int C, int nv, int np) {
+    return (size_t)ln_depth(nv) * 3 * C * 2 > (size_t)np * C * 4 ? (size_t)ln_depth(nv) * 3 * C * 2
+                                                                 : (size_t)np * C * 4;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int NV, bool RES, bool F16>
 __global__ void __launch_bounds__(LNV_WARPS * 32, 2)
 k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
               const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
               float* __restrict__ part, int M, int C, int accumulate) {
     constexpr int NP = RES ? 3 : 2;
-    extern __shared__ float s_part[];  // [LNV_WARPS][NP C]: each warp's dw | db (| dres) partials
-    __shared__ uint4 s_gamma[128];        // gamma, 8 bf16 per entry (C <= 1024)
+    constexpr int DEPTH = ln_depth(NV);
+    extern __shared__ __align__(16) uint8_t s_dyn[];  // [LNV_WARPS][ln_bwd_warp_bytes]
+    __shared__ uint4 s_gamma[128];        // gamma, 8 values per entry (C <= 1024)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvec = C >> 3;
     const float inv_c = 1.0f / (float)C;
+    const size_t wbytes = ln_bwd_warp_bytes(C, NV, NP);
+    uint8_t* wbase = s_dyn + warp * wbytes;
+    // slot d of this warp: x | dy | old dx, C values each
+    auto slot = [&](int d, int k) { return reinterpret_cast<uint4*>(wbase + ((size_t)d * 3 + k) * C * 2); };
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) s_gamma[v] = reinterpret_cast<const uint4*>(w)[v];
     float aw[NV][8], ab[NV][8], ar[RES ? NV : 1][8];
 #pragma unroll
@@ -134,32 +160,47 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
 #pragma unroll
         for (int e = 0; e < 8; e++) { aw[i][e] = 0.0f; ab[i][e] = 0.0f; if (RES) ar[RES ? i : 0][e] = 0.0f; }
     __syncthreads();
-    for (long long row = (long long)blockIdx.x * LNV_WARPS + warp; row < M;
-         row += (long long)gridDim.x * LNV_WARPS) {
-        const uint4* xr = reinterpret_cast<const uint4*>(x + row * C);
-        const uint4* dr = reinterpret_cast<const uint4*>(dy + row * C);
-        uint4* xo = reinterpret_cast<uint4*>(dx + row * C);
-        // every load of the row is issued before any arithmetic
-        uint4 xv[NV], dv[NV], ov[NV];
+    const long long stride = (long long)gridDim.x * LNV_WARPS;
+    const long long row0 = (long long)blockIdx.x * LNV_WARPS + warp;
+    auto issue = [&](long long row, int d) {
+        if (row < M) {
 #pragma unroll
-        for (int i = 0; i < NV; i++) {
-            const int vi = lane + 32 * i;
-            if (vi < nvec) {
-                xv[i] = xr[vi];
-                dv[i] = dr[vi];
-                if (accumulate) ov[i] = xo[vi];
+            for (int i = 0; i < NV; i++) {
+                const int vi = lane + 32 * i;
+                if (vi < nvec) {
+                    cp_async16(slot(d, 0) + vi, reinterpret_cast<const uint4*>(x + row * C) + vi);
+                    cp_async16(slot(d, 1) + vi, reinterpret_cast<const uint4*>(dy + row * C) + vi);
+                    if (accumulate) cp_async16(slot(d, 2) + vi, reinterpret_cast<const uint4*>(dx + row * C) + vi);
+                }
             }
         }
-        const float mu = mean[row], rs = rstd[row];
+        cp_async_commit();  // a group per row, empty past the end, so the waits count evenly
+    };
+#pragma unroll
+    for (int d = 0; d < DEPTH - 1; d++) issue(row0 + d * stride, d);
+    float mu_n = 0.0f, rs_n = 0.0f;
+    if (row0 < M) { mu_n = mean[row0]; rs_n = rstd[row0]; }
+    int k = 0;
+    for (long long row = row0; row < M; row += stride, k++) {
+        issue(row + (DEPTH - 1) * stride, (k + DEPTH - 1) % DEPTH);
+        const float mu = mu_n, rs = rs_n;
+        if (row + stride < M) { mu_n = mean[row + stride]; rs_n = rstd[row + stride]; }  // one row ahead
+        cp_async_wait<DEPTH - 1>();  // this row's group has landed
+        const int d = k % DEPTH;
+        const uint4* sx = slot(d, 0);
+        const uint4* sd = slot(d, 1);
+        const uint4* so = slot(d, 2);
+        uint4* xo = reinterpret_cast<uint4*>(dx + row * C);
         // pass 1: the two row sums, and this row's dw/db contributions
         float sg = 0.0f, sgx = 0.0f;
 #pragma unroll
         for (int i = 0; i < NV; i++) {
-            if (lane + 32 * i < nvec) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
                 float xf[8], df[8], wf[8];
-                unpack8<F16>(xv[i], xf);
-                unpack8<F16>(dv[i], df);
-                unpack8<F16>(s_gamma[lane + 32 * i], wf);
+                unpack8<F16>(sx[vi], xf);
+                unpack8<F16>(sd[vi], df);
+                unpack8<F16>(s_gamma[vi], wf);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const float xh = (xf[e] - mu) * rs;
@@ -172,14 +213,14 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
             }
         }
         const float mg = wsum(sg) * inv_c, mgx = wsum(sgx) * inv_c;
-        // pass 2: dx from the same registers
+        // pass 2: dx
 #pragma unroll
         for (int i = 0; i < NV; i++) {
             const int vi = lane + 32 * i;
             if (vi < nvec) {
                 float xf[8], df[8], wf[8], o[8];
-                unpack8<F16>(xv[i], xf);
-                unpack8<F16>(dv[i], df);
+                unpack8<F16>(sx[vi], xf);
+                unpack8<F16>(sd[vi], df);
                 unpack8<F16>(s_gamma[vi], wf);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
@@ -188,7 +229,7 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
                 }
                 if (accumulate) {
                     float old[8];
-                    unpack8<F16>(ov[i], old);
+                    unpack8<F16>(so[vi], old);
 #pragma unroll
                     for (int e = 0; e < 8; e++) o[e] += old[e];
                 }
@@ -200,8 +241,9 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
             }
         }
     }
-    // the block's partials: warps in warp order
-    float* pw = s_part + warp * NP * C;
+    cp_async_wait<0>();  // the empty trailing groups
+    // the block's partials: warps in warp order (each warp over its own row slots)
+    float* pw = reinterpret_cast<float*>(wbase);
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int vi = lane + 32 * i;
@@ -224,7 +266,8 @@ k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const floa
     for (int c = threadIdx.x; c < NP * C; c += blockDim.x) {
         float s = 0.0f;
 #pragma unroll
-        for (int k = 0; k < LNV_WARPS; k++) s += s_part[k * NP * C + c];
+        for (int kk = 0; kk < LNV_WARPS; kk++)
+            s += reinterpret_cast<const float*>(s_dyn + kk * wbytes)[c];
         part[(long long)blockIdx.x * NP * C + c] = s;
     }
 }
@@ -286,7 +329,7 @@ static int ln_bwd_blocks(const Launch& L, int M) {
     const int b = per_sm.value([] {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_ln_bwd_bf16<NV, RES, false>, LNV_WARPS * 32,
-                                                          (LNV_WARPS * (RES ? 3 : 2)) * 1024 * sizeof(float)) !=
+                                                          LNV_WARPS * ln_bwd_warp_bytes(NV * 256, NV, RES ? 3 : 2)) !=
                 cudaSuccess || n < 1) {
             cudaGetLastError();
             n = 1;
@@ -326,11 +369,16 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     if (L.dry) return true;
     const int nv = (C / 8 + 31) / 32;
     const int np = dres ? 3 : 2;
-    const size_t smem = (size_t)(LNV_WARPS * np) * C * sizeof(float);
+    const size_t smem = LNV_WARPS * ln_bwd_warp_bytes(C, nv, np);
     static PerDevice attr;
     attr.once([] {
-        const int mx2 = (LNV_WARPS * 2) * 1024 * (int)sizeof(float);
-        const int mx3 = (LNV_WARPS * 3) * 1024 * (int)sizeof(float);
+        // the largest any C <= 1024 needs
+        int mx2 = 0, mx3 = 0;
+        for (int c = 8; c <= 1024; c += 8) {
+            const int v = (c / 8 + 31) / 32;
+            mx2 = std::max(mx2, (int)(LNV_WARPS * ln_bwd_warp_bytes(c, v, 2)));
+            mx3 = std::max(mx3, (int)(LNV_WARPS * ln_bwd_warp_bytes(c, v, 3)));
+        }
 #define LNA(NV, F)                                                                                        \
         cudaFuncSetAttribute(k_ln_bwd_bf16<NV, false, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx2); \
         cudaFuncSetAttribute(k_ln_bwd_bf16<NV, true, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx3)
