@@ -228,27 +228,33 @@ OP_SHAPES = {
 }
 
 
-# DRAM bytes per launch group of each op kind (dram__bytes_read.sum +
-# dram__bytes_write.sum summed over the kind's kernels in one ncu capture of a
-# whole step of the workload, divided by the kind's launch groups per step),
-# valid only for the kernel sources whose digest is recorded: once any kernel
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch group
+# of each op kind, from single-kernel ncu captures at the workload's full size,
+# one launch per shape after a warm-up launch (a few GB on the device at
+# most):
+#   gemm_*: `bench.py --op gemm_shapes --kinds fwd|dx|dw --warmup 1 --reps 1`,
+#           each of the five shapes (qkv, proj, fc, fcproj per layer; the LM
+#           head once) weighted by its launches per step: (12 x the four layer
+#           shapes + the LM head) / 49; the weight-gradient groups include
+#           their split-K reduction;
+#   the others: `bench.py --op NAME --warmup 1 --reps 1`, the last call's
+#           kernels.
+# Valid only for the kernel sources whose digest is recorded: once any kernel
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "8b0edd2a44713283",
+    "sources": "b05ab55b806df720",
     "bytes_per_launch_group": {
-        "gemm_fwd": 349031581,
-        "gemm_dx": 339794667,
-        "gemm_dw": 331005853,
-        "attn_fwd": 178190912,
-        "attn_bwd": 559331797,
-        "xent": 6543062272,
-        "colsum": 114252992,
-        "ln_fwd": 54011341,
-        "ln_bwd": 170545644,
-        "adamw": 3672140544,
-        "embed_fwd": 12711936,
-        "embed_bwd": 124966144,
+        "gemm_fwd": 346649715,
+        "gemm_dx": 348104359,
+        "gemm_dw": 344119385,
+        "attn_fwd": 178639616,
+        "attn_bwd": 559203328,
+        "xent": 6542648576,
+        "ln_fwd": 54671360,
+        "ln_bwd": 168009472,
+        "adamw": 3673257472,
+        "embed_bwd": 124973824,
     },
 }
 
