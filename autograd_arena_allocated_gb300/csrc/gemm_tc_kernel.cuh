@@ -62,14 +62,56 @@ __device__ __forceinline__ float tanh_hw(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float gelu_tanh(float u) {
-    const float k = 0.7978845608028654f, a = 0.044715f;
-    return 0.5f * u * (1.0f + tanh_hw(k * (u + a * u * u * u)));
+
+// The epilogue's elementwise work on pairs of values, in the packed fp32x2
+// instructions of sm_100 and later (one instruction for both lanes, each
+// lane rounded as the scalar instruction would): half the issue slots of the
+// scalar form, which is what bounds the epilogue warps.
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+// GELU, tanh form: 0.5 u (1 + tanh(w)), w = k u (1 + a u^2)
+__device__ __forceinline__ float2 gelu_tanh2(float2 u) {
+    const float2 s = __fmul2_rn(u, u);
+    const float2 w = __fmul2_rn(__fmul2_rn(f2(0.7978845608028654f), u), __ffma2_rn(f2(0.044715f), s, f2(1.0f)));
+    const float2 t = make_float2(tanh_hw(w.x), tanh_hw(w.y));
+    const float2 hu = __fmul2_rn(f2(0.5f), u);
+    return __ffma2_rn(hu, t, hu);
 }
-__device__ __forceinline__ float dgelu_tanh(float u) {
-    const float k = 0.7978845608028654f, a = 0.044715f;
-    const float tau = tanh_hw(k * (u + a * u * u * u));
-    return 0.5f * (1.0f + tau) + 0.5f * u * (1.0f - tau * tau) * k * (1.0f + 3.0f * a * u * u);
+// its derivative: 0.5 (1 + tau + k u (1 + 3 a u^2) (1 - tau^2)), tau = tanh(w);
+// written with the signs folded into constants, (-r)(tau^2 - 1) = r (1 - tau^2)
+__device__ __forceinline__ float2 dgelu_tanh2(float2 u) {
+    const float2 s = __fmul2_rn(u, u);
+    const float2 ku = __fmul2_rn(f2(0.7978845608028654f), u);
+    const float2 w = __fmul2_rn(ku, __ffma2_rn(f2(0.044715f), s, f2(1.0f)));
+    const float2 t = make_float2(tanh_hw(w.x), tanh_hw(w.y));
+    const float2 nr = __fmul2_rn(ku, __ffma2_rn(f2(-3.0f * 0.044715f), s, f2(-1.0f)));
+    const float2 y = __ffma2_rn(nr, __ffma2_rn(t, t, f2(-1.0f)), t);
+    return __ffma2_rn(f2(0.5f), y, f2(0.5f));
+}
+__device__ __forceinline__ void add32(float* v, const float* w) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 r = __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(w[j], w[j + 1]));
+        v[j] = r.x;
+        v[j + 1] = r.y;
+    }
+}
+__device__ __forceinline__ void gelu32(float* v) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 r = gelu_tanh2(make_float2(v[j], v[j + 1]));
+        v[j] = r.x;
+        v[j + 1] = r.y;
+    }
+}
+// v *= gelu'(u)
+__device__ __forceinline__ void mul_dgelu32(float* v, const float* u) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 r = __fmul2_rn(make_float2(v[j], v[j + 1]), dgelu_tanh2(make_float2(u[j], u[j + 1])));
+        v[j] = r.x;
+        v[j + 1] = r.y;
+    }
 }
 
 // One warp's 32 x 32 bf16 staging tile (row = lane, 64 bytes per row) in the
@@ -511,21 +553,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (p.bias) {
                         float bb[32];
                         load32_16<F16>(p.bias + n, 32, true, bb);
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] += bb[j];
+                        add32(v, bb);
                     }
                     if (!mbar_wait_warp(&eb[b], (eph >> b) & 1u, abort_flag, p.flags, 0x400 + 5, p.wait_limit)) { ok = false; break; }
                     eph ^= 1u << b;
                     pending &= ~(1u << b);
                     float e[32];
                     load_row32<F16>(stg + b * 2048, lane, e);
-                    if (p.epi == EPI_DGELU) {
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(e[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] += e[j];
-                    }
+                    if (p.epi == EPI_DGELU) mul_dgelu32(v, e);
+                    else add32(v, e);
                     stage_row32<F16>(stg + b * 2048, lane, v);
                     if (p.colsum) {
                         // this chunk's 32 rows summed per column (rows past M
@@ -575,8 +611,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (p.bias) {
                         float b[32];
                         load32_16<F16>(p.bias + n, valid, true, b);
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] += b[j];
+                        add32(v, b);
                     }
                     const bool gelu = p.epi == EPI_GELU;
                     if (lane == 0) {
@@ -585,8 +620,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     __syncwarp();
                     if (gelu) {
                         stage_row32<F16>(stg, lane, v);  // pre-activation
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] = gelu_tanh(v[j]);
+                        gelu32(v);
                     } else if (p.epi == EPI_DGELU) {
                         float u_[32];
                         if (row_ok) load32_16<F16>(p.aux + o, valid, aux_vec, u_);
@@ -594,14 +628,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                             for (int j = 0; j < 32; j++) u_[j] = 0.0f;
                         }
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(u_[j]);
+                        mul_dgelu32(v, u_);
                     }
                     if (p.residual && row_ok) {
                         float rr[32];
                         load32_16<F16>(p.residual + o, valid, res_vec, rr);
-#pragma unroll
-                        for (int j = 0; j < 32; j++) v[j] += rr[j];
+                        add32(v, rr);
                     }
                     uint8_t* dbuf = gelu ? stg + 2048 : stg + sbuf * 2048;
                     stage_row32<F16>(dbuf, lane, v);
@@ -639,31 +671,26 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if (p.bias) {
                     float b[32];
                     load32_16<F16>(p.bias + n, valid, true, b);
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] += b[j];
+                    add32(v, b);
                 }
                 if (p.epi == EPI_GELU) {
                     store32_16<F16>(p.aux + o, valid, aux_vec, v);
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = gelu_tanh(v[j]);
+                    gelu32(v);
                 } else if (p.epi == EPI_DGELU) {
                     float u_[32];
                     load32_16<F16>(p.aux + o, valid, aux_vec, u_);
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] *= dgelu_tanh(u_[j]);
+                    mul_dgelu32(v, u_);
                 }
                 if (p.residual) {
                     float rr[32];
                     load32_16<F16>(p.residual + o, valid, res_vec, rr);
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] += rr[j];
+                    add32(v, rr);
                 }
                 uint16_t* d = (uint16_t*)p.D + o;
                 if (p.accumulate) {
                     float old[32];
                     load32_16<F16>(d, valid, out_vec, old);
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] += old[j];
+                    add32(v, old);
                 }
                 store32_16<F16>(d, valid, out_vec, v);
             }

@@ -256,16 +256,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // order of the additions is fixed, so the result is deterministic.
 __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
+    for (int s = 16; s >= 2; s >>= 1) {
         const bool up = (lane & s) != 0;
 #pragma unroll
-        for (int i = 0; i < s; i++) {
-            const float send = up ? v[i] : v[i + s];
-            const float keep = up ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        for (int i = 0; i < s; i += 2) {  // two columns per packed fp32x2 add
+            float2 send, keep;
+            send.x = up ? v[i] : v[i + s];
+            send.y = up ? v[i + 1] : v[i + s + 1];
+            keep.x = up ? v[i + s] : v[i];
+            keep.y = up ? v[i + s + 1] : v[i + 1];
+            const float2 got = make_float2(__shfl_xor_sync(0xffffffffu, send.x, s),
+                                           __shfl_xor_sync(0xffffffffu, send.y, s));
+            const float2 r = __fadd2_rn(keep, got);
+            v[i] = r.x;
+            v[i + 1] = r.y;
         }
     }
-    return v[0];
+    const bool up = (lane & 1) != 0;
+    return (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, up ? v[0] : v[1], 1);
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
