@@ -293,37 +293,29 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             }
             // P = 2^(s*scale - m) as bf16, each 32-column half straight to shared memory
             uint8_t* pbuf = sm + F_P + pb * T128;
-            float rs0 = 0.0f, rs1 = 0.0f;  // two independent chains
-            {
+            // (packed fp32x2 scale-and-subtract and sums: two lanes per instruction;
+            // the sums in two independent packed chains)
+            float2 rsa = make_float2(0.0f, 0.0f), rsb = make_float2(0.0f, 0.0f);
+            const float2 sl2 = make_float2(SL2, SL2), nm = make_float2(-m, -m);
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+                const uint32_t(&w)[32] = c ? w1 : w0;
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2(fmaf(__uint_as_float(w0[e]), SL2, -m));
-                    float p1 = ex2(fmaf(__uint_as_float(w0[e + 1]), SL2, -m));
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(w[e]), __uint_as_float(w[e + 1])), sl2, nm);
+                    float2 p = make_float2(ex2(x.x), ex2(x.y));
                     if (diag) {
-                        if (e > kq) p0 = 0.0f;
-                        if (e + 1 > kq) p1 = 0.0f;
+                        if (32 * c + e > kq) p.x = 0.0f;
+                        if (32 * c + e + 1 > kq) p.y = 0.0f;
                     }
-                    rs0 += p0;
-                    rs1 += p1;
-                    pk[e >> 1] = pack2<F16>(p0, p1);
+                    if (e & 2) rsb = __fadd2_rn(rsb, p);
+                    else rsa = __fadd2_rn(rsa, p);
+                    pk[e >> 1] = pack2<F16>(p.x, p.y);
                 }
-                store_row32(pbuf, r, 0, pk);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2(fmaf(__uint_as_float(w1[e]), SL2, -m));
-                    float p1 = ex2(fmaf(__uint_as_float(w1[e + 1]), SL2, -m));
-                    if (diag) {
-                        if (32 + e > kq) p0 = 0.0f;
-                        if (33 + e > kq) p1 = 0.0f;
-                    }
-                    rs0 += p0;
-                    rs1 += p1;
-                    pk[e >> 1] = pack2<F16>(p0, p1);
-                }
-                store_row32(pbuf, r, 32, pk);
+                store_row32(pbuf, r, 32 * c, pk);
             }
-            const float rs = rs0 + rs1;
+            const float rs = (rsa.x + rsb.x) + (rsa.y + rsb.y);
             if (rescale) {
                 // O must hold P_{j-1} V_{j-1} before it is scaled
                 if (!mbar_wait_warp(&o_full[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag, flags, 0x100 + 10, wl)) {
@@ -624,16 +616,19 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             uint32_t sw[32], pw[32];
             tmem_ld32x2(tl + Q_TS + 32 * half, sw, tl + Q_TP + 32 * half, pw);
             // dS = P o (dP - D), packed bf16
+            // (packed fp32x2: the same roundings as the scalar fma, sub and mul)
             uint32_t pk[16];
+            const float2 sl2 = make_float2(SL2, SL2), nl = make_float2(-Lq, -Lq), nd = make_float2(-Dq, -Dq);
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-                float d0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -Lq)) * (__uint_as_float(pw[e]) - Dq);
-                float d1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -Lq)) * (__uint_as_float(pw[e + 1]) - Dq);
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sw[e]), __uint_as_float(sw[e + 1])), sl2, nl);
+                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pw[e]), __uint_as_float(pw[e + 1])), nd);
+                float2 d = __fmul2_rn(make_float2(ex2(x.x), ex2(x.y)), dd);
                 if (diag) {
-                    if (e > kq) d0 = 0.0f;
-                    if (e + 1 > kq) d1 = 0.0f;
+                    if (e > kq) d.x = 0.0f;
+                    if (e + 1 > kq) d.y = 0.0f;
                 }
-                pk[e >> 1] = pack2<F16>(qv ? d0 : 0.0f, qv ? d1 : 0.0f);
+                pk[e >> 1] = pack2<F16>(qv ? d.x : 0.0f, qv ? d.y : 0.0f);
             }
             tmem_st16(tl + Q_TDS + 32 * (j & 1) + 16 * half, pk);
             tmem_st_wait();
