@@ -808,8 +808,8 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
         for (int i = 0; i < nq; i++) {
             const int j = j0 + i;
             __syncwarp();  // the previous block's reads of the slice are done
-            sl[lane] = Ln;
-            sl[32 + lane] = Dn;
+            sl[lane] = -Ln;  // negated: the packed fma and add below take them as addends
+            sl[32 + lane] = -Dn;
             __syncwarp();
             if (i + 1 < nq) fetch(i + 1);
             if (!mbar_wait_warp(st_full, i & 1, abort_flag, flags, 0x300 + 6, wl)) { ok = false; break; }
@@ -820,24 +820,22 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tmem_ld32x2(tl + K_TS + 32 * half, sw, tl + K_TP + 32 * half, dw);
             uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                const float4 L4 = *reinterpret_cast<const float4*>(sl + e);
-                const float4 D4 = *reinterpret_cast<const float4*>(sl + 32 + e);
-                float p0 = ex2(fmaf(__uint_as_float(sw[e]), SL2, -L4.x));
-                float p1 = ex2(fmaf(__uint_as_float(sw[e + 1]), SL2, -L4.y));
-                float p2 = ex2(fmaf(__uint_as_float(sw[e + 2]), SL2, -L4.z));
-                float p3 = ex2(fmaf(__uint_as_float(sw[e + 3]), SL2, -L4.w));
+            for (int e = 0; e < 32; e += 2) {
+                // -L and -D from the slice; packed fp32x2 with the scalar
+                // operations' roundings
+                const float2 L2 = *reinterpret_cast<const float2*>(sl + e);
+                const float2 D2 = *reinterpret_cast<const float2*>(sl + 32 + e);
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sw[e]), __uint_as_float(sw[e + 1])),
+                                            make_float2(SL2, SL2), L2);
+                float2 p = make_float2(ex2(x.x), ex2(x.y));
                 if (diag) {
-                    if (q0 + e < key) p0 = 0.0f;
-                    if (q0 + e + 1 < key) p1 = 0.0f;
-                    if (q0 + e + 2 < key) p2 = 0.0f;
-                    if (q0 + e + 3 < key) p3 = 0.0f;
+                    if (q0 + e < key) p.x = 0.0f;
+                    if (q0 + e + 1 < key) p.y = 0.0f;
                 }
-                pk[e >> 1] = pack2<F16>(p0, p1);
-                pk[(e >> 1) + 1] = pack2<F16>(p2, p3);
-                dk[e >> 1] = pack2<F16>(p0 * (__uint_as_float(dw[e]) - D4.x), p1 * (__uint_as_float(dw[e + 1]) - D4.y));
-                dk[(e >> 1) + 1] =
-                    pack2<F16>(p2 * (__uint_as_float(dw[e + 2]) - D4.z), p3 * (__uint_as_float(dw[e + 3]) - D4.w));
+                pk[e >> 1] = pack2<F16>(p.x, p.y);
+                const float2 d =
+                    __fmul2_rn(p, __fadd2_rn(make_float2(__uint_as_float(dw[e]), __uint_as_float(dw[e + 1])), D2));
+                dk[e >> 1] = pack2<F16>(d.x, d.y);
             }
             tmem_st16(tl + K_TS + 32 * half, pk);
             tmem_st16(tl + K_TP + 32 * half, dk);
