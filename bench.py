@@ -243,18 +243,18 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "b05ab55b806df720",
+    "sources": "9470148af83b837e",
     "bytes_per_launch_group": {
-        "gemm_fwd": 346649715,
-        "gemm_dx": 348104359,
-        "gemm_dw": 344119385,
-        "attn_fwd": 178639616,
-        "attn_bwd": 559203328,
-        "xent": 6542648576,
-        "ln_fwd": 54671360,
-        "ln_bwd": 168009472,
-        "adamw": 3673257472,
-        "embed_bwd": 124973824,
+        "gemm_fwd": 344785664,
+        "gemm_dx": 311672853,
+        "gemm_dw": 305877985,
+        "attn_fwd": 178769408,
+        "attn_bwd": 560025856,
+        "xent": 6543663360,
+        "ln_fwd": 54798080,
+        "ln_bwd": 167800832,
+        "adamw": 3673080064,
+        "embed_bwd": 124909312,
     },
 }
 
