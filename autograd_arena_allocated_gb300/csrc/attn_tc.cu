@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(THREADS, 3)
 k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int nbh, int* flags,
               long long wl) {
+    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + F_BAR);
@@ -450,6 +451,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
                  const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
                  float* __restrict__ bpart, int T, int C, int H, int nbh, int* flags, long long wl) {
+    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
@@ -682,6 +684,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
                    const float* __restrict__ Dlt, bf16* __restrict__ dqkv, float* __restrict__ bpart, int T,
                    int C, int H, int nbh, int* flags, long long wl) {
+    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + K_BAR);
@@ -905,7 +908,7 @@ static bool attn_fwd_tc(const Launch& L, const void* qkv, void* y, float* lse, i
     if (!attn_set_smem<F16>()) return false;
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
-    fa5::k_attn_fwd_tc<F16><<<grid, fa5::THREADS, fa5::F_SMEM, L.stream>>>(tq, tk, (fa5::bf16*)y, lse, T, C, H,
+    launch_k(L, fa5::k_attn_fwd_tc<F16>, dim3(grid), dim3(fa5::THREADS), fa5::F_SMEM, tq, tk, (fa5::bf16*)y, lse, T, C, H,
                                                                           B * H, L.flags, L.wait_cycles);
     return true;
 }
@@ -924,11 +927,11 @@ static bool attn_bwd_tc(const Launch& L, const void* qkv, const void* y, const f
     if (!attn_set_smem<F16>()) return false;
     const dim3 grid = attn_grid(B * H, (T + fa5::BQ - 1) / fa5::BQ);
     L.count();
-    fa5::k_attn_bwd_dq_tc<F16><<<grid, fa5::BW_THREADS, fa5::Q_SMEM, L.stream>>>(
+    launch_k(L, fa5::k_attn_bwd_dq_tc<F16>, dim3(grid), dim3(fa5::BW_THREADS), fa5::Q_SMEM, 
         tq, tk, to128, (const fa5::bf16*)y, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags,
         L.wait_cycles);
     L.count();
-    fa5::k_attn_bwd_dkdv_tc<F16><<<grid, fa5::BW_THREADS, fa5::K_SMEM, L.stream>>>(
+    launch_k(L, fa5::k_attn_bwd_dkdv_tc<F16>, dim3(grid), dim3(fa5::BW_THREADS), fa5::K_SMEM, 
         tq, tk, to64, lse, Dlt, (fa5::bf16*)dqkv, bpart, T, C, H, B * H, L.flags, L.wait_cycles);
     return true;
 }

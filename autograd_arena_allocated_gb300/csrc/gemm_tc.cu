@@ -50,6 +50,7 @@ namespace tc {
 // D[m, n] (+)= sum_s ws[s][m][n] in split order (fp32 output, n < n_store)
 __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M, int N, int n_store,
                                 float* __restrict__ D, long long ldd, int accumulate) {
+    pdl_enter();
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     long long total = (long long)M * n_store;
     if (i >= total) return;
@@ -65,6 +66,7 @@ __global__ void k_splitk_reduce(const float* __restrict__ ws, int splits, int M,
 // loads of up to eight splits in flight before their adds, in split order.
 __global__ void k_splitk_reduce4(const float* __restrict__ ws, int splits, int M, int N, int n_store,
                                  float* __restrict__ D, long long ldd, int accumulate) {
+    pdl_enter();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const int nq = n_store >> 2;
     if (i >= (long long)M * nq) return;
@@ -363,11 +365,11 @@ bool gemm_tc_launch(const Launch& L, const GemmArgs& g, float* workspace, size_t
         L.count();
         if (vec) {
             const long long total = (long long)g.M * (pl.p.n_store / 4);
-            tc::k_splitk_reduce4<<<(unsigned)((total + 255) / 256), 256, 0, L.stream>>>(
+            launch_k(L, tc::k_splitk_reduce4, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, 
                 workspace, pl.p.splits, g.M, g.N, pl.p.n_store, (float*)g.D, g.ldd, g.accumulate ? 1 : 0);
         } else {
             const long long total = (long long)g.M * pl.p.n_store;
-            tc::k_splitk_reduce<<<(unsigned)((total + 255) / 256), 256, 0, L.stream>>>(
+            launch_k(L, tc::k_splitk_reduce, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, 
                 workspace, pl.p.splits, g.M, g.N, pl.p.n_store, (float*)g.D, g.ldd, g.accumulate ? 1 : 0);
         }
     }

@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
           const Params p) {
+    pdl_enter();
     using CF = Cfg<BN, PAIR>;
     constexpr int S = CF::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -737,22 +738,27 @@ bool launch_tc(const Launch& L, const Plan& pl, const CUtensorMap& ma, const CUt
         return false;
     }
     L.count();
-    if (!PAIR) {
-        kern<<<pl.grid, THREADS, smem, L.stream>>>(ma, mb, md, mx, pl.p);
-        return true;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute at[2];
+    int na = 0;
+    if (PAIR) {
+        at[na].id = cudaLaunchAttributeClusterDimension;
+        at[na].val.clusterDim.x = 2;
+        at[na].val.clusterDim.y = 1;
+        at[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (L.pdl) {  // the kernel waits for its predecessor before any global access
+        at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, md, mx, pl.p) == cudaSuccess;
 }
 

@@ -61,6 +61,7 @@ template <typename T>
 __global__ void k_embed_fwd(const T* __restrict__ wte, const T* __restrict__ wpe,
                             const int32_t* __restrict__ tok, T* __restrict__ x,
                             int T_, int C, int V, long long total, int* flags) {
+    pdl_enter();
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total) return;
     long long m = i / C;
@@ -82,15 +83,15 @@ void launch_embed_fwd(const Launch& L, bool bf16, const void* wte, const void* w
     long long total = (long long)B * T * C;
     L.count();
     if (bf16 && L.f16)
-        k_embed_fwd<__half><<<blocks_for(total, 256), 256, 0, L.stream>>>(
+        launch_k(L, k_embed_fwd<__half>, dim3(blocks_for(total, 256)), dim3(256), 0, 
             (const __half*)wte, (const __half*)wpe, tok, (__half*)x, T, C, V,
             total, L.flags);
     else if (bf16)
-        k_embed_fwd<__nv_bfloat16><<<blocks_for(total, 256), 256, 0, L.stream>>>(
+        launch_k(L, k_embed_fwd<__nv_bfloat16>, dim3(blocks_for(total, 256)), dim3(256), 0, 
             (const __nv_bfloat16*)wte, (const __nv_bfloat16*)wpe, tok, (__nv_bfloat16*)x, T, C, V,
             total, L.flags);
     else
-        k_embed_fwd<float><<<blocks_for(total, 256), 256, 0, L.stream>>>(
+        launch_k(L, k_embed_fwd<float>, dim3(blocks_for(total, 256)), dim3(256), 0, 
             (const float*)wte, (const float*)wpe, tok, (float*)x, T, C, V, total, L.flags);
 }
 
@@ -115,6 +116,7 @@ __device__ __forceinline__ int rs_key(const int32_t* __restrict__ in, int from_t
 
 __global__ void __launch_bounds__(RS_THREADS)
 k_rs_hist(const int32_t* __restrict__ in, int from_tok, int V, int M, int shift, int G, int* __restrict__ hist) {
+    pdl_enter();
     __shared__ int s_h[RS_BINS];
     s_h[threadIdx.x] = 0;
     __syncthreads();
@@ -131,6 +133,7 @@ k_rs_hist(const int32_t* __restrict__ in, int from_tok, int V, int M, int shift,
 // exclusive scan of n ints in place, one block of 1024 threads: thread t
 // takes a contiguous run of ceil(n/1024) entries
 __global__ void __launch_bounds__(1024) k_rs_scan(int* __restrict__ a, int n) {
+    pdl_enter();
     __shared__ int s_w[32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int per = (n + 1023) / 1024;
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(RS_THREADS)
 k_rs_scatter(const int32_t* __restrict__ kin, const int32_t* __restrict__ vin, int from_tok, int V, int M,
              int shift, int G, const int* __restrict__ scan, int32_t* __restrict__ kout,
              int32_t* __restrict__ vout) {
+    pdl_enter();
     __shared__ int s_base[RS_BINS];
     __shared__ int s_wc[RS_THREADS / 32][RS_BINS];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -210,6 +214,7 @@ template <typename T>
 __global__ void k_embed_segsum(const T* __restrict__ dx, const int32_t* __restrict__ keys,
                                const int32_t* __restrict__ vals, int M, int C, int V,
                                float* __restrict__ dwte) {
+    pdl_enter();
     const int i = blockIdx.x;
     const int key = keys[i];
     if (key >= V) return;
@@ -236,6 +241,7 @@ __global__ void k_embed_segsum(const T* __restrict__ dx, const int32_t* __restri
 template <typename T>
 __global__ void k_embed_wpe(const T* __restrict__ dx, int B, int T_, int C, int maxT,
                             float* __restrict__ dwpe, int acc) {
+    pdl_enter();
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long long)maxT * C) return;
     int t = (int)(i / C), c = (int)(i % C);
@@ -273,11 +279,11 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
     for (int p = 0; p < passes; p++) {
         const int from_tok = p == 0;
         L.count();
-        k_rs_hist<<<G, RS_THREADS, 0, L.stream>>>(ki, from_tok, V, M, 8 * p, G, hist);
+        launch_k(L, k_rs_hist, dim3(G), dim3(RS_THREADS), 0, ki, from_tok, V, M, 8 * p, G, hist);
         L.count();
-        k_rs_scan<<<1, 1024, 0, L.stream>>>(hist, RS_BINS * G);
+        launch_k(L, k_rs_scan, dim3(1), dim3(1024), 0, hist, RS_BINS * G);
         L.count();
-        k_rs_scatter<<<G, RS_THREADS, 0, L.stream>>>(ki, vi, from_tok, V, M, 8 * p, G, hist, ko, vo);
+        launch_k(L, k_rs_scatter, dim3(G), dim3(RS_THREADS), 0, ki, vi, from_tok, V, M, 8 * p, G, hist, ko, vo);
         ki = ko; vi = vo;
         ko = (ko == kA) ? kB : kA;
         vo = (vo == vA) ? vB : vA;
@@ -288,24 +294,24 @@ void launch_embed_bwd(const Launch& L, bool bf16, const void* dx, const int32_t*
         threads = ((threads + 31) / 32) * 32;
         L.count();
         if (bf16 && L.f16)
-            k_embed_segsum<__half><<<M, threads, 0, L.stream>>>(
+            launch_k(L, k_embed_segsum<__half>, dim3(M), dim3(threads), 0, 
                 (const __half*)dx, s, s + M, M, C, V, dwte);
         else if (bf16)
-            k_embed_segsum<__nv_bfloat16><<<M, threads, 0, L.stream>>>(
+            launch_k(L, k_embed_segsum<__nv_bfloat16>, dim3(M), dim3(threads), 0, 
                 (const __nv_bfloat16*)dx, s, s + M, M, C, V, dwte);
         else
-            k_embed_segsum<float><<<M, threads, 0, L.stream>>>((const float*)dx, s, s + M, M, C, V, dwte);
+            launch_k(L, k_embed_segsum<float>, dim3(M), dim3(threads), 0, (const float*)dx, s, s + M, M, C, V, dwte);
     }
     long long n = (long long)maxT * C;
     L.count();
     if (bf16 && L.f16)
-        k_embed_wpe<__half><<<blocks_for(n, 256), 256, 0, L.stream>>>(
+        launch_k(L, k_embed_wpe<__half>, dim3(blocks_for(n, 256)), dim3(256), 0, 
             (const __half*)dx, B, T, C, maxT, dwpe, acc_params ? 1 : 0);
     else if (bf16)
-        k_embed_wpe<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, L.stream>>>(
+        launch_k(L, k_embed_wpe<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, 
             (const __nv_bfloat16*)dx, B, T, C, maxT, dwpe, acc_params ? 1 : 0);
     else
-        k_embed_wpe<float><<<blocks_for(n, 256), 256, 0, L.stream>>>((const float*)dx, B, T, C,
+        launch_k(L, k_embed_wpe<float>, dim3(blocks_for(n, 256)), dim3(256), 0, (const float*)dx, B, T, C,
                                                                      maxT, dwpe, acc_params ? 1 : 0);
 }
 
@@ -551,6 +557,7 @@ k_xent(T* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict
 // combined in thread order)
 __global__ void k_mean_loss(const float* __restrict__ row_loss, int M, float* __restrict__ out,
                             int* flags) {
+    pdl_enter();
     __shared__ float s_p[1024];
     float s = 0.0f;
     for (int i = threadIdx.x; i < M; i += blockDim.x) s += row_loss[i];
@@ -572,7 +579,7 @@ void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* target
     if (bf16 && launch_xent_bf16(L, logits, targets, row_loss, M, V, ld_, dscale, scale_dev)) {
         if (mean_loss) {
             L.count();
-            k_mean_loss<<<1, 1024, 0, L.stream>>>(row_loss, M, mean_loss, L.flags);
+            launch_k(L, k_mean_loss, dim3(1), dim3(1024), 0, row_loss, M, mean_loss, L.flags);
         }
         return;
     }
@@ -588,7 +595,7 @@ void launch_xent(const Launch& L, bool bf16, void* logits, const int32_t* target
                                                         dscale, scale_dev, L.flags);
     if (mean_loss) {
         L.count();
-        k_mean_loss<<<1, 1024, 0, L.stream>>>(row_loss, M, mean_loss, L.flags);
+        launch_k(L, k_mean_loss, dim3(1), dim3(1024), 0, row_loss, M, mean_loss, L.flags);
     }
 }
 
@@ -646,6 +653,7 @@ __global__ void k_adamw(float* __restrict__ p, LT* __restrict__ lowp,
                         const float* __restrict__ g, float* __restrict__ m, float* __restrict__ v,
                         size_t n, float lr, float b1, float b2, float eps, float wd, float c1,
                         float c2) {
+    pdl_enter();
     const size_t n4 = n / 4;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -688,9 +696,9 @@ void launch_adamw(const Launch& L, float* master, void* lowp, const float* g, fl
     int grid = (int)(want < (long long)L.num_sms * 8 ? (want < 1 ? 1 : want) : (long long)L.num_sms * 8);
     L.count();
     if (L.f16)
-        k_adamw<<<grid, 256, 0, L.stream>>>(master, (__half*)lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
+        launch_k(L, k_adamw<__half>, dim3(grid), dim3(256), 0, master, (__half*)lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
     else
-        k_adamw<<<grid, 256, 0, L.stream>>>(master, (__nv_bfloat16*)lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
+        launch_k(L, k_adamw<__nv_bfloat16>, dim3(grid), dim3(256), 0, master, (__nv_bfloat16*)lowp, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
 }
 
 template <typename T>

@@ -63,6 +63,7 @@ template <int NV, bool F16>
 __global__ void __launch_bounds__(LNV_WARPS * 32)
 k_ln_fwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const bf16* __restrict__ b,
               bf16* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, int M, int C) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * LNV_WARPS + (threadIdx.x >> 5);
     if (row >= M) return;
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(LNV_WARPS * 32, 2)
 k_ln_bwd_bf16(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ mean,
               const float* __restrict__ rstd, const bf16* __restrict__ dy, bf16* __restrict__ dx,
               float* __restrict__ part, int M, int C, int accumulate) {
+    pdl_enter();
     constexpr int NP = RES ? 3 : 2;
     constexpr int DEPTH = ln_depth(NV);
     extern __shared__ __align__(16) uint8_t s_dyn[];  // [LNV_WARPS][ln_bwd_warp_bytes]
@@ -284,6 +286,7 @@ constexpr int SR_WARPS = 32;
 __global__ void __launch_bounds__(SR_WARPS * 32)
 k_sum_rows(const float* __restrict__ part, int G, int ncols, int split, float* __restrict__ out_a,
            float* __restrict__ out_b, float* __restrict__ out_c, int acc) {
+    pdl_enter();
     __shared__ float sm[SR_WARPS][33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
@@ -315,7 +318,7 @@ void launch_sum_rows(const Launch& L, const float* part, int G, int ncols, int s
                      float* out_b, bool acc, float* out_c) {
     if (L.dry) return;
     L.count();
-    k_sum_rows<<<(ncols + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(part, G, ncols, split, out_a, out_b, out_c,
+    launch_k(L, k_sum_rows, dim3((ncols + 31) / 32), dim3(SR_WARPS * 32), 0, part, G, ncols, split, out_a, out_b, out_c,
                                                                   acc ? 1 : 0);
 }
 
@@ -351,7 +354,7 @@ bool launch_ln_fwd_bf16(const Launch& L, const void* x, const void* w, const voi
     const unsigned grid = (unsigned)((M + LNV_WARPS - 1) / LNV_WARPS);
     const int nv = (C / 8 + 31) / 32;
     L.count();
-#define LNF(NV, F) k_ln_fwd_bf16<NV, F><<<grid, LNV_WARPS * 32, 0, L.stream>>>( \
+#define LNF(NV, F) launch_k(L, k_ln_fwd_bf16<NV, F>, dim3(grid), dim3(LNV_WARPS * 32), 0,  \
         (const bf16*)x, (const bf16*)w, (const bf16*)b, (bf16*)y, mean, rstd, M, C)
     if (L.f16) {
         if (nv == 1) LNF(1, true); else if (nv == 2) LNF(2, true); else if (nv == 3) LNF(3, true); else LNF(4, true);
@@ -390,7 +393,7 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
     L.count();
     int G = 0;
 #define LNB(NV, RES, F) G = ln_bwd_blocks<NV, RES>(L, M); \
-    k_ln_bwd_bf16<NV, RES, F><<<G, LNV_WARPS * 32, smem, L.stream>>>( \
+    launch_k(L, k_ln_bwd_bf16<NV, RES, F>, dim3(G), dim3(LNV_WARPS * 32), smem,  \
         (const bf16*)x, (const bf16*)w, mean, rstd, (const bf16*)dy, (bf16*)dx, scratch, M, C, \
         accumulate ? 1 : 0)
 #define LNB_NV(RES, F) \
@@ -403,7 +406,7 @@ bool launch_ln_bwd_bf16(const Launch& L, const void* x, const void* w, const flo
 #undef LNB_NV
 #undef LNB
     L.count();
-    k_sum_rows<<<(np * C + 31) / 32, SR_WARPS * 32, 0, L.stream>>>(scratch, G, np * C, C, dw, db, dres,
+    launch_k(L, k_sum_rows, dim3((np * C + 31) / 32), dim3(SR_WARPS * 32), 0, scratch, G, np * C, C, dw, db, dres,
                                                                    acc_params ? 1 : 0);
     return true;
 }
@@ -431,6 +434,7 @@ template <bool F16>
 __global__ void __launch_bounds__(XS_THREADS)
 k_xent_bf16(bf16* __restrict__ z, const int32_t* __restrict__ targets, float* __restrict__ row_loss,
             int V, int ld, float dscale, const float* __restrict__ scale_dev, int* flags) {
+    pdl_enter();
     __shared__ float sm[XS_THREADS / 32];
     if (scale_dev) dscale *= *scale_dev;
     const long long row = blockIdx.x;
@@ -527,10 +531,10 @@ bool launch_xent_bf16(const Launch& L, void* logits, const int32_t* targets, flo
     if (L.dry) return true;
     L.count();
     if (L.f16)
-        k_xent_bf16<true><<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
+        launch_k(L, k_xent_bf16<true>, dim3(M), dim3(XS_THREADS), 0, (bf16*)logits, targets, row_loss, V, ld, dscale,
                                                            scale_dev, L.flags);
     else
-        k_xent_bf16<false><<<M, XS_THREADS, 0, L.stream>>>((bf16*)logits, targets, row_loss, V, ld, dscale,
+        launch_k(L, k_xent_bf16<false>, dim3(M), dim3(XS_THREADS), 0, (bf16*)logits, targets, row_loss, V, ld, dscale,
                                                             scale_dev, L.flags);
     return true;
 }
@@ -543,6 +547,7 @@ constexpr int CS_ROWS = 256;  // rows per partial (the same chunking as the gene
 template <bool F16>
 __global__ void __launch_bounds__(256)
 k_colsum_bf16(const bf16* __restrict__ x, int M, int N, float* __restrict__ part) {
+    pdl_enter();
     __shared__ float sm[8][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n8 = blockIdx.x * 256 + lane * 8;
@@ -589,8 +594,8 @@ bool launch_colsum_bf16(const Launch& L, const void* x, int M, int N, float* par
     if (L.dry) return true;
     dim3 grid((N + 255) / 256, (M + CS_ROWS - 1) / CS_ROWS);
     L.count();
-    if (L.f16) k_colsum_bf16<true><<<grid, 256, 0, L.stream>>>((const bf16*)x, M, N, part);
-    else k_colsum_bf16<false><<<grid, 256, 0, L.stream>>>((const bf16*)x, M, N, part);
+    if (L.f16) launch_k(L, k_colsum_bf16<true>, dim3(grid), dim3(256), 0, (const bf16*)x, M, N, part);
+    else launch_k(L, k_colsum_bf16<false>, dim3(grid), dim3(256), 0, (const bf16*)x, M, N, part);
     return true;
 }
 
@@ -645,6 +650,7 @@ __global__ void k_embed_chunks(const T* __restrict__ dx, const int32_t* __restri
                                const int32_t* __restrict__ vals, int M, int C, int V,
                                float* __restrict__ dwte, float* __restrict__ first,
                                float* __restrict__ last) {
+    pdl_enter();
     const int c = blockIdx.x;
     const int col = threadIdx.x * 8;
     if (col >= C) return;
@@ -683,6 +689,7 @@ template <typename T>
 __global__ void k_embed_gather(const int32_t* __restrict__ keys, int M, int C, int V,
                                float* __restrict__ dwte, const float* __restrict__ first,
                                const float* __restrict__ last) {
+    pdl_enter();
     const int c = blockIdx.x;
     const int col = threadIdx.x * 8;
     if (col >= C) return;
@@ -722,16 +729,16 @@ bool launch_embed_chunks(const Launch& L, bool is_bf16, const void* dx, const in
     const int threads = ((C / 8 + 31) / 32) * 32;
     L.count();
     if (is_bf16 && L.f16)
-        k_embed_chunks<__half><<<nchunk, threads, 0, L.stream>>>((const __half*)dx, keys, vals, M, C, V,
+        launch_k(L, k_embed_chunks<__half>, dim3(nchunk), dim3(threads), 0, (const __half*)dx, keys, vals, M, C, V,
                                                                  dwte, first, last);
     else if (is_bf16)
-        k_embed_chunks<bf16><<<nchunk, threads, 0, L.stream>>>((const bf16*)dx, keys, vals, M, C, V,
+        launch_k(L, k_embed_chunks<bf16>, dim3(nchunk), dim3(threads), 0, (const bf16*)dx, keys, vals, M, C, V,
                                                                dwte, first, last);
     else
-        k_embed_chunks<float><<<nchunk, threads, 0, L.stream>>>((const float*)dx, keys, vals, M, C, V,
+        launch_k(L, k_embed_chunks<float>, dim3(nchunk), dim3(threads), 0, (const float*)dx, keys, vals, M, C, V,
                                                                 dwte, first, last);
     L.count();
-    k_embed_gather<float><<<nchunk, threads, 0, L.stream>>>(keys, M, C, V, dwte, first, last);
+    launch_k(L, k_embed_gather<float>, dim3(nchunk), dim3(threads), 0, keys, M, C, V, dwte, first, last);
     return true;
 }
 

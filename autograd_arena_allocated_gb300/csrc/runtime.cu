@@ -24,6 +24,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <unordered_set>
 
@@ -188,8 +189,20 @@ static tt_status fail(tt_ctx* c, tt_status s, const char* fmt, ...) {
     return s;
 }
 
+// Programmatic dependent launch for every kernel that supports it (each such
+// kernel waits for its predecessor before touching global memory), unless
+// TT_PDL=0 is in the environment (for comparisons).
+static bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("TT_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 static Launch launch_of(tt_ctx* c) {
     Launch L;
+    L.pdl = pdl_enabled();
     L.stream = c->stream;
     L.flags = (int*)c->arena;
     L.launches = &c->launches;

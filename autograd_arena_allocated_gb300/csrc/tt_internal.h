@@ -9,6 +9,7 @@
 
 #include <string>
 #include <vector>
+#include <utility>
 
 #include "../../include/tt.h"
 #include "../../include/tt_ops.h"
@@ -36,12 +37,46 @@ struct Launch {
     bool dry = false;      // plan only: allocate, launch nothing
     int gemm_backend = 0;  // 0 auto, 1 SIMT only
     int num_sms = 148;
-    bool pdl = false;      // decode kernels: programmatic dependent launch
+    bool pdl = false;      // programmatic dependent launch (kernels launched by launch_k or the GEMM)
     bool f16 = false;      // 16-bit storage is IEEE half, not bf16 (the model's TT_FP16 mode)
     bool no_pair = false;  // tensor-core GEMMs without the two-CTA pair form
     long long wait_cycles = 4000000000LL;  // limit of every bounded device-side wait (clock64 cycles)
     void count() const { if (launches) ++*launches; }
 };
+
+// ------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched by launch_k with L.pdl set
+// may be scheduled while the kernel before it on the stream is finishing.
+// Every such kernel calls pdl_enter() before it touches global memory: the
+// wait returns once the previous grid has completed and its writes are
+// visible, so stream order holds for every read and write; the trigger lets
+// the next kernel be scheduled once all of this grid's CTAs have started.
+// Both instructions are no-ops in a kernel launched without the attribute.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+inline void launch_k(const Launch& L, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute at[1];
+    if (L.pdl) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+    }
+    cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+#endif
 
 // ------------------------------------------------------------ per-device set-up
 // Kernel attributes (the dynamic shared-memory limit) and occupancy results
