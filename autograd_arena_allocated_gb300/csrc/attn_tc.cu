@@ -117,7 +117,6 @@ __global__ void __launch_bounds__(THREADS, 3)
 k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               bf16* __restrict__ y, float* __restrict__ lse, int T, int C, int H, int nbh, int* flags,
               long long wl) {
-    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + F_BAR);
@@ -166,6 +165,7 @@ k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    pdl_enter();  // the set-up above overlaps the previous kernel's end; global memory only from here
 
     if (warp == 0) {
         if (lane == 0) {
@@ -451,7 +451,6 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                  const __grid_constant__ CUtensorMap to, const bf16* __restrict__ y,
                  const float* __restrict__ lse, float* __restrict__ Dlt, bf16* __restrict__ dqkv,
                  float* __restrict__ bpart, int T, int C, int H, int nbh, int* flags, long long wl) {
-    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + Q_BAR);
@@ -498,6 +497,7 @@ k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    pdl_enter();  // the set-up above overlaps the previous kernel's end; global memory only from here
 
     if (warp == 0) {
         if (lane == 0) {
@@ -684,7 +684,6 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
                    const __grid_constant__ CUtensorMap to, const float* __restrict__ lse,
                    const float* __restrict__ Dlt, bf16* __restrict__ dqkv, float* __restrict__ bpart, int T,
                    int C, int H, int nbh, int* flags, long long wl) {
-    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint64_t* bars = (uint64_t*)(sm + K_BAR);
@@ -726,6 +725,7 @@ k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    pdl_enter();  // the set-up above overlaps the previous kernel's end; global memory only from here
 
     if (warp == 0) {
         if (lane == 0) {

@@ -289,7 +289,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
           const Params p) {
-    pdl_enter();
     using CF = Cfg<BN, PAIR>;
     constexpr int S = CF::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -348,6 +347,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_holder;
     if (PAIR) cluster_sync_all();  // the peer's barriers exist before any copy or commit reaches them
+    // everything above touches only this CTA's (and its peer's) shared and
+    // tensor memory: it overlaps the previous kernel's end under a dependent
+    // launch; global memory is read and written only after this wait
+    pdl_enter();
     const UnitIter U = unit_iter(p);
     const bool leader = U.rank == 0;
 
