@@ -243,18 +243,18 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "9470148af83b837e",
+    "sources": "30b239fddbc88d4b",
     "bytes_per_launch_group": {
-        "gemm_fwd": 344785664,
-        "gemm_dx": 311672853,
-        "gemm_dw": 305877985,
-        "attn_fwd": 178769408,
-        "attn_bwd": 560025856,
-        "xent": 6543663360,
-        "ln_fwd": 54798080,
-        "ln_bwd": 167800832,
-        "adamw": 3673080064,
-        "embed_bwd": 124909312,
+        "gemm_fwd": 349406438,
+        "gemm_dx": 308658521,
+        "gemm_dw": 304108690,
+        "attn_fwd": 178593792,
+        "attn_bwd": 559948544,
+        "xent": 6542702336,
+        "ln_fwd": 54795264,
+        "ln_bwd": 167937280,
+        "adamw": 3672777728,
+        "embed_bwd": 124914432,
     },
 }
 
