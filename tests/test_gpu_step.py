@@ -290,6 +290,50 @@ def test_step_is_bitwise_deterministic_and_host_tokens_match(ctx):
     assert l3 == l1 and torch.equal(g1, run.grads)
 
 
+_PDL_OFF_STEP = r"""
+import sys
+import numpy as np, torch
+from autograd_arena_allocated_gb300 import api, synth
+w = synth.WORKLOADS["char_bf16"]
+sh = w.shape
+p = synth.init_params(sh, jitter=0.05)
+tok, tgt = synth.token_stream(8, 256, sh.V, "zipf")
+with api.Context(1 << 30) as ctx:
+    cfg = api.make_config(sh.L, sh.C, sh.H, sh.V, sh.maxT, "bf16")
+    ctx.set_model(cfg)
+    master = torch.from_numpy(p).cuda()
+    low = torch.empty(master.numel(), device="cuda", dtype=torch.bfloat16)
+    ctx.cast_bf16(master, low)
+    grads = torch.empty(master.numel(), device="cuda")
+    ctx.reset()
+    loss = ctx.step(low, grads, torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda(), 8, 256)
+    np.savez(sys.argv[1], loss=np.array([loss]), grads=grads.cpu().numpy())
+"""
+
+
+def test_step_is_the_same_without_dependent_launch(ctx, tmp_path):
+    """Programmatic dependent launch changes when a kernel's CTAs are
+    scheduled, never what they compute: each waits for its predecessor before
+    touching global memory.  The same bf16 step in a process with TT_PDL=0
+    (every kernel launched in plain stream order) gives the same bits."""
+    import subprocess
+    import sys
+
+    w = synth.WORKLOADS["char_bf16"]
+    sh = w.shape
+    p, tok, tgt = make_inputs(sh, 8, 256, "zipf", jitter=0.05)
+    run = Run(ctx, sh, "bf16", p)
+    loss = run.step(tok, tgt)
+    g = run.grads.cpu().numpy()
+    out = tmp_path / "pdl_off.npz"
+    env = dict(os.environ, TT_PDL="0")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([sys.executable, "-c", _PDL_OFF_STEP, str(out)], check=True, env=env, cwd=root, timeout=600)
+    r = np.load(out)
+    assert float(r["loss"][0]) == loss
+    assert np.array_equal(r["grads"], g)
+
+
 # ----------------------------------------------------------------- boundary
 def test_arena_oom_is_detected_before_launch():
     sh = synth.WORKLOADS["tiny_fp32"].shape
