@@ -243,18 +243,18 @@ OP_SHAPES = {
 # source differs, the roofline reports no traffic.
 MEASURED_TRAFFIC = {
     "workload": "gpt2_124m_b32",
-    "sources": "30b239fddbc88d4b",
+    "sources": "2b3b81b188f634b9",
     "bytes_per_launch_group": {
-        "gemm_fwd": 349406438,
-        "gemm_dx": 308658521,
-        "gemm_dw": 304108690,
-        "attn_fwd": 178593792,
-        "attn_bwd": 559948544,
-        "xent": 6542702336,
-        "ln_fwd": 54795264,
-        "ln_bwd": 167937280,
-        "adamw": 3672777728,
-        "embed_bwd": 124914432,
+        "gemm_fwd": 347090761,
+        "gemm_dx": 299981605,
+        "gemm_dw": 294930312,
+        "attn_fwd": 178761216,
+        "attn_bwd": 560265984,
+        "xent": 6543418112,
+        "ln_fwd": 54743808,
+        "ln_bwd": 167860736,
+        "adamw": 3673016064,
+        "embed_bwd": 124952320,
     },
 }
 
